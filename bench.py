@@ -1,0 +1,413 @@
+"""Benchmark of the fp8 MoE decode / speculative-verify layer on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload verify8]
+                [--impl ours|reference]
+
+One step = one pass of the whole layer (route, union, dispatch, gate/up GEMM,
+down GEMM, combine) over one batch of seeded synthetic inputs already
+resident in HBM.  The step runs through the C ABI's step entry points with a
+CUDA event between consecutive kernels on the launching stream, so every
+kernel's device time is measured live; L2 is flushed (a 256 MB write) before
+every step, outside the events.  `value` = rows processed by all ranks / max
+over ranks of the summed step time.  Under torchrun every rank runs its own
+replica (the layer has no exchange step on one GPU): scaling "weak".
+
+`e2e` measures the same metric through moe_layer with host buffers: per step
+the rows go from pinned host memory to the device, the layer runs, and the
+bf16 output comes back to pinned host memory.
+
+`--impl reference` times the CPU oracle (the plain restatement the tests
+check the kernels against) on the host cores, on a bounded sample of the same
+workload, and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = ("MoE-layer rows/s and achieved HBM GB/s (% of 8 TB/s) at 8-row verify; "
+          "fp8 TFLOPS at 4096")
+PHASES = ["router", "union", "dispatch", "gate_up", "down", "combine"]
+KERNELS_PER_STEP = 7          # router logits + select, union, dispatch, gate/up, down, combine
+FLUSH_BYTES = 256 << 20       # > 129 MB L2
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------- algorithmics --
+def algorithmic(wl, ids: np.ndarray, valid: np.ndarray) -> dict:
+    """Bytes each kernel must move at minimum and the layer's fp8 MMA flops."""
+    s = wl.shape
+    H, I, E, K, S = s.hidden, s.inter, s.n_experts, s.topk, s.n_shared
+    R = wl.rows
+    Rv = int(valid.sum())
+    U = len(np.unique(ids[ids >= 0]))
+    T = Rv * (K + S)
+    ent = U + (S if Rv else 0)
+    w_gu = ent * (2 * I * H + 2 * (I // 128) * (H // 128) * 4)
+    w_dn = ent * (H * I + (H // 128) * (I // 128) * 4)
+    b = {
+        "router": E * H * 4 + R * H * 2 + E * 4 + 2 * R * E * 4 + R * K * 8,
+        "union": R * K * 4 + (R * (K + S) * 2) * 4,
+        "dispatch": Rv * H * 2 + T * H + T * (H // 128) * 4,
+        "gate_up": w_gu + T * H + T * (H // 128) * 4 + T * I + T * (I // 128) * 4,
+        "down": w_dn + T * I + T * (I // 128) * 4 + T * H * 4,
+        "combine": Rv * (K + S) * H * 4 + Rv * K * 4 + R * H * 2,
+    }
+    flops = 2 * T * (2 * I * H) + 2 * T * (H * I)
+    return {"bytes": b, "total_bytes": sum(b.values()), "flops": flops, "U": U, "T": T,
+            "Rv": Rv, "weights_bytes": w_gu + w_dn}
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", gpu_index, "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ oracle --
+def oracle_baseline(wl, t_dev: dict, target_s: float = 12.0) -> dict:
+    """The CPU oracle, as it stands, on a bounded sample of the workload's rows."""
+    import oracle
+    host = {k: (v.detach().cpu().view(torch.int16).numpy().view(np.uint16)
+                if v.dtype == torch.bfloat16 else v.detach().cpu().numpy())
+            for k, v in t_dev.items()}
+    cores = oracle.num_threads()
+    valid = np.nonzero(host["row_valid"])[0]
+    t0 = time.perf_counter()
+    oracle.moe_layer(wl.shape, host, rows=valid[:1])
+    one = max(time.perf_counter() - t0, 1e-3)
+    n = int(max(1, min(len(valid), target_s / one)))
+    rows = valid[np.linspace(0, len(valid) - 1, n).astype(int)]
+    t0 = time.perf_counter()
+    oracle.moe_layer(wl.shape, host, rows=rows)
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "rows/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of the {len(valid)} valid rows of {wl.name}, full layer per row "
+                      f"(routing + {wl.shape.topk} routed + {wl.shape.n_shared} shared experts), "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args, wl) -> None:
+    """Reference arm: the CPU oracle on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    t0 = time.perf_counter()
+    # inputs only: generated where it is quick, then handed to the oracle on the host
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    host = synth.to_numpy(synth.make_layer(wl, device=gen_dev))
+    if gen_dev == "cuda":
+        torch.cuda.empty_cache()
+    valid = np.nonzero(host["row_valid"])[0]
+    cores = oracle.num_threads()
+    # each step: a bounded sample of rows, sized so the whole run takes about 2 minutes
+    per_step = max(1.0, min(10.0, 120.0 / max(1, args.steps)))
+    t1 = time.perf_counter()
+    oracle.moe_layer(wl.shape, host, rows=valid[:1])
+    one = max(time.perf_counter() - t1, 1e-3)
+    n = int(max(1, min(len(valid), per_step / one)))
+    rows = valid[:n]
+    if args.warmup > 0:
+        oracle.moe_layer(wl.shape, host, rows=rows[:1])
+    times = []
+    for _ in range(args.steps):
+        t1 = time.perf_counter()
+        oracle.moe_layer(wl.shape, host, rows=rows)
+        times.append(time.perf_counter() - t1)
+    step = statistics.mean(times)
+    value = n / step
+    line = {"metric": METRIC, "value": value, "unit": "rows/s", "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp32 dequant / fp64 accumulate (CPU)",
+            "data": "synthetic (seeded)",
+            "config": {"workload": wl.name, "rows": wl.rows, "sample_rows": n},
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{n} rows of {wl.name} per step"},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "setup_s": round(t1 - t0, 1)}
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------------- ours --
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="verify8", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extra", default="verify64,decode512,prefill4096",
+                    help="other workloads measured on the same weights (summary only)")
+    args = ap.parse_args()
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import moe_speculative_verify_gb300 as m
+    m.build()
+    m.load()
+
+    weights = synth.make_expert_weights(wl, device=dev)
+    W = m.Weights.from_tensors(weights)
+    cfg = m.Config.from_shape(wl.shape)
+    pk = peaks()
+
+    def measure(wl_m, steps, warmup, record_clocks):
+        R = wl_m.rows
+        s = wl_m.shape
+        ri = synth.make_router_inputs(wl_m, device=dev)
+        ids = torch.empty((R, s.topk), dtype=torch.int32, device=dev)
+        wts = torch.empty((R, s.topk), dtype=torch.float32, device=dev)
+        logits = torch.empty((R, s.n_experts), dtype=torch.float32, device=dev)
+        ub = torch.zeros(m.moe_union_bytes(cfg, R) // 4, dtype=torch.int32, device=dev)
+        ws = torch.zeros(m.moe_ffn_workspace_bytes(cfg, R), dtype=torch.uint8, device=dev)
+        y_slots = torch.empty((R * s.topk, s.hidden), dtype=torch.float32, device=dev)
+        y_sh = torch.empty((R, s.hidden), dtype=torch.float32, device=dev)
+        out = torch.empty((R, s.hidden), dtype=torch.bfloat16, device=dev)
+        flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        stream = torch.cuda.current_stream()
+
+        def step(ev=None):
+            def mark(i):
+                if ev is not None:
+                    ev[i].record(stream)
+            mark(0)
+            m.moe_route(cfg, ri["x"], ri["wr"], ri["bias"], ri["row_valid"], ids, wts, logits)
+            mark(1)
+            m.moe_build_union(cfg, ids, ub)
+            mark(2)
+            m.moe_dispatch(cfg, ri["x"], ub, ws)
+            mark(3)
+            m.moe_gate_up_fp8(cfg, W, ub, R, ws)
+            mark(4)
+            m.moe_down_fp8(cfg, W, ub, R, y_slots, y_sh, ws)
+            mark(5)
+            m.moe_combine(cfg, y_slots, y_sh, wts, ub, out)
+            mark(6)
+
+        for _ in range(warmup):
+            flush.zero_()
+            step()
+        torch.cuda.synchronize()
+        assert m.moe_get_device_error(ws) == 0
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        clk = ClockSampler(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
+            if record_clocks else None
+        wall0 = time.perf_counter()
+        for i in range(steps):
+            flush.zero_()
+            step(evs[i])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+        if world > 1:
+            torch.distributed.barrier()
+        clocks = clk.stop() if clk else None
+        err = m.moe_get_device_error(ws)
+        assert err == 0, err
+        ph = {p: [] for p in PHASES}
+        tot = []
+        for e in evs:
+            for i, p in enumerate(PHASES):
+                ph[p].append(e[i].elapsed_time(e[i + 1]))
+            tot.append(e[0].elapsed_time(e[6]))
+        alg = algorithmic(wl_m, ids.cpu().numpy(), ri["row_valid"].cpu().numpy())
+        return {"ri": ri, "phase_ms": {p: statistics.mean(v) for p, v in ph.items()},
+                "step_ms": statistics.mean(tot), "wall_s": wall, "alg": alg, "clocks": clocks,
+                "out": out}
+
+    res = measure(wl, args.steps, max(args.warmup, 3), True)
+    step_ms = res["step_ms"]
+    if world > 1:
+        t = torch.tensor([step_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+    alg = res["alg"]
+    R = wl.rows
+    value = world * R / (step_ms / 1e3)
+    layer_gbs = alg["total_bytes"] / (step_ms / 1e3) / 1e9
+    tflops = alg["flops"] / (step_ms / 1e3) / 1e12
+
+    # roofline of the dominant kernel (the gate/up GEMM: two thirds of the weight bytes)
+    dom = max(res["phase_ms"], key=res["phase_ms"].get)
+    dom_ms = res["phase_ms"][dom]
+    dom_bytes = alg["bytes"][dom]
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    roofline = {"kernel": {"gate_up": "ffn_kernel<NT,gate_up>", "down": "ffn_kernel<NT,down>"}
+                .get(dom, dom), "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                "traffic": None, "peak_source": pk["source"],
+                "algorithmic_bytes_per_launch": dom_bytes}
+
+    extra = {}
+    if rank == 0 and args.extra:
+        for name in [n for n in args.extra.split(",") if n and n != wl.name]:
+            wl2 = synth.WORKLOADS[name]
+            r2 = measure(wl2, 5, 3, False)
+            a2 = r2["alg"]
+            extra[name] = {
+                "rows": wl2.rows, "rows_per_s": round(wl2.rows / (r2["step_ms"] / 1e3), 1),
+                "ms_per_step": round(r2["step_ms"], 4),
+                "hbm_gbs": round(a2["total_bytes"] / (r2["step_ms"] / 1e3) / 1e9, 1),
+                "fp8_tflops": round(a2["flops"] / (r2["step_ms"] / 1e3) / 1e12, 1),
+                "distinct_experts": a2["U"],
+                "phase_ms": {k: round(v, 4) for k, v in r2["phase_ms"].items()}}
+            del r2
+
+    # end to end through moe_layer with host buffers
+    import moe_speculative_verify_gb300 as m2
+    ri = res["ri"]
+    x_host = ri["x"].cpu().pin_memory()
+    v_host = ri["row_valid"].cpu().pin_memory()
+    out_host = torch.empty((R, wl.shape.hidden), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(ri["x"])
+    v_dev = torch.empty_like(ri["row_valid"])
+    out_dev = torch.empty((R, wl.shape.hidden), dtype=torch.bfloat16, device=dev)
+    lws = torch.zeros(m2.moe_workspace_bytes(cfg, R), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        v_dev.copy_(v_host, non_blocking=True)
+        m2.moe_layer(cfg, x_dev, ri["wr"], ri["bias"], W, v_dev, out_dev, lws)
+        out_host.copy_(out_dev, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(3):
+        flush.zero_()
+        e2e_step()
+    e2e_times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_step()
+        e2e_times.append(time.perf_counter() - t0)
+    e2e_s = statistics.mean(e2e_times)
+    e2e_same = bool(torch.equal(out_host.to(dev), res["out"]))
+
+    cpu = None
+    if rank == 0 and world >= 1 and not args.no_cpu_baseline:
+        t_all = dict(res["ri"])
+        t_all.update(weights)
+        cpu = oracle_baseline(wl, t_all)
+
+    if rank == 0:
+        clocks = res["clocks"]
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(step_ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8_e4m3 (fp32 accumulate; bf16 in/out)", "data": "synthetic (seeded)",
+            "config": {"workload": wl.name, "rows": R, "valid_rows": alg["Rv"],
+                       "hidden": wl.shape.hidden, "inter": wl.shape.inter,
+                       "experts": wl.shape.n_experts, "groups": wl.shape.n_groups,
+                       "topk_groups": wl.shape.topk_groups, "topk": wl.shape.topk,
+                       "shared": wl.shape.n_shared, "distinct_experts": alg["U"],
+                       "l2": "flushed before every step (256 MB write, outside the events)",
+                       "parallelism": f"replicas x{world}"},
+            "hbm": {"achieved_gbs": round(layer_gbs, 1),
+                    "frac_of_measured": round(layer_gbs / pk["hbm_gbs"], 4),
+                    "frac_of_8tbs": round(layer_gbs / 8000.0, 4),
+                    "algorithmic_bytes_per_step": alg["total_bytes"]},
+            "fp8_tflops": round(tflops, 2),
+            "phase_ms": {k: round(v, 4) for k, v in res["phase_ms"].items()},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(world * R / e2e_s, 1), "unit": "rows/s",
+                    "h2d_bytes_per_step": x_host.numel() * 2 + v_host.numel(),
+                    "d2h_bytes_per_step": out_host.numel() * 2,
+                    "note": "moe_layer, pinned host x -> device -> pinned host out, per step",
+                    "bit_identical_to_step_path": e2e_same},
+            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "clocks": clocks,
+            "also": extra,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,281 @@
+/*
+ * moe_verify.h -- C ABI of the fine-grained fp8 MoE layer for decode and
+ * speculative verify on one GB300 (sm_103a).
+ *
+ * The problem, as the source pages state it:
+ *   - openinfer #610 "TP8 span row mapping -- single-user speculative decode at
+ *     186 tok/s", section "What": an 8-row block holds 1 committed token and up
+ *     to 7 speculative drafts; the MoE phases are an expert union, a gate/up
+ *     GEMM with SiLU and a down GEMM, with fixed-order reductions; pad rows are
+ *     zero-filled so no NaN leaks (section "Gates": the same rows through any
+ *     mapping must be bit-identical).
+ *   - mstar #388 "Speed up GLM-5.2 with fp8 kernels and one-graph MTP", commit
+ *     on kernel switches: the router kernel (NoAuxTcRouter's top-k op), the
+ *     fused fp8 MoE decode chain over routed and shared experts, the MoE's
+ *     partials reduced once; commit on FlashInfer's block-scale GEMM:
+ *     activations quantised to e4m3 per 128 columns.
+ *   - MoE-Infinity #140 "converge spec-decode stack", commit list: the sigmoid
+ *     router's e_score_correction_bias; expert tensors [gate_proj, up_proj,
+ *     down_proj] stored e4m3 with 128x128 FP8 block scales.
+ *   - pypto-serving #223 "DSpark speculation (K=7)", "What this adds": the
+ *     router gate kept in FP32; idle (pad) rows carry -1 and produce nothing.
+ *
+ * Conventions for every entry point:
+ *   - All pointers are DEVICE pointers unless stated otherwise; the caller owns
+ *     every buffer and every stream.  The library allocates nothing, holds no
+ *     state between calls, and never synchronises the stream except in
+ *     moe_get_device_error.  Calls are asynchronous on `stream` and can be
+ *     captured in a CUDA graph.
+ *   - Refusals are synchronous: a NULL required pointer, a misaligned pointer
+ *     (16 bytes for bf16 / e4m3 / output arrays, 4 bytes for fp32 / int32), an
+ *     unsupported shape or a short buffer returns an error code and launches
+ *     nothing.  R == 0 returns MOE_OK and launches nothing.  R above
+ *     MOE_MAX_ROWS returns MOE_ERR_UNSUPPORTED (no silent truncation).
+ *   - A launch failure is read back with cudaGetLastError right after the
+ *     launch and returned as MOE_ERR_CUDA, so it never surfaces in a later,
+ *     unrelated kernel.
+ *   - A pad row (row_valid[r] == 0) may hold NaN in x.  It is not routed
+ *     (ids -1, weights 0), takes no place in the union, and its output row is
+ *     +0.0 in every column.
+ *   - For a fixed R the kernel configuration is fixed, and no reduction depends
+ *     on which slot of the batch a row occupies: a row's outputs are bit-
+ *     identical wherever it sits and whatever its neighbours hold.
+ */
+#ifndef MOE_VERIFY_H
+#define MOE_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* NULL / misaligned pointer, bad shape or ids   */
+    MOE_ERR_UNSUPPORTED = 2,   /* shape or row count beyond the compiled limits */
+    MOE_ERR_CUDA = 3,          /* a CUDA runtime or launch error                */
+    MOE_ERR_TIMEOUT = 4,       /* a bounded device-side wait ran out            */
+    MOE_ERR_WORKSPACE = 5      /* workspace or buffer smaller than required     */
+} moe_status_t;
+
+/* Compiled limits. */
+#define MOE_MAX_ROWS 4096      /* rows per call                                   */
+#define MOE_MAX_EXPERTS 256    /* routed experts                                  */
+#define MOE_MAX_TOPK 16        /* experts per row                                 */
+#define MOE_MAX_GROUPS 32      /* expert groups                                   */
+#define MOE_BLOCK 128          /* quantisation block: 1x128 activations, 128x128 weights */
+
+/*
+ * Layer shape.  hidden (H) and inter (I) are multiples of 128 (128..16384);
+ * n_experts (E) <= 256 is a multiple of n_groups (G <= 32); topk_groups (TG)
+ * <= G; topk (K) <= min(16, TG*E/G); n_shared (S) is 0 or 1; routed_scaling
+ * multiplies the normalised routing weights (2.5 for GLM-5.2-class layers).
+ * wait_timeout_us bounds every device-side wait (0 = 2 000 000 us).
+ */
+typedef struct {
+    int32_t hidden;
+    int32_t inter;
+    int32_t n_experts;
+    int32_t n_groups;
+    int32_t topk_groups;
+    int32_t topk;
+    int32_t n_shared;
+    float routed_scaling;
+    uint32_t wait_timeout_us;
+} moe_config_t;
+
+/*
+ * Expert weights: e4m3 (OCP e4m3fn) codes, output-major (K contiguous), with
+ * one fp32 scale per 128x128 block; the dequantised weight is code * scale.
+ *   w_gate, w_up : uint8 [E, I, H]      s_gate, s_up : fp32 [E, I/128, H/128]
+ *   w_down       : uint8 [E, H, I]      s_down       : fp32 [E, H/128, I/128]
+ *   sh_*         : the shared expert, same layouts with S in place of E
+ *                  (ignored when n_shared == 0).
+ * Device memory, read only; 16-byte aligned codes, 4-byte aligned scales.
+ */
+typedef struct {
+    const uint8_t* w_gate;
+    const uint8_t* w_up;
+    const uint8_t* w_down;
+    const float* s_gate;
+    const float* s_up;
+    const float* s_down;
+    const uint8_t* sh_gate;
+    const uint8_t* sh_up;
+    const uint8_t* sh_down;
+    const float* sh_s_gate;
+    const float* sh_s_up;
+    const float* sh_s_down;
+} moe_weights_t;
+
+/*
+ * moe_route -- router logits, sigmoid scores with correction bias, grouped
+ * top-k and weight normalisation (mstar #388, NoAuxTcRouter; MoE-Infinity
+ * #140, e_score_correction_bias; pypto-serving #223, router gate in FP32).
+ *
+ *   x_bf16    bf16 [R, H] row-major          w_router fp32 [E, H] (16-byte aligned)
+ *   bias      fp32 [E]                        row_valid uint8 [R] or NULL (all valid)
+ *   topk_ids  int32 [R, K]  (out)             topk_w   fp32 [R, K] (out)
+ *   logits    fp32 [R, E]   (out, required: also the scratch between the
+ *                            logits and the selection kernels)
+ *
+ * Definition (all IEEE fp32, fixed order, so a CPU restatement reproduces the
+ * ids bit for bit):
+ *   logit[r,e] = sum_h x[r,h] * w_router[e,h] reduced as follows: h is cut
+ *     into chunks of 1024 (the last may be shorter); inside chunk c, lane
+ *     l = 0..31 owns h = c*1024 + 128*i + 4*l + j (i ascending, j = 0..3) and
+ *     forms p = fma(x, w, p) from p = 0; per lane q = p(chunk 0), then
+ *     q = q + p(chunk c) for c = 1, 2, ...; the 32 lane values are combined by
+ *     the butterfly v[l] = v[l] + v[l ^ d], d = 16, 8, 4, 2, 1.
+ *   s = 1 / (1 + exp(-logit)) with exp evaluated by Cody-Waite reduction
+ *     (ln2 split into a 16-significant-bit head and an fp32 tail) and the
+ *     degree-7 Taylor series in Horner form, argument clamped to [-87, 87];
+ *   b = s + bias[e];
+ *   group score = the sum of the two largest b of the group (the largest
+ *     alone for single-expert groups); the TG best groups are kept, ties to
+ *     the lower group id;
+ *   the K best experts of the kept groups by b, ties to the lower expert id,
+ *     listed by b descending;
+ *   w_k = (s_k / (s_0 + ... + s_{K-1})) * routed_scaling, the sum in k order.
+ *   Pad rows: ids -1, weights 0, logits untouched.
+ */
+moe_status_t moe_route(const moe_config_t* cfg, const void* x_bf16, const float* w_router,
+                       const float* bias, const uint8_t* row_valid, int32_t R,
+                       int32_t* topk_ids, float* topk_w, float* logits, moe_stream_t stream);
+
+/*
+ * moe_build_union -- the deduplicated expert union of the batch and its
+ * dispatch order (openinfer #610, "What": the union phase; MoE-Infinity #140:
+ * the per-token union of the verify block's routed experts).
+ *
+ *   topk_ids   int32 [R, K]: per valid row K distinct ids in [0, E); a pad row
+ *              holds -1 in every slot.  A row breaking this is treated as a pad
+ *              row and union_buf[5] is set to MOE_ERR_INVALID_ARG.
+ *   union_buf  int32, at least moe_union_bytes(cfg, R) bytes (out).
+ *
+ * union_buf layout (int32 words; KS = K + S slots per row):
+ *   [0] U  number of distinct routed experts hit    [1] R_v valid rows
+ *   [2] T  gathered slots = R_v * KS                [3] GEMM work items
+ *   [4] rows per work item                          [5] error code (0 = OK)
+ *   [6], [7] reserved
+ *   counts  [E+1]   at word 8: slots per expert; counts[E] = R_v * S
+ *   offsets [E+2]   exclusive prefix of counts (experts ascending, shared last)
+ *   ulist   [E+1]   the U experts hit, ascending, then E (the shared entry)
+ *   pos     [R*KS]  gathered position of slot (r, k); k = K is the shared
+ *                   slot; -1 for pad rows
+ *   src     [R*KS]  r*KS + k of gathered position p (p < T)
+ *   items   [.. *4] work items (entry, first gathered row, row count, 0)
+ * Inside an expert, slots are placed in (row, k) order; shared rows in row
+ * order.  Word offsets of each array follow from E, K, S and R as listed.
+ */
+size_t moe_union_bytes(const moe_config_t* cfg, int32_t max_rows);
+moe_status_t moe_build_union(const moe_config_t* cfg, const int32_t* topk_ids, int32_t R,
+                             int32_t* union_buf, size_t union_bytes, moe_stream_t stream);
+
+/*
+ * moe_expert_ffn_fp8 -- dispatch and the expert FFNs of the union
+ * (openinfer #610, "What": union / GEMM / SiLU phases; mstar #388: fused fp8
+ * MoE over routed and shared experts; FlashInfer commit: activations to e4m3
+ * per 128 columns).  For every gathered slot (row r, expert e):
+ *   x is quantised per row and 128 columns: scale = amax/448 (1 for an
+ *     all-zero block), code = e4m3_rn_satfinite(x / scale) (fp32 divide);
+ *   g = x^.Wg^T, u = x^.Wu^T with fp32 accumulation; h = silu(g) * u;
+ *   h is quantised per 128 columns by the same rule;
+ *   o = h^.Wd^T with fp32 accumulation.
+ * Every GEMM runs on tcgen05 fp8 tensor cores with the 128x128 block scales
+ * applied to each 128-wide K-block partial (fp32 scales are not expressible
+ * in the MMA's own block-scale format).
+ *
+ *   x_bf16    bf16 [R, H]                     union_buf from moe_build_union
+ *   y_slots   fp32 [R*K, H] (out): o of slot (r, k) at row r*K + k
+ *   y_shared  fp32 [R, H]   (out): the shared expert's o (NULL if S == 0)
+ *   ws        device scratch of at least moe_ffn_workspace_bytes(cfg, R) bytes,
+ *             256-byte aligned; its first 256 bytes hold the device error word,
+ *             which the caller zeroes once before first use (errors stay
+ *             recorded until moe_get_device_error clears them).
+ * Rows of y_* that belong to pad rows are left untouched.
+ */
+size_t moe_ffn_workspace_bytes(const moe_config_t* cfg, int32_t max_rows);
+moe_status_t moe_expert_ffn_fp8(const moe_config_t* cfg, const void* x_bf16,
+                                const moe_weights_t* w, const int32_t* union_buf, int32_t R,
+                                float* y_slots, float* y_shared, void* ws, size_t ws_bytes,
+                                moe_stream_t stream);
+
+/*
+ * The three steps of moe_expert_ffn_fp8, callable one by one (same arguments,
+ * same workspace; moe_expert_ffn_fp8 is exactly these three in order):
+ *   moe_dispatch     quantise each valid row per 1x128 and write it to its K+S
+ *                    gathered positions (workspace);
+ *   moe_gate_up_fp8  g and u GEMMs, h = silu(g) * u, h quantised per 1x128
+ *                    (workspace);
+ *   moe_down_fp8     the down GEMM, fp32 rows to y_slots / y_shared.
+ */
+moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x_bf16, const int32_t* union_buf,
+                          int32_t R, void* ws, size_t ws_bytes, moe_stream_t stream);
+moe_status_t moe_gate_up_fp8(const moe_config_t* cfg, const moe_weights_t* w,
+                             const int32_t* union_buf, int32_t R, void* ws, size_t ws_bytes,
+                             moe_stream_t stream);
+moe_status_t moe_down_fp8(const moe_config_t* cfg, const moe_weights_t* w,
+                          const int32_t* union_buf, int32_t R, float* y_slots, float* y_shared,
+                          void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_combine -- fixed-order weighted combine plus the shared expert, pads
+ * zero-filled (openinfer #610, "What"/"Gates": same fixed-order reductions,
+ * pad rows zero-filled with no NaN leak; mstar #388: the MoE's partials
+ * reduced once):
+ *   acc = w_0 * o_0; acc = fma(w_k, o_k, acc) for k = 1..K-1;
+ *   acc = acc + o_shared (weight 1); out = bf16_rne(acc); pad rows: +0.0.
+ *   topk_w fp32 [R, K]; out_bf16 bf16 [R, H] (out).
+ */
+moe_status_t moe_combine(const moe_config_t* cfg, const float* y_slots, const float* y_shared,
+                         const float* topk_w, const int32_t* union_buf, int32_t R,
+                         void* out_bf16, moe_stream_t stream);
+
+/*
+ * moe_layer -- the whole layer: moe_route, moe_build_union,
+ * moe_expert_ffn_fp8 and moe_combine on one stream, intermediates in `ws`.
+ * Arguments follow the problem statement of openinfer #610 ("What"): R rows
+ * (1 committed + up to 7 drafts per request, 8-row blocks, pads marked in
+ * row_valid).
+ *   out_bf16      bf16 [R, H] (out)
+ *   topk_ids_out  int32 [R, K] or NULL;  topk_w_out fp32 [R, K] or NULL
+ *   ws            at least moe_workspace_bytes(cfg, R) bytes, 256-byte aligned.
+ */
+size_t moe_workspace_bytes(const moe_config_t* cfg, int32_t max_rows);
+moe_status_t moe_layer(const moe_config_t* cfg, const void* x_bf16, const float* w_router,
+                       const float* bias, const moe_weights_t* w, const uint8_t* row_valid,
+                       int32_t R, void* out_bf16, int32_t* topk_ids_out, float* topk_w_out,
+                       void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_get_device_error -- synchronises `stream`, then reads (and clears when
+ * `clear` != 0) the device error word at the start of a workspace given to
+ * moe_expert_ffn_fp8 or moe_layer.  Returns MOE_OK, MOE_ERR_TIMEOUT (a bounded
+ * wait ran out: the kernel stopped, released its tensor memory and returned)
+ * or MOE_ERR_CUDA.
+ */
+moe_status_t moe_get_device_error(void* ws, int32_t clear, moe_stream_t stream);
+
+/*
+ * moe_diag_wait_timeout -- diagnostic: launches one block that waits, with the
+ * library's bounded wait, on a barrier nothing ever arrives on, for at most
+ * timeout_us microseconds; it then records MOE_ERR_TIMEOUT in the error word
+ * of `ws` (>= 256 bytes) and returns.  Exercises the timeout path without any
+ * fault.
+ */
+moe_status_t moe_diag_wait_timeout(void* ws, uint32_t timeout_us, moe_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_VERIFY_H */

@@ -1,0 +1,246 @@
+"""Python binding of the fp8 MoE decode / speculative-verify layer (libmoe_verify.so).
+
+Argument marshalling only: every function forwards to the C entry point of
+the same name in include/moe_verify.h, passing torch tensors' device
+pointers and the current CUDA stream.  Every step of the layer runs in the
+library's sm_103a kernels; there is no Python or CPU fallback.  A missing
+library raises at import of the first call.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "MoeError", "Config", "Weights", "load", "build", "moe_route", "moe_build_union",
+    "moe_expert_ffn_fp8", "moe_combine", "moe_layer", "moe_union_bytes",
+    "moe_ffn_workspace_bytes", "moe_workspace_bytes", "moe_get_device_error",
+    "moe_diag_wait_timeout", "moe_status_string", "moe_dispatch", "moe_gate_up_fp8",
+    "moe_down_fp8", "ffn_layout", "union_layout", "rows_per_item",
+    "MOE_MAX_ROWS",
+]
+
+MOE_MAX_ROWS = 4096
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
+          4: "MOE_ERR_TIMEOUT", 5: "MOE_ERR_WORKSPACE"}
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+class Config(C.Structure):
+    _fields_ = [("hidden", C.c_int32), ("inter", C.c_int32), ("n_experts", C.c_int32),
+                ("n_groups", C.c_int32), ("topk_groups", C.c_int32), ("topk", C.c_int32),
+                ("n_shared", C.c_int32), ("routed_scaling", C.c_float),
+                ("wait_timeout_us", C.c_uint32)]
+
+    @classmethod
+    def from_shape(cls, s, wait_timeout_us: int = 0) -> "Config":
+        return cls(s.hidden, s.inter, s.n_experts, s.n_groups, s.topk_groups, s.topk,
+                   s.n_shared, s.routed_scaling, wait_timeout_us)
+
+
+class Weights(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in (
+        "w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down",
+        "sh_gate", "sh_up", "sh_down", "sh_s_gate", "sh_s_up", "sh_s_down")]
+
+    @classmethod
+    def from_tensors(cls, t: dict) -> "Weights":
+        """From a dict with w_gate/s_gate/... and sh_gate/sh_s_gate/... tensors."""
+        def p(k):
+            v = t.get(k)
+            return None if v is None else v.data_ptr()
+        return cls(p("w_gate"), p("w_up"), p("w_down"), p("s_gate"), p("s_up"), p("s_down"),
+                   p("sh_gate"), p("sh_up"), p("sh_down"), p("sh_s_gate"), p("sh_s_up"),
+                   p("sh_s_down"))
+
+
+_LIB: Optional[C.CDLL] = None
+
+
+def build(force: bool = False) -> str:
+    return _build.build(force=force)
+
+
+def load() -> C.CDLL:
+    """Load the in-tree library; raises if it has not been built."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(_build.LIB):
+        raise ImportError(f"libmoe_verify.so is not built ({_build.LIB}); run "
+                          "moe_speculative_verify_gb300.build()")
+    L = C.CDLL(_build.LIB)
+    P, I32, SZ = C.c_void_p, C.c_int32, C.c_size_t
+    cfg = C.POINTER(Config)
+    L.moe_status_string.restype = C.c_char_p
+    L.moe_status_string.argtypes = [C.c_int]
+    for n in ("moe_union_bytes", "moe_ffn_workspace_bytes", "moe_workspace_bytes"):
+        getattr(L, n).restype = SZ
+        getattr(L, n).argtypes = [cfg, I32]
+    L.moe_route.argtypes = [cfg, P, P, P, P, I32, P, P, P, P]
+    L.moe_build_union.argtypes = [cfg, P, I32, P, SZ, P]
+    L.moe_expert_ffn_fp8.argtypes = [cfg, P, C.POINTER(Weights), P, I32, P, P, P, SZ, P]
+    L.moe_combine.argtypes = [cfg, P, P, P, P, I32, P, P]
+    L.moe_dispatch.argtypes = [cfg, P, P, I32, P, SZ, P]
+    L.moe_gate_up_fp8.argtypes = [cfg, C.POINTER(Weights), P, I32, P, SZ, P]
+    L.moe_down_fp8.argtypes = [cfg, C.POINTER(Weights), P, I32, P, P, P, SZ, P]
+    L.moe_layer.argtypes = [cfg, P, P, P, C.POINTER(Weights), P, I32, P, P, P, P, SZ, P]
+    L.moe_get_device_error.argtypes = [P, I32, P]
+    L.moe_diag_wait_timeout.argtypes = [P, C.c_uint32, P]
+    for n in ("moe_route", "moe_build_union", "moe_expert_ffn_fp8", "moe_combine", "moe_layer",
+              "moe_get_device_error", "moe_diag_wait_timeout", "moe_dispatch",
+              "moe_gate_up_fp8", "moe_down_fp8"):
+        getattr(L, n).restype = C.c_int
+    _LIB = L
+    return L
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise MoeError(status, where)
+
+
+def moe_status_string(status: int) -> str:
+    return load().moe_status_string(status).decode()
+
+
+def moe_union_bytes(cfg: Config, max_rows: int) -> int:
+    return load().moe_union_bytes(C.byref(cfg), max_rows)
+
+
+def moe_ffn_workspace_bytes(cfg: Config, max_rows: int) -> int:
+    return load().moe_ffn_workspace_bytes(C.byref(cfg), max_rows)
+
+
+def moe_workspace_bytes(cfg: Config, max_rows: int) -> int:
+    return load().moe_workspace_bytes(C.byref(cfg), max_rows)
+
+
+def moe_route(cfg: Config, x, w_router, bias, row_valid, topk_ids, topk_w, logits,
+              stream=None) -> None:
+    R = 0 if x is None else x.shape[0]
+    _check(load().moe_route(C.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(row_valid),
+                            R, _ptr(topk_ids), _ptr(topk_w), _ptr(logits), _stream(stream)),
+           "moe_route")
+
+
+def moe_build_union(cfg: Config, topk_ids, union_buf, stream=None) -> None:
+    R = topk_ids.shape[0]
+    _check(load().moe_build_union(C.byref(cfg), _ptr(topk_ids), R, _ptr(union_buf),
+                                  union_buf.numel() * union_buf.element_size(), _stream(stream)),
+           "moe_build_union")
+
+
+def moe_expert_ffn_fp8(cfg: Config, x, weights: Weights, union_buf, y_slots, y_shared, ws,
+                       stream=None) -> None:
+    R = x.shape[0]
+    _check(load().moe_expert_ffn_fp8(C.byref(cfg), _ptr(x), C.byref(weights), _ptr(union_buf), R,
+                                     _ptr(y_slots), _ptr(y_shared), _ptr(ws),
+                                     ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_expert_ffn_fp8")
+
+
+def moe_dispatch(cfg: Config, x, union_buf, ws, stream=None) -> None:
+    _check(load().moe_dispatch(C.byref(cfg), _ptr(x), _ptr(union_buf), x.shape[0], _ptr(ws),
+                               ws.numel() * ws.element_size(), _stream(stream)), "moe_dispatch")
+
+
+def moe_gate_up_fp8(cfg: Config, weights: Weights, union_buf, R: int, ws, stream=None) -> None:
+    _check(load().moe_gate_up_fp8(C.byref(cfg), C.byref(weights), _ptr(union_buf), R, _ptr(ws),
+                                  ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_gate_up_fp8")
+
+
+def moe_down_fp8(cfg: Config, weights: Weights, union_buf, R: int, y_slots, y_shared, ws,
+                 stream=None) -> None:
+    _check(load().moe_down_fp8(C.byref(cfg), C.byref(weights), _ptr(union_buf), R,
+                               _ptr(y_slots), _ptr(y_shared), _ptr(ws),
+                               ws.numel() * ws.element_size(), _stream(stream)), "moe_down_fp8")
+
+
+def moe_combine(cfg: Config, y_slots, y_shared, topk_w, union_buf, out, stream=None) -> None:
+    R = out.shape[0]
+    _check(load().moe_combine(C.byref(cfg), _ptr(y_slots), _ptr(y_shared), _ptr(topk_w),
+                              _ptr(union_buf), R, _ptr(out), _stream(stream)), "moe_combine")
+
+
+def moe_layer(cfg: Config, x, w_router, bias, weights: Weights, row_valid, out, ws,
+              topk_ids=None, topk_w=None, stream=None) -> None:
+    R = x.shape[0]
+    _check(load().moe_layer(C.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias), C.byref(weights),
+                            _ptr(row_valid), R, _ptr(out), _ptr(topk_ids), _ptr(topk_w),
+                            _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_layer")
+
+
+def moe_get_device_error(ws, clear: bool = True, stream=None) -> int:
+    """Synchronises the stream; returns the workspace's device error code (0 = OK)."""
+    return load().moe_get_device_error(_ptr(ws), 1 if clear else 0, _stream(stream))
+
+
+def moe_diag_wait_timeout(ws, timeout_us: int, stream=None) -> None:
+    _check(load().moe_diag_wait_timeout(_ptr(ws), timeout_us, _stream(stream)),
+           "moe_diag_wait_timeout")
+
+
+# ---------------------------------------------------------------- layouts --
+def rows_per_item(R: int) -> int:
+    """Rows per GEMM work item chosen for a call with R rows (mirrors the library)."""
+    return 16 if R <= 64 else (32 if R <= 512 else 64)
+
+
+def union_layout(cfg: Config, R: int) -> dict:
+    """Word offsets of the union buffer arrays (moe_build_union's documented layout)."""
+    E, K, S = cfg.n_experts, cfg.topk, cfg.n_shared
+    KS = K + S
+    w = 8
+    out = {"counts": w}
+    w += E + 1
+    out["offsets"] = w
+    w += E + 2
+    out["ulist"] = w
+    w += E + 1
+    out["pos"] = w
+    w += R * KS
+    out["src"] = w
+    w += R * KS
+    w = (w + 3) // 4 * 4
+    out["items"] = w
+    return out
+
+
+def ffn_layout(cfg: Config, R: int) -> dict:
+    """Byte offsets of the FFN workspace regions (mirrors the library's carve-up)."""
+    def up(v, mlt):
+        return (v + mlt - 1) // mlt * mlt
+    H, I, K, S = cfg.hidden, cfg.inter, cfg.topk, cfg.n_shared
+    rows = up(R * (K + S), 64) + 64
+    out = {"rows": rows, "ctl": 0, "xg": 256}
+    b = up(256 + rows * H, 256)
+    out["xs"] = b
+    b = up(b + rows * (H // 128) * 4, 256)
+    out["hq"] = b
+    b = up(b + rows * I, 256)
+    out["hs"] = b
+    out["bytes"] = up(b + rows * (I // 128) * 4, 256)
+    return out

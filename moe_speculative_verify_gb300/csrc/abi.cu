@@ -1,0 +1,444 @@
+// abi.cu -- host side of the C ABI declared in include/moe_verify.h:
+// argument validation, workspace carving, TMA tensor maps and kernel
+// launches.  No allocation, no state between calls beyond cached device
+// attributes and the driver entry point, no host synchronisation except in
+// moe_get_device_error.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "layout.h"
+
+namespace {
+
+using moe::FfnLayout;
+using moe::LayerLayout;
+using moe::UnionLayout;
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shape checks: malformed shapes are invalid; well-formed ones beyond the
+// compiled limits are unsupported.
+moe_status_t check_cfg(const moe_config_t* c) {
+    if (c == nullptr) return MOE_ERR_INVALID_ARG;
+    if (c->hidden <= 0 || c->inter <= 0 || c->hidden % MOE_BLOCK || c->inter % MOE_BLOCK)
+        return MOE_ERR_INVALID_ARG;
+    if (c->n_experts <= 0 || c->n_groups <= 0 || c->n_experts % c->n_groups) return MOE_ERR_INVALID_ARG;
+    if (c->topk_groups <= 0 || c->topk_groups > c->n_groups) return MOE_ERR_INVALID_ARG;
+    if (c->topk <= 0 || c->topk > c->topk_groups * (c->n_experts / c->n_groups))
+        return MOE_ERR_INVALID_ARG;
+    if (c->n_shared < 0 || !std::isfinite(c->routed_scaling)) return MOE_ERR_INVALID_ARG;
+    if (c->hidden > 16384 || c->inter > 16384 || c->n_experts > MOE_MAX_EXPERTS ||
+        c->n_groups > MOE_MAX_GROUPS || c->topk > MOE_MAX_TOPK || c->n_shared > 1)
+        return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+moe_status_t check_rows(int32_t R) {
+    if (R < 0) return MOE_ERR_INVALID_ARG;
+    if (R > MOE_MAX_ROWS) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+uint64_t timeout_ns(const moe_config_t* c) {
+    return static_cast<uint64_t>(c->wait_timeout_us ? c->wait_timeout_us : 2000000u) * 1000ull;
+}
+
+struct DeviceInfo {
+    int sms = 0;
+    int smem_optin = 0;
+};
+
+DeviceInfo device_info() {
+    static std::mutex mu;
+    static DeviceInfo cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DeviceInfo{};
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev].sms == 0) {
+        DeviceInfo d;
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cache[dev] = d;
+    }
+    return cache[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D uint8 tensor [rows, cols] (cols contiguous), 128-byte-swizzled boxes of
+// 128 columns x box_rows rows; out-of-range rows read as zero.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols};
+    const cuuint32_t box[2] = {128, box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+moe_status_t check_weights(const moe_config_t* c, const moe_weights_t* w) {
+    if (w == nullptr) return MOE_ERR_INVALID_ARG;
+    const void* codes[3] = {w->w_gate, w->w_up, w->w_down};
+    const float* scales[3] = {w->s_gate, w->s_up, w->s_down};
+    for (int i = 0; i < 3; ++i) {
+        if (!codes[i] || !scales[i] || !aligned(codes[i], 16) || !aligned(scales[i], 4))
+            return MOE_ERR_INVALID_ARG;
+    }
+    if (c->n_shared > 0) {
+        const void* sc[3] = {w->sh_gate, w->sh_up, w->sh_down};
+        const float* ss[3] = {w->sh_s_gate, w->sh_s_up, w->sh_s_down};
+        for (int i = 0; i < 3; ++i)
+            if (!sc[i] || !ss[i] || !aligned(sc[i], 16) || !aligned(ss[i], 4))
+                return MOE_ERR_INVALID_ARG;
+    }
+    return MOE_OK;
+}
+
+moe_status_t route_impl(const moe_config_t* c, const void* x, const float* wr, const float* bias,
+                        const uint8_t* valid, int32_t R, int32_t* ids, float* wts, float* logits,
+                        cudaStream_t s) {
+    return cuda_status(moe::launch_router(static_cast<const uint16_t*>(x), wr, bias, valid, R,
+                                          c->hidden, c->n_experts, c->n_groups, c->topk_groups,
+                                          c->topk, c->routed_scaling, ids, wts, logits, s));
+}
+
+moe_status_t union_impl(const moe_config_t* c, const int32_t* ids, int32_t R, int32_t* ub,
+                        cudaStream_t s) {
+    const UnionLayout L = moe::union_layout(c->n_experts, c->topk, c->n_shared, R);
+    return cuda_status(moe::launch_union(ids, R, c->n_experts, c->topk, c->n_shared,
+                                         moe::rows_per_item(R), ub, L, s));
+}
+
+// Pointers into the FFN workspace and the tensor maps of one call.
+struct FfnCall {
+    FfnLayout FL;
+    UnionLayout UL;
+    int32_t* err;
+    uint8_t* xg;
+    float* xs;
+    uint8_t* hq;
+    float* hs;
+    int nt;
+};
+
+FfnCall ffn_call(const moe_config_t* c, int32_t R, void* ws) {
+    FfnCall f;
+    f.FL = moe::ffn_layout(c->hidden, c->inter, c->topk, c->n_shared, R);
+    f.UL = moe::union_layout(c->n_experts, c->topk, c->n_shared, R);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    f.err = reinterpret_cast<int32_t*>(base + f.FL.ctl);
+    f.xg = base + f.FL.xg;
+    f.xs = reinterpret_cast<float*>(base + f.FL.xs);
+    f.hq = base + f.FL.hq;
+    f.hs = reinterpret_cast<float*>(base + f.FL.hs);
+    f.nt = moe::rows_per_item(R);
+    return f;
+}
+
+moe::FfnArgs ffn_args(const moe_config_t* c, const int32_t* ub, const FfnCall& f) {
+    moe::FfnArgs a{};
+    a.ub = ub;
+    a.ul = f.UL;
+    a.err = f.err;
+    a.E = c->n_experts;
+    a.K = c->topk;
+    a.KS = c->topk + c->n_shared;
+    a.timeout_ns = timeout_ns(c);
+    return a;
+}
+
+moe_status_t dispatch_impl(const moe_config_t* c, const void* x, const int32_t* ub, int32_t R,
+                           void* ws, cudaStream_t s) {
+    const FfnCall f = ffn_call(c, R, ws);
+    return cuda_status(moe::launch_dispatch(static_cast<const uint16_t*>(x), ub, f.UL, R, c->hidden,
+                                            c->topk + c->n_shared, f.xg, f.xs, s));
+}
+
+moe_status_t gate_up_impl(const moe_config_t* c, const moe_weights_t* w, const int32_t* ub,
+                          int32_t R, void* ws, cudaStream_t s) {
+    const int H = c->hidden, I = c->inter, E = c->n_experts, S = c->n_shared;
+    const FfnCall f = ffn_call(c, R, ws);
+    const DeviceInfo dev = device_info();
+    if (dev.sms <= 0) return MOE_ERR_CUDA;
+    // shared-expert maps fall back to the routed tensors when S == 0 (never read)
+    const uint8_t* shg = S ? w->sh_gate : w->w_gate;
+    const uint8_t* shu = S ? w->sh_up : w->w_up;
+    const uint64_t srows = S ? uint64_t(S) : 1ull;
+    CUtensorMap m_g, m_u, m_sg, m_su, m_x;
+    if (!make_map(&m_g, w->w_gate, uint64_t(E) * I, H, 128) ||
+        !make_map(&m_u, w->w_up, uint64_t(E) * I, H, 128) ||
+        !make_map(&m_sg, shg, srows * I, H, 128) || !make_map(&m_su, shu, srows * I, H, 128) ||
+        !make_map(&m_x, f.xg, f.FL.rows, H, f.nt))
+        return MOE_ERR_CUDA;
+    moe::FfnArgs g = ffn_args(c, ub, f);
+    g.s_a0 = w->s_gate;
+    g.s_a1 = w->s_up;
+    g.sh_s_a0 = S ? w->sh_s_gate : w->s_gate;
+    g.sh_s_a1 = S ? w->sh_s_up : w->s_up;
+    g.bs = f.xs;
+    g.hq = f.hq;
+    g.hs = f.hs;
+    g.M = I;
+    g.Kd = H;
+    return cuda_status(moe::launch_ffn(f.nt, true, m_g, m_u, m_sg, m_su, m_x, g, dev.sms,
+                                       f.UL.max_items * (I / MOE_BLOCK), dev.smem_optin, s));
+}
+
+moe_status_t down_impl(const moe_config_t* c, const moe_weights_t* w, const int32_t* ub, int32_t R,
+                       float* y_slots, float* y_shared, void* ws, cudaStream_t s) {
+    const int H = c->hidden, I = c->inter, E = c->n_experts, S = c->n_shared;
+    const FfnCall f = ffn_call(c, R, ws);
+    const DeviceInfo dev = device_info();
+    if (dev.sms <= 0) return MOE_ERR_CUDA;
+    const uint8_t* shd = S ? w->sh_down : w->w_down;
+    const uint64_t srows = S ? uint64_t(S) : 1ull;
+    CUtensorMap m_d, m_sd, m_h;
+    if (!make_map(&m_d, w->w_down, uint64_t(E) * H, I, 128) ||
+        !make_map(&m_sd, shd, srows * H, I, 128) || !make_map(&m_h, f.hq, f.FL.rows, I, f.nt))
+        return MOE_ERR_CUDA;
+    moe::FfnArgs d = ffn_args(c, ub, f);
+    d.s_a0 = w->s_down;
+    d.s_a1 = w->s_down;
+    d.sh_s_a0 = S ? w->sh_s_down : w->s_down;
+    d.sh_s_a1 = d.sh_s_a0;
+    d.bs = f.hs;
+    d.y_slots = y_slots;
+    d.y_shared = y_shared;
+    d.M = H;
+    d.Kd = I;
+    return cuda_status(moe::launch_ffn(f.nt, false, m_d, m_d, m_sd, m_sd, m_h, d, dev.sms,
+                                       f.UL.max_items * (H / MOE_BLOCK), dev.smem_optin, s));
+}
+
+moe_status_t ffn_impl(const moe_config_t* c, const void* x, const moe_weights_t* w,
+                      const int32_t* ub, int32_t R, float* y_slots, float* y_shared, void* ws,
+                      cudaStream_t s) {
+    moe_status_t st = dispatch_impl(c, x, ub, R, ws, s);
+    if (st != MOE_OK) return st;
+    if ((st = gate_up_impl(c, w, ub, R, ws, s)) != MOE_OK) return st;
+    return down_impl(c, w, ub, R, y_slots, y_shared, ws, s);
+}
+
+moe_status_t combine_impl(const moe_config_t* c, const float* y_slots, const float* y_shared,
+                          const float* wts, const int32_t* ub, int32_t R, void* out,
+                          cudaStream_t s) {
+    const UnionLayout UL = moe::union_layout(c->n_experts, c->topk, c->n_shared, R);
+    return cuda_status(moe::launch_combine(y_slots, y_shared, wts, ub, UL, R, c->hidden, c->topk,
+                                           c->n_shared, static_cast<uint16_t*>(out), s));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    }
+    return "MOE_ERR_UNKNOWN";
+}
+
+size_t moe_union_bytes(const moe_config_t* cfg, int32_t max_rows) {
+    if (check_cfg(cfg) != MOE_OK || check_rows(max_rows) != MOE_OK) return 0;
+    return size_t(moe::union_layout(cfg->n_experts, cfg->topk, cfg->n_shared, max_rows).words) * 4;
+}
+
+size_t moe_ffn_workspace_bytes(const moe_config_t* cfg, int32_t max_rows) {
+    if (check_cfg(cfg) != MOE_OK || check_rows(max_rows) != MOE_OK) return 0;
+    return size_t(moe::ffn_layout(cfg->hidden, cfg->inter, cfg->topk, cfg->n_shared, max_rows).bytes);
+}
+
+size_t moe_workspace_bytes(const moe_config_t* cfg, int32_t max_rows) {
+    if (check_cfg(cfg) != MOE_OK || check_rows(max_rows) != MOE_OK) return 0;
+    return size_t(moe::layer_layout(cfg->hidden, cfg->inter, cfg->n_experts, cfg->topk,
+                                    cfg->n_shared, max_rows)
+                      .bytes);
+}
+
+moe_status_t moe_route(const moe_config_t* cfg, const void* x_bf16, const float* w_router,
+                       const float* bias, const uint8_t* row_valid, int32_t R, int32_t* topk_ids,
+                       float* topk_w, float* logits, moe_stream_t stream) {
+    moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if ((st = check_rows(R)) != MOE_OK) return st;
+    if (!x_bf16 || !w_router || !bias || !topk_ids || !topk_w || !logits) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x_bf16, 16) || !aligned(w_router, 16) || !aligned(bias, 4) ||
+        !aligned(topk_ids, 4) || !aligned(topk_w, 4) || !aligned(logits, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (R == 0) return MOE_OK;
+    return route_impl(cfg, x_bf16, w_router, bias, row_valid, R, topk_ids, topk_w, logits,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_build_union(const moe_config_t* cfg, const int32_t* topk_ids, int32_t R,
+                             int32_t* union_buf, size_t union_bytes, moe_stream_t stream) {
+    moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if ((st = check_rows(R)) != MOE_OK) return st;
+    if (!topk_ids || !union_buf || !aligned(topk_ids, 4) || !aligned(union_buf, 16))
+        return MOE_ERR_INVALID_ARG;
+    if (union_bytes < moe_union_bytes(cfg, R)) return MOE_ERR_WORKSPACE;
+    if (R == 0) return MOE_OK;
+    return union_impl(cfg, topk_ids, R, union_buf, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_expert_ffn_fp8(const moe_config_t* cfg, const void* x_bf16,
+                                const moe_weights_t* w, const int32_t* union_buf, int32_t R,
+                                float* y_slots, float* y_shared, void* ws, size_t ws_bytes,
+                                moe_stream_t stream) {
+    moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if ((st = check_rows(R)) != MOE_OK) return st;
+    if ((st = check_weights(cfg, w)) != MOE_OK) return st;
+    if (!x_bf16 || !union_buf || !y_slots || !ws) return MOE_ERR_INVALID_ARG;
+    if (cfg->n_shared > 0 && !y_shared) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x_bf16, 16) || !aligned(union_buf, 16) || !aligned(y_slots, 4) ||
+        (y_shared && !aligned(y_shared, 4)) || !aligned(ws, 256))
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe_ffn_workspace_bytes(cfg, R)) return MOE_ERR_WORKSPACE;
+    if (R == 0) return MOE_OK;
+    return ffn_impl(cfg, x_bf16, w, union_buf, R, y_slots, y_shared, ws,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Common checks of the FFN-stage entry points.
+static moe_status_t check_ffn_call(const moe_config_t* cfg, const int32_t* union_buf, int32_t R,
+                                   void* ws, size_t ws_bytes) {
+    moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if ((st = check_rows(R)) != MOE_OK) return st;
+    if (!union_buf || !ws || !aligned(union_buf, 16) || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe_ffn_workspace_bytes(cfg, R)) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x_bf16, const int32_t* union_buf,
+                          int32_t R, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    moe_status_t st = check_ffn_call(cfg, union_buf, R, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    if (!x_bf16 || !aligned(x_bf16, 16)) return MOE_ERR_INVALID_ARG;
+    if (R == 0) return MOE_OK;
+    return dispatch_impl(cfg, x_bf16, union_buf, R, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_gate_up_fp8(const moe_config_t* cfg, const moe_weights_t* w,
+                             const int32_t* union_buf, int32_t R, void* ws, size_t ws_bytes,
+                             moe_stream_t stream) {
+    moe_status_t st = check_ffn_call(cfg, union_buf, R, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    if ((st = check_weights(cfg, w)) != MOE_OK) return st;
+    if (R == 0) return MOE_OK;
+    return gate_up_impl(cfg, w, union_buf, R, ws, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_down_fp8(const moe_config_t* cfg, const moe_weights_t* w,
+                          const int32_t* union_buf, int32_t R, float* y_slots, float* y_shared,
+                          void* ws, size_t ws_bytes, moe_stream_t stream) {
+    moe_status_t st = check_ffn_call(cfg, union_buf, R, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    if ((st = check_weights(cfg, w)) != MOE_OK) return st;
+    if (!y_slots || !aligned(y_slots, 4) || (cfg->n_shared > 0 && (!y_shared || !aligned(y_shared, 4))))
+        return MOE_ERR_INVALID_ARG;
+    if (R == 0) return MOE_OK;
+    return down_impl(cfg, w, union_buf, R, y_slots, y_shared, ws,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const float* y_slots, const float* y_shared,
+                         const float* topk_w, const int32_t* union_buf, int32_t R, void* out_bf16,
+                         moe_stream_t stream) {
+    moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if ((st = check_rows(R)) != MOE_OK) return st;
+    if (!y_slots || !topk_w || !union_buf || !out_bf16) return MOE_ERR_INVALID_ARG;
+    if (cfg->n_shared > 0 && !y_shared) return MOE_ERR_INVALID_ARG;
+    if (!aligned(y_slots, 16) || (y_shared && !aligned(y_shared, 16)) || !aligned(topk_w, 4) ||
+        !aligned(union_buf, 16) || !aligned(out_bf16, 16))
+        return MOE_ERR_INVALID_ARG;
+    if (R == 0) return MOE_OK;
+    return combine_impl(cfg, y_slots, y_shared, topk_w, union_buf, R, out_bf16,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_layer(const moe_config_t* cfg, const void* x_bf16, const float* w_router,
+                       const float* bias, const moe_weights_t* w, const uint8_t* row_valid,
+                       int32_t R, void* out_bf16, int32_t* topk_ids_out, float* topk_w_out,
+                       void* ws, size_t ws_bytes, moe_stream_t stream) {
+    moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if ((st = check_rows(R)) != MOE_OK) return st;
+    if ((st = check_weights(cfg, w)) != MOE_OK) return st;
+    if (!x_bf16 || !w_router || !bias || !out_bf16 || !ws) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x_bf16, 16) || !aligned(w_router, 16) || !aligned(bias, 4) ||
+        !aligned(out_bf16, 16) || !aligned(ws, 256) ||
+        (topk_ids_out && !aligned(topk_ids_out, 4)) || (topk_w_out && !aligned(topk_w_out, 4)))
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe_workspace_bytes(cfg, R)) return MOE_ERR_WORKSPACE;
+    if (R == 0) return MOE_OK;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const LayerLayout L = moe::layer_layout(cfg->hidden, cfg->inter, cfg->n_experts, cfg->topk,
+                                            cfg->n_shared, R);
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    float* logits = reinterpret_cast<float*>(base + L.logits);
+    int32_t* ids = topk_ids_out ? topk_ids_out : reinterpret_cast<int32_t*>(base + L.ids);
+    float* wts = topk_w_out ? topk_w_out : reinterpret_cast<float*>(base + L.wts);
+    int32_t* ub = reinterpret_cast<int32_t*>(base + L.ubuf);
+    float* y_slots = reinterpret_cast<float*>(base + L.y_slots);
+    float* y_shared = reinterpret_cast<float*>(base + L.y_shared);
+    if ((st = route_impl(cfg, x_bf16, w_router, bias, row_valid, R, ids, wts, logits, s)) != MOE_OK)
+        return st;
+    if ((st = union_impl(cfg, ids, R, ub, s)) != MOE_OK) return st;
+    if ((st = ffn_impl(cfg, x_bf16, w, ub, R, y_slots, y_shared, ws, s)) != MOE_OK) return st;
+    return combine_impl(cfg, y_slots, y_shared, wts, ub, R, out_bf16, s);
+}
+
+moe_status_t moe_get_device_error(void* ws, int32_t clear, moe_stream_t stream) {
+    if (!ws || !aligned(ws, 4)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t err = 0;
+    if (cudaMemcpyAsync(&err, ws, sizeof(err), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (clear && err != 0) {
+        if (cudaMemsetAsync(ws, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    if (err < 0 || err > MOE_ERR_WORKSPACE) return MOE_ERR_CUDA;
+    return static_cast<moe_status_t>(err);
+}
+
+moe_status_t moe_diag_wait_timeout(void* ws, uint32_t timeout_us, moe_stream_t stream) {
+    if (!ws || !aligned(ws, 4) || timeout_us == 0 || timeout_us > 10000000u) return MOE_ERR_INVALID_ARG;
+    return cuda_status(moe::launch_wait_timeout(static_cast<int32_t*>(ws),
+                                                uint64_t(timeout_us) * 1000ull,
+                                                reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

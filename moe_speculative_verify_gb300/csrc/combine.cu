@@ -1,0 +1,84 @@
+// combine.cu -- fixed-order weighted combine of the expert outputs plus the
+// shared expert, pad rows zero-filled (sm_103a).
+//
+// openinfer #610 "TP8 span row mapping -- single-user speculative decode at
+// 186 tok/s", sections "What" and "Gates": same fixed-order reductions
+// whichever mapping carries a row; span pad ranks zero-fill their rows so no
+// NaN leaks.  mstar #388 "Speed up GLM-5.2 with fp8 kernels and one-graph
+// MTP": the MoE's partials reduced once, routed and shared experts together.
+#include "common.cuh"
+#include "kernels.h"
+#include "layout.h"
+
+namespace moe {
+
+// One thread per (row, 4 columns).  acc = w0*o0, then fma over k = 1..K-1,
+// then + shared, rounded once to bf16.  No atomics: the order is fixed.
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y_slots,
+                                                      const float* __restrict__ y_shared,
+                                                      const float* __restrict__ wts,
+                                                      const int32_t* __restrict__ ub,
+                                                      UnionLayout L, int R, int H, int K, int S,
+                                                      uint16_t* __restrict__ out) {
+    const int r = blockIdx.x;
+    const int h = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
+    if (h >= H) return;
+    const int KS = K + S;
+    uint2* dst = reinterpret_cast<uint2*>(out + size_t(r) * H + h);
+    if (ub[L.pos + size_t(r) * KS] < 0) {
+        *dst = make_uint2(0u, 0u);
+        return;
+    }
+    const float* w = wts + size_t(r) * K;
+    float4 y = __ldg(reinterpret_cast<const float4*>(y_slots + size_t(r) * K * H + h));
+    const float w0 = w[0];
+    float a0 = __fmul_rn(w0, y.x), a1 = __fmul_rn(w0, y.y), a2 = __fmul_rn(w0, y.z),
+          a3 = __fmul_rn(w0, y.w);
+    for (int k = 1; k < K; ++k) {
+        const float wk = w[k];
+        y = __ldg(reinterpret_cast<const float4*>(y_slots + (size_t(r) * K + k) * H + h));
+        a0 = __fmaf_rn(wk, y.x, a0);
+        a1 = __fmaf_rn(wk, y.y, a1);
+        a2 = __fmaf_rn(wk, y.z, a2);
+        a3 = __fmaf_rn(wk, y.w, a3);
+    }
+    if (S) {
+        y = __ldg(reinterpret_cast<const float4*>(y_shared + size_t(r) * H + h));
+        a0 = __fadd_rn(a0, y.x);
+        a1 = __fadd_rn(a1, y.y);
+        a2 = __fadd_rn(a2, y.z);
+        a3 = __fadd_rn(a3, y.w);
+    }
+    const uint32_t b0 = __bfloat16_as_ushort(__float2bfloat16_rn(a0));
+    const uint32_t b1 = __bfloat16_as_ushort(__float2bfloat16_rn(a1));
+    const uint32_t b2 = __bfloat16_as_ushort(__float2bfloat16_rn(a2));
+    const uint32_t b3 = __bfloat16_as_ushort(__float2bfloat16_rn(a3));
+    *dst = make_uint2(b0 | (b1 << 16), b2 | (b3 << 16));
+}
+
+cudaError_t launch_combine(const float* y_slots, const float* y_shared, const float* wts,
+                           const int32_t* ub, const UnionLayout& L, int R, int H, int K, int S,
+                           uint16_t* out, cudaStream_t stream) {
+    dim3 grid(R, (H / 4 + 255) / 256);
+    combine_kernel<<<grid, 256, 0, stream>>>(y_slots, y_shared, wts, ub, L, R, H, K, S, out);
+    return cudaGetLastError();
+}
+
+// Diagnostic: one block waits on a barrier nothing arrives on; the bounded
+// wait gives up after timeout_ns and records MOE_ERR_TIMEOUT.
+__global__ void wait_timeout_kernel(int32_t* err, uint64_t timeout_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, err, timeout_ns);
+}
+
+cudaError_t launch_wait_timeout(int32_t* err, uint64_t timeout_ns, cudaStream_t stream) {
+    wait_timeout_kernel<<<1, 32, 0, stream>>>(err, timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

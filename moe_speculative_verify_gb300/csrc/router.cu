@@ -1,0 +1,264 @@
+// router.cu -- router logits and grouped top-k selection (sm_103a).
+//
+// The router of a sigmoid-scored, bias-corrected, group-limited MoE (mstar
+// #388 "Speed up GLM-5.2 with fp8 kernels and one-graph MTP", commit moving
+// NoAuxTcRouter's top-k op; MoE-Infinity #140, e_score_correction_bias;
+// pypto-serving #223 "What this adds": router gate kept in FP32).
+//
+// Every floating-point step is an explicitly rounded IEEE fp32 operation in
+// a fixed order (the order is part of the ABI contract in moe_verify.h), so
+// the chosen expert ids do not depend on launch shape, batch slot or compiler
+// contraction.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// ------------------------------------------------------ router logits ----
+// logits[r, e] for a tile of RT rows and EC experts per block.  Warp c of the
+// block computes, for chunk c of the hidden dimension (1024 columns), the 32
+// per-lane partial sums of every (row, expert) pair of the tile; the block then
+// folds the chunks in ascending order per lane and finishes with the xor
+// butterfly across lanes.
+template <int RT, int EC>
+__global__ void __launch_bounds__(512) router_logits_kernel(
+    const uint16_t* __restrict__ x, const float* __restrict__ wr,
+    const uint8_t* __restrict__ row_valid, int R, int H, int E, float* __restrict__ logits) {
+    extern __shared__ float part[];  // [nchunks][EC][RT][32]
+    const int nchunks = (H + 1023) / 1024;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e0 = blockIdx.x * EC;
+    const int r0 = blockIdx.y * RT;
+
+    if (warp < nchunks) {
+        const int c = warp;
+        float p[EC][RT];
+#pragma unroll
+        for (int a = 0; a < EC; ++a)
+#pragma unroll
+            for (int b = 0; b < RT; ++b) p[a][b] = 0.0f;
+        const int h_end = min(H, (c + 1) * 1024);
+        for (int h0 = c * 1024; h0 < h_end; h0 += 128) {
+            const int h = h0 + 4 * lane;
+            float4 w4[EC];
+#pragma unroll
+            for (int a = 0; a < EC; ++a) {
+                const int e = min(e0 + a, E - 1);
+                w4[a] = __ldg(reinterpret_cast<const float4*>(wr + size_t(e) * H + h));
+            }
+#pragma unroll
+            for (int b = 0; b < RT; ++b) {
+                const int r = min(r0 + b, R - 1);
+                const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + size_t(r) * H + h));
+                const float x0 = bf16_bits_to_f32(xv.x & 0xFFFFu);
+                const float x1 = bf16_bits_to_f32(xv.x >> 16);
+                const float x2 = bf16_bits_to_f32(xv.y & 0xFFFFu);
+                const float x3 = bf16_bits_to_f32(xv.y >> 16);
+#pragma unroll
+                for (int a = 0; a < EC; ++a) {
+                    float q = p[a][b];
+                    q = __fmaf_rn(x0, w4[a].x, q);
+                    q = __fmaf_rn(x1, w4[a].y, q);
+                    q = __fmaf_rn(x2, w4[a].z, q);
+                    q = __fmaf_rn(x3, w4[a].w, q);
+                    p[a][b] = q;
+                }
+            }
+        }
+#pragma unroll
+        for (int a = 0; a < EC; ++a)
+#pragma unroll
+            for (int b = 0; b < RT; ++b) part[((c * EC + a) * RT + b) * 32 + lane] = p[a][b];
+    }
+    __syncthreads();
+
+    const int nwarps = blockDim.x >> 5;
+    for (int pair = warp; pair < EC * RT; pair += nwarps) {
+        const int a = pair / RT, b = pair % RT;
+        const int e = e0 + a, r = r0 + b;
+        float q = part[((0 * EC + a) * RT + b) * 32 + lane];
+        for (int c = 1; c < nchunks; ++c) q = __fadd_rn(q, part[((c * EC + a) * RT + b) * 32 + lane]);
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1) q = __fadd_rn(q, __shfl_xor_sync(0xFFFFFFFFu, q, d));
+        if (lane == 0 && e < E && r < R && (row_valid == nullptr || row_valid[r] != 0))
+            logits[size_t(r) * E + e] = q;
+    }
+}
+
+// -------------------------------------------------- sigmoid with own exp ----
+// exp by Cody-Waite range reduction (Cody and Waite, "Software Manual for the
+// Elementary Functions", 1980): a = n*ln2 + r with ln2 split into a head of 16
+// significant bits (n*head exact) and an fp32 tail, then the Taylor series of
+// e^r to degree 7 in Horner form, then scaling by 2^n through the exponent
+// field.  Argument clamped to [-87, 87] so 2^n stays a normal number.
+__device__ __forceinline__ float cw_exp(float a) {
+    const float kLog2e = 0x1.715476p+0f;
+    const float kLn2Hi = 0x1.62e4p-1f;
+    const float kLn2Lo = 0x1.7f7d1cp-20f;
+    if (a != a) return a;
+    if (a > 87.0f) a = 87.0f;
+    if (a < -87.0f) a = -87.0f;
+    const float n = rintf(__fmul_rn(a, kLog2e));
+    float r = __fmaf_rn(-n, kLn2Hi, a);
+    r = __fmaf_rn(-n, kLn2Lo, r);
+    float p = 0x1.a01a02p-13f;              // 1/7!
+    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);   // 1/6!
+    p = __fmaf_rn(p, r, 0x1.111112p-7f);    // 1/5!
+    p = __fmaf_rn(p, r, 0x1.555556p-5f);    // 1/4!
+    p = __fmaf_rn(p, r, 0x1.555556p-3f);    // 1/3!
+    p = __fmaf_rn(p, r, 0x1p-1f);           // 1/2!
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    const float two_n = __int_as_float((static_cast<int>(n) + 127) << 23);
+    return __fmul_rn(p, two_n);
+}
+
+__device__ __forceinline__ float router_sigmoid(float l) {
+    return __fdiv_rn(1.0f, __fadd_rn(1.0f, cw_exp(-l)));
+}
+
+// Total order of fp32 values as unsigned keys (-0 folded onto +0).
+__device__ __forceinline__ uint32_t ordered_key(float f) {
+    if (f == 0.0f) f = 0.0f;
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Larger value first; on equal values the lower index wins.
+__device__ __forceinline__ uint64_t rank_key(float v, int idx) {
+    return (static_cast<uint64_t>(ordered_key(v)) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(idx));
+}
+
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) {
+        const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, v, d);
+        v = o > v ? o : v;
+    }
+    return v;
+}
+
+// ------------------------------------------------------ grouped top-k ----
+// One warp per row: sigmoid scores, biased scores, group scores (sum of the
+// two largest biased scores), the topk_groups best groups, the topk best
+// experts inside them, and the normalised weights.
+constexpr int kSelWarps = 8;
+
+__global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(
+    const float* __restrict__ logits, const float* __restrict__ bias,
+    const uint8_t* __restrict__ row_valid, int R, int E, int G, int TG, int K, float scaling,
+    int32_t* __restrict__ ids, float* __restrict__ wts) {
+    __shared__ float s_s[kSelWarps][MOE_MAX_EXPERTS];
+    __shared__ float s_b[kSelWarps][MOE_MAX_EXPERTS];
+    __shared__ int s_id[kSelWarps][MOE_MAX_TOPK];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x * kSelWarps + warp;
+    if (r >= R) return;
+    if (row_valid != nullptr && row_valid[r] == 0) {
+        if (lane < K) {
+            ids[size_t(r) * K + lane] = -1;
+            wts[size_t(r) * K + lane] = 0.0f;
+        }
+        return;
+    }
+    float* sv = s_s[warp];
+    float* bv = s_b[warp];
+    for (int e = lane; e < E; e += 32) {
+        const float s = router_sigmoid(logits[size_t(r) * E + e]);
+        sv[e] = s;
+        bv[e] = __fadd_rn(s, bias[e]);
+    }
+    __syncwarp();
+
+    // group scores: lane g scans its group
+    const int epg = E / G;
+    uint64_t gkey = 0;
+    if (lane < G) {
+        float t1 = -INFINITY, t2 = -INFINITY;
+        for (int i = 0; i < epg; ++i) {
+            const float v = bv[lane * epg + i];
+            if (v > t1) {
+                t2 = t1;
+                t1 = v;
+            } else if (v > t2) {
+                t2 = v;
+            }
+        }
+        const float gs = (epg >= 2) ? __fadd_rn(t1, t2) : t1;
+        gkey = rank_key(gs, lane);
+    }
+    uint32_t gmask = 0;
+    for (int t = 0; t < TG; ++t) {
+        const uint64_t best = warp_max_u64(gkey);
+        const int g = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFu));
+        gmask |= 1u << g;
+        if (lane == g) gkey = 0;
+    }
+
+    // expert keys of the lane's experts inside the kept groups
+    constexpr int kPer = MOE_MAX_EXPERTS / 32;
+    uint64_t ekey[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int e = lane + 32 * j;
+        ekey[j] = (e < E && ((gmask >> (e / epg)) & 1u)) ? rank_key(bv[e], e) : 0ull;
+    }
+    for (int k = 0; k < K; ++k) {
+        uint64_t mine = 0;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) mine = ekey[j] > mine ? ekey[j] : mine;
+        const uint64_t best = warp_max_u64(mine);
+        const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFu));
+        if ((e & 31) == lane) {
+#pragma unroll
+            for (int j = 0; j < kPer; ++j)
+                if (lane + 32 * j == e) ekey[j] = 0;
+        }
+        if (lane == 0) s_id[warp][k] = e;
+    }
+    __syncwarp();
+    if (lane == 0) {
+        float den = sv[s_id[warp][0]];
+        for (int k = 1; k < K; ++k) den = __fadd_rn(den, sv[s_id[warp][k]]);
+        for (int k = 0; k < K; ++k) {
+            const int e = s_id[warp][k];
+            ids[size_t(r) * K + k] = e;
+            wts[size_t(r) * K + k] = __fmul_rn(__fdiv_rn(sv[e], den), scaling);
+        }
+    }
+}
+
+// ----------------------------------------------------------- launchers ----
+cudaError_t launch_router(const uint16_t* x, const float* wr, const float* bias,
+                          const uint8_t* row_valid, int R, int H, int E, int G, int TG, int K,
+                          float scaling, int32_t* ids, float* wts, float* logits,
+                          cudaStream_t stream) {
+    const int nchunks = (H + 1023) / 1024;
+    const int threads = max(32, nchunks * 32);
+    if (R <= 64) {
+        constexpr int RT = 8, EC = 1;
+        dim3 grid(E / EC, (R + RT - 1) / RT);
+        const size_t smem = size_t(nchunks) * EC * RT * 32 * sizeof(float);
+        router_logits_kernel<RT, EC><<<grid, threads, smem, stream>>>(x, wr, row_valid, R, H, E,
+                                                                      logits);
+    } else {
+        constexpr int RT = 8, EC = 4;
+        dim3 grid((E + EC - 1) / EC, (R + RT - 1) / RT);
+        const size_t smem = size_t(nchunks) * EC * RT * 32 * sizeof(float);
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(router_logits_kernel<RT, EC>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(smem));
+            if (e != cudaSuccess) return e;
+        }
+        router_logits_kernel<RT, EC><<<grid, threads, smem, stream>>>(x, wr, row_valid, R, H, E,
+                                                                      logits);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    route_select_kernel<<<(R + kSelWarps - 1) / kSelWarps, kSelWarps * 32, 0, stream>>>(
+        logits, bias, row_valid, R, E, G, TG, K, scaling, ids, wts);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

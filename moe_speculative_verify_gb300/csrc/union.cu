@@ -1,0 +1,232 @@
+// union.cu -- expert union of a batch and the dispatch of its rows (sm_103a).
+//
+// openinfer #610 "TP8 span row mapping -- single-user speculative decode at
+// 186 tok/s", section "What": the union phase over the block's rows, mapping-
+// agnostic, deterministic; MoE-Infinity #140, route-ahead prefetch: the
+// per-token union of the verify block's routed experts.  mstar #388, FlashInfer
+// commit: activations quantised to e4m3 per 128 columns before the fp8 GEMM.
+//
+// The union is integer work and fully deterministic: per-expert row sets are
+// built as bitmaps (order-independent atomics), and positions are assigned by
+// walking each bitmap in row order.
+#include "common.cuh"
+#include "kernels.h"
+#include "layout.h"
+
+namespace moe {
+
+constexpr int kUnionThreads = 1024;
+
+// Exclusive scan of one value per thread over a 1024-thread block.
+__device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d) incl += o;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = s_warp[lane];
+        int wi = w;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int o = __shfl_up_sync(0xFFFFFFFFu, wi, d);
+            if (lane >= d) wi += o;
+        }
+        s_warp[lane] = wi - w;
+        if (lane == 31) *total = wi;
+    }
+    __syncthreads();
+    return s_warp[warp] + incl - v;
+}
+
+__global__ void __launch_bounds__(kUnionThreads) union_kernel(const int32_t* __restrict__ ids,
+                                                              int R, int E, int K, int S,
+                                                              int n_tile, int32_t* __restrict__ ub,
+                                                              UnionLayout L) {
+    extern __shared__ uint32_t sm[];
+    const int W = (R + 31) / 32;
+    uint32_t* bm = sm;                               // [E][W] row bitmaps
+    uint8_t* s_valid = reinterpret_cast<uint8_t*>(bm + size_t(E) * W);   // [R]
+    int* s_cnt = reinterpret_cast<int*>(s_valid + ((R + 15) & ~15));     // [E+1]
+    int* s_off = s_cnt + (E + 1);                    // [E+2]
+    int* s_ioff = s_off + (E + 2);                   // [E+1] first item of each entry
+    __shared__ int s_warp[32];
+    __shared__ int s_total, s_err, s_nvalid;
+    const int tid = threadIdx.x;
+    const int KS = K + S;
+
+    for (int i = tid; i < E * W; i += kUnionThreads) bm[i] = 0u;
+    if (tid == 0) {
+        s_err = 0;
+        s_nvalid = 0;
+    }
+    __syncthreads();
+
+    // 1. row validity: all -1 (pad), or K distinct ids in [0, E)
+    for (int r = tid; r < R; r += kUnionThreads) {
+        const int32_t* row = ids + size_t(r) * K;
+        bool pad = true, ok = true;
+        for (int k = 0; k < K; ++k) {
+            const int e = row[k];
+            if (e != -1) pad = false;
+            if (e < 0 || e >= E) ok = false;
+            for (int j = 0; j < k; ++j)
+                if (row[j] == e) ok = false;
+        }
+        if (!pad && !ok) atomicExch(&s_err, MOE_ERR_INVALID_ARG);
+        const bool v = !pad && ok;
+        s_valid[r] = v ? 1 : 0;
+        if (v) atomicAdd(&s_nvalid, 1);
+    }
+    __syncthreads();
+
+    // 2. per-expert row bitmaps
+    for (int i = tid; i < R * K; i += kUnionThreads) {
+        const int r = i / K;
+        if (!s_valid[r]) continue;
+        const int e = ids[i];
+        atomicOr(&bm[size_t(e) * W + (r >> 5)], 1u << (r & 31));
+    }
+    __syncthreads();
+
+    // 3. counts
+    for (int e = tid; e < E; e += kUnionThreads) {
+        int c = 0;
+        for (int w = 0; w < W; ++w) c += __popc(bm[size_t(e) * W + w]);
+        s_cnt[e] = c;
+    }
+    if (tid == 0) s_cnt[E] = S ? s_nvalid : 0;
+    __syncthreads();
+
+    // 4. offsets, union list, item offsets (shared entry's items first)
+    if (tid == 0) {
+        s_off[0] = 0;
+        int u = 0;
+        for (int e = 0; e <= E; ++e) {
+            s_off[e + 1] = s_off[e] + s_cnt[e];
+            if (e < E && s_cnt[e] > 0) ub[L.ulist + u++] = e;
+        }
+        ub[L.ulist + u] = E;
+        int it = (s_cnt[E] + n_tile - 1) / n_tile;
+        s_ioff[E] = 0;
+        for (int e = 0; e < E; ++e) {
+            s_ioff[e] = it;
+            it += (s_cnt[e] + n_tile - 1) / n_tile;
+        }
+        ub[0] = u;
+        ub[1] = s_nvalid;
+        ub[2] = s_off[E + 1];
+        ub[3] = it;
+        ub[4] = n_tile;
+        ub[5] = s_err;
+        ub[6] = 0;
+        ub[7] = 0;
+    }
+    __syncthreads();
+    for (int e = tid; e <= E; e += kUnionThreads) ub[L.counts + e] = s_cnt[e];
+    for (int e = tid; e <= E + 1; e += kUnionThreads) ub[L.offsets + e] = s_off[e];
+
+    // 5. routed positions: expert e walks its bitmap in row order
+    for (int e = tid; e < E; e += kUnionThreads) {
+        int p = s_off[e];
+        for (int w = 0; w < W; ++w) {
+            uint32_t bits = bm[size_t(e) * W + w];
+            while (bits) {
+                const int b = __ffs(bits) - 1;
+                bits &= bits - 1;
+                const int r = w * 32 + b;
+                int k = 0;
+                while (ids[size_t(r) * K + k] != e) ++k;
+                ub[L.pos + r * KS + k] = p;
+                ub[L.src + p] = r * KS + k;
+                ++p;
+            }
+        }
+    }
+
+    // 6. shared positions (valid rows in row order) and pad rows
+    const int per = (R + kUnionThreads - 1) / kUnionThreads;
+    const int rb = tid * per;
+    int local = 0;
+    for (int r = rb; r < min(R, rb + per); ++r) local += s_valid[r];
+    const int rank0 = block_exclusive_scan(local, s_warp, &s_total);
+    int rank = rank0;
+    for (int r = rb; r < min(R, rb + per); ++r) {
+        if (!s_valid[r]) {
+            for (int k = 0; k < KS; ++k) ub[L.pos + r * KS + k] = -1;
+        } else if (S) {
+            const int p = s_off[E] + rank;
+            ub[L.pos + r * KS + K] = p;
+            ub[L.src + p] = r * KS + K;
+            ++rank;
+        }
+    }
+
+    // 7. work items: rows of each entry in chunks of n_tile
+    for (int e = tid; e <= E; e += kUnionThreads) {
+        const int c = s_cnt[e];
+        for (int j = 0; j * n_tile < c; ++j) {
+            int4 item;
+            item.x = e;
+            item.y = s_off[e] + j * n_tile;
+            item.z = min(n_tile, c - j * n_tile);
+            item.w = 0;
+            reinterpret_cast<int4*>(ub + L.items)[s_ioff[e] + j] = item;
+        }
+    }
+}
+
+// Quantise each valid row per 128 columns to e4m3 and write it to its gathered
+// positions (K routed slots, then the shared slot).  One warp per (row, block).
+__global__ void __launch_bounds__(256) dispatch_kernel(const uint16_t* __restrict__ x,
+                                                       const int32_t* __restrict__ ub, UnionLayout L,
+                                                       int R, int H, int KS,
+                                                       uint8_t* __restrict__ xg,
+                                                       float* __restrict__ xs) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x;
+    const int HB = H / kBlock;
+    const int b = blockIdx.y * 8 + warp;
+    if (b >= HB) return;
+    const int32_t* pos = ub + L.pos + size_t(r) * KS;
+    if (pos[0] < 0) return;  // pad row
+    const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + size_t(r) * H + b * kBlock + 4 * lane));
+    const float f0 = bf16_bits_to_f32(xv.x & 0xFFFFu), f1 = bf16_bits_to_f32(xv.x >> 16);
+    const float f2 = bf16_bits_to_f32(xv.y & 0xFFFFu), f3 = bf16_bits_to_f32(xv.y >> 16);
+    float amax = fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3)));
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, d));
+    const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+    const uint32_t q = to_e4m3x4(__fdiv_rn(f0, sc), __fdiv_rn(f1, sc), __fdiv_rn(f2, sc),
+                                 __fdiv_rn(f3, sc));
+    for (int k = 0; k < KS; ++k) {
+        const int p = pos[k];
+        reinterpret_cast<uint32_t*>(xg + size_t(p) * H + b * kBlock)[lane] = q;
+        if (lane == 0) xs[size_t(p) * HB + b] = sc;
+    }
+}
+
+cudaError_t launch_union(const int32_t* ids, int R, int E, int K, int S, int n_tile,
+                         int32_t* ub, const UnionLayout& L, cudaStream_t stream) {
+    const int W = (R + 31) / 32;
+    const size_t smem = size_t(E) * W * 4 + ((R + 15) & ~15) + size_t(4 * E + 8) * 4;
+    cudaError_t e = cudaFuncSetAttribute(union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    union_kernel<<<1, kUnionThreads, smem, stream>>>(ids, R, E, K, S, n_tile, ub, L);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch(const uint16_t* x, const int32_t* ub, const UnionLayout& L, int R,
+                            int H, int KS, uint8_t* xg, float* xs, cudaStream_t stream) {
+    const int HB = H / kBlock;
+    dim3 grid(R, (HB + 7) / 8);
+    dispatch_kernel<<<grid, 256, 0, stream>>>(x, ub, L, R, H, KS, xg, xs);
+    return cudaGetLastError();
+}
+
+}  // namespace moe
