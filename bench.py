@@ -54,6 +54,25 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
+# ------------------------------------------------------------------ ranks --
+def max_over_ranks(x: float) -> float:
+    """Largest value of x over the ranks of the default process group (x itself
+    without one).  The job's step time is the slowest replica's."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" \
+        else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rows_per_s(rows_per_rank: int, world: int, step_ms_max: float) -> float:
+    """Whole-job throughput: every replica processes rows_per_rank rows per step."""
+    return world * rows_per_rank / (step_ms_max / 1e3)
+
+
 # ----------------------------------------------------------- algorithmics --
 def algorithmic(wl, ids: np.ndarray, valid: np.ndarray) -> dict:
     """Bytes each kernel must move at minimum and the layer's fp8 MMA flops."""
@@ -298,14 +317,10 @@ def main() -> None:
                 "out": out}
 
     res = measure(wl, args.steps, max(args.warmup, 3), True)
-    step_ms = res["step_ms"]
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(res["step_ms"])
     alg = res["alg"]
     R = wl.rows
-    value = world * R / (step_ms / 1e3)
+    value = job_rows_per_s(R, world, step_ms)
     layer_gbs = alg["total_bytes"] / (step_ms / 1e3) / 1e9
     tflops = alg["flops"] / (step_ms / 1e3) / 1e12
 
