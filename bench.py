@@ -295,9 +295,11 @@ def main() -> None:
         clk = ClockSampler(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
             if record_clocks else None
         wall0 = time.perf_counter()
+        torch.cuda.nvtx.range_push(f"timed:{wl_m.name}")
         for i in range(steps):
             flush.zero_()
             step(evs[i])
+        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
         if world > 1:

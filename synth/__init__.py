@@ -45,6 +45,10 @@ class LayerShape:
 
 GLM52 = LayerShape(hidden=6144, inter=2048, n_experts=256, n_groups=8, topk_groups=4,
                    topk=8, n_shared=1, routed_scaling=2.5)
+# GLM-5.2 expert shape with 32 experts: the small case for full profiler captures
+# (about 1.2 GB of weights: above L2, a few GB on the device at most)
+GLM52_E32 = LayerShape(hidden=6144, inter=2048, n_experts=32, n_groups=4, topk_groups=2,
+                       topk=8, n_shared=1, routed_scaling=2.5)
 TINY = LayerShape(hidden=256, inter=128, n_experts=16, n_groups=4, topk_groups=2, topk=4,
                   n_shared=1, routed_scaling=2.5)
 
@@ -76,6 +80,9 @@ WORKLOADS = {
                           note="mixed decode batch, Zipf(1.1) expert popularity"),
     "prefill4096": Workload("prefill4096", GLM52, rows=4096,
                             note="prefill chunk, uniform routing"),
+    "profile8": Workload("profile8", GLM52_E32, rows=8,
+                         note="8 rows on 32 experts of the GLM-5.2 shape, for profiler "
+                              "captures"),
 }
 
 
