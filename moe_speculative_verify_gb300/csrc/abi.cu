@@ -288,11 +288,11 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x_bf16, const float*
     moe_status_t st = check_cfg(cfg);
     if (st != MOE_OK) return st;
     if ((st = check_rows(R)) != MOE_OK) return st;
+    if (R == 0) return MOE_OK;  // nothing to do; empty arrays may be NULL
     if (!x_bf16 || !w_router || !bias || !topk_ids || !topk_w || !logits) return MOE_ERR_INVALID_ARG;
     if (!aligned(x_bf16, 16) || !aligned(w_router, 16) || !aligned(bias, 4) ||
         !aligned(topk_ids, 4) || !aligned(topk_w, 4) || !aligned(logits, 4))
         return MOE_ERR_INVALID_ARG;
-    if (R == 0) return MOE_OK;
     return route_impl(cfg, x_bf16, w_router, bias, row_valid, R, topk_ids, topk_w, logits,
                       reinterpret_cast<cudaStream_t>(stream));
 }
@@ -302,10 +302,10 @@ moe_status_t moe_build_union(const moe_config_t* cfg, const int32_t* topk_ids, i
     moe_status_t st = check_cfg(cfg);
     if (st != MOE_OK) return st;
     if ((st = check_rows(R)) != MOE_OK) return st;
+    if (R == 0) return MOE_OK;  // nothing to do; empty arrays may be NULL
     if (!topk_ids || !union_buf || !aligned(topk_ids, 4) || !aligned(union_buf, 16))
         return MOE_ERR_INVALID_ARG;
     if (union_bytes < moe_union_bytes(cfg, R)) return MOE_ERR_WORKSPACE;
-    if (R == 0) return MOE_OK;
     return union_impl(cfg, topk_ids, R, union_buf, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -316,6 +316,7 @@ moe_status_t moe_expert_ffn_fp8(const moe_config_t* cfg, const void* x_bf16,
     moe_status_t st = check_cfg(cfg);
     if (st != MOE_OK) return st;
     if ((st = check_rows(R)) != MOE_OK) return st;
+    if (R == 0) return MOE_OK;  // nothing to do; empty arrays may be NULL
     if ((st = check_weights(cfg, w)) != MOE_OK) return st;
     if (!x_bf16 || !union_buf || !y_slots || !ws) return MOE_ERR_INVALID_ARG;
     if (cfg->n_shared > 0 && !y_shared) return MOE_ERR_INVALID_ARG;
@@ -323,7 +324,6 @@ moe_status_t moe_expert_ffn_fp8(const moe_config_t* cfg, const void* x_bf16,
         (y_shared && !aligned(y_shared, 4)) || !aligned(ws, 256))
         return MOE_ERR_INVALID_ARG;
     if (ws_bytes < moe_ffn_workspace_bytes(cfg, R)) return MOE_ERR_WORKSPACE;
-    if (R == 0) return MOE_OK;
     return ffn_impl(cfg, x_bf16, w, union_buf, R, y_slots, y_shared, ws,
                     reinterpret_cast<cudaStream_t>(stream));
 }
@@ -334,6 +334,7 @@ static moe_status_t check_ffn_call(const moe_config_t* cfg, const int32_t* union
     moe_status_t st = check_cfg(cfg);
     if (st != MOE_OK) return st;
     if ((st = check_rows(R)) != MOE_OK) return st;
+    if (R == 0) return MOE_OK;
     if (!union_buf || !ws || !aligned(union_buf, 16) || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
     if (ws_bytes < moe_ffn_workspace_bytes(cfg, R)) return MOE_ERR_WORKSPACE;
     return MOE_OK;
@@ -342,9 +343,8 @@ static moe_status_t check_ffn_call(const moe_config_t* cfg, const int32_t* union
 moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x_bf16, const int32_t* union_buf,
                           int32_t R, void* ws, size_t ws_bytes, moe_stream_t stream) {
     moe_status_t st = check_ffn_call(cfg, union_buf, R, ws, ws_bytes);
-    if (st != MOE_OK) return st;
+    if (st != MOE_OK || R == 0) return st;
     if (!x_bf16 || !aligned(x_bf16, 16)) return MOE_ERR_INVALID_ARG;
-    if (R == 0) return MOE_OK;
     return dispatch_impl(cfg, x_bf16, union_buf, R, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -352,9 +352,8 @@ moe_status_t moe_gate_up_fp8(const moe_config_t* cfg, const moe_weights_t* w,
                              const int32_t* union_buf, int32_t R, void* ws, size_t ws_bytes,
                              moe_stream_t stream) {
     moe_status_t st = check_ffn_call(cfg, union_buf, R, ws, ws_bytes);
-    if (st != MOE_OK) return st;
+    if (st != MOE_OK || R == 0) return st;
     if ((st = check_weights(cfg, w)) != MOE_OK) return st;
-    if (R == 0) return MOE_OK;
     return gate_up_impl(cfg, w, union_buf, R, ws, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -362,11 +361,10 @@ moe_status_t moe_down_fp8(const moe_config_t* cfg, const moe_weights_t* w,
                           const int32_t* union_buf, int32_t R, float* y_slots, float* y_shared,
                           void* ws, size_t ws_bytes, moe_stream_t stream) {
     moe_status_t st = check_ffn_call(cfg, union_buf, R, ws, ws_bytes);
-    if (st != MOE_OK) return st;
+    if (st != MOE_OK || R == 0) return st;
     if ((st = check_weights(cfg, w)) != MOE_OK) return st;
     if (!y_slots || !aligned(y_slots, 4) || (cfg->n_shared > 0 && (!y_shared || !aligned(y_shared, 4))))
         return MOE_ERR_INVALID_ARG;
-    if (R == 0) return MOE_OK;
     return down_impl(cfg, w, union_buf, R, y_slots, y_shared, ws,
                      reinterpret_cast<cudaStream_t>(stream));
 }
@@ -377,12 +375,12 @@ moe_status_t moe_combine(const moe_config_t* cfg, const float* y_slots, const fl
     moe_status_t st = check_cfg(cfg);
     if (st != MOE_OK) return st;
     if ((st = check_rows(R)) != MOE_OK) return st;
+    if (R == 0) return MOE_OK;  // nothing to do; empty arrays may be NULL
     if (!y_slots || !topk_w || !union_buf || !out_bf16) return MOE_ERR_INVALID_ARG;
     if (cfg->n_shared > 0 && !y_shared) return MOE_ERR_INVALID_ARG;
     if (!aligned(y_slots, 16) || (y_shared && !aligned(y_shared, 16)) || !aligned(topk_w, 4) ||
         !aligned(union_buf, 16) || !aligned(out_bf16, 16))
         return MOE_ERR_INVALID_ARG;
-    if (R == 0) return MOE_OK;
     return combine_impl(cfg, y_slots, y_shared, topk_w, union_buf, R, out_bf16,
                         reinterpret_cast<cudaStream_t>(stream));
 }
@@ -394,6 +392,7 @@ moe_status_t moe_layer(const moe_config_t* cfg, const void* x_bf16, const float*
     moe_status_t st = check_cfg(cfg);
     if (st != MOE_OK) return st;
     if ((st = check_rows(R)) != MOE_OK) return st;
+    if (R == 0) return MOE_OK;  // nothing to do; empty arrays may be NULL
     if ((st = check_weights(cfg, w)) != MOE_OK) return st;
     if (!x_bf16 || !w_router || !bias || !out_bf16 || !ws) return MOE_ERR_INVALID_ARG;
     if (!aligned(x_bf16, 16) || !aligned(w_router, 16) || !aligned(bias, 4) ||
@@ -401,7 +400,6 @@ moe_status_t moe_layer(const moe_config_t* cfg, const void* x_bf16, const float*
         (topk_ids_out && !aligned(topk_ids_out, 4)) || (topk_w_out && !aligned(topk_w_out, 4)))
         return MOE_ERR_INVALID_ARG;
     if (ws_bytes < moe_workspace_bytes(cfg, R)) return MOE_ERR_WORKSPACE;
-    if (R == 0) return MOE_OK;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const LayerLayout L = moe::layer_layout(cfg->hidden, cfg->inter, cfg->n_experts, cfg->topk,
                                             cfg->n_shared, R);
