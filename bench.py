@@ -100,8 +100,13 @@ def algorithmic(wl, ids: np.ndarray, valid: np.ndarray) -> dict:
 
 # ------------------------------------------------------------------ clocks --
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples (every 20 ms) of SM clock, power and throttle reasons.
+
+    Started before the warm-up; stop(t0, t1) keeps the samples taken inside the
+    timed region [t0, t1] (wall clock), widening the window symmetrically until
+    it holds at least 3 samples when the region is shorter than the sampling
+    period, and reports the window used."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -113,39 +118,49 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-i", gpu_index, "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-i", gpu_index, "-lms", "20"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
         except Exception:
             self.proc = None
 
-    def stop(self) -> dict:
+    def stop(self, t0: float, t1: float) -> dict:
+        import datetime
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
         self.f.close()
-        sm, smax, reasons, power = [], [], set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-                power.append(float(parts[3]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), float(parts[4]),
+                             [n for n, v in zip(names, parts[6:10]) if v.lower() == "active"]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "power_w_max": max(power) if power else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+        half = 0.0
+        while True:
+            sel = [r for r in rows if t0 - half <= r[0] <= t1 + half]
+            if len(sel) >= 3 or half > 5.0:
+                break
+            half += 0.02
+        if not sel:
+            sel = rows
+        reasons = sorted({n for r in sel for n in r[4]})
+        return {"sm_mhz": statistics.median(r[1] for r in sel),
+                "sm_max_mhz": max(r[2] for r in sel),
+                "power_w_max": max(r[3] for r in sel), "samples": len(sel),
+                "window_s": round((t1 - t0) + 2 * half, 3), "reasons": reasons}
 
 
 # ------------------------------------------------------------------ oracle --
@@ -283,6 +298,8 @@ def main() -> None:
             m.moe_combine(cfg, y_slots, y_sh, wts, ub, out)
             mark(6)
 
+        clk = ClockSampler(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
+            if record_clocks else None
         for _ in range(warmup):
             flush.zero_()
             step()
@@ -292,19 +309,19 @@ def main() -> None:
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
-        clk = ClockSampler(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
-            if record_clocks else None
         wall0 = time.perf_counter()
-        torch.cuda.nvtx.range_push(f"timed:{wl_m.name}")
+        t_start = time.time()
+        torch.cuda.nvtx.range_push(f"timed_{wl_m.name}")
         for i in range(steps):
             flush.zero_()
             step(evs[i])
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
+        t_end = time.time()
         if world > 1:
             torch.distributed.barrier()
-        clocks = clk.stop() if clk else None
+        clocks = clk.stop(t_start, t_end) if clk else None
         err = m.moe_get_device_error(ws)
         assert err == 0, err
         ph = {p: [] for p in PHASES}
