@@ -24,8 +24,8 @@
  *   - All pointers are DEVICE pointers unless stated otherwise; the caller owns
  *     every buffer and every stream.  The library allocates nothing, holds no
  *     state between calls, and never synchronises the stream except in
- *     moe_get_device_error.  Calls are asynchronous on `stream` and can be
- *     captured in a CUDA graph.
+ *     moe_get_device_error.  Calls are asynchronous on `stream`; all but
+ *     moe_layer_noalloc (see its own notes) can be captured in a CUDA graph.
  *   - Refusals are synchronous: a NULL required pointer, a misaligned pointer
  *     (16 bytes for bf16 / e4m3 / output arrays, 4 bytes for fp32 / int32), an
  *     unsupported shape or a short buffer returns an error code and launches
@@ -252,6 +252,37 @@ moe_status_t moe_layer(const moe_config_t* cfg, const void* x_bf16, const float*
                        const float* bias, const moe_weights_t* w, const uint8_t* row_valid,
                        int32_t R, void* out_bf16, int32_t* topk_ids_out, float* topk_w_out,
                        void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_layer_noalloc -- moe_layer without a caller-provided workspace.  The
+ * source pages have no counterpart of this entry point; it exists for callers
+ * that cannot allocate device memory: a plugin whose host framework owns every
+ * device allocation and hands out no scratch, code on a path that must not call
+ * cudaMalloc, or a caller that cannot size a workspace ahead of the call.
+ *
+ * The layer's scratch is one array of 32 MiB (33 554 432 bytes) compiled into
+ * this library; every GPU that loads the library holds it until the process
+ * exits.  A call whose moe_workspace_bytes(cfg, R) exceeds it is refused with
+ * MOE_ERR_UNSUPPORTED (at the GLM-5.2 shape -- H 6144, I 2048, E 256, K 8,
+ * one shared expert -- up to 109 rows fit, e.g. a 64-row batched verify).  Nothing is allocated: no
+ * cudaMalloc, cudaFree or allocating library call.
+ *
+ * The first call on a device looks up the array's device address with that
+ * device current (cudaGetSymbolAddress) and caches it; make that first call
+ * outside any stream capture.  Every call shares the one array and leaves its
+ * contents behind; the call clears the error word at its head itself.  Calls
+ * that overlap on the GPU (concurrent streams, or several host threads) race on
+ * the array and corrupt each other: serialise them.
+ *
+ * Arguments as moe_layer, without ws / ws_bytes, plus:
+ *   device_status  int32 device word or NULL: receives the layer's device error
+ *                  code (MOE_OK, MOE_ERR_TIMEOUT, ...) in stream order.
+ */
+moe_status_t moe_layer_noalloc(const moe_config_t* cfg, const void* x_bf16,
+                               const float* w_router, const float* bias, const moe_weights_t* w,
+                               const uint8_t* row_valid, int32_t R, void* out_bf16,
+                               int32_t* topk_ids_out, float* topk_w_out, int32_t* device_status,
+                               moe_stream_t stream);
 
 /*
  * moe_get_device_error -- synchronises `stream`, then reads (and clears when

@@ -21,7 +21,7 @@ __all__ = [
     "moe_expert_ffn_fp8", "moe_combine", "moe_layer", "moe_union_bytes",
     "moe_ffn_workspace_bytes", "moe_workspace_bytes", "moe_get_device_error",
     "moe_diag_wait_timeout", "moe_status_string", "moe_dispatch", "moe_gate_up_fp8",
-    "moe_down_fp8", "ffn_layout", "union_layout", "rows_per_item",
+    "moe_down_fp8", "ffn_layout", "moe_layer_noalloc", "union_layout", "rows_per_item",
     "MOE_MAX_ROWS",
 ]
 
@@ -96,9 +96,10 @@ def load() -> C.CDLL:
     L.moe_down_fp8.argtypes = [cfg, C.POINTER(Weights), P, I32, P, P, P, SZ, P]
     L.moe_layer.argtypes = [cfg, P, P, P, C.POINTER(Weights), P, I32, P, P, P, P, SZ, P]
     L.moe_get_device_error.argtypes = [P, I32, P]
+    L.moe_layer_noalloc.argtypes = [cfg, P, P, P, C.POINTER(Weights), P, I32, P, P, P, P, P]
     L.moe_diag_wait_timeout.argtypes = [P, C.c_uint32, P]
     for n in ("moe_route", "moe_build_union", "moe_expert_ffn_fp8", "moe_combine", "moe_layer",
-              "moe_get_device_error", "moe_diag_wait_timeout", "moe_dispatch",
+              "moe_get_device_error", "moe_diag_wait_timeout", "moe_dispatch", "moe_layer_noalloc",
               "moe_gate_up_fp8", "moe_down_fp8"):
         getattr(L, n).restype = C.c_int
     _LIB = L
@@ -191,6 +192,16 @@ def moe_layer(cfg: Config, x, w_router, bias, weights: Weights, row_valid, out, 
                             _ptr(row_valid), R, _ptr(out), _ptr(topk_ids), _ptr(topk_w),
                             _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "moe_layer")
+
+
+def moe_layer_noalloc(cfg: Config, x, w_router, bias, weights: Weights, row_valid, out,
+                      topk_ids=None, topk_w=None, device_status=None, stream=None) -> None:
+    """moe_layer with the library's own fixed scratch array (no workspace argument)."""
+    R = x.shape[0]
+    _check(load().moe_layer_noalloc(C.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias),
+                                    C.byref(weights), _ptr(row_valid), R, _ptr(out),
+                                    _ptr(topk_ids), _ptr(topk_w), _ptr(device_status),
+                                    _stream(stream)), "moe_layer_noalloc")
 
 
 def moe_get_device_error(ws, clear: bool = True, stream=None) -> int:

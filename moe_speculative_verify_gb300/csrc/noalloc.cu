@@ -1,0 +1,81 @@
+// noalloc.cu -- moe_layer for callers that cannot allocate device memory.
+//
+// Some callers have no way to hand this library a workspace: a plugin whose
+// host framework owns every device allocation and gives plugins none, code on
+// a latency-critical path that is not allowed to call cudaMalloc, or a caller
+// that only learns the row count when the layer runs.  For them the layer's
+// scratch lives in one fixed-size array in the library's own device memory.
+// The array is reserved on every GPU that loads the library, for as long as the
+// process runs, so it is kept modest: kStaticScratchBytes (32 MiB), enough for
+// up to 109 rows at the GLM-5.2 layer shape (hidden 6144, inter 2048, 256
+// experts, top-8, one shared expert).
+#include <mutex>
+
+#include "common.cuh"
+#include "layout.h"
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;
+
+// The layer's whole workspace (error word, routing, union, FFN scratch, slot
+// outputs) for calls of moe_layer_noalloc.  Host code must not use this name
+// as an address: it is resolved per device with cudaGetSymbolAddress below.
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (with that device current) and cached.
+moe_status_t scratch_address(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr)
+            return MOE_ERR_CUDA;
+        g_addr[dev] = p;
+    }
+    *out = g_addr[dev];
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_layer_noalloc(const moe_config_t* cfg, const void* x_bf16,
+                                          const float* w_router, const float* bias,
+                                          const moe_weights_t* w, const uint8_t* row_valid,
+                                          int32_t R, void* out_bf16, int32_t* topk_ids_out,
+                                          float* topk_w_out, int32_t* device_status,
+                                          moe_stream_t stream) {
+    if (cfg == nullptr) return MOE_ERR_INVALID_ARG;
+    if (R < 0) return MOE_ERR_INVALID_ARG;
+    if (R == 0) return MOE_OK;
+    const size_t need = moe_workspace_bytes(cfg, R);
+    if (need == 0) {
+        // the shape or the row count is refused: report it as moe_layer would
+        return moe_layer(cfg, x_bf16, w_router, bias, w, row_valid, R, out_bf16, topk_ids_out,
+                         topk_w_out, nullptr, 0, stream);
+    }
+    if (need > kStaticScratchBytes) return MOE_ERR_UNSUPPORTED;
+    if (device_status && (reinterpret_cast<uintptr_t>(device_status) % 4) != 0)
+        return MOE_ERR_INVALID_ARG;
+    void* scratch = nullptr;
+    moe_status_t st = scratch_address(&scratch);
+    if (st != MOE_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // The array keeps the previous call's contents; only the error word at its
+    // head must start at zero (every other byte the layer reads it writes first).
+    if (cudaMemsetAsync(scratch, 0, moe::kCtlBytes, s) != cudaSuccess) return MOE_ERR_CUDA;
+    st = moe_layer(cfg, x_bf16, w_router, bias, w, row_valid, R, out_bf16, topk_ids_out,
+                   topk_w_out, scratch, kStaticScratchBytes, stream);
+    if (st != MOE_OK) return st;
+    if (device_status &&
+        cudaMemcpyAsync(device_status, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) !=
+            cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
