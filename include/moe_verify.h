@@ -34,6 +34,10 @@
  *   - A launch failure is read back with cudaGetLastError right after the
  *     launch and returned as MOE_ERR_CUDA, so it never surfaces in a later,
  *     unrelated kernel.
+ *   - Kernels are launched with programmatic dependent launch: a kernel may
+ *     start while the previous kernel on the stream finishes; it waits for
+ *     that kernel's completion before reading its outputs or writing anything
+ *     but may fetch read-only weights early.  Stream order is preserved.
  *   - A pad row (row_valid[r] == 0) may hold NaN in x.  It is not routed
  *     (ids -1, weights 0), takes no place in the union, and its output row is
  *     +0.0 in every column.
@@ -207,13 +211,23 @@ moe_status_t moe_expert_ffn_fp8(const moe_config_t* cfg, const void* x_bf16,
                                 moe_stream_t stream);
 
 /*
- * The three steps of moe_expert_ffn_fp8, callable one by one (same arguments,
- * same workspace; moe_expert_ffn_fp8 is exactly these three in order):
- *   moe_dispatch     quantise each valid row per 1x128 and write it to its K+S
- *                    gathered positions (workspace);
- *   moe_gate_up_fp8  g and u GEMMs, h = silu(g) * u, h quantised per 1x128
- *                    (workspace);
- *   moe_down_fp8     the down GEMM, fp32 rows to y_slots / y_shared.
+ * The steps of moe_expert_ffn_fp8, callable one by one (same arguments, same
+ * workspace).  moe_expert_ffn_fp8 is moe_dispatch followed by
+ * moe_expert_gemms_fp8; moe_gate_up_fp8 followed by moe_down_fp8 computes the
+ * same values as moe_expert_gemms_fp8 in two launches.
+ *   moe_dispatch          quantise each valid row per 1x128 and write it to its
+ *                         K+S gathered positions (workspace); clears the fused
+ *                         GEMM's per-item counters;
+ *   moe_expert_gemms_fp8  gate/up GEMMs + SiLU*mul + h quantisation and the down
+ *                         GEMM in one persistent launch (a down tile starts once
+ *                         every gate/up tile of its rows has stored its h);
+ *   moe_gate_up_fp8       g and u GEMMs, h = silu(g) * u, h quantised per 1x128
+ *                         (workspace);
+ *   moe_down_fp8          the down GEMM, fp32 rows to y_slots / y_shared.
+ * Order: each GEMM call must come after moe_dispatch of the same call on the
+ * same stream, with no other launch of this library in between except
+ * moe_gate_up_fp8 before moe_down_fp8 (kernels start while their predecessor
+ * finishes, see the launch note below).
  */
 moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x_bf16, const int32_t* union_buf,
                           int32_t R, void* ws, size_t ws_bytes, moe_stream_t stream);
@@ -223,6 +237,9 @@ moe_status_t moe_gate_up_fp8(const moe_config_t* cfg, const moe_weights_t* w,
 moe_status_t moe_down_fp8(const moe_config_t* cfg, const moe_weights_t* w,
                           const int32_t* union_buf, int32_t R, float* y_slots, float* y_shared,
                           void* ws, size_t ws_bytes, moe_stream_t stream);
+moe_status_t moe_expert_gemms_fp8(const moe_config_t* cfg, const moe_weights_t* w,
+                                  const int32_t* union_buf, int32_t R, float* y_slots,
+                                  float* y_shared, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
  * moe_combine -- fixed-order weighted combine plus the shared expert, pads

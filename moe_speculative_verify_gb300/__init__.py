@@ -21,7 +21,7 @@ __all__ = [
     "moe_expert_ffn_fp8", "moe_combine", "moe_layer", "moe_union_bytes",
     "moe_ffn_workspace_bytes", "moe_workspace_bytes", "moe_get_device_error",
     "moe_diag_wait_timeout", "moe_status_string", "moe_dispatch", "moe_gate_up_fp8",
-    "moe_down_fp8", "ffn_layout", "moe_layer_noalloc", "union_layout", "rows_per_item",
+    "moe_down_fp8", "ffn_layout", "moe_layer_noalloc", "moe_expert_gemms_fp8", "union_layout", "rows_per_item",
     "MOE_MAX_ROWS",
 ]
 
@@ -94,13 +94,14 @@ def load() -> C.CDLL:
     L.moe_dispatch.argtypes = [cfg, P, P, I32, P, SZ, P]
     L.moe_gate_up_fp8.argtypes = [cfg, C.POINTER(Weights), P, I32, P, SZ, P]
     L.moe_down_fp8.argtypes = [cfg, C.POINTER(Weights), P, I32, P, P, P, SZ, P]
+    L.moe_expert_gemms_fp8.argtypes = [cfg, C.POINTER(Weights), P, I32, P, P, P, SZ, P]
     L.moe_layer.argtypes = [cfg, P, P, P, C.POINTER(Weights), P, I32, P, P, P, P, SZ, P]
     L.moe_get_device_error.argtypes = [P, I32, P]
     L.moe_layer_noalloc.argtypes = [cfg, P, P, P, C.POINTER(Weights), P, I32, P, P, P, P, P]
     L.moe_diag_wait_timeout.argtypes = [P, C.c_uint32, P]
     for n in ("moe_route", "moe_build_union", "moe_expert_ffn_fp8", "moe_combine", "moe_layer",
               "moe_get_device_error", "moe_diag_wait_timeout", "moe_dispatch", "moe_layer_noalloc",
-              "moe_gate_up_fp8", "moe_down_fp8"):
+              "moe_gate_up_fp8", "moe_down_fp8", "moe_expert_gemms_fp8"):
         getattr(L, n).restype = C.c_int
     _LIB = L
     return L
@@ -179,6 +180,14 @@ def moe_down_fp8(cfg: Config, weights: Weights, union_buf, R: int, y_slots, y_sh
                                ws.numel() * ws.element_size(), _stream(stream)), "moe_down_fp8")
 
 
+def moe_expert_gemms_fp8(cfg: Config, weights: Weights, union_buf, R: int, y_slots, y_shared, ws,
+                         stream=None) -> None:
+    _check(load().moe_expert_gemms_fp8(C.byref(cfg), C.byref(weights), _ptr(union_buf), R,
+                                       _ptr(y_slots), _ptr(y_shared), _ptr(ws),
+                                       ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_expert_gemms_fp8")
+
+
 def moe_combine(cfg: Config, y_slots, y_shared, topk_w, union_buf, out, stream=None) -> None:
     R = out.shape[0]
     _check(load().moe_combine(C.byref(cfg), _ptr(y_slots), _ptr(y_shared), _ptr(topk_w),
@@ -244,10 +253,13 @@ def ffn_layout(cfg: Config, R: int) -> dict:
     """Byte offsets of the FFN workspace regions (mirrors the library's carve-up)."""
     def up(v, mlt):
         return (v + mlt - 1) // mlt * mlt
-    H, I, K, S = cfg.hidden, cfg.inter, cfg.topk, cfg.n_shared
+    H, I, E, K, S = cfg.hidden, cfg.inter, cfg.n_experts, cfg.topk, cfg.n_shared
     rows = up(R * (K + S), 64) + 64
-    out = {"rows": rows, "ctl": 0, "xg": 256}
-    b = up(256 + rows * H, 256)
+    n_ready = R * (K + S) // 16 + min(E, R * K) + S + 1
+    out = {"rows": rows, "ctl": 0, "ready": 256, "n_ready": n_ready}
+    b = up(256 + n_ready * 4, 256)
+    out["xg"] = b
+    b = up(b + rows * H, 256)
     out["xs"] = b
     b = up(b + rows * (H // 128) * 4, 256)
     out["hq"] = b

@@ -131,11 +131,12 @@ moe_status_t union_impl(const moe_config_t* c, const int32_t* ids, int32_t R, in
                                          moe::rows_per_item(R), ub, L, s));
 }
 
-// Pointers into the FFN workspace and the tensor maps of one call.
+// Pointers into the FFN workspace of one call.
 struct FfnCall {
     FfnLayout FL;
     UnionLayout UL;
     int32_t* err;
+    int32_t* ready;
     uint8_t* xg;
     float* xs;
     uint8_t* hq;
@@ -145,10 +146,11 @@ struct FfnCall {
 
 FfnCall ffn_call(const moe_config_t* c, int32_t R, void* ws) {
     FfnCall f;
-    f.FL = moe::ffn_layout(c->hidden, c->inter, c->topk, c->n_shared, R);
+    f.FL = moe::ffn_layout(c->hidden, c->inter, c->n_experts, c->topk, c->n_shared, R);
     f.UL = moe::union_layout(c->n_experts, c->topk, c->n_shared, R);
     uint8_t* base = static_cast<uint8_t*>(ws);
     f.err = reinterpret_cast<int32_t*>(base + f.FL.ctl);
+    f.ready = reinterpret_cast<int32_t*>(base + f.FL.ready);
     f.xg = base + f.FL.xg;
     f.xs = reinterpret_cast<float*>(base + f.FL.xs);
     f.hq = base + f.FL.hq;
@@ -157,14 +159,45 @@ FfnCall ffn_call(const moe_config_t* c, int32_t R, void* ws) {
     return f;
 }
 
-moe::FfnArgs ffn_args(const moe_config_t* c, const int32_t* ub, const FfnCall& f) {
+// The eight tensor maps of the expert GEMMs.  Shared-expert maps fall back to
+// the routed tensors when there is no shared expert (never read then).
+bool make_maps(const moe_config_t* c, const moe_weights_t* w, const FfnCall& f, moe::FfnMaps* mp) {
+    const int H = c->hidden, I = c->inter, E = c->n_experts, S = c->n_shared;
+    const uint64_t srows = S ? uint64_t(S) : 1ull;
+    return make_map(&mp->g, w->w_gate, uint64_t(E) * I, H, 128) &&
+           make_map(&mp->u, w->w_up, uint64_t(E) * I, H, 128) &&
+           make_map(&mp->sg, S ? w->sh_gate : w->w_gate, srows * I, H, 128) &&
+           make_map(&mp->su, S ? w->sh_up : w->w_up, srows * I, H, 128) &&
+           make_map(&mp->x, f.xg, f.FL.rows, H, f.nt) &&
+           make_map(&mp->d, w->w_down, uint64_t(E) * H, I, 128) &&
+           make_map(&mp->sd, S ? w->sh_down : w->w_down, srows * H, I, 128) &&
+           make_map(&mp->h, f.hq, f.FL.rows, I, f.nt);
+}
+
+moe::FfnArgs ffn_args(const moe_config_t* c, const moe_weights_t* w, const int32_t* ub,
+                      const FfnCall& f, float* y_slots, float* y_shared) {
+    const int S = c->n_shared;
     moe::FfnArgs a{};
     a.ub = ub;
     a.ul = f.UL;
+    a.s_gate = w->s_gate;
+    a.s_up = w->s_up;
+    a.sh_s_gate = S ? w->sh_s_gate : w->s_gate;
+    a.sh_s_up = S ? w->sh_s_up : w->s_up;
+    a.s_down = w->s_down;
+    a.sh_s_down = S ? w->sh_s_down : w->s_down;
+    a.xs = f.xs;
+    a.hq = f.hq;
+    a.hs = f.hs;
+    a.y_slots = y_slots;
+    a.y_shared = y_shared;
+    a.ready = f.ready;
     a.err = f.err;
+    a.H = c->hidden;
+    a.I = c->inter;
     a.E = c->n_experts;
     a.K = c->topk;
-    a.KS = c->topk + c->n_shared;
+    a.KS = c->topk + S;
     a.timeout_ns = timeout_ns(c);
     return a;
 }
@@ -173,63 +206,20 @@ moe_status_t dispatch_impl(const moe_config_t* c, const void* x, const int32_t* 
                            void* ws, cudaStream_t s) {
     const FfnCall f = ffn_call(c, R, ws);
     return cuda_status(moe::launch_dispatch(static_cast<const uint16_t*>(x), ub, f.UL, R, c->hidden,
-                                            c->topk + c->n_shared, f.xg, f.xs, s));
+                                            c->topk + c->n_shared, f.xg, f.xs, f.ready,
+                                            f.FL.n_ready, s));
 }
 
-moe_status_t gate_up_impl(const moe_config_t* c, const moe_weights_t* w, const int32_t* ub,
-                          int32_t R, void* ws, cudaStream_t s) {
-    const int H = c->hidden, I = c->inter, E = c->n_experts, S = c->n_shared;
+// One of the three expert-GEMM modes (gate/up, down, or both fused).
+moe_status_t gemm_impl(int mode, const moe_config_t* c, const moe_weights_t* w, const int32_t* ub,
+                       int32_t R, float* y_slots, float* y_shared, void* ws, cudaStream_t s) {
     const FfnCall f = ffn_call(c, R, ws);
     const DeviceInfo dev = device_info();
     if (dev.sms <= 0) return MOE_ERR_CUDA;
-    // shared-expert maps fall back to the routed tensors when S == 0 (never read)
-    const uint8_t* shg = S ? w->sh_gate : w->w_gate;
-    const uint8_t* shu = S ? w->sh_up : w->w_up;
-    const uint64_t srows = S ? uint64_t(S) : 1ull;
-    CUtensorMap m_g, m_u, m_sg, m_su, m_x;
-    if (!make_map(&m_g, w->w_gate, uint64_t(E) * I, H, 128) ||
-        !make_map(&m_u, w->w_up, uint64_t(E) * I, H, 128) ||
-        !make_map(&m_sg, shg, srows * I, H, 128) || !make_map(&m_su, shu, srows * I, H, 128) ||
-        !make_map(&m_x, f.xg, f.FL.rows, H, f.nt))
-        return MOE_ERR_CUDA;
-    moe::FfnArgs g = ffn_args(c, ub, f);
-    g.s_a0 = w->s_gate;
-    g.s_a1 = w->s_up;
-    g.sh_s_a0 = S ? w->sh_s_gate : w->s_gate;
-    g.sh_s_a1 = S ? w->sh_s_up : w->s_up;
-    g.bs = f.xs;
-    g.hq = f.hq;
-    g.hs = f.hs;
-    g.M = I;
-    g.Kd = H;
-    return cuda_status(moe::launch_ffn(f.nt, true, m_g, m_u, m_sg, m_su, m_x, g, dev.sms,
-                                       f.UL.max_items * (I / MOE_BLOCK), dev.smem_optin, s));
-}
-
-moe_status_t down_impl(const moe_config_t* c, const moe_weights_t* w, const int32_t* ub, int32_t R,
-                       float* y_slots, float* y_shared, void* ws, cudaStream_t s) {
-    const int H = c->hidden, I = c->inter, E = c->n_experts, S = c->n_shared;
-    const FfnCall f = ffn_call(c, R, ws);
-    const DeviceInfo dev = device_info();
-    if (dev.sms <= 0) return MOE_ERR_CUDA;
-    const uint8_t* shd = S ? w->sh_down : w->w_down;
-    const uint64_t srows = S ? uint64_t(S) : 1ull;
-    CUtensorMap m_d, m_sd, m_h;
-    if (!make_map(&m_d, w->w_down, uint64_t(E) * H, I, 128) ||
-        !make_map(&m_sd, shd, srows * H, I, 128) || !make_map(&m_h, f.hq, f.FL.rows, I, f.nt))
-        return MOE_ERR_CUDA;
-    moe::FfnArgs d = ffn_args(c, ub, f);
-    d.s_a0 = w->s_down;
-    d.s_a1 = w->s_down;
-    d.sh_s_a0 = S ? w->sh_s_down : w->s_down;
-    d.sh_s_a1 = d.sh_s_a0;
-    d.bs = f.hs;
-    d.y_slots = y_slots;
-    d.y_shared = y_shared;
-    d.M = H;
-    d.Kd = I;
-    return cuda_status(moe::launch_ffn(f.nt, false, m_d, m_d, m_sd, m_sd, m_h, d, dev.sms,
-                                       f.UL.max_items * (H / MOE_BLOCK), dev.smem_optin, s));
+    moe::FfnMaps mp;
+    if (!make_maps(c, w, f, &mp)) return MOE_ERR_CUDA;
+    return cuda_status(moe::launch_ffn(f.nt, mode, mp, ffn_args(c, w, ub, f, y_slots, y_shared),
+                                       dev.sms, dev.smem_optin, s));
 }
 
 moe_status_t ffn_impl(const moe_config_t* c, const void* x, const moe_weights_t* w,
@@ -237,8 +227,7 @@ moe_status_t ffn_impl(const moe_config_t* c, const void* x, const moe_weights_t*
                       cudaStream_t s) {
     moe_status_t st = dispatch_impl(c, x, ub, R, ws, s);
     if (st != MOE_OK) return st;
-    if ((st = gate_up_impl(c, w, ub, R, ws, s)) != MOE_OK) return st;
-    return down_impl(c, w, ub, R, y_slots, y_shared, ws, s);
+    return gemm_impl(moe::kFfnFused, c, w, ub, R, y_slots, y_shared, ws, s);
 }
 
 moe_status_t combine_impl(const moe_config_t* c, const float* y_slots, const float* y_shared,
@@ -272,7 +261,9 @@ size_t moe_union_bytes(const moe_config_t* cfg, int32_t max_rows) {
 
 size_t moe_ffn_workspace_bytes(const moe_config_t* cfg, int32_t max_rows) {
     if (check_cfg(cfg) != MOE_OK || check_rows(max_rows) != MOE_OK) return 0;
-    return size_t(moe::ffn_layout(cfg->hidden, cfg->inter, cfg->topk, cfg->n_shared, max_rows).bytes);
+    return size_t(moe::ffn_layout(cfg->hidden, cfg->inter, cfg->n_experts, cfg->topk, cfg->n_shared,
+                                  max_rows)
+                      .bytes);
 }
 
 size_t moe_workspace_bytes(const moe_config_t* cfg, int32_t max_rows) {
@@ -354,7 +345,8 @@ moe_status_t moe_gate_up_fp8(const moe_config_t* cfg, const moe_weights_t* w,
     moe_status_t st = check_ffn_call(cfg, union_buf, R, ws, ws_bytes);
     if (st != MOE_OK || R == 0) return st;
     if ((st = check_weights(cfg, w)) != MOE_OK) return st;
-    return gate_up_impl(cfg, w, union_buf, R, ws, reinterpret_cast<cudaStream_t>(stream));
+    return gemm_impl(moe::kFfnGateUp, cfg, w, union_buf, R, nullptr, nullptr, ws,
+                     reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_down_fp8(const moe_config_t* cfg, const moe_weights_t* w,
@@ -365,7 +357,19 @@ moe_status_t moe_down_fp8(const moe_config_t* cfg, const moe_weights_t* w,
     if ((st = check_weights(cfg, w)) != MOE_OK) return st;
     if (!y_slots || !aligned(y_slots, 4) || (cfg->n_shared > 0 && (!y_shared || !aligned(y_shared, 4))))
         return MOE_ERR_INVALID_ARG;
-    return down_impl(cfg, w, union_buf, R, y_slots, y_shared, ws,
+    return gemm_impl(moe::kFfnDown, cfg, w, union_buf, R, y_slots, y_shared, ws,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_expert_gemms_fp8(const moe_config_t* cfg, const moe_weights_t* w,
+                                  const int32_t* union_buf, int32_t R, float* y_slots,
+                                  float* y_shared, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    moe_status_t st = check_ffn_call(cfg, union_buf, R, ws, ws_bytes);
+    if (st != MOE_OK || R == 0) return st;
+    if ((st = check_weights(cfg, w)) != MOE_OK) return st;
+    if (!y_slots || !aligned(y_slots, 4) || (cfg->n_shared > 0 && (!y_shared || !aligned(y_shared, 4))))
+        return MOE_ERR_INVALID_ARG;
+    return gemm_impl(moe::kFfnFused, cfg, w, union_buf, R, y_slots, y_shared, ws,
                      reinterpret_cast<cudaStream_t>(stream));
 }
 

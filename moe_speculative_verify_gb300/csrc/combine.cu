@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const int32_t* __restrict__ ub,
                                                       UnionLayout L, int R, int H, int K, int S,
                                                       uint16_t* __restrict__ out) {
+    pdl_wait();
+    pdl_launch_dependents();
     const int r = blockIdx.x;
     const int h = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
     if (h >= H) return;
@@ -60,7 +62,9 @@ cudaError_t launch_combine(const float* y_slots, const float* y_shared, const fl
                            const int32_t* ub, const UnionLayout& L, int R, int H, int K, int S,
                            uint16_t* out, cudaStream_t stream) {
     dim3 grid(R, (H / 4 + 255) / 256);
-    combine_kernel<<<grid, 256, 0, stream>>>(y_slots, y_shared, wts, ub, L, R, H, K, S, out);
+    cudaError_t e = launch_pdl(combine_kernel, grid, dim3(256), 0, stream, y_slots, y_shared, wts, ub,
+                               L, R, H, K, S, out);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -9,7 +9,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/moe_verify.h"
+#include <utility>
+
+#include "moe_verify.h"
 
 namespace moe {
 
@@ -220,6 +222,19 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
 
 __device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31u) == 0u; }
 
+// ------------------------------------------- programmatic dependent launch ----
+// Every kernel of the layer is launched with programmatic stream
+// serialisation: it may start while the previous kernel of the stream is
+// finishing.  pdl_wait() blocks the calling thread until that kernel has
+// completed and its memory is visible; pdl_launch_dependents() lets the next
+// kernel start.  Each kernel triggers only after its own wait, so when a
+// kernel starts, every kernel two or more places before it has completed.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // -------------------------------------------------------------- formats ----
 // e4m3 (OCP e4m3fn) code of an fp32, round-to-nearest-even, saturating.
 __device__ __forceinline__ uint8_t to_e4m3(float v) {
@@ -234,6 +249,23 @@ __device__ __forceinline__ uint32_t to_e4m3x4(float v0, float v1, float v2, floa
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) {
     return __uint_as_float(b16 << 16);
+}
+
+// Host: launch `kernel` on `stream` with programmatic stream serialisation.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace moe

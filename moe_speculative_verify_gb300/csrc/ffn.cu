@@ -8,15 +8,22 @@
 // columns (FlashInfer commit).  MoE-Infinity #140: expert tensors
 // [gate_proj, up_proj, down_proj], output-major.
 //
-// One persistent kernel per GEMM.  Work = (item, 128-row block of the output
-// features); an item is up to NT gathered rows of one expert (union entry).
-// Swap-AB: the weight tile is the MMA's A operand (M = 128 output features),
-// the rows are the B operand (N = NT), so a verify batch of a few rows still
-// fills the 128-row MMA.  Per 128-wide K-block the MMA writes a fresh fp32
-// partial to tensor memory; the epilogue warps read it back and fold it into
-// fp32 register accumulators with the block's weight scale times the row's
-// activation scale (fp32 128x128 scales cannot be expressed in the MMA's own
-// block-scale format).
+// One persistent kernel, three modes: the gate/up GEMM alone, the down GEMM
+// alone, or both in one launch (Fused) over a single tile queue -- every
+// gate/up tile first, then every down tile -- so the SMs that finish their
+// gate/up work early go on with down tiles instead of idling.  A down tile
+// needs the whole h of its item: the item's gate/up tiles each release a
+// per-item counter after storing their block of h, and the down tile's
+// producer and epilogue acquire it (a bounded wait) before reading h.
+//
+// Work unit = (item, 128-row block of the output features); an item is up to
+// NT gathered rows of one expert (union entry).  Swap-AB: the weight tile is
+// the MMA's A operand (M = 128 output features), the rows are the B operand
+// (N = NT), so a verify batch of a few rows still fills the 128-row MMA.  Per
+// 128-wide K-block the MMA writes a fresh fp32 partial to tensor memory; the
+// epilogue warps read it back and fold it into fp32 register accumulators with
+// the block's weight scale times the row's activation scale (fp32 128x128
+// scales cannot be expressed in the MMA's own block-scale format).
 //
 // Warp roles (one CTA per SM):
 //   warp 0 lane 0: TMA producer -- weight tiles (evict-first) and row tiles
@@ -27,20 +34,21 @@
 //                  32*(w%4).. and 16 columns, promotes the partials, then
 //                  gate/up: h = silu(g) * u, per-row 1x128 e4m3 quantisation
 //                  of h, coalesced row stores; down: fp32 rows to their slot.
-// Every barrier wait is bounded; a timeout records MOE_ERR_TIMEOUT, winds the
-// roles down, drains in-flight copies and MMAs, frees tensor memory, returns.
+// Every wait is bounded; a timeout records MOE_ERR_TIMEOUT, winds the roles
+// down, drains in-flight copies and MMAs, frees tensor memory and returns.
 #include "common.cuh"
 #include "kernels.h"
 #include "layout.h"
 
 namespace moe {
 
-template <int NT, bool GU>
+template <int NT, int MODE>
 struct FfnCfg {
-    static constexpr int NA = GU ? 2 : 1;            // weight operands per stage
+    static constexpr int NA = (MODE == kFfnDown) ? 1 : 2;   // weight operands per stage (max)
     static constexpr int A_BYTES = 128 * 128;
+    static constexpr int B_OFF = NA * A_BYTES;
     static constexpr int B_BYTES = NT * 128;
-    static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;
+    static constexpr int STAGE_BYTES = B_OFF + B_BYTES;
     static constexpr int CSPLIT = NT / 16;
     static constexpr int EPI_WARPS = 4 * CSPLIT;
     static constexpr int EPI_THREADS = 32 * EPI_WARPS;
@@ -54,20 +62,22 @@ struct FfnCfg {
     static_assert(ACC_BUFS * ACC_COLS <= 512, "tensor memory");
 };
 
+constexpr int kMaxStages = 12;
+
 // Shared-memory carve-up, identical on host (size) and device (pointers).
 struct FfnSmem {
     int stages, sa, sw, red, tile, src, bars, tmem, flag, bytes;
 };
 
-__host__ __device__ inline FfnSmem ffn_smem(int nt, int na, int n_stages, int kb, int stage_bytes) {
+__host__ __device__ inline FfnSmem ffn_smem(int nt, int n_stages, int kbmax, int stage_bytes) {
     FfnSmem s;
     int b = 0;
     s.stages = b;
     b += n_stages * stage_bytes;
     s.sa = b;
-    b += nt * kb * 4;
+    b += nt * kbmax * 4;
     s.sw = b;
-    b += na * kb * 4;
+    b += 2 * kbmax * 4;
     s.red = b;
     b += 4 * nt * 4;
     s.tile = b;
@@ -99,22 +109,71 @@ __device__ __forceinline__ bool epi_bar_and(bool ok, int nthreads) {
     return r != 0;
 }
 
-template <int NT, bool GU>
-__global__ void __launch_bounds__(FfnCfg<NT, GU>::THREADS, 1)
-    ffn_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
-               const __grid_constant__ CUtensorMap map_sh0,
-               const __grid_constant__ CUtensorMap map_sh1,
-               const __grid_constant__ CUtensorMap map_b, const FfnArgs p) {
-    using C = FfnCfg<NT, GU>;
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Bounded wait until *ctr >= target (acquire).  False on timeout.
+__device__ __forceinline__ bool wait_counter(const int32_t* ctr, int target, int32_t* err,
+                                             uint64_t timeout_ns, volatile int* abort_flag) {
+    if (ld_acquire(ctr) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0; it < (1u << 28); ++it) {
+        __nanosleep(32);
+        if (ld_acquire(ctr) >= target) return true;
+        if ((it & 31u) == 31u && (*abort_flag || globaltimer_ns() - t0 > timeout_ns)) break;
+    }
+    record_error(err, MOE_ERR_TIMEOUT);
+    return false;
+}
+
+struct Tile {
+    int item, blk;
+    bool gu;
+};
+
+// Tile t of the queue: gate/up tiles (item-major, I/128 blocks each) first,
+// then down tiles (item-major, H/128 blocks each).
+__device__ __forceinline__ Tile tile_of(int t, int n_gu, int mb_i, int mb_h) {
+    Tile x;
+    if (t < n_gu) {
+        x.item = t / mb_i;
+        x.blk = t - x.item * mb_i;
+        x.gu = true;
+    } else {
+        t -= n_gu;
+        x.item = t / mb_h;
+        x.blk = t - x.item * mb_h;
+        x.gu = false;
+    }
+    return x;
+}
+
+template <int NT, int MODE>
+__global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
+    ffn_kernel(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUtensorMap map_u,
+               const __grid_constant__ CUtensorMap map_sg, const __grid_constant__ CUtensorMap map_su,
+               const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_d,
+               const __grid_constant__ CUtensorMap map_sd, const __grid_constant__ CUtensorMap map_h,
+               const FfnArgs p) {
+    using C = FfnCfg<NT, MODE>;
+    constexpr bool kFused = (MODE == kFfnFused);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const int KB = p.Kd / kBlock;
-    const int MB = p.M / kBlock;
-    const FfnSmem L = ffn_smem(NT, C::NA, p.n_stages, KB, C::STAGE_BYTES);
+    const int KB_H = p.H / kBlock, KB_I = p.I / kBlock;   // K-blocks of gate/up, of down
+    const int MB_I = p.I / kBlock, MB_H = p.H / kBlock;   // output blocks of gate/up, of down
+    const int KBMAX = (MODE == kFfnGateUp) ? KB_H : (MODE == kFfnDown) ? KB_I : max(KB_H, KB_I);
+    const FfnSmem L = ffn_smem(NT, p.n_stages, KBMAX, C::STAGE_BYTES);
     uint8_t* st_base = smem + L.stages;
-    float* s_sa = reinterpret_cast<float*>(smem + L.sa);     // [NT][KB]
-    float* s_sw = reinterpret_cast<float*>(smem + L.sw);     // [NA][KB]
+    float* s_sa = reinterpret_cast<float*>(smem + L.sa);     // [NT][KBMAX]
+    float* s_sw = reinterpret_cast<float*>(smem + L.sw);     // [2][KBMAX]
     float* s_red = reinterpret_cast<float*>(smem + L.red);   // [4][NT]
     uint8_t* s_tile = smem + L.tile;                         // [NT][128]
     int* s_src = reinterpret_cast<int*>(smem + L.src);       // [NT]
@@ -140,8 +199,14 @@ __global__ void __launch_bounds__(FfnCfg<NT, GU>::THREADS, 1)
         mbar_init(drain, 1);
         *s_abort = 0;
         fence_barrier_init();
-        prefetch_tensormap(&map_a0);
-        prefetch_tensormap(&map_b);
+        if (MODE != kFfnDown) {
+            prefetch_tensormap(&map_g);
+            prefetch_tensormap(&map_x);
+        }
+        if (MODE != kFfnGateUp) {
+            prefetch_tensormap(&map_d);
+            prefetch_tensormap(&map_h);
+        }
     }
     if (warp == 1) {
         tmem_alloc(s_tmem, C::TMEM_COLS);
@@ -152,10 +217,13 @@ __global__ void __launch_bounds__(FfnCfg<NT, GU>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
 
-    // Items must have been cut to this kernel's row tile.
+    // The union buffer comes from a kernel at least two launches back: it is
+    // complete when this kernel starts (see pdl_wait).  Items must have been
+    // cut to this kernel's row tile.
     const int n_items = (p.ub[4] == NT) ? p.ub[3] : 0;
     if (threadIdx.x == 0 && p.ub[4] != NT && p.ub[3] > 0) record_error(p.err, MOE_ERR_INVALID_ARG);
-    const int n_tiles = n_items * MB;
+    const int n_gu = (MODE == kFfnDown) ? 0 : n_items * MB_I;
+    const int n_tiles = n_gu + ((MODE == kFfnGateUp) ? 0 : n_items * MB_H);
     const int4* items = reinterpret_cast<const int4*>(p.ub + p.ul.items);
     uint32_t issued = 0;
 
@@ -165,35 +233,96 @@ __global__ void __launch_bounds__(FfnCfg<NT, GU>::THREADS, 1)
             const uint64_t pol = policy_evict_first();
             int stage = 0;
             uint32_t phase = 0;
-            for (int t = blockIdx.x; t < n_tiles && !*s_abort; t += gridDim.x) {
-                const int4 it = items[t / MB];
-                const int mb = t % MB;
+            auto a_load = [&](const Tile& tl, const int4& it, int kb, int s) {
                 const bool sh = it.x == p.E;
-                const CUtensorMap* m0 = sh ? &map_sh0 : &map_a0;
-                const CUtensorMap* m1 = sh ? &map_sh1 : &map_a1;
-                const int arow = (sh ? 0 : it.x) * p.M + mb * kBlock;
-                bool ok = true;
-                for (int kb = 0; kb < KB; ++kb) {
+                const int ex = sh ? 0 : it.x;
+                uint8_t* st = st_base + s * C::STAGE_BYTES;
+                if (tl.gu) {
+                    mbar_arrive_expect_tx(&full[s], 2 * C::A_BYTES + C::B_BYTES);
+                    const int arow = ex * p.I + tl.blk * kBlock;
+                    tma_load_2d_hint(st, sh ? &map_sg : &map_g, &full[s], kb * kBlock, arow, pol);
+                    tma_load_2d_hint(st + C::A_BYTES, sh ? &map_su : &map_u, &full[s], kb * kBlock,
+                                     arow, pol);
+                } else {
+                    mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::B_BYTES);
+                    const int arow = ex * p.H + tl.blk * kBlock;
+                    tma_load_2d_hint(st, sh ? &map_sd : &map_d, &full[s], kb * kBlock, arow, pol);
+                }
+            };
+            auto b_load = [&](const Tile& tl, const int4& it, int kb, int s) {
+                tma_load_2d(st_base + s * C::STAGE_BYTES + C::B_OFF, tl.gu ? &map_x : &map_h,
+                            &full[s], kb * kBlock, it.y);
+            };
+            auto next_stage = [&]() {
+                if (++stage == p.n_stages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            };
+            // Weights are inputs of the layer, not outputs of the previous
+            // kernel: the first tile's first weight tiles are requested before
+            // the wait on that kernel, its row tiles after.
+            const int t0 = blockIdx.x;
+            int pre = 0;
+            Tile tl0{0, 0, true};
+            int4 it0 = make_int4(0, 0, 0, 0);
+            if (t0 < n_tiles) {
+                tl0 = tile_of(t0, n_gu, MB_I, MB_H);
+                it0 = items[tl0.item];
+                pre = min(tl0.gu ? KB_H : KB_I, p.n_stages);
+                for (int kb = 0; kb < pre; ++kb) a_load(tl0, it0, kb, kb);
+            }
+            pdl_wait();
+            pdl_launch_dependents();
+            bool ok = true;
+            if (kFused && t0 < n_tiles && !tl0.gu) {
+                // the first tile is a down tile: its h comes from this launch
+                ok = wait_counter(p.ready + tl0.item, MB_I, p.err, p.timeout_ns, s_abort);
+                fence_proxy_async_global();
+            }
+            for (int kb = 0; kb < pre && ok; ++kb) b_load(tl0, it0, kb, kb);
+            issued = static_cast<uint32_t>(pre);
+            stage = pre % p.n_stages;
+            phase = (pre == p.n_stages) ? 1u : 0u;
+            for (int t = t0; t < n_tiles && ok && !*s_abort; t += gridDim.x) {
+                const Tile tl = tile_of(t, n_gu, MB_I, MB_H);
+                const int4 it = items[tl.item];
+                const int KB = tl.gu ? KB_H : KB_I;
+                int kb = (t == t0) ? pre : 0;
+                if (kFused && !tl.gu && t != t0) {
+                    // h of this item comes from other tiles of this launch: request
+                    // up to a ring of weight tiles, then wait for h, then its rows.
+                    int nd = 0, dst[kMaxStages];
+                    if (ld_acquire(p.ready + tl.item) < MB_I) {
+                        while (nd < KB && nd < p.n_stages) {
+                            if (!mbar_wait(&empty[stage], phase ^ 1u, p.err, p.timeout_ns)) {
+                                ok = false;
+                                break;
+                            }
+                            a_load(tl, it, nd, stage);
+                            dst[nd++] = stage;
+                            ++issued;
+                            next_stage();
+                        }
+                        if (ok && !wait_counter(p.ready + tl.item, MB_I, p.err, p.timeout_ns, s_abort))
+                            ok = false;
+                    }
+                    fence_proxy_async_global();
+                    for (int j = 0; j < nd && ok; ++j) b_load(tl, it, j, dst[j]);
+                    kb = nd;
+                }
+                for (; kb < KB && ok; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, p.err, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
-                    uint8_t* st = st_base + stage * C::STAGE_BYTES;
-                    tma_load_2d_hint(st, m0, &full[stage], kb * kBlock, arow, pol);
-                    if (GU) tma_load_2d_hint(st + C::A_BYTES, m1, &full[stage], kb * kBlock, arow, pol);
-                    tma_load_2d(st + C::NA * C::A_BYTES, &map_b, &full[stage], kb * kBlock, it.y);
+                    a_load(tl, it, kb, stage);
+                    b_load(tl, it, kb, stage);
                     ++issued;
-                    if (++stage == p.n_stages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!ok) {
-                    *s_abort = 1;
-                    break;
+                    next_stage();
                 }
             }
+            if (!ok) *s_abort = 1;
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -203,6 +332,8 @@ __global__ void __launch_bounds__(FfnCfg<NT, GU>::THREADS, 1)
             uint32_t phase = 0, aph = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+                const bool gu = t < n_gu;
+                const int KB = gu ? KB_H : KB_I;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (*s_abort || !mbar_wait(&acc_empty[ab], aph ^ 1u, p.err, p.timeout_ns) ||
                         !mbar_wait(&full[stage], phase, p.err, p.timeout_ns)) {
@@ -211,13 +342,13 @@ __global__ void __launch_bounds__(FfnCfg<NT, GU>::THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t a0 = smem_u32(st_base + stage * C::STAGE_BYTES);
-                    const uint32_t bb = a0 + C::NA * C::A_BYTES;
+                    const uint32_t bb = a0 + C::B_OFF;
                     const uint32_t d0 = tmem + ab * C::ACC_COLS;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         mma_e4m3(d0, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(bb + 32 * k), idesc,
                                  k > 0);
-                        if (GU)
+                        if (C::NA == 2 && gu)
                             mma_e4m3(d0 + NT, sdesc_k_sw128(a0 + C::A_BYTES + 32 * k),
                                      sdesc_k_sw128(bb + 32 * k), idesc, k > 0);
                     }
@@ -245,27 +376,44 @@ __global__ void __launch_bounds__(FfnCfg<NT, GU>::THREADS, 1)
         int ab = 0;
         uint32_t aph = 0;
         bool ok = true;
+        pdl_wait();   // row scales and outputs belong to the previous kernel
         for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-            const int4 it = items[t / MB];
-            const int mb = t % MB;
+            const Tile tl = tile_of(t, n_gu, MB_I, MB_H);
+            const int4 it = items[tl.item];
             const bool sh = it.x == p.E;
             const int ex = sh ? 0 : it.x;
             const int row0 = it.y, nrow = it.z;
+            const int KB = tl.gu ? KB_H : KB_I;
+            const int MB = tl.gu ? MB_I : MB_H;
             // previous tile's readers are done with the scale / tile buffers
             ok = epi_bar_and(ok, C::EPI_THREADS);
             if (!ok) break;
+            if (kFused && !tl.gu) {
+                // h and its scales come from this launch's gate/up tiles
+                if (et == 0 && !wait_counter(p.ready + tl.item, MB_I, p.err, p.timeout_ns, s_abort))
+                    ok = false;
+                ok = epi_bar_and(ok, C::EPI_THREADS);
+                if (!ok) break;
+                (void)ld_acquire(p.ready + tl.item);
+            }
+            const float* bs = tl.gu ? p.xs : p.hs;
             for (int i = et; i < NT * KB; i += C::EPI_THREADS) {
                 const int n = i / KB, kb = i - n * KB;
-                s_sa[i] = (n < nrow) ? p.bs[size_t(row0 + n) * KB + kb] : 0.0f;
+                s_sa[i] = (n < nrow) ? bs[size_t(row0 + n) * KB + kb] : 0.0f;
             }
-            for (int i = et; i < C::NA * KB; i += C::EPI_THREADS) {
-                const int a = i / KB, kb = i - a * KB;
-                const float* sp = (a == 0) ? (sh ? p.sh_s_a0 : p.s_a0) : (sh ? p.sh_s_a1 : p.s_a1);
-                s_sw[i] = sp[(size_t(ex) * MB + mb) * KB + kb];
-            }
-            if (!GU)
+            if (tl.gu) {
+                for (int i = et; i < 2 * KB; i += C::EPI_THREADS) {
+                    const int a = i / KB, kb = i - a * KB;
+                    const float* sp = (a == 0) ? (sh ? p.sh_s_gate : p.s_gate)
+                                               : (sh ? p.sh_s_up : p.s_up);
+                    s_sw[i] = sp[(size_t(ex) * MB + tl.blk) * KB + kb];
+                }
+            } else {
+                for (int i = et; i < KB; i += C::EPI_THREADS)
+                    s_sw[i] = (sh ? p.sh_s_down : p.s_down)[(size_t(ex) * MB + tl.blk) * KB + i];
                 for (int i = et; i < NT; i += C::EPI_THREADS)
                     s_src[i] = (i < nrow) ? p.ub[p.ul.src + row0 + i] : -1;
+            }
             ok = epi_bar_and(ok, C::EPI_THREADS);
             if (!ok) break;
 
@@ -286,25 +434,31 @@ __global__ void __launch_bounds__(FfnCfg<NT, GU>::THREADS, 1)
                                     ab * C::ACC_COLS + cg * 16;
                 float v0[16], v1[16];
                 tmem_ld16(ta, v0);
-                if (GU) tmem_ld16(ta + NT, v1);
+                if (C::NA == 2 && tl.gu) tmem_ld16(ta + NT, v1);
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[ab]);
                 const float w0 = s_sw[kb];
-                const float w1 = GU ? s_sw[KB + kb] : 0.0f;
+                if (C::NA == 2 && tl.gu) {
+                    const float w1 = s_sw[KB + kb];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float a = s_sa[(cg * 16 + j) * KB + kb];
-                    acc0[j] = fmaf(v0[j], w0 * a, acc0[j]);
-                    if (GU) acc1[j] = fmaf(v1[j], w1 * a, acc1[j]);
+                    for (int j = 0; j < 16; ++j) {
+                        const float a = s_sa[(cg * 16 + j) * KB + kb];
+                        acc0[j] = fmaf(v0[j], w0 * a, acc0[j]);
+                        acc1[j] = fmaf(v1[j], w1 * a, acc1[j]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        acc0[j] = fmaf(v0[j], w0 * s_sa[(cg * 16 + j) * KB + kb], acc0[j]);
                 }
                 if (++ab == C::ACC_BUFS) {
                     ab = 0;
                     aph ^= 1u;
                 }
             }
-            if (GU) {
+            if (C::NA == 2 && tl.gu) {
                 // h = silu(g) * u; per-row amax over the 128 features
                 float h[16];
 #pragma unroll
@@ -326,14 +480,24 @@ __global__ void __launch_bounds__(FfnCfg<NT, GU>::THREADS, 1)
                                              fmaxf(s_red[2 * NT + c], s_red[3 * NT + c]));
                     const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
                     s_tile[c * 128 + m] = to_e4m3(__fdiv_rn(h[j], sc));
-                    if (m == 0 && c < nrow) p.hs[size_t(row0 + c) * MB + mb] = sc;
+                    if (m == 0 && c < nrow) p.hs[size_t(row0 + c) * MB + tl.blk] = sc;
                 }
                 ok = epi_bar_and(ok, C::EPI_THREADS);
                 if (!ok) break;
                 for (int i = et; i < nrow * 8; i += C::EPI_THREADS) {
                     const int c = i >> 3, ch = i & 7;
-                    *reinterpret_cast<uint4*>(p.hq + size_t(row0 + c) * p.M + mb * kBlock + ch * 16) =
+                    *reinterpret_cast<uint4*>(p.hq + size_t(row0 + c) * p.I + tl.blk * kBlock + ch * 16) =
                         *reinterpret_cast<const uint4*>(s_tile + c * 128 + ch * 16);
+                }
+                if (kFused) {
+                    // release this block of h to the item's down tiles
+                    ok = epi_bar_and(ok, C::EPI_THREADS);
+                    if (!ok) break;
+                    if (et == 0) {
+                        fence_proxy_async_global();
+                        __threadfence();
+                        atomicAdd(p.ready + tl.item, 1);
+                    }
                 }
             } else {
 #pragma unroll
@@ -342,9 +506,9 @@ __global__ void __launch_bounds__(FfnCfg<NT, GU>::THREADS, 1)
                     if (ok && c < nrow) {
                         const int slot = s_src[c];
                         const int r = slot / p.KS, k = slot - r * p.KS;
-                        float* dst = (k < p.K) ? p.y_slots + (size_t(r) * p.K + k) * p.M
-                                               : p.y_shared + size_t(r) * p.M;
-                        dst[mb * kBlock + m] = acc0[j];
+                        float* dst = (k < p.K) ? p.y_slots + (size_t(r) * p.K + k) * p.H
+                                               : p.y_shared + size_t(r) * p.H;
+                        dst[tl.blk * kBlock + m] = acc0[j];
                     }
                 }
             }
@@ -375,44 +539,46 @@ __global__ void __launch_bounds__(FfnCfg<NT, GU>::THREADS, 1)
 }
 
 // ----------------------------------------------------------- launchers ----
-template <int NT, bool GU>
-static cudaError_t launch_ffn_t(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& sh0,
-                                const CUtensorMap& sh1, const CUtensorMap& b, FfnArgs args,
-                                int n_sms, int max_tiles, int smem_limit, cudaStream_t stream) {
-    using C = FfnCfg<NT, GU>;
-    const int KB = args.Kd / kBlock;
-    int stages = 12;
-    FfnSmem L = ffn_smem(NT, C::NA, stages, KB, C::STAGE_BYTES);
+template <int NT, int MODE>
+static cudaError_t launch_ffn_t(const FfnMaps& mp, FfnArgs args, int n_sms, int smem_limit,
+                                cudaStream_t stream) {
+    using C = FfnCfg<NT, MODE>;
+    const int KB_H = args.H / kBlock, KB_I = args.I / kBlock;
+    const int kbmax = (MODE == kFfnGateUp) ? KB_H : (MODE == kFfnDown) ? KB_I : max(KB_H, KB_I);
+    int stages = kMaxStages;
+    FfnSmem L = ffn_smem(NT, stages, kbmax, C::STAGE_BYTES);
     while (stages > 2 && L.bytes > smem_limit) {
         --stages;
-        L = ffn_smem(NT, C::NA, stages, KB, C::STAGE_BYTES);
+        L = ffn_smem(NT, stages, kbmax, C::STAGE_BYTES);
     }
     if (L.bytes > smem_limit) return cudaErrorInvalidConfiguration;
     args.n_stages = stages;
-    cudaError_t e = cudaFuncSetAttribute(ffn_kernel<NT, GU>,
+    cudaError_t e = cudaFuncSetAttribute(ffn_kernel<NT, MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L.bytes);
     if (e != cudaSuccess) return e;
-    const int grid = max(1, min(n_sms, max_tiles));
-    ffn_kernel<NT, GU><<<grid, C::THREADS, L.bytes, stream>>>(a0, a1, sh0, sh1, b, args);
+    e = launch_pdl(ffn_kernel<NT, MODE>, dim3(max(1, n_sms)), dim3(C::THREADS), L.bytes, stream,
+                   mp.g, mp.u, mp.sg, mp.su, mp.x, mp.d, mp.sd, mp.h, args);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-cudaError_t launch_ffn(int nt, bool gate_up, const CUtensorMap& a0, const CUtensorMap& a1,
-                       const CUtensorMap& sh0, const CUtensorMap& sh1, const CUtensorMap& b,
-                       const FfnArgs& args, int n_sms, int max_tiles, int smem_limit,
-                       cudaStream_t stream) {
-    if (gate_up) {
-        switch (nt) {
-            case 16: return launch_ffn_t<16, true>(a0, a1, sh0, sh1, b, args, n_sms, max_tiles, smem_limit, stream);
-            case 32: return launch_ffn_t<32, true>(a0, a1, sh0, sh1, b, args, n_sms, max_tiles, smem_limit, stream);
-            case 64: return launch_ffn_t<64, true>(a0, a1, sh0, sh1, b, args, n_sms, max_tiles, smem_limit, stream);
-        }
-    } else {
-        switch (nt) {
-            case 16: return launch_ffn_t<16, false>(a0, a1, sh0, sh1, b, args, n_sms, max_tiles, smem_limit, stream);
-            case 32: return launch_ffn_t<32, false>(a0, a1, sh0, sh1, b, args, n_sms, max_tiles, smem_limit, stream);
-            case 64: return launch_ffn_t<64, false>(a0, a1, sh0, sh1, b, args, n_sms, max_tiles, smem_limit, stream);
-        }
+template <int MODE>
+static cudaError_t launch_ffn_mode(int nt, const FfnMaps& mp, const FfnArgs& args, int n_sms,
+                                   int smem_limit, cudaStream_t stream) {
+    switch (nt) {
+        case 16: return launch_ffn_t<16, MODE>(mp, args, n_sms, smem_limit, stream);
+        case 32: return launch_ffn_t<32, MODE>(mp, args, n_sms, smem_limit, stream);
+        case 64: return launch_ffn_t<64, MODE>(mp, args, n_sms, smem_limit, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_ffn(int nt, int mode, const FfnMaps& mp, const FfnArgs& args, int n_sms,
+                       int smem_limit, cudaStream_t stream) {
+    switch (mode) {
+        case kFfnGateUp: return launch_ffn_mode<kFfnGateUp>(nt, mp, args, n_sms, smem_limit, stream);
+        case kFfnDown: return launch_ffn_mode<kFfnDown>(nt, mp, args, n_sms, smem_limit, stream);
+        case kFfnFused: return launch_ffn_mode<kFfnFused>(nt, mp, args, n_sms, smem_limit, stream);
     }
     return cudaErrorInvalidValue;
 }

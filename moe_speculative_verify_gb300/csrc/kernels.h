@@ -9,22 +9,35 @@
 
 namespace moe {
 
+// Modes of the persistent expert-GEMM kernel (ffn.cu).
+constexpr int kFfnGateUp = 0;   // gate/up GEMMs + SiLU*mul + h quantisation
+constexpr int kFfnDown = 1;     // down GEMM
+constexpr int kFfnFused = 2;    // both, one launch, one tile queue
+
+// Tensor maps of the expert GEMMs: gate, up, shared gate, shared up, gathered
+// rows x; down, shared down, quantised h.
+struct FfnMaps {
+    CUtensorMap g, u, sg, su, x, d, sd, h;
+};
+
 // Arguments of the persistent expert-GEMM kernel (ffn.cu).
 struct FfnArgs {
     const int32_t* ub;         // union buffer
     UnionLayout ul;
-    const float* s_a0;         // routed scales of A0 (gate or down) [E, M/128, Kd/128]
-    const float* s_a1;         // routed scales of A1 (up)
-    const float* sh_s_a0;      // shared-expert scales
-    const float* sh_s_a1;
-    const float* bs;           // row (B operand) scales [rows, Kd/128]
-    uint8_t* hq;               // gate/up: quantised h [rows, M]
-    float* hs;                 // gate/up: h scales [rows, M/128]
-    float* y_slots;            // down: [R*K, M]
-    float* y_shared;           // down: [R, M]
+    const float* s_gate;       // routed scales [E, I/128, H/128]
+    const float* s_up;
+    const float* sh_s_gate;    // shared-expert scales [S, I/128, H/128]
+    const float* sh_s_up;
+    const float* s_down;       // [E, H/128, I/128]
+    const float* sh_s_down;
+    const float* xs;           // gathered-row scales [rows, H/128]
+    uint8_t* hq;               // quantised h [rows, I]
+    float* hs;                 // h scales [rows, I/128]
+    float* y_slots;            // [R*K, H]
+    float* y_shared;           // [R, H]
+    int32_t* ready;            // [max_items] gate/up blocks of h finished (fused mode)
     int32_t* err;              // device error word
-    int M;                     // output features per expert
-    int Kd;                    // reduction length
+    int H, I;
     int E, K, KS;
     int n_stages;
     uint64_t timeout_ns;
@@ -37,11 +50,10 @@ cudaError_t launch_router(const uint16_t* x, const float* wr, const float* bias,
 cudaError_t launch_union(const int32_t* ids, int R, int E, int K, int S, int n_tile, int32_t* ub,
                          const UnionLayout& L, cudaStream_t stream);
 cudaError_t launch_dispatch(const uint16_t* x, const int32_t* ub, const UnionLayout& L, int R,
-                            int H, int KS, uint8_t* xg, float* xs, cudaStream_t stream);
-cudaError_t launch_ffn(int nt, bool gate_up, const CUtensorMap& a0, const CUtensorMap& a1,
-                       const CUtensorMap& sh0, const CUtensorMap& sh1, const CUtensorMap& b,
-                       const FfnArgs& args, int n_sms, int max_tiles, int smem_limit,
-                       cudaStream_t stream);
+                            int H, int KS, uint8_t* xg, float* xs, int32_t* ready, int n_ready,
+                            cudaStream_t stream);
+cudaError_t launch_ffn(int nt, int mode, const FfnMaps& mp, const FfnArgs& args, int n_sms,
+                       int smem_limit, cudaStream_t stream);
 cudaError_t launch_combine(const float* y_slots, const float* y_shared, const float* wts,
                            const int32_t* ub, const UnionLayout& L, int R, int H, int K, int S,
                            uint16_t* out, cudaStream_t stream);

@@ -49,16 +49,20 @@ inline UnionLayout union_layout(int32_t E, int32_t K, int32_t S, int32_t R) {
 
 // Scratch of the expert FFN stage (byte offsets from the workspace base).
 struct FfnLayout {
-    int64_t ctl, xg, xs, hq, hs, bytes;
-    int64_t rows;  // capacity in gathered rows
+    int64_t ctl, ready, xg, xs, hq, hs, bytes;
+    int64_t rows;       // capacity in gathered rows
+    int32_t n_ready;    // per-item counters of the fused GEMM
 };
 
-inline FfnLayout ffn_layout(int32_t H, int32_t I, int32_t K, int32_t S, int32_t R) {
+inline FfnLayout ffn_layout(int32_t H, int32_t I, int32_t E, int32_t K, int32_t S, int32_t R) {
     FfnLayout L;
     L.rows = round_up(int64_t(R) * (K + S), 64) + 64;
+    L.n_ready = union_layout(E, K, S, R).max_items;
     int64_t b = 0;
     L.ctl = b;
     b += 256;
+    L.ready = b;
+    b = round_up(b + int64_t(L.n_ready) * 4, 256);
     L.xg = b;
     b = round_up(b + L.rows * H, 256);
     L.xs = b;
@@ -82,7 +86,7 @@ struct LayerLayout {
 inline LayerLayout layer_layout(int32_t H, int32_t I, int32_t E, int32_t K, int32_t S,
                                 int32_t R) {
     LayerLayout L;
-    L.ffn = ffn_layout(H, I, K, S, R);
+    L.ffn = ffn_layout(H, I, E, K, S, R);
     L.un = union_layout(E, K, S, R);
     int64_t b = L.ffn.bytes;
     L.logits = b;

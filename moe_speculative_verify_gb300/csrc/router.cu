@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(512) router_logits_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ wr,
     const uint8_t* __restrict__ row_valid, int R, int H, int E, float* __restrict__ logits) {
     extern __shared__ float part[];  // [nchunks][EC][RT][32]
+    pdl_wait();
+    pdl_launch_dependents();
     const int nchunks = (H + 1023) / 1024;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e0 = blockIdx.x * EC;
@@ -81,6 +83,103 @@ __global__ void __launch_bounds__(512) router_logits_kernel(
 #pragma unroll
         for (int d = 16; d >= 1; d >>= 1) q = __fadd_rn(q, __shfl_xor_sync(0xFFFFFFFFu, q, d));
         if (lane == 0 && e < E && r < R && (row_valid == nullptr || row_valid[r] != 0))
+            logits[size_t(r) * E + e] = q;
+    }
+}
+
+// Large-R variant: a block computes a tile of 32 rows x 32 experts with 16
+// warps; the warp (wr, we) owns rows 8*wr.. and experts 8*we.. (64 pairs) and
+// lane l of the warp is lane l of the reduction tree for every one of them.
+// Per 128-column step the block stages x (bf16) and w (fp32) in shared memory;
+// a thread accumulates its 64 lane partials of the current 1024-column chunk in
+// registers (fma in column order), folds them into the per-lane chunk sums in
+// shared memory at the end of each chunk (q = p for the first chunk, then
+// q = q + p), and the warp finishes every pair with the xor butterfly: the same
+// IEEE operations in the same order as the small-R kernel.
+constexpr int kTileR = 32, kTileE = 32, kTileThreads = 512;
+
+__global__ void __launch_bounds__(kTileThreads, 1) router_logits_tiled_kernel(
+    const uint16_t* __restrict__ x, const float* __restrict__ wr,
+    const uint8_t* __restrict__ row_valid, int R, int H, int E, float* __restrict__ logits) {
+    extern __shared__ __align__(16) uint8_t rsm[];
+    uint16_t* xs = reinterpret_cast<uint16_t*>(rsm);                          // [2][32][128]
+    float* wsm = reinterpret_cast<float*>(rsm + 2 * kTileR * 128 * 2);        // [2][32][128]
+    float* qsm = wsm + 2 * kTileE * 128;                                      // [16 warps][64][32]
+    pdl_wait();
+    pdl_launch_dependents();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wrow = (warp >> 2) * 8, wexp = (warp & 3) * 8;
+    const int r0 = blockIdx.y * kTileR, e0 = blockIdx.x * kTileE;
+    const int steps = H / 128;
+
+    auto stage = [&](int i, int buf) {
+        // x tile: 32 rows x 128 bf16 = 512 x 16 bytes; w tile: 32 x 128 fp32 = 1024 x 16 bytes
+        {
+            const int row = tid >> 4, c = (tid & 15) * 8;
+            const int r = min(r0 + row, R - 1);
+            *reinterpret_cast<uint4*>(xs + (buf * kTileR + row) * 128 + c) =
+                __ldg(reinterpret_cast<const uint4*>(x + size_t(r) * H + i * 128 + c));
+        }
+        for (int q = tid; q < kTileE * 32; q += kTileThreads) {
+            const int ex = q >> 5, c = (q & 31) * 4;
+            const int e = min(e0 + ex, E - 1);
+            *reinterpret_cast<float4*>(wsm + (buf * kTileE + ex) * 128 + c) =
+                __ldg(reinterpret_cast<const float4*>(wr + size_t(e) * H + i * 128 + c));
+        }
+    };
+
+    float p[8][8];
+    stage(0, 0);
+    __syncthreads();
+    for (int i = 0; i < steps; ++i) {
+        const int buf = i & 1;
+        if (i + 1 < steps) stage(i + 1, buf ^ 1);
+        if ((i & 7) == 0) {
+#pragma unroll
+            for (int a = 0; a < 8; ++a)
+#pragma unroll
+                for (int b = 0; b < 8; ++b) p[a][b] = 0.0f;
+        }
+        float4 wv[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b)
+            wv[b] = *reinterpret_cast<const float4*>(wsm + (buf * kTileE + wexp + b) * 128 + 4 * lane);
+#pragma unroll
+        for (int a = 0; a < 8; ++a) {
+            const uint2 xv =
+                *reinterpret_cast<const uint2*>(xs + (buf * kTileR + wrow + a) * 128 + 4 * lane);
+            const float x0 = bf16_bits_to_f32(xv.x & 0xFFFFu), x1 = bf16_bits_to_f32(xv.x >> 16);
+            const float x2 = bf16_bits_to_f32(xv.y & 0xFFFFu), x3 = bf16_bits_to_f32(xv.y >> 16);
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                float q = p[a][b];
+                q = __fmaf_rn(x0, wv[b].x, q);
+                q = __fmaf_rn(x1, wv[b].y, q);
+                q = __fmaf_rn(x2, wv[b].z, q);
+                q = __fmaf_rn(x3, wv[b].w, q);
+                p[a][b] = q;
+            }
+        }
+        if ((i & 7) == 7 || i + 1 == steps) {   // end of a 1024-column chunk
+            float* qw = qsm + size_t(warp) * 64 * 32;
+            const bool first = (i < 8);
+#pragma unroll
+            for (int a = 0; a < 8; ++a)
+#pragma unroll
+                for (int b = 0; b < 8; ++b) {
+                    float* slot = qw + (a * 8 + b) * 32 + lane;
+                    *slot = first ? p[a][b] : __fadd_rn(*slot, p[a][b]);
+                }
+        }
+        __syncthreads();
+    }
+    const float* qw = qsm + size_t(warp) * 64 * 32;
+    for (int pair = 0; pair < 64; ++pair) {
+        float q = qw[pair * 32 + lane];
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1) q = __fadd_rn(q, __shfl_xor_sync(0xFFFFFFFFu, q, d));
+        const int r = r0 + wrow + pair / 8, e = e0 + wexp + pair % 8;
+        if (lane == 0 && r < R && e < E && (row_valid == nullptr || row_valid[r] != 0))
             logits[size_t(r) * E + e] = q;
     }
 }
@@ -151,6 +250,8 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(
     __shared__ float s_s[kSelWarps][MOE_MAX_EXPERTS];
     __shared__ float s_b[kSelWarps][MOE_MAX_EXPERTS];
     __shared__ int s_id[kSelWarps][MOE_MAX_TOPK];
+    pdl_wait();
+    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x * kSelWarps + warp;
     if (r >= R) return;
@@ -239,25 +340,26 @@ cudaError_t launch_router(const uint16_t* x, const float* wr, const float* bias,
         constexpr int RT = 8, EC = 1;
         dim3 grid(E / EC, (R + RT - 1) / RT);
         const size_t smem = size_t(nchunks) * EC * RT * 32 * sizeof(float);
-        router_logits_kernel<RT, EC><<<grid, threads, smem, stream>>>(x, wr, row_valid, R, H, E,
-                                                                      logits);
+        cudaError_t e = launch_pdl(router_logits_kernel<RT, EC>, grid, dim3(threads), smem, stream,
+                                   x, wr, row_valid, R, H, E, logits);
+        if (e != cudaSuccess) return e;
     } else {
-        constexpr int RT = 8, EC = 4;
-        dim3 grid((E + EC - 1) / EC, (R + RT - 1) / RT);
-        const size_t smem = size_t(nchunks) * EC * RT * 32 * sizeof(float);
-        if (smem > 48 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(router_logits_kernel<RT, EC>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 static_cast<int>(smem));
-            if (e != cudaSuccess) return e;
-        }
-        router_logits_kernel<RT, EC><<<grid, threads, smem, stream>>>(x, wr, row_valid, R, H, E,
-                                                                      logits);
+        dim3 grid((E + kTileE - 1) / kTileE, (R + kTileR - 1) / kTileR);
+        const size_t smem = size_t(2) * kTileR * 128 * 2 + size_t(2) * kTileE * 128 * 4 +
+                            size_t(kTileThreads / 32) * 64 * 32 * 4;
+        cudaError_t e = cudaFuncSetAttribute(router_logits_tiled_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(router_logits_tiled_kernel, grid, dim3(kTileThreads), smem, stream, x, wr,
+                       row_valid, R, H, E, logits);
+        if (e != cudaSuccess) return e;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    route_select_kernel<<<(R + kSelWarps - 1) / kSelWarps, kSelWarps * 32, 0, stream>>>(
-        logits, bias, row_valid, R, E, G, TG, K, scaling, ids, wts);
+    e = launch_pdl(route_select_kernel, dim3((R + kSelWarps - 1) / kSelWarps), dim3(kSelWarps * 32),
+                   0, stream, logits, bias, row_valid, R, E, G, TG, K, scaling, ids, wts);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

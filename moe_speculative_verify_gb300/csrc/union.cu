@@ -49,13 +49,16 @@ __global__ void __launch_bounds__(kUnionThreads) union_kernel(const int32_t* __r
                                                               UnionLayout L) {
     extern __shared__ uint32_t sm[];
     const int W = (R + 31) / 32;
-    uint32_t* bm = sm;                               // [E][W] row bitmaps
-    uint8_t* s_valid = reinterpret_cast<uint8_t*>(bm + size_t(E) * W);   // [R]
+    uint32_t* bm = sm;                                                   // [E][W] row bitmaps
+    uint16_t* wpre = reinterpret_cast<uint16_t*>(bm + size_t(E) * W);    // [E][W] rows before word
+    uint8_t* s_valid = reinterpret_cast<uint8_t*>(wpre + ((size_t(E) * W + 1) & ~size_t(1)));
     int* s_cnt = reinterpret_cast<int*>(s_valid + ((R + 15) & ~15));     // [E+1]
-    int* s_off = s_cnt + (E + 1);                    // [E+2]
-    int* s_ioff = s_off + (E + 2);                   // [E+1] first item of each entry
+    int* s_off = s_cnt + (E + 1);                                        // [E+2]
+    int* s_ioff = s_off + (E + 2);                                       // [E+1]
     __shared__ int s_warp[32];
-    __shared__ int s_total, s_err, s_nvalid;
+    __shared__ int s_total, s_err, s_nvalid, s_items, s_nunion;
+    pdl_wait();
+    pdl_launch_dependents();
     const int tid = threadIdx.x;
     const int KS = K + S;
 
@@ -84,68 +87,65 @@ __global__ void __launch_bounds__(kUnionThreads) union_kernel(const int32_t* __r
     }
     __syncthreads();
 
-    // 2. per-expert row bitmaps
+    // 2. per-expert row bitmaps (order-independent)
     for (int i = tid; i < R * K; i += kUnionThreads) {
         const int r = i / K;
         if (!s_valid[r]) continue;
-        const int e = ids[i];
-        atomicOr(&bm[size_t(e) * W + (r >> 5)], 1u << (r & 31));
+        atomicOr(&bm[size_t(ids[i]) * W + (r >> 5)], 1u << (r & 31));
     }
     __syncthreads();
 
-    // 3. counts
+    // 3. per-expert counts and per-word prefix counts
     for (int e = tid; e < E; e += kUnionThreads) {
         int c = 0;
-        for (int w = 0; w < W; ++w) c += __popc(bm[size_t(e) * W + w]);
+        for (int w = 0; w < W; ++w) {
+            wpre[size_t(e) * W + w] = static_cast<uint16_t>(c);
+            c += __popc(bm[size_t(e) * W + w]);
+        }
         s_cnt[e] = c;
     }
     if (tid == 0) s_cnt[E] = S ? s_nvalid : 0;
     __syncthreads();
 
-    // 4. offsets, union list, item offsets (shared entry's items first)
+    // 4. offsets (experts ascending, shared last), union list, item offsets
+    //    (the shared entry's items first), by block scans
+    const int cnt = (tid <= E) ? s_cnt[tid] : 0;
+    const int off = block_exclusive_scan(cnt, s_warp, &s_total);
+    if (tid <= E) s_off[tid] = off;
+    if (tid == E) s_off[E + 1] = off + cnt;
+    const int hit = (tid < E && cnt > 0) ? 1 : 0;
+    const int upos = block_exclusive_scan(hit, s_warp, &s_nunion);
+    if (hit) ub[L.ulist + upos] = tid;
+    const int entry = (tid == 0) ? E : tid - 1;          // item order: shared, 0, 1, ...
+    const int nit = (tid <= E) ? (s_cnt[entry] + n_tile - 1) / n_tile : 0;
+    const int ioff = block_exclusive_scan(nit, s_warp, &s_items);
+    if (tid <= E) s_ioff[entry] = ioff;
+    __syncthreads();
     if (tid == 0) {
-        s_off[0] = 0;
-        int u = 0;
-        for (int e = 0; e <= E; ++e) {
-            s_off[e + 1] = s_off[e] + s_cnt[e];
-            if (e < E && s_cnt[e] > 0) ub[L.ulist + u++] = e;
-        }
-        ub[L.ulist + u] = E;
-        int it = (s_cnt[E] + n_tile - 1) / n_tile;
-        s_ioff[E] = 0;
-        for (int e = 0; e < E; ++e) {
-            s_ioff[e] = it;
-            it += (s_cnt[e] + n_tile - 1) / n_tile;
-        }
-        ub[0] = u;
+        ub[L.ulist + s_nunion] = E;
+        ub[0] = s_nunion;
         ub[1] = s_nvalid;
         ub[2] = s_off[E + 1];
-        ub[3] = it;
+        ub[3] = s_items;
         ub[4] = n_tile;
         ub[5] = s_err;
         ub[6] = 0;
         ub[7] = 0;
     }
-    __syncthreads();
     for (int e = tid; e <= E; e += kUnionThreads) ub[L.counts + e] = s_cnt[e];
     for (int e = tid; e <= E + 1; e += kUnionThreads) ub[L.offsets + e] = s_off[e];
 
-    // 5. routed positions: expert e walks its bitmap in row order
-    for (int e = tid; e < E; e += kUnionThreads) {
-        int p = s_off[e];
-        for (int w = 0; w < W; ++w) {
-            uint32_t bits = bm[size_t(e) * W + w];
-            while (bits) {
-                const int b = __ffs(bits) - 1;
-                bits &= bits - 1;
-                const int r = w * 32 + b;
-                int k = 0;
-                while (ids[size_t(r) * K + k] != e) ++k;
-                ub[L.pos + r * KS + k] = p;
-                ub[L.src + p] = r * KS + k;
-                ++p;
-            }
-        }
+    // 5. routed positions: slot (r, k) of expert e goes after every slot of e
+    //    in an earlier row -- offsets[e] + (rows of e before r)
+    for (int i = tid; i < R * K; i += kUnionThreads) {
+        const int r = i / K, k = i - r * K;
+        if (!s_valid[r]) continue;
+        const int e = ids[i];
+        const int w = r >> 5;
+        const uint32_t below = bm[size_t(e) * W + w] & ((1u << (r & 31)) - 1u);
+        const int p = s_off[e] + wpre[size_t(e) * W + w] + __popc(below);
+        ub[L.pos + r * KS + k] = p;
+        ub[L.src + p] = r * KS + k;
     }
 
     // 6. shared positions (valid rows in row order) and pad rows
@@ -153,8 +153,7 @@ __global__ void __launch_bounds__(kUnionThreads) union_kernel(const int32_t* __r
     const int rb = tid * per;
     int local = 0;
     for (int r = rb; r < min(R, rb + per); ++r) local += s_valid[r];
-    const int rank0 = block_exclusive_scan(local, s_warp, &s_total);
-    int rank = rank0;
+    int rank = block_exclusive_scan(local, s_warp, &s_total);
     for (int r = rb; r < min(R, rb + per); ++r) {
         if (!s_valid[r]) {
             for (int k = 0; k < KS; ++k) ub[L.pos + r * KS + k] = -1;
@@ -186,7 +185,13 @@ __global__ void __launch_bounds__(256) dispatch_kernel(const uint16_t* __restric
                                                        const int32_t* __restrict__ ub, UnionLayout L,
                                                        int R, int H, int KS,
                                                        uint8_t* __restrict__ xg,
-                                                       float* __restrict__ xs) {
+                                                       float* __restrict__ xs,
+                                                       int32_t* __restrict__ ready, int n_ready) {
+    pdl_wait();
+    pdl_launch_dependents();
+    // the fused expert GEMM's per-item counters start at zero every call
+    if (blockIdx.x == 0 && blockIdx.y == 0)
+        for (int i = threadIdx.x; i < n_ready; i += blockDim.x) ready[i] = 0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x;
     const int HB = H / kBlock;
@@ -213,19 +218,26 @@ __global__ void __launch_bounds__(256) dispatch_kernel(const uint16_t* __restric
 cudaError_t launch_union(const int32_t* ids, int R, int E, int K, int S, int n_tile,
                          int32_t* ub, const UnionLayout& L, cudaStream_t stream) {
     const int W = (R + 31) / 32;
-    const size_t smem = size_t(E) * W * 4 + ((R + 15) & ~15) + size_t(4 * E + 8) * 4;
+    const size_t words = size_t(E) * W;
+    const size_t smem = words * 4 + ((words + 1) & ~size_t(1)) * 2 + ((R + 15) & ~15) +
+                        size_t(4 * E + 8) * 4;
     cudaError_t e = cudaFuncSetAttribute(union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    union_kernel<<<1, kUnionThreads, smem, stream>>>(ids, R, E, K, S, n_tile, ub, L);
+    e = launch_pdl(union_kernel, dim3(1), dim3(kUnionThreads), smem, stream, ids, R, E, K, S, n_tile,
+                   ub, L);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 cudaError_t launch_dispatch(const uint16_t* x, const int32_t* ub, const UnionLayout& L, int R,
-                            int H, int KS, uint8_t* xg, float* xs, cudaStream_t stream) {
+                            int H, int KS, uint8_t* xg, float* xs, int32_t* ready, int n_ready,
+                            cudaStream_t stream) {
     const int HB = H / kBlock;
     dim3 grid(R, (HB + 7) / 8);
-    dispatch_kernel<<<grid, 256, 0, stream>>>(x, ub, L, R, H, KS, xg, xs);
+    cudaError_t e = launch_pdl(dispatch_kernel, grid, dim3(256), 0, stream, x, ub, L, R, H, KS, xg, xs,
+                               ready, n_ready);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -141,6 +141,39 @@ def test_stepwise_entry_points():
     assert np.all(bf16_to_np(out)[~valid] == 0)
 
 
+@pytest.mark.parametrize("shape,R", [(synth.TINY, 8), (MEDIUM, 37), (MEDIUM, 200), (synth.TINY, 600)])
+def test_fused_gemms_match_two_launches(shape, R):
+    """moe_expert_gemms_fp8 (one persistent launch, down tiles gated by per-item
+    counters) gives the same bits as moe_gate_up_fp8 followed by moe_down_fp8."""
+    wl, t, h = _make(shape, R, pads=(1,) if R > 2 else ())
+    cfg = m.Config.from_shape(shape)
+    dev = torch.device("cuda")
+    K, H = shape.topk, shape.hidden
+    ids = torch.empty((R, K), dtype=torch.int32, device=dev)
+    w = torch.empty((R, K), dtype=torch.float32, device=dev)
+    logits = torch.empty((R, shape.n_experts), dtype=torch.float32, device=dev)
+    m.moe_route(cfg, t["x"], t["wr"], t["bias"], t["row_valid"], ids, w, logits)
+    ub = torch.zeros(m.moe_union_bytes(cfg, R) // 4, dtype=torch.int32, device=dev)
+    m.moe_build_union(cfg, ids, ub)
+    W = m.Weights.from_tensors(t)
+    outs = []
+    for fused in (True, False):
+        ws = torch.zeros(m.moe_ffn_workspace_bytes(cfg, R), dtype=torch.uint8, device=dev)
+        ys = torch.zeros((R * K, H), dtype=torch.float32, device=dev)
+        ysh = torch.zeros((R, H), dtype=torch.float32, device=dev)
+        m.moe_dispatch(cfg, t["x"], ub, ws)
+        if fused:
+            m.moe_expert_gemms_fp8(cfg, W, ub, R, ys, ysh, ws)
+        else:
+            m.moe_gate_up_fp8(cfg, W, ub, R, ws)
+            m.moe_down_fp8(cfg, W, ub, R, ys, ysh, ws)
+        torch.cuda.synchronize()
+        assert m.moe_get_device_error(ws) == 0
+        outs.append((ys.cpu().numpy(), ysh.cpu().numpy()))
+    assert np.array_equal(outs[0][0].view(np.uint32), outs[1][0].view(np.uint32))
+    assert np.array_equal(outs[0][1].view(np.uint32), outs[1][1].view(np.uint32))
+
+
 def test_pads_nan_zero_filled():
     wl, t, h = _make(synth.TINY, 16, pads=(0, 7, 15))
     cfg = m.Config.from_shape(synth.TINY)
