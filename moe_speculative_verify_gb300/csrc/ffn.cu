@@ -66,7 +66,7 @@ constexpr int kMaxStages = 12;
 
 // Shared-memory carve-up, identical on host (size) and device (pointers).
 struct FfnSmem {
-    int stages, sa, sw, red, tile, src, bars, tmem, flag, bytes;
+    int stages, sc, red, tile, src, bars, tmem, flag, bytes;
 };
 
 __host__ __device__ inline FfnSmem ffn_smem(int nt, int n_stages, int kbmax, int stage_bytes) {
@@ -74,10 +74,8 @@ __host__ __device__ inline FfnSmem ffn_smem(int nt, int n_stages, int kbmax, int
     int b = 0;
     s.stages = b;
     b += n_stages * stage_bytes;
-    s.sa = b;
-    b += nt * kbmax * 4;
-    s.sw = b;
-    b += 2 * kbmax * 4;
+    s.sc = b;
+    b += 2 * kbmax * nt * 4;
     s.red = b;
     b += 4 * nt * 4;
     s.tile = b;
@@ -172,8 +170,8 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
     const int KBMAX = (MODE == kFfnGateUp) ? KB_H : (MODE == kFfnDown) ? KB_I : max(KB_H, KB_I);
     const FfnSmem L = ffn_smem(NT, p.n_stages, KBMAX, C::STAGE_BYTES);
     uint8_t* st_base = smem + L.stages;
-    float* s_sa = reinterpret_cast<float*>(smem + L.sa);     // [NT][KBMAX]
-    float* s_sw = reinterpret_cast<float*>(smem + L.sw);     // [2][KBMAX]
+    // per-tile scale table: weight block scale x row scale, [operand][kb][n]
+    float* s_sc = reinterpret_cast<float*>(smem + L.sc);
     float* s_red = reinterpret_cast<float*>(smem + L.red);   // [4][NT]
     uint8_t* s_tile = smem + L.tile;                         // [NT][128]
     int* s_src = reinterpret_cast<int*>(smem + L.src);       // [NT]
@@ -397,23 +395,19 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
                 (void)ld_acquire(p.ready + tl.item);
             }
             const float* bs = tl.gu ? p.xs : p.hs;
-            for (int i = et; i < NT * KB; i += C::EPI_THREADS) {
-                const int n = i / KB, kb = i - n * KB;
-                s_sa[i] = (n < nrow) ? bs[size_t(row0 + n) * KB + kb] : 0.0f;
+            const int na = tl.gu ? 2 : 1;
+            for (int i = et; i < na * KB * NT; i += C::EPI_THREADS) {
+                const int a = i / (KB * NT), rem = i - a * (KB * NT);
+                const int kb = rem / NT, n = rem - kb * NT;
+                const float* sp = tl.gu ? ((a == 0) ? (sh ? p.sh_s_gate : p.s_gate)
+                                                    : (sh ? p.sh_s_up : p.s_up))
+                                        : (sh ? p.sh_s_down : p.s_down);
+                const float w = sp[(size_t(ex) * MB + tl.blk) * KB + kb];
+                s_sc[i] = (n < nrow) ? w * bs[size_t(row0 + n) * KB + kb] : 0.0f;
             }
-            if (tl.gu) {
-                for (int i = et; i < 2 * KB; i += C::EPI_THREADS) {
-                    const int a = i / KB, kb = i - a * KB;
-                    const float* sp = (a == 0) ? (sh ? p.sh_s_gate : p.s_gate)
-                                               : (sh ? p.sh_s_up : p.s_up);
-                    s_sw[i] = sp[(size_t(ex) * MB + tl.blk) * KB + kb];
-                }
-            } else {
-                for (int i = et; i < KB; i += C::EPI_THREADS)
-                    s_sw[i] = (sh ? p.sh_s_down : p.s_down)[(size_t(ex) * MB + tl.blk) * KB + i];
+            if (!tl.gu)
                 for (int i = et; i < NT; i += C::EPI_THREADS)
                     s_src[i] = (i < nrow) ? p.ub[p.ul.src + row0 + i] : -1;
-            }
             ok = epi_bar_and(ok, C::EPI_THREADS);
             if (!ok) break;
 
@@ -439,19 +433,36 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[ab]);
-                const float w0 = s_sw[kb];
-                if (C::NA == 2 && tl.gu) {
-                    const float w1 = s_sw[KB + kb];
+                float sc0[16];
+                {
+                    const float4* q4 = reinterpret_cast<const float4*>(s_sc + kb * NT + cg * 16);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float a = s_sa[(cg * 16 + j) * KB + kb];
-                        acc0[j] = fmaf(v0[j], w0 * a, acc0[j]);
-                        acc1[j] = fmaf(v1[j], w1 * a, acc1[j]);
+                    for (int v = 0; v < 4; ++v) {
+                        const float4 t4 = q4[v];
+                        sc0[4 * v] = t4.x;
+                        sc0[4 * v + 1] = t4.y;
+                        sc0[4 * v + 2] = t4.z;
+                        sc0[4 * v + 3] = t4.w;
+                    }
+                }
+                if (C::NA == 2 && tl.gu) {
+                    const float4* q4 =
+                        reinterpret_cast<const float4*>(s_sc + (KB + kb) * NT + cg * 16);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const float4 t4 = q4[v];
+                        acc0[4 * v] = fmaf(v0[4 * v], sc0[4 * v], acc0[4 * v]);
+                        acc0[4 * v + 1] = fmaf(v0[4 * v + 1], sc0[4 * v + 1], acc0[4 * v + 1]);
+                        acc0[4 * v + 2] = fmaf(v0[4 * v + 2], sc0[4 * v + 2], acc0[4 * v + 2]);
+                        acc0[4 * v + 3] = fmaf(v0[4 * v + 3], sc0[4 * v + 3], acc0[4 * v + 3]);
+                        acc1[4 * v] = fmaf(v1[4 * v], t4.x, acc1[4 * v]);
+                        acc1[4 * v + 1] = fmaf(v1[4 * v + 1], t4.y, acc1[4 * v + 1]);
+                        acc1[4 * v + 2] = fmaf(v1[4 * v + 2], t4.z, acc1[4 * v + 2]);
+                        acc1[4 * v + 3] = fmaf(v1[4 * v + 3], t4.w, acc1[4 * v + 3]);
                     }
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        acc0[j] = fmaf(v0[j], w0 * s_sa[(cg * 16 + j) * KB + kb], acc0[j]);
+                    for (int j = 0; j < 16; ++j) acc0[j] = fmaf(v0[j], sc0[j], acc0[j]);
                 }
                 if (++ab == C::ACC_BUFS) {
                     ab = 0;

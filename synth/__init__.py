@@ -83,6 +83,9 @@ WORKLOADS = {
     "profile8": Workload("profile8", GLM52_E32, rows=8,
                          note="8 rows on 32 experts of the GLM-5.2 shape, for profiler "
                               "captures"),
+    "profile1024": Workload("profile1024", GLM52_E32, rows=1024,
+                            note="1024 rows on 32 experts of the GLM-5.2 shape (256 rows per "
+                                 "expert, the 64-row tile): prefill-like profiler captures"),
 }
 
 
