@@ -44,9 +44,12 @@ namespace moe {
 
 template <int NT, int MODE>
 struct FfnCfg {
-    static constexpr int NA = (MODE == kFfnDown) ? 1 : 2;   // weight operands per stage (max)
+    // One stage = one 128x128 weight tile + the item's 128-column row tile; a
+    // gate/up K-block takes two stages (gate, then up), a down K-block one, so
+    // both phases share one uniform ring.
+    static constexpr int NA = (MODE == kFfnDown) ? 1 : 2;   // weight operands per K-block (max)
     static constexpr int A_BYTES = 128 * 128;
-    static constexpr int B_OFF = NA * A_BYTES;
+    static constexpr int B_OFF = A_BYTES;
     static constexpr int B_BYTES = NT * 128;
     static constexpr int STAGE_BYTES = B_OFF + B_BYTES;
     static constexpr int CSPLIT = NT / 16;
@@ -62,7 +65,7 @@ struct FfnCfg {
     static_assert(ACC_BUFS * ACC_COLS <= 512, "tensor memory");
 };
 
-constexpr int kMaxStages = 12;
+constexpr int kMaxStages = 16;
 
 // Shared-memory carve-up, identical on host (size) and device (pointers).
 struct FfnSmem {
@@ -231,23 +234,24 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
             const uint64_t pol = policy_evict_first();
             int stage = 0;
             uint32_t phase = 0;
-            auto a_load = [&](const Tile& tl, const int4& it, int kb, int s) {
+            // Stage j of a tile: gate/up tiles alternate gate and up weight
+            // tiles per K-block (j = 2*kb + {0, 1}); down tiles one per K-block.
+            auto a_load = [&](const Tile& tl, const int4& it, int j, int s) {
                 const bool sh = it.x == p.E;
                 const int ex = sh ? 0 : it.x;
                 uint8_t* st = st_base + s * C::STAGE_BYTES;
+                mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
                 if (tl.gu) {
-                    mbar_arrive_expect_tx(&full[s], 2 * C::A_BYTES + C::B_BYTES);
-                    const int arow = ex * p.I + tl.blk * kBlock;
-                    tma_load_2d_hint(st, sh ? &map_sg : &map_g, &full[s], kb * kBlock, arow, pol);
-                    tma_load_2d_hint(st + C::A_BYTES, sh ? &map_su : &map_u, &full[s], kb * kBlock,
-                                     arow, pol);
+                    const CUtensorMap* m = (j & 1) ? (sh ? &map_su : &map_u) : (sh ? &map_sg : &map_g);
+                    tma_load_2d_hint(st, m, &full[s], (j >> 1) * kBlock, ex * p.I + tl.blk * kBlock,
+                                     pol);
                 } else {
-                    mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::B_BYTES);
-                    const int arow = ex * p.H + tl.blk * kBlock;
-                    tma_load_2d_hint(st, sh ? &map_sd : &map_d, &full[s], kb * kBlock, arow, pol);
+                    tma_load_2d_hint(st, sh ? &map_sd : &map_d, &full[s], j * kBlock,
+                                     ex * p.H + tl.blk * kBlock, pol);
                 }
             };
-            auto b_load = [&](const Tile& tl, const int4& it, int kb, int s) {
+            auto b_load = [&](const Tile& tl, const int4& it, int j, int s) {
+                const int kb = tl.gu ? (j >> 1) : j;
                 tma_load_2d(st_base + s * C::STAGE_BYTES + C::B_OFF, tl.gu ? &map_x : &map_h,
                             &full[s], kb * kBlock, it.y);
             };
@@ -267,8 +271,8 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
             if (t0 < n_tiles) {
                 tl0 = tile_of(t0, n_gu, MB_I, MB_H);
                 it0 = items[tl0.item];
-                pre = min(tl0.gu ? KB_H : KB_I, p.n_stages);
-                for (int kb = 0; kb < pre; ++kb) a_load(tl0, it0, kb, kb);
+                pre = min(tl0.gu ? 2 * KB_H : KB_I, p.n_stages);
+                for (int j = 0; j < pre; ++j) a_load(tl0, it0, j, j);
             }
             pdl_wait();
             pdl_launch_dependents();
@@ -278,21 +282,25 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
                 ok = wait_counter(p.ready + tl0.item, MB_I, p.err, p.timeout_ns, s_abort);
                 fence_proxy_async_global();
             }
-            for (int kb = 0; kb < pre && ok; ++kb) b_load(tl0, it0, kb, kb);
+            for (int j = 0; j < pre && ok; ++j) b_load(tl0, it0, j, j);
             issued = static_cast<uint32_t>(pre);
             stage = pre % p.n_stages;
             phase = (pre == p.n_stages) ? 1u : 0u;
+            // the next tile's descriptor is fetched one tile ahead
+            int4 it_next = it0;
             for (int t = t0; t < n_tiles && ok && !*s_abort; t += gridDim.x) {
                 const Tile tl = tile_of(t, n_gu, MB_I, MB_H);
-                const int4 it = items[tl.item];
-                const int KB = tl.gu ? KB_H : KB_I;
-                int kb = (t == t0) ? pre : 0;
+                const int4 it = it_next;
+                const int tn = t + gridDim.x;
+                if (tn < n_tiles) it_next = items[tile_of(tn, n_gu, MB_I, MB_H).item];
+                const int NS = tl.gu ? 2 * KB_H : KB_I;
+                int j = (t == t0) ? pre : 0;
                 if (kFused && !tl.gu && t != t0) {
                     // h of this item comes from other tiles of this launch: request
                     // up to a ring of weight tiles, then wait for h, then its rows.
                     int nd = 0, dst[kMaxStages];
                     if (ld_acquire(p.ready + tl.item) < MB_I) {
-                        while (nd < KB && nd < p.n_stages) {
+                        while (nd < NS && nd < p.n_stages) {
                             if (!mbar_wait(&empty[stage], phase ^ 1u, p.err, p.timeout_ns)) {
                                 ok = false;
                                 break;
@@ -306,16 +314,16 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
                             ok = false;
                     }
                     fence_proxy_async_global();
-                    for (int j = 0; j < nd && ok; ++j) b_load(tl, it, j, dst[j]);
-                    kb = nd;
+                    for (int q = 0; q < nd && ok; ++q) b_load(tl, it, q, dst[q]);
+                    j = nd;
                 }
-                for (; kb < KB && ok; ++kb) {
+                for (; j < NS && ok; ++j) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, p.err, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
-                    a_load(tl, it, kb, stage);
-                    b_load(tl, it, kb, stage);
+                    a_load(tl, it, j, stage);
+                    b_load(tl, it, j, stage);
                     ++issued;
                     next_stage();
                 }
@@ -332,30 +340,33 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
                 const bool gu = t < n_gu;
                 const int KB = gu ? KB_H : KB_I;
-                for (int kb = 0; kb < KB; ++kb) {
-                    if (*s_abort || !mbar_wait(&acc_empty[ab], aph ^ 1u, p.err, p.timeout_ns) ||
-                        !mbar_wait(&full[stage], phase, p.err, p.timeout_ns)) {
+                for (int kb = 0; kb < KB && ok; ++kb) {
+                    if (*s_abort || !mbar_wait(&acc_empty[ab], aph ^ 1u, p.err, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const uint32_t a0 = smem_u32(st_base + stage * C::STAGE_BYTES);
-                    const uint32_t bb = a0 + C::B_OFF;
                     const uint32_t d0 = tmem + ab * C::ACC_COLS;
+                    for (int op = 0; op < (gu ? 2 : 1); ++op) {
+                        if (!mbar_wait(&full[stage], phase, p.err, p.timeout_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a0 = smem_u32(st_base + stage * C::STAGE_BYTES);
+                        const uint32_t bb = a0 + C::B_OFF;
+                        const uint32_t d = d0 + op * NT;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        mma_e4m3(d0, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(bb + 32 * k), idesc,
-                                 k > 0);
-                        if (C::NA == 2 && gu)
-                            mma_e4m3(d0 + NT, sdesc_k_sw128(a0 + C::A_BYTES + 32 * k),
-                                     sdesc_k_sw128(bb + 32 * k), idesc, k > 0);
+                        for (int k = 0; k < 4; ++k)
+                            mma_e4m3(d, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(bb + 32 * k), idesc,
+                                     k > 0);
+                        mma_commit(&empty[stage]);
+                        if (++stage == p.n_stages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
-                    mma_commit(&empty[stage]);
+                    if (!ok) break;
                     mma_commit(&acc_full[ab]);
-                    if (++stage == p.n_stages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
                     if (++ab == C::ACC_BUFS) {
                         ab = 0;
                         aph ^= 1u;
@@ -396,14 +407,15 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
             }
             const float* bs = tl.gu ? p.xs : p.hs;
             const int na = tl.gu ? 2 : 1;
-            for (int i = et; i < na * KB * NT; i += C::EPI_THREADS) {
-                const int a = i / (KB * NT), rem = i - a * (KB * NT);
-                const int kb = rem / NT, n = rem - kb * NT;
+            // read row-major (kb fastest: coalesced), store [operand][kb][n]
+            for (int i = et; i < na * NT * KB; i += C::EPI_THREADS) {
+                const int a = i / (NT * KB), rem = i - a * (NT * KB);
+                const int n = rem / KB, kb = rem - n * KB;
                 const float* sp = tl.gu ? ((a == 0) ? (sh ? p.sh_s_gate : p.s_gate)
                                                     : (sh ? p.sh_s_up : p.s_up))
                                         : (sh ? p.sh_s_down : p.s_down);
                 const float w = sp[(size_t(ex) * MB + tl.blk) * KB + kb];
-                s_sc[i] = (n < nrow) ? w * bs[size_t(row0 + n) * KB + kb] : 0.0f;
+                s_sc[(a * KB + kb) * NT + n] = (n < nrow) ? w * bs[size_t(row0 + n) * KB + kb] : 0.0f;
             }
             if (!tl.gu)
                 for (int i = et; i < NT; i += C::EPI_THREADS)
@@ -530,16 +542,24 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
     __syncthreads();
     if (*s_abort) {
         // Wind down: let every copy this CTA issued land and every MMA finish
-        // before the CTA releases tensor memory and exits.
+        // before the CTA releases tensor memory and exits.  A stage whose row
+        // tile was never requested cannot complete its barrier, so the copies
+        // get one shared budget of kDrainNs (they land within microseconds).
+        constexpr uint64_t kDrainNs = 2000000;   // 2 ms
         if (threadIdx.x == 0) {
+            const uint64_t t0 = globaltimer_ns();
             const uint32_t first = issued > static_cast<uint32_t>(p.n_stages)
                                        ? issued - static_cast<uint32_t>(p.n_stages) : 0u;
-            for (uint32_t i = first; i < issued; ++i)
-                mbar_wait(&full[i % p.n_stages], (i / p.n_stages) & 1u, nullptr, p.timeout_ns);
+            for (uint32_t i = first; i < issued; ++i) {
+                const uint64_t used = globaltimer_ns() - t0;
+                if (used >= kDrainNs) break;
+                mbar_wait(&full[i % p.n_stages], (i / p.n_stages) & 1u, nullptr, kDrainNs - used);
+            }
+            while (globaltimer_ns() - t0 < kDrainNs / 4) __nanosleep(1000);
         }
         if (threadIdx.x == 32) {
             mma_commit(drain);
-            mbar_wait(drain, 0, nullptr, p.timeout_ns);
+            mbar_wait(drain, 0, nullptr, kDrainNs);
         }
         __syncthreads();
     }

@@ -39,31 +39,48 @@ __global__ void __launch_bounds__(512) router_logits_kernel(
         for (int a = 0; a < EC; ++a)
 #pragma unroll
             for (int b = 0; b < RT; ++b) p[a][b] = 0.0f;
-        const int h_end = min(H, (c + 1) * 1024);
-        for (int h0 = c * 1024; h0 < h_end; h0 += 128) {
-            const int h = h0 + 4 * lane;
-            float4 w4[EC];
+        const int nsteps = min(8, (H - c * 1024) / 128);   // 128-column steps of this chunk
+        // Loads of four steps are issued together, then consumed in column
+        // order: the fma sequence per lane is unchanged.
 #pragma unroll
-            for (int a = 0; a < EC; ++a) {
-                const int e = min(e0 + a, E - 1);
-                w4[a] = __ldg(reinterpret_cast<const float4*>(wr + size_t(e) * H + h));
+        for (int s0 = 0; s0 < 8; s0 += 4) {
+            float4 w4[4][EC];
+            uint2 xv[4][RT];
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                if (s0 + s < nsteps) {
+                    const int h = c * 1024 + (s0 + s) * 128 + 4 * lane;
+#pragma unroll
+                    for (int a = 0; a < EC; ++a) {
+                        const int e = min(e0 + a, E - 1);
+                        w4[s][a] = __ldg(reinterpret_cast<const float4*>(wr + size_t(e) * H + h));
+                    }
+#pragma unroll
+                    for (int b = 0; b < RT; ++b) {
+                        const int r = min(r0 + b, R - 1);
+                        xv[s][b] = __ldg(reinterpret_cast<const uint2*>(x + size_t(r) * H + h));
+                    }
+                }
             }
 #pragma unroll
-            for (int b = 0; b < RT; ++b) {
-                const int r = min(r0 + b, R - 1);
-                const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + size_t(r) * H + h));
-                const float x0 = bf16_bits_to_f32(xv.x & 0xFFFFu);
-                const float x1 = bf16_bits_to_f32(xv.x >> 16);
-                const float x2 = bf16_bits_to_f32(xv.y & 0xFFFFu);
-                const float x3 = bf16_bits_to_f32(xv.y >> 16);
+            for (int s = 0; s < 4; ++s) {
+                if (s0 + s < nsteps) {
 #pragma unroll
-                for (int a = 0; a < EC; ++a) {
-                    float q = p[a][b];
-                    q = __fmaf_rn(x0, w4[a].x, q);
-                    q = __fmaf_rn(x1, w4[a].y, q);
-                    q = __fmaf_rn(x2, w4[a].z, q);
-                    q = __fmaf_rn(x3, w4[a].w, q);
-                    p[a][b] = q;
+                    for (int b = 0; b < RT; ++b) {
+                        const float x0 = bf16_bits_to_f32(xv[s][b].x & 0xFFFFu);
+                        const float x1 = bf16_bits_to_f32(xv[s][b].x >> 16);
+                        const float x2 = bf16_bits_to_f32(xv[s][b].y & 0xFFFFu);
+                        const float x3 = bf16_bits_to_f32(xv[s][b].y >> 16);
+#pragma unroll
+                        for (int a = 0; a < EC; ++a) {
+                            float q = p[a][b];
+                            q = __fmaf_rn(x0, w4[s][a].x, q);
+                            q = __fmaf_rn(x1, w4[s][a].y, q);
+                            q = __fmaf_rn(x2, w4[s][a].z, q);
+                            q = __fmaf_rn(x3, w4[s][a].w, q);
+                            p[a][b] = q;
+                        }
+                    }
                 }
             }
         }

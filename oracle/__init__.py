@@ -59,6 +59,7 @@ def lib() -> C.CDLL:
         L.orc_moe_layer.argtypes = [C.POINTER(_Cfg)] + [P] * 15 + [P, C.c_int32, P,
                                                                    C.c_int32, P, P, P, P,
                                                                    C.c_int32]
+        L.orc_greedy_verify.argtypes = [P, C.c_int32, C.c_int32, P, P, C.c_int32, P, P, P]
         L.orc_num_threads.restype = C.c_int
         L.orc_set_num_threads.argtypes = [C.c_int]
         _LIB = L
@@ -223,3 +224,23 @@ def moe_layer(cfg, t: dict, rows=None, acc64: bool = True):
                         0 if rl is None else rl.size, _p(out), _p(ids), _p(wts), _p(y),
                         1 if acc64 else 0)
     return {"out": out, "ids": ids, "wts": wts, "y_acc": y}
+
+
+# ----------------------------------------------------- greedy verify + accept --
+def greedy_verify(logits, draft, n_draft):
+    """Spans of 8 rows: returns (accept_len [n_span], out [n_span*8], argmax [R]).
+
+    logits: fp32 [R, V] or bf16 bit patterns (uint16) [R, V]; draft int32 [R];
+    n_draft int32 [n_span] (drafts in each span, 0..7)."""
+    lg = np.ascontiguousarray(logits)
+    is_bf16 = 1 if lg.dtype == np.uint16 else 0
+    if not is_bf16:
+        lg = _c(lg, np.float32)
+    R, V = lg.shape
+    n_span = R // 8
+    acc = np.empty(n_span, dtype=np.int32)
+    out = np.empty(R, dtype=np.int32)
+    am = np.empty(R, dtype=np.int32)
+    lib().orc_greedy_verify(_p(lg), is_bf16, V, _p(_c(draft, np.int32)), _p(_c(n_draft, np.int32)),
+                            n_span, _p(acc), _p(out), _p(am))
+    return acc, out, am

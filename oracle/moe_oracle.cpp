@@ -545,4 +545,48 @@ void orc_moe_layer(const orc_config* cfg, const uint16_t* x, const float* wr, co
     }
 }
 
+// ------------------------------------------------- greedy verify + accept ----
+// Speculative verify of spans of 8 rows (openinfer #610 "What": 1 committed
+// token + up to 7 drafts per span; pypto-serving #223 "What this adds": accept
+// the longest matching prefix plus the bonus prediction, 1..8 tokens per step;
+// mstar #388: greedy verify run on the device).  Span q covers rows
+// 8q .. 8q+7; row 0 of the span holds the committed token's position, row j
+// (1 <= j <= n_draft[q]) the j-th draft.  The target's greedy token at row j is
+// argmax_v logits[8q+j, v] (ties to the lower index) and predicts the token
+// after row j.  Draft j (draft[8q+j]) is accepted when every draft before it
+// was and draft[8q+j] == argmax(row j-1).  With m drafts accepted the span
+// emits draft_1 .. draft_m and then the bonus argmax(row m): accept_len = m+1
+// tokens, out[8q .. 8q+m], the rest of the span's out set to -1.
+// logits_is_bf16 != 0: logits are bf16 bit patterns, else fp32.
+void orc_greedy_verify(const void* logits, int32_t logits_is_bf16, int32_t V,
+                       const int32_t* draft, const int32_t* n_draft, int32_t n_span,
+                       int32_t* accept_len, int32_t* out, int32_t* argmax_out) {
+    const int S = 8;
+    std::vector<int32_t> am(size_t(n_span) * S);
+    for (int r = 0; r < n_span * S; ++r) {
+        int best = 0;
+        float bv = 0.0f;
+        for (int v = 0; v < V; ++v) {
+            float x = logits_is_bf16
+                          ? bf16_to_f32(static_cast<const uint16_t*>(logits)[size_t(r) * V + v])
+                          : static_cast<const float*>(logits)[size_t(r) * V + v];
+            if (v == 0 || x > bv) {
+                bv = x;
+                best = v;
+            }
+        }
+        am[r] = best;
+        if (argmax_out) argmax_out[r] = best;
+    }
+    for (int q = 0; q < n_span; ++q) {
+        const int nd = std::max(0, std::min(S - 1, int(n_draft[q])));
+        int m = 0;
+        while (m < nd && draft[q * S + m + 1] == am[q * S + m]) ++m;
+        for (int j = 0; j < S; ++j) out[q * S + j] = -1;
+        for (int j = 0; j < m; ++j) out[q * S + j] = draft[q * S + j + 1];
+        out[q * S + m] = am[q * S + m];
+        accept_len[q] = m + 1;
+    }
+}
+
 }  // extern "C"

@@ -45,6 +45,10 @@ class LayerShape:
 
 GLM52 = LayerShape(hidden=6144, inter=2048, n_experts=256, n_groups=8, topk_groups=4,
                    topk=8, n_shared=1, routed_scaling=2.5)
+# GLM-5.2 router shape (hidden 6144, 256 experts, top-8 of top-4 groups) with
+# 128-wide experts: the small kernels at their real size, for profiler captures
+GLM52_ROUTER = LayerShape(hidden=6144, inter=128, n_experts=256, n_groups=8, topk_groups=4,
+                          topk=8, n_shared=1, routed_scaling=2.5)
 # GLM-5.2 expert shape with 32 experts: the small case for full profiler captures
 # (about 1.2 GB of weights: above L2, a few GB on the device at most)
 GLM52_E32 = LayerShape(hidden=6144, inter=2048, n_experts=32, n_groups=4, topk_groups=2,
@@ -83,6 +87,10 @@ WORKLOADS = {
     "profile8": Workload("profile8", GLM52_E32, rows=8,
                          note="8 rows on 32 experts of the GLM-5.2 shape, for profiler "
                               "captures"),
+    "profile8r": Workload("profile8r", GLM52_ROUTER, rows=8, routing="hot", hot_per_group=10,
+                          hot_delta=1.0,
+                          note="verify8's routing at 128-wide experts, for profiler captures of "
+                               "the router, union, dispatch and combine kernels"),
     "profile1024": Workload("profile1024", GLM52_E32, rows=1024,
                             note="1024 rows on 32 experts of the GLM-5.2 shape (256 rows per "
                                  "expert, the 64-row tile): prefill-like profiler captures"),
