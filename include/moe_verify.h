@@ -302,6 +302,33 @@ moe_status_t moe_layer_noalloc(const moe_config_t* cfg, const void* x_bf16,
                                moe_stream_t stream);
 
 /*
+ * moe_greedy_verify -- greedy verify and acceptance of speculative spans on
+ * the device (openinfer #610 "What": spans of 8 rows, 1 committed token + up to
+ * 7 drafts; pypto-serving #223 "What this adds": accept the longest matching
+ * prefix plus the bonus prediction, 1..8 tokens per step; mstar #388: the
+ * verify runs on the device inside the step).
+ *   logits       fp32 (logits_bf16 == 0) or bf16 [R, V]: the target model's
+ *                logits at every row of every span
+ *   R            rows, a multiple of 8 (span q = rows 8q .. 8q+7), <= 65536
+ *   draft        int32 [R]: draft[8q + j] is span q's draft j (1 <= j <= 7);
+ *                row 0's entry of a span is not read
+ *   n_draft      int32 [R/8]: drafts present in span q (clamped to 0..7)
+ *   argmax_out   int32 [R] (out): the target's greedy token of every row --
+ *                the largest logit, the lowest index on ties, NaN never chosen
+ *                (a row of NaN gives 0)
+ *   accept_len   int32 [R/8] (out): 1 + the number of accepted drafts
+ *   out_tokens   int32 [R] (out): per span the accepted drafts, then the bonus
+ *                token, then -1 in the remaining slots
+ * Draft j is accepted when every draft before it was and it equals the greedy
+ * token of row j-1; the bonus is the greedy token of the row after the last
+ * accepted draft.  V >= 1; pointers 4-byte aligned (logits 16-byte aligned
+ * rows are read with vector loads when V * element size is a multiple of 16).
+ */
+moe_status_t moe_greedy_verify(const void* logits, int32_t logits_bf16, int32_t V, int32_t R,
+                               const int32_t* draft, const int32_t* n_draft, int32_t* argmax_out,
+                               int32_t* accept_len, int32_t* out_tokens, moe_stream_t stream);
+
+/*
  * moe_get_device_error -- synchronises `stream`, then reads (and clears when
  * `clear` != 0) the device error word at the start of a workspace given to
  * moe_expert_ffn_fp8 or moe_layer.  Returns MOE_OK, MOE_ERR_TIMEOUT (a bounded

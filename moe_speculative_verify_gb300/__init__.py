@@ -21,7 +21,8 @@ __all__ = [
     "moe_expert_ffn_fp8", "moe_combine", "moe_layer", "moe_union_bytes",
     "moe_ffn_workspace_bytes", "moe_workspace_bytes", "moe_get_device_error",
     "moe_diag_wait_timeout", "moe_status_string", "moe_dispatch", "moe_gate_up_fp8",
-    "moe_down_fp8", "ffn_layout", "moe_layer_noalloc", "moe_expert_gemms_fp8", "union_layout", "rows_per_item",
+    "moe_down_fp8", "ffn_layout", "moe_layer_noalloc", "moe_expert_gemms_fp8",
+    "moe_greedy_verify", "union_layout", "rows_per_item",
     "MOE_MAX_ROWS",
 ]
 
@@ -97,10 +98,11 @@ def load() -> C.CDLL:
     L.moe_expert_gemms_fp8.argtypes = [cfg, C.POINTER(Weights), P, I32, P, P, P, SZ, P]
     L.moe_layer.argtypes = [cfg, P, P, P, C.POINTER(Weights), P, I32, P, P, P, P, SZ, P]
     L.moe_get_device_error.argtypes = [P, I32, P]
+    L.moe_greedy_verify.argtypes = [P, I32, I32, I32, P, P, P, P, P, P]
     L.moe_layer_noalloc.argtypes = [cfg, P, P, P, C.POINTER(Weights), P, I32, P, P, P, P, P]
     L.moe_diag_wait_timeout.argtypes = [P, C.c_uint32, P]
     for n in ("moe_route", "moe_build_union", "moe_expert_ffn_fp8", "moe_combine", "moe_layer",
-              "moe_get_device_error", "moe_diag_wait_timeout", "moe_dispatch", "moe_layer_noalloc",
+              "moe_get_device_error", "moe_diag_wait_timeout", "moe_dispatch", "moe_layer_noalloc", "moe_greedy_verify",
               "moe_gate_up_fp8", "moe_down_fp8", "moe_expert_gemms_fp8"):
         getattr(L, n).restype = C.c_int
     _LIB = L
@@ -211,6 +213,15 @@ def moe_layer_noalloc(cfg: Config, x, w_router, bias, weights: Weights, row_vali
                                     C.byref(weights), _ptr(row_valid), R, _ptr(out),
                                     _ptr(topk_ids), _ptr(topk_w), _ptr(device_status),
                                     _stream(stream)), "moe_layer_noalloc")
+
+
+def moe_greedy_verify(logits, draft, n_draft, argmax_out, accept_len, out_tokens,
+                      stream=None) -> None:
+    """Greedy verify of spans of 8 rows; logits fp32 or bf16 [R, V] on the device."""
+    R, V = logits.shape
+    _check(load().moe_greedy_verify(_ptr(logits), 1 if logits.dtype == torch.bfloat16 else 0, V, R,
+                                    _ptr(draft), _ptr(n_draft), _ptr(argmax_out), _ptr(accept_len),
+                                    _ptr(out_tokens), _stream(stream)), "moe_greedy_verify")
 
 
 def moe_get_device_error(ws, clear: bool = True, stream=None) -> int:

@@ -421,6 +421,22 @@ moe_status_t moe_layer(const moe_config_t* cfg, const void* x_bf16, const float*
     return combine_impl(cfg, y_slots, y_shared, wts, ub, R, out_bf16, s);
 }
 
+moe_status_t moe_greedy_verify(const void* logits, int32_t logits_bf16, int32_t V, int32_t R,
+                               const int32_t* draft, const int32_t* n_draft, int32_t* argmax_out,
+                               int32_t* accept_len, int32_t* out_tokens, moe_stream_t stream) {
+    if (R < 0 || (R % 8) != 0 || V < 1) return MOE_ERR_INVALID_ARG;
+    if (R > 65536) return MOE_ERR_UNSUPPORTED;
+    if (R == 0) return MOE_OK;
+    if (!logits || !draft || !n_draft || !argmax_out || !accept_len || !out_tokens)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(logits, logits_bf16 ? 2 : 4) || !aligned(draft, 4) || !aligned(n_draft, 4) ||
+        !aligned(argmax_out, 4) || !aligned(accept_len, 4) || !aligned(out_tokens, 4))
+        return MOE_ERR_INVALID_ARG;
+    return cuda_status(moe::launch_greedy_verify(logits, logits_bf16 != 0, V, R, draft, n_draft,
+                                                 argmax_out, accept_len, out_tokens,
+                                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_get_device_error(void* ws, int32_t clear, moe_stream_t stream) {
     if (!ws || !aligned(ws, 4)) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -563,20 +563,24 @@ void orc_greedy_verify(const void* logits, int32_t logits_is_bf16, int32_t V,
                        int32_t* accept_len, int32_t* out, int32_t* argmax_out) {
     const int S = 8;
     std::vector<int32_t> am(size_t(n_span) * S);
+    // argmax: the first index of the largest value; NaN never wins (a row of
+    // NaN gives index 0).  READING: the pages do not say how ties or NaN are
+    // treated; the first maximal index is numpy's and torch's CPU convention.
     for (int r = 0; r < n_span * S; ++r) {
-        int best = 0;
+        int best = -1;
         float bv = 0.0f;
         for (int v = 0; v < V; ++v) {
             float x = logits_is_bf16
                           ? bf16_to_f32(static_cast<const uint16_t*>(logits)[size_t(r) * V + v])
                           : static_cast<const float*>(logits)[size_t(r) * V + v];
-            if (v == 0 || x > bv) {
+            if (std::isnan(x)) continue;
+            if (best < 0 || x > bv) {
                 bv = x;
                 best = v;
             }
         }
-        am[r] = best;
-        if (argmax_out) argmax_out[r] = best;
+        am[r] = best < 0 ? 0 : best;
+        if (argmax_out) argmax_out[r] = am[r];
     }
     for (int q = 0; q < n_span; ++q) {
         const int nd = std::max(0, std::min(S - 1, int(n_draft[q])));

@@ -22,12 +22,17 @@ def test_argmax_ties_and_dtypes(orc):
     V = 1000
     lg = rng.normal(0, 1, (16, V)).astype(np.float32)
     lg[3, [5, 900]] = 50.0                    # a tie: the lower index wins
+    lg[4, 0] = np.nan                         # NaN never wins
+    lg[5, :] = np.nan                         # an all-NaN row gives index 0
+    lg[6, :] = -np.inf
     _, _, am = orc.greedy_verify(lg, np.zeros(16, np.int32), np.zeros(2, np.int32))
-    assert np.array_equal(am, np.argmax(lg, axis=1)) and am[3] == 5
+    ref = np.argmax(np.where(np.isnan(lg), -np.inf, lg), axis=1)
+    assert np.array_equal(am, ref) and am[3] == 5 and am[5] == 0 and am[6] == 0
     bf = torch.from_numpy(lg).to(torch.bfloat16)
     bits = bf.view(torch.int16).numpy().view(np.uint16)
     _, _, am2 = orc.greedy_verify(bits, np.zeros(16, np.int32), np.zeros(2, np.int32))
-    assert np.array_equal(am2, np.argmax(bf.float().numpy(), axis=1))
+    f = bf.float().numpy()
+    assert np.array_equal(am2, np.argmax(np.where(np.isnan(f), -np.inf, f), axis=1))
 
 
 def test_acceptance_every_m(orc):
