@@ -56,8 +56,10 @@ struct FfnCfg {
     static constexpr int EPI_WARPS = 4 * CSPLIT;
     static constexpr int EPI_THREADS = 32 * EPI_WARPS;
     static constexpr int THREADS = 64 + EPI_THREADS;
-    static constexpr int ACC_BUFS = 4;
     static constexpr int ACC_COLS = NA * NT;
+    // as many tensor-memory partials as fit (at most 16): the MMA may run that
+    // many K-blocks ahead of the epilogue across its tile transitions
+    static constexpr int ACC_BUFS = (512 / ACC_COLS) < 16 ? (512 / ACC_COLS) : 16;
     static constexpr int TMEM_COLS = (ACC_BUFS * ACC_COLS <= 32) ? 32
                                      : (ACC_BUFS * ACC_COLS <= 64) ? 64
                                      : (ACC_BUFS * ACC_COLS <= 128) ? 128
@@ -87,7 +89,7 @@ __host__ __device__ inline FfnSmem ffn_smem(int nt, int n_stages, int kbmax, int
     b += nt * 4;
     b = (b + 7) & ~7;
     s.bars = b;
-    b += (2 * n_stages + 2 * 8 + 1) * 8;
+    b += (2 * n_stages + 2 * 16 + 1) * 8;
     s.tmem = b;
     b += 4;
     s.flag = b;
@@ -181,8 +183,8 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
     uint64_t* empty = full + p.n_stages;
     uint64_t* acc_full = empty + p.n_stages;
-    uint64_t* acc_empty = acc_full + 8;
-    uint64_t* drain = acc_empty + 8;
+    uint64_t* acc_empty = acc_full + 16;
+    uint64_t* drain = acc_empty + 16;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L.tmem);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L.flag);
 
