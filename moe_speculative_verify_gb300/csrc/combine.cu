@@ -32,24 +32,33 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
         return;
     }
     const float* w = wts + size_t(r) * K;
-    float4 y = __ldg(reinterpret_cast<const float4*>(y_slots + size_t(r) * K * H + h));
-    const float w0 = w[0];
-    float a0 = __fmul_rn(w0, y.x), a1 = __fmul_rn(w0, y.y), a2 = __fmul_rn(w0, y.z),
-          a3 = __fmul_rn(w0, y.w);
-    for (int k = 1; k < K; ++k) {
-        const float wk = w[k];
-        y = __ldg(reinterpret_cast<const float4*>(y_slots + (size_t(r) * K + k) * H + h));
-        a0 = __fmaf_rn(wk, y.x, a0);
-        a1 = __fmaf_rn(wk, y.y, a1);
-        a2 = __fmaf_rn(wk, y.z, a2);
-        a3 = __fmaf_rn(wk, y.w, a3);
+    // every slot's row is requested before the fixed-order accumulation
+    float4 y[MOE_MAX_TOPK + 1];
+    float wk[MOE_MAX_TOPK];
+#pragma unroll
+    for (int k = 0; k < MOE_MAX_TOPK; ++k) {
+        if (k < K) {
+            y[k] = __ldg(reinterpret_cast<const float4*>(y_slots + (size_t(r) * K + k) * H + h));
+            wk[k] = w[k];
+        }
+    }
+    if (S) y[MOE_MAX_TOPK] = __ldg(reinterpret_cast<const float4*>(y_shared + size_t(r) * H + h));
+    float a0 = __fmul_rn(wk[0], y[0].x), a1 = __fmul_rn(wk[0], y[0].y),
+          a2 = __fmul_rn(wk[0], y[0].z), a3 = __fmul_rn(wk[0], y[0].w);
+#pragma unroll
+    for (int k = 1; k < MOE_MAX_TOPK; ++k) {
+        if (k < K) {
+            a0 = __fmaf_rn(wk[k], y[k].x, a0);
+            a1 = __fmaf_rn(wk[k], y[k].y, a1);
+            a2 = __fmaf_rn(wk[k], y[k].z, a2);
+            a3 = __fmaf_rn(wk[k], y[k].w, a3);
+        }
     }
     if (S) {
-        y = __ldg(reinterpret_cast<const float4*>(y_shared + size_t(r) * H + h));
-        a0 = __fadd_rn(a0, y.x);
-        a1 = __fadd_rn(a1, y.y);
-        a2 = __fadd_rn(a2, y.z);
-        a3 = __fadd_rn(a3, y.w);
+        a0 = __fadd_rn(a0, y[MOE_MAX_TOPK].x);
+        a1 = __fadd_rn(a1, y[MOE_MAX_TOPK].y);
+        a2 = __fadd_rn(a2, y[MOE_MAX_TOPK].z);
+        a3 = __fadd_rn(a3, y[MOE_MAX_TOPK].w);
     }
     const uint32_t b0 = __bfloat16_as_ushort(__float2bfloat16_rn(a0));
     const uint32_t b1 = __bfloat16_as_ushort(__float2bfloat16_rn(a1));

@@ -257,16 +257,16 @@ __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
 // ------------------------------------------------------ grouped top-k ----
 // One warp per row: sigmoid scores, biased scores, group scores (sum of the
 // two largest biased scores), the topk_groups best groups, the topk best
-// experts inside them, and the normalised weights.
+// experts inside them, and the normalised weights.  Lane l holds experts
+// l, l+32, l+64, ...; every reduction is over exact comparisons (no
+// arithmetic), so its order does not matter.
 constexpr int kSelWarps = 8;
+constexpr int kPer = MOE_MAX_EXPERTS / 32;
 
 __global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(
     const float* __restrict__ logits, const float* __restrict__ bias,
     const uint8_t* __restrict__ row_valid, int R, int E, int G, int TG, int K, float scaling,
     int32_t* __restrict__ ids, float* __restrict__ wts) {
-    __shared__ float s_s[kSelWarps][MOE_MAX_EXPERTS];
-    __shared__ float s_b[kSelWarps][MOE_MAX_EXPERTS];
-    __shared__ int s_id[kSelWarps][MOE_MAX_TOPK];
     pdl_wait();
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -279,70 +279,95 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(
         }
         return;
     }
-    float* sv = s_s[warp];
-    float* bv = s_b[warp];
-    for (int e = lane; e < E; e += 32) {
-        const float s = router_sigmoid(logits[size_t(r) * E + e]);
-        sv[e] = s;
-        bv[e] = __fadd_rn(s, bias[e]);
-    }
-    __syncwarp();
-
-    // group scores: lane g scans its group
     const int epg = E / G;
-    uint64_t gkey = 0;
-    if (lane < G) {
-        float t1 = -INFINITY, t2 = -INFINITY;
-        for (int i = 0; i < epg; ++i) {
-            const float v = bv[lane * epg + i];
-            if (v > t1) {
-                t2 = t1;
-                t1 = v;
-            } else if (v > t2) {
-                t2 = v;
-            }
-        }
-        const float gs = (epg >= 2) ? __fadd_rn(t1, t2) : t1;
-        gkey = rank_key(gs, lane);
-    }
-    uint32_t gmask = 0;
-    for (int t = 0; t < TG; ++t) {
-        const uint64_t best = warp_max_u64(gkey);
-        const int g = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFu));
-        gmask |= 1u << g;
-        if (lane == g) gkey = 0;
-    }
-
-    // expert keys of the lane's experts inside the kept groups
-    constexpr int kPer = MOE_MAX_EXPERTS / 32;
-    uint64_t ekey[kPer];
+    float sv[kPer], bv[kPer];
+    float lg[kPer], bi[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
         const int e = lane + 32 * j;
-        ekey[j] = (e < E && ((gmask >> (e / epg)) & 1u)) ? rank_key(bv[e], e) : 0ull;
+        lg[j] = (e < E) ? logits[size_t(r) * E + e] : 0.0f;
+        bi[j] = (e < E) ? bias[e] : 0.0f;
     }
-    for (int k = 0; k < K; ++k) {
-        uint64_t mine = 0;
 #pragma unroll
-        for (int j = 0; j < kPer; ++j) mine = ekey[j] > mine ? ekey[j] : mine;
-        const uint64_t best = warp_max_u64(mine);
-        const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFu));
-        if ((e & 31) == lane) {
+    for (int j = 0; j < kPer; ++j) {
+        sv[j] = router_sigmoid(lg[j]);
+        bv[j] = __fadd_rn(sv[j], bi[j]);
+    }
+
+    // group scores: per group, the two largest biased scores, merged over the warp
+    float gscore_mine = -INFINITY;               // lane g keeps group g's score
+    for (int g = 0; g < G; ++g) {
+        float t1 = -INFINITY, t2 = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int e = lane + 32 * j;
+            if (e < E && e / epg == g) {
+                const float v = bv[j];
+                if (v > t1) {
+                    t2 = t1;
+                    t1 = v;
+                } else if (v > t2) {
+                    t2 = v;
+                }
+            }
+        }
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1) {
+            const float o1 = __shfl_xor_sync(0xFFFFFFFFu, t1, d);
+            const float o2 = __shfl_xor_sync(0xFFFFFFFFu, t2, d);
+            const float hi = fmaxf(t1, o1), lo = fminf(t1, o1);
+            t2 = fmaxf(lo, fmaxf(t2, o2));
+            t1 = hi;
+        }
+        if (lane == g) gscore_mine = (epg >= 2) ? __fadd_rn(t1, t2) : t1;
+    }
+    // the topk_groups best groups: rank of each group among all (ties: lower id)
+    const uint64_t gkey = (lane < G) ? rank_key(gscore_mine, lane) : 0ull;
+    int grank = 0;
+    for (int g = 0; g < G; ++g) grank += (__shfl_sync(0xFFFFFFFFu, gkey, g) > gkey) ? 1 : 0;
+    const uint32_t gmask = __ballot_sync(0xFFFFFFFFu, lane < G && grank < TG);
+
+    // the topk best experts of the kept groups: K rounds of a warp-wide max of
+    // the ordered score, then the lowest id among the lanes holding it
+    uint32_t vkey[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int e = lane + 32 * j;
+        vkey[j] = (e < E && ((gmask >> (e / epg)) & 1u)) ? ordered_key(bv[j]) : 0u;
+    }
+    int my_id = -1;       // lane k keeps the k-th chosen expert
+    float my_s = 0.0f;
+    for (int k = 0; k < K; ++k) {
+        uint32_t bk = 0u, bid = 0xFFFFFFFFu;
+#pragma unroll
+        for (int j = 0; j < kPer; ++j)
+            if (vkey[j] > bk) {
+                bk = vkey[j];
+                bid = static_cast<uint32_t>(lane + 32 * j);
+            }
+        const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, bk);
+        const uint32_t e = __reduce_min_sync(0xFFFFFFFFu, (bk == top) ? bid : 0xFFFFFFFFu);
+        float s_e = 0.0f;
+        if ((e & 31u) == static_cast<uint32_t>(lane)) {
 #pragma unroll
             for (int j = 0; j < kPer; ++j)
-                if (lane + 32 * j == e) ekey[j] = 0;
+                if (static_cast<uint32_t>(lane + 32 * j) == e) {
+                    vkey[j] = 0u;
+                    s_e = sv[j];
+                }
         }
-        if (lane == 0) s_id[warp][k] = e;
+        s_e = __shfl_sync(0xFFFFFFFFu, s_e, static_cast<int>(e & 31u));
+        if (lane == k) {
+            my_id = static_cast<int>(e);
+            my_s = s_e;
+        }
     }
-    __syncwarp();
-    if (lane == 0) {
-        float den = sv[s_id[warp][0]];
-        for (int k = 1; k < K; ++k) den = __fadd_rn(den, sv[s_id[warp][k]]);
-        for (int k = 0; k < K; ++k) {
-            const int e = s_id[warp][k];
-            ids[size_t(r) * K + k] = e;
-            wts[size_t(r) * K + k] = __fmul_rn(__fdiv_rn(sv[e], den), scaling);
-        }
+    // weights: the denominator summed in k order, then every lane its own w_k
+    float den = __shfl_sync(0xFFFFFFFFu, my_s, 0);
+    for (int k = 1; k < K; ++k) den = __fadd_rn(den, __shfl_sync(0xFFFFFFFFu, my_s, k));
+    if (lane < K) {
+        ids[size_t(r) * K + lane] = my_id;
+        wts[size_t(r) * K + lane] = __fmul_rn(__fdiv_rn(my_s, den), scaling);
     }
 }
 
