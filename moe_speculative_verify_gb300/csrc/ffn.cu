@@ -30,8 +30,9 @@
 //                  into an n_stages ring of shared-memory stages;
 //   warp 1 lane 0: MMA issuer -- 4 x tcgen05.mma (K = 32) per operand per
 //                  K-block into a ring of ACC_BUFS tensor-memory partials;
-//   warps 2.. : epilogue -- 4 * NT/16 warps; warp w reads TMEM lanes
-//                  32*(w%4).. and 16 columns, promotes the partials, then
+//   warps 2.. : epilogue -- 4 * NT/CW warps; warp w reads TMEM lanes
+//                  32*(w%4).. and CW columns (16, or 32 at 64-row tiles),
+//                  promotes the partials, then
 //                  gate/up: h = silu(g) * u, per-row 1x128 e4m3 quantisation
 //                  of h, coalesced row stores; down: fp32 rows to their slot.
 // Every wait is bounded; a timeout records MOE_ERR_TIMEOUT, winds the roles
@@ -52,10 +53,15 @@ struct FfnCfg {
     static constexpr int B_OFF = A_BYTES;
     static constexpr int B_BYTES = NT * 128;
     static constexpr int STAGE_BYTES = B_OFF + B_BYTES;
-    static constexpr int CSPLIT = NT / 16;
+    static constexpr int CW = (NT >= 64) ? 32 : 16;           // columns per epilogue warp
+    static constexpr int CSPLIT = NT / CW;
     static constexpr int EPI_WARPS = 4 * CSPLIT;
     static constexpr int EPI_THREADS = 32 * EPI_WARPS;
     static constexpr int THREADS = 64 + EPI_THREADS;
+    // registers per thread for one block per SM: 64K registers over the
+    // block's warps, in steps of 8, at most 255
+    static constexpr int MAX_REGS_RAW = (65536 / THREADS) / 8 * 8;
+    static constexpr int MAX_REGS = MAX_REGS_RAW > 255 ? 255 : MAX_REGS_RAW;
     static constexpr int ACC_COLS = NA * NT;
     // as many tensor-memory partials as fit (at most 16): the MMA may run that
     // many K-blocks ahead of the epilogue across its tile transitions
@@ -139,27 +145,37 @@ __device__ __forceinline__ bool wait_counter(const int32_t* ctr, int target, int
 struct Tile {
     int item, blk;
     bool gu;
+    bool shared_w;   // the weight tile is read by several items (row chunks)
 };
 
-// Tile t of the queue: gate/up tiles (item-major, I/128 blocks each) first,
-// then down tiles (item-major, H/128 blocks each).
-__device__ __forceinline__ Tile tile_of(int t, int n_gu, int mb_i, int mb_h) {
+// Tile t of the queue: gate/up tiles first, then down tiles.  Within a phase
+// the order is entry-major, then output block, then row chunk: every row chunk
+// of an expert that uses the same weight tile sits on adjacent tiles, so they
+// run at the same time on neighbouring CTAs and the weight tile comes from
+// DRAM once.  An item's w word holds its entry's first item * 1024 + items.
+__device__ __forceinline__ Tile tile_of(int t, int n_gu, int mb_i, int mb_h,
+                                        const int4* __restrict__ items) {
     Tile x;
+    int mb;
     if (t < n_gu) {
-        x.item = t / mb_i;
-        x.blk = t - x.item * mb_i;
+        mb = mb_i;
         x.gu = true;
     } else {
         t -= n_gu;
-        x.item = t / mb_h;
-        x.blk = t - x.item * mb_h;
+        mb = mb_h;
         x.gu = false;
     }
+    const int w = __ldg(&items[t / mb].w);
+    const int first = w >> 10, n = w & 1023;
+    const int local = t - first * mb;
+    x.blk = local / n;
+    x.item = first + (local - x.blk * n);
+    x.shared_w = n > 1;
     return x;
 }
 
 template <int NT, int MODE>
-__global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
+__global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
     ffn_kernel(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUtensorMap map_u,
                const __grid_constant__ CUtensorMap map_sg, const __grid_constant__ CUtensorMap map_su,
                const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_d,
@@ -233,7 +249,8 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA producer
-            const uint64_t pol = policy_evict_first();
+            const uint64_t pol_once = policy_evict_first();   // a weight tile read once
+            const uint64_t pol_shared = policy_evict_last();  // read by several row chunks
             int stage = 0;
             uint32_t phase = 0;
             // Stage j of a tile: gate/up tiles alternate gate and up weight
@@ -242,6 +259,7 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
                 const bool sh = it.x == p.E;
                 const int ex = sh ? 0 : it.x;
                 uint8_t* st = st_base + s * C::STAGE_BYTES;
+                const uint64_t pol = tl.shared_w ? pol_shared : pol_once;
                 mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
                 if (tl.gu) {
                     const CUtensorMap* m = (j & 1) ? (sh ? &map_su : &map_u) : (sh ? &map_sg : &map_g);
@@ -268,10 +286,10 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
             // the wait on that kernel, its row tiles after.
             const int t0 = blockIdx.x;
             int pre = 0;
-            Tile tl0{0, 0, true};
+            Tile tl0{0, 0, true, false};
             int4 it0 = make_int4(0, 0, 0, 0);
             if (t0 < n_tiles) {
-                tl0 = tile_of(t0, n_gu, MB_I, MB_H);
+                tl0 = tile_of(t0, n_gu, MB_I, MB_H, items);
                 it0 = items[tl0.item];
                 pre = min(tl0.gu ? 2 * KB_H : KB_I, p.n_stages);
                 for (int j = 0; j < pre; ++j) a_load(tl0, it0, j, j);
@@ -288,13 +306,17 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
             issued = static_cast<uint32_t>(pre);
             stage = pre % p.n_stages;
             phase = (pre == p.n_stages) ? 1u : 0u;
-            // the next tile's descriptor is fetched one tile ahead
+            // the next tile and its item are fetched one tile ahead
+            Tile tl_next = tl0;
             int4 it_next = it0;
             for (int t = t0; t < n_tiles && ok && !*s_abort; t += gridDim.x) {
-                const Tile tl = tile_of(t, n_gu, MB_I, MB_H);
+                const Tile tl = tl_next;
                 const int4 it = it_next;
                 const int tn = t + gridDim.x;
-                if (tn < n_tiles) it_next = items[tile_of(tn, n_gu, MB_I, MB_H).item];
+                if (tn < n_tiles) {
+                    tl_next = tile_of(tn, n_gu, MB_I, MB_H, items);
+                    it_next = items[tl_next.item];
+                }
                 const int NS = tl.gu ? 2 * KB_H : KB_I;
                 int j = (t == t0) ? pre : 0;
                 if (kFused && !tl.gu && t != t0) {
@@ -388,9 +410,19 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
         uint32_t aph = 0;
         bool ok = true;
         pdl_wait();   // row scales and outputs belong to the previous kernel
+        Tile tl_next{0, 0, true, false};
+        int4 it_next = make_int4(0, 0, 0, 0);
+        if (blockIdx.x < n_tiles) {
+            tl_next = tile_of(blockIdx.x, n_gu, MB_I, MB_H, items);
+            it_next = items[tl_next.item];
+        }
         for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-            const Tile tl = tile_of(t, n_gu, MB_I, MB_H);
-            const int4 it = items[tl.item];
+            const Tile tl = tl_next;
+            const int4 it = it_next;
+            if (t + gridDim.x < n_tiles) {
+                tl_next = tile_of(t + gridDim.x, n_gu, MB_I, MB_H, items);
+                it_next = items[tl_next.item];
+            }
             const bool sh = it.x == p.E;
             const int ex = sh ? 0 : it.x;
             const int row0 = it.y, nrow = it.z;
@@ -425,9 +457,10 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
             ok = epi_bar_and(ok, C::EPI_THREADS);
             if (!ok) break;
 
-            float acc0[16], acc1[16];
+            constexpr int CW = C::CW;
+            float acc0[CW], acc1[CW];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < CW; ++j) {
                 acc0[j] = 0.0f;
                 acc1[j] = 0.0f;
             }
@@ -439,19 +472,19 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) +
-                                    ab * C::ACC_COLS + cg * 16;
-                float v0[16], v1[16];
-                tmem_ld16(ta, v0);
-                if (C::NA == 2 && tl.gu) tmem_ld16(ta + NT, v1);
+                                    ab * C::ACC_COLS + cg * CW;
+                float v0[CW], v1[CW];
+                tmem_ld<CW>(ta, v0);
+                if (C::NA == 2 && tl.gu) tmem_ld<CW>(ta + NT, v1);
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[ab]);
-                float sc0[16];
+                float sc0[CW];
                 {
-                    const float4* q4 = reinterpret_cast<const float4*>(s_sc + kb * NT + cg * 16);
+                    const float4* q4 = reinterpret_cast<const float4*>(s_sc + kb * NT + cg * CW);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
+                    for (int v = 0; v < CW / 4; ++v) {
                         const float4 t4 = q4[v];
                         sc0[4 * v] = t4.x;
                         sc0[4 * v + 1] = t4.y;
@@ -461,9 +494,9 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
                 }
                 if (C::NA == 2 && tl.gu) {
                     const float4* q4 =
-                        reinterpret_cast<const float4*>(s_sc + (KB + kb) * NT + cg * 16);
+                        reinterpret_cast<const float4*>(s_sc + (KB + kb) * NT + cg * CW);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
+                    for (int v = 0; v < CW / 4; ++v) {
                         const float4 t4 = q4[v];
                         acc0[4 * v] = fmaf(v0[4 * v], sc0[4 * v], acc0[4 * v]);
                         acc0[4 * v + 1] = fmaf(v0[4 * v + 1], sc0[4 * v + 1], acc0[4 * v + 1]);
@@ -476,7 +509,7 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
                     }
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) acc0[j] = fmaf(v0[j], sc0[j], acc0[j]);
+                    for (int j = 0; j < CW; ++j) acc0[j] = fmaf(v0[j], sc0[j], acc0[j]);
                 }
                 if (++ab == C::ACC_BUFS) {
                     ab = 0;
@@ -485,10 +518,10 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
             }
             if (C::NA == 2 && tl.gu) {
                 // h = silu(g) * u; per-row amax over the 128 features
-                float h[16];
+                float h[CW];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int c = cg * 16 + j;
+                for (int j = 0; j < CW; ++j) {
+                    const int c = cg * CW + j;
                     const float g = acc0[j];
                     h[j] = (c < nrow) ? (g / (1.0f + __expf(-g))) * acc1[j] : 0.0f;
                     float a = fabsf(h[j]);
@@ -499,8 +532,8 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
                 ok = epi_bar_and(ok, C::EPI_THREADS);
                 if (!ok) break;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int c = cg * 16 + j;
+                for (int j = 0; j < CW; ++j) {
+                    const int c = cg * CW + j;
                     const float amax = fmaxf(fmaxf(s_red[c], s_red[NT + c]),
                                              fmaxf(s_red[2 * NT + c], s_red[3 * NT + c]));
                     const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
@@ -526,8 +559,8 @@ __global__ void __launch_bounds__(FfnCfg<NT, MODE>::THREADS, 1)
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int c = cg * 16 + j;
+                for (int j = 0; j < CW; ++j) {
+                    const int c = cg * CW + j;
                     if (ok && c < nrow) {
                         const int slot = s_src[c];
                         const int r = slot / p.KS, k = slot - r * p.KS;

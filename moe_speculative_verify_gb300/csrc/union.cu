@@ -173,7 +173,8 @@ __global__ void __launch_bounds__(kUnionThreads) union_kernel(const int32_t* __r
             item.x = e;
             item.y = s_off[e] + j * n_tile;
             item.z = min(n_tile, c - j * n_tile);
-            item.w = 0;
+            // the entry's first item and item count, for the GEMM's tile order
+            item.w = s_ioff[e] * 1024 + (c + n_tile - 1) / n_tile;
             reinterpret_cast<int4*>(ub + L.items)[s_ioff[e] + j] = item;
         }
     }
