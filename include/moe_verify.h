@@ -255,6 +255,23 @@ moe_status_t moe_combine(const moe_config_t* cfg, const float* y_slots, const fl
                          void* out_bf16, moe_stream_t stream);
 
 /*
+ * moe_combine_add_rmsnorm -- moe_combine fused with the next layer's residual
+ * add and RMSNorm (mstar #388, commit on kernel switches: the MoE's partials
+ * reduced once, fused with the next add + RMSNorm).  Per valid row:
+ *   acc = the combine sum of moe_combine, before its rounding;
+ *   z = residual + acc;   residual_out = bf16_rne(z);
+ *   normed = bf16_rne(z * rsqrt(sum_h(z^2) / H + eps) * gamma)
+ * (sum of squares reduced in a fixed order; pad rows: +0.0 in both outputs).
+ *   residual_bf16 bf16 [R, H]; gamma fp32 [H]; eps >= 0;
+ *   residual_out_bf16, normed_bf16 bf16 [R, H] (out).  All 16-byte aligned.
+ */
+moe_status_t moe_combine_add_rmsnorm(const moe_config_t* cfg, const float* y_slots,
+                                     const float* y_shared, const float* topk_w,
+                                     const int32_t* union_buf, int32_t R, const void* residual_bf16,
+                                     const float* gamma, float eps, void* residual_out_bf16,
+                                     void* normed_bf16, moe_stream_t stream);
+
+/*
  * moe_layer -- the whole layer: moe_route, moe_build_union,
  * moe_expert_ffn_fp8 and moe_combine on one stream, intermediates in `ws`.
  * Arguments follow the problem statement of openinfer #610 ("What"): R rows

@@ -22,7 +22,7 @@ __all__ = [
     "moe_ffn_workspace_bytes", "moe_workspace_bytes", "moe_get_device_error",
     "moe_diag_wait_timeout", "moe_status_string", "moe_dispatch", "moe_gate_up_fp8",
     "moe_down_fp8", "ffn_layout", "moe_layer_noalloc", "moe_expert_gemms_fp8",
-    "moe_greedy_verify", "union_layout", "rows_per_item",
+    "moe_greedy_verify", "moe_combine_add_rmsnorm", "union_layout", "rows_per_item",
     "MOE_MAX_ROWS",
 ]
 
@@ -98,11 +98,12 @@ def load() -> C.CDLL:
     L.moe_expert_gemms_fp8.argtypes = [cfg, C.POINTER(Weights), P, I32, P, P, P, SZ, P]
     L.moe_layer.argtypes = [cfg, P, P, P, C.POINTER(Weights), P, I32, P, P, P, P, SZ, P]
     L.moe_get_device_error.argtypes = [P, I32, P]
+    L.moe_combine_add_rmsnorm.argtypes = [cfg, P, P, P, P, I32, P, P, C.c_float, P, P, P]
     L.moe_greedy_verify.argtypes = [P, I32, I32, I32, P, P, P, P, P, P]
     L.moe_layer_noalloc.argtypes = [cfg, P, P, P, C.POINTER(Weights), P, I32, P, P, P, P, P]
     L.moe_diag_wait_timeout.argtypes = [P, C.c_uint32, P]
     for n in ("moe_route", "moe_build_union", "moe_expert_ffn_fp8", "moe_combine", "moe_layer",
-              "moe_get_device_error", "moe_diag_wait_timeout", "moe_dispatch", "moe_layer_noalloc", "moe_greedy_verify",
+              "moe_get_device_error", "moe_diag_wait_timeout", "moe_dispatch", "moe_layer_noalloc", "moe_greedy_verify", "moe_combine_add_rmsnorm",
               "moe_gate_up_fp8", "moe_down_fp8", "moe_expert_gemms_fp8"):
         getattr(L, n).restype = C.c_int
     _LIB = L
@@ -194,6 +195,16 @@ def moe_combine(cfg: Config, y_slots, y_shared, topk_w, union_buf, out, stream=N
     R = out.shape[0]
     _check(load().moe_combine(C.byref(cfg), _ptr(y_slots), _ptr(y_shared), _ptr(topk_w),
                               _ptr(union_buf), R, _ptr(out), _stream(stream)), "moe_combine")
+
+
+def moe_combine_add_rmsnorm(cfg: Config, y_slots, y_shared, topk_w, union_buf, residual, gamma,
+                            eps: float, residual_out, normed, stream=None) -> None:
+    R = residual.shape[0]
+    _check(load().moe_combine_add_rmsnorm(C.byref(cfg), _ptr(y_slots), _ptr(y_shared),
+                                          _ptr(topk_w), _ptr(union_buf), R, _ptr(residual),
+                                          _ptr(gamma), float(eps), _ptr(residual_out),
+                                          _ptr(normed), _stream(stream)),
+           "moe_combine_add_rmsnorm")
 
 
 def moe_layer(cfg: Config, x, w_router, bias, weights: Weights, row_valid, out, ws,

@@ -389,6 +389,31 @@ moe_status_t moe_combine(const moe_config_t* cfg, const float* y_slots, const fl
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
+moe_status_t moe_combine_add_rmsnorm(const moe_config_t* cfg, const float* y_slots,
+                                     const float* y_shared, const float* topk_w,
+                                     const int32_t* union_buf, int32_t R, const void* residual_bf16,
+                                     const float* gamma, float eps, void* residual_out_bf16,
+                                     void* normed_bf16, moe_stream_t stream) {
+    moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if ((st = check_rows(R)) != MOE_OK) return st;
+    if (R == 0) return MOE_OK;
+    if (!y_slots || !topk_w || !union_buf || !residual_bf16 || !gamma || !residual_out_bf16 ||
+        !normed_bf16 || !(eps >= 0.0f))
+        return MOE_ERR_INVALID_ARG;
+    if (cfg->n_shared > 0 && !y_shared) return MOE_ERR_INVALID_ARG;
+    if (!aligned(y_slots, 16) || (y_shared && !aligned(y_shared, 16)) || !aligned(topk_w, 4) ||
+        !aligned(union_buf, 16) || !aligned(residual_bf16, 16) || !aligned(gamma, 16) ||
+        !aligned(residual_out_bf16, 16) || !aligned(normed_bf16, 16))
+        return MOE_ERR_INVALID_ARG;
+    const UnionLayout UL = moe::union_layout(cfg->n_experts, cfg->topk, cfg->n_shared, R);
+    return cuda_status(moe::launch_combine_add_rmsnorm(
+        y_slots, y_shared, topk_w, union_buf, UL, R, cfg->hidden, cfg->topk, cfg->n_shared,
+        static_cast<const uint16_t*>(residual_bf16), gamma, eps,
+        static_cast<uint16_t*>(residual_out_bf16), static_cast<uint16_t*>(normed_bf16),
+        reinterpret_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_layer(const moe_config_t* cfg, const void* x_bf16, const float* w_router,
                        const float* bias, const moe_weights_t* w, const uint8_t* row_valid,
                        int32_t R, void* out_bf16, int32_t* topk_ids_out, float* topk_w_out,

@@ -77,6 +77,127 @@ cudaError_t launch_combine(const float* y_slots, const float* y_shared, const fl
     return cudaGetLastError();
 }
 
+// Combine fused with the residual add and the RMSNorm of the next layer
+// (mstar #388 "Speed up GLM-5.2 with fp8 kernels and one-graph MTP", commit on
+// kernel switches: the MoE's partials reduced once, fused with the next
+// add + RMSNorm).  One block per row:
+//   acc = the fixed-order combine sum (as combine_kernel, before rounding);
+//   z = residual + acc;  residual_out = bf16_rne(z);
+//   normed = bf16_rne(z * rsqrt(sum(z^2) / H + eps) * gamma).
+// The sum of squares is reduced in a fixed order (per thread in column order,
+// xor butterfly in the warp, warps in index order), so a row's bits do not
+// depend on the batch.  Pad rows give +0.0 in both outputs.
+constexpr int kNormThreads = 256;
+constexpr int kNormMaxChunks = 16;     // H / 4 / kNormThreads, H <= 16384
+
+__global__ void __launch_bounds__(kNormThreads) combine_add_rmsnorm_kernel(
+    const float* __restrict__ y_slots, const float* __restrict__ y_shared,
+    const float* __restrict__ wts, const int32_t* __restrict__ ub, UnionLayout L, int H, int K,
+    int S, const uint16_t* __restrict__ residual, const float* __restrict__ gamma, float eps,
+    uint16_t* __restrict__ residual_out, uint16_t* __restrict__ normed) {
+    __shared__ float s_warp[kNormThreads / 32];
+    __shared__ float s_inv;
+    pdl_wait();
+    pdl_launch_dependents();
+    const int r = blockIdx.x;
+    const int KS = K + S;
+    const int nchunks = H / 4;
+    const bool valid = ub[L.pos + size_t(r) * KS] >= 0;
+    if (!valid) {
+        for (int c = threadIdx.x; c < nchunks; c += kNormThreads) {
+            reinterpret_cast<uint2*>(residual_out + size_t(r) * H)[c] = make_uint2(0u, 0u);
+            reinterpret_cast<uint2*>(normed + size_t(r) * H)[c] = make_uint2(0u, 0u);
+        }
+        return;
+    }
+    const float* w = wts + size_t(r) * K;
+    float4 z[kNormMaxChunks];
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kNormMaxChunks; ++i) {
+        const int c = threadIdx.x + i * kNormThreads;
+        if (c < nchunks) {
+            const int h = 4 * c;
+            float4 y[MOE_MAX_TOPK + 1];
+#pragma unroll
+            for (int k = 0; k < MOE_MAX_TOPK; ++k)
+                if (k < K) y[k] = __ldg(reinterpret_cast<const float4*>(y_slots + (size_t(r) * K + k) * H + h));
+            if (S) y[MOE_MAX_TOPK] = __ldg(reinterpret_cast<const float4*>(y_shared + size_t(r) * H + h));
+            const float w0 = w[0];
+            float a0 = __fmul_rn(w0, y[0].x), a1 = __fmul_rn(w0, y[0].y),
+                  a2 = __fmul_rn(w0, y[0].z), a3 = __fmul_rn(w0, y[0].w);
+#pragma unroll
+            for (int k = 1; k < MOE_MAX_TOPK; ++k) {
+                if (k < K) {
+                    const float wk = w[k];
+                    a0 = __fmaf_rn(wk, y[k].x, a0);
+                    a1 = __fmaf_rn(wk, y[k].y, a1);
+                    a2 = __fmaf_rn(wk, y[k].z, a2);
+                    a3 = __fmaf_rn(wk, y[k].w, a3);
+                }
+            }
+            if (S) {
+                a0 = __fadd_rn(a0, y[MOE_MAX_TOPK].x);
+                a1 = __fadd_rn(a1, y[MOE_MAX_TOPK].y);
+                a2 = __fadd_rn(a2, y[MOE_MAX_TOPK].z);
+                a3 = __fadd_rn(a3, y[MOE_MAX_TOPK].w);
+            }
+            const uint2 rb = *reinterpret_cast<const uint2*>(residual + size_t(r) * H + h);
+            float4 zz;
+            zz.x = __fadd_rn(bf16_bits_to_f32(rb.x & 0xFFFFu), a0);
+            zz.y = __fadd_rn(bf16_bits_to_f32(rb.x >> 16), a1);
+            zz.z = __fadd_rn(bf16_bits_to_f32(rb.y & 0xFFFFu), a2);
+            zz.w = __fadd_rn(bf16_bits_to_f32(rb.y >> 16), a3);
+            z[i] = zz;
+            ss = __fmaf_rn(zz.x, zz.x, ss);
+            ss = __fmaf_rn(zz.y, zz.y, ss);
+            ss = __fmaf_rn(zz.z, zz.z, ss);
+            ss = __fmaf_rn(zz.w, zz.w, ss);
+            const uint32_t b0 = __bfloat16_as_ushort(__float2bfloat16_rn(zz.x));
+            const uint32_t b1 = __bfloat16_as_ushort(__float2bfloat16_rn(zz.y));
+            const uint32_t b2 = __bfloat16_as_ushort(__float2bfloat16_rn(zz.z));
+            const uint32_t b3 = __bfloat16_as_ushort(__float2bfloat16_rn(zz.w));
+            *reinterpret_cast<uint2*>(residual_out + size_t(r) * H + h) =
+                make_uint2(b0 | (b1 << 16), b2 | (b3 << 16));
+        }
+    }
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, d));
+    if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = s_warp[0];
+        for (int i = 1; i < kNormThreads / 32; ++i) t = __fadd_rn(t, s_warp[i]);
+        s_inv = __frsqrt_rn(__fadd_rn(__fdiv_rn(t, static_cast<float>(H)), eps));
+    }
+    __syncthreads();
+    const float inv = s_inv;
+#pragma unroll
+    for (int i = 0; i < kNormMaxChunks; ++i) {
+        const int c = threadIdx.x + i * kNormThreads;
+        if (c < nchunks) {
+            const int h = 4 * c;
+            const float4 g = __ldg(reinterpret_cast<const float4*>(gamma + h));
+            const uint32_t b0 = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(__fmul_rn(z[i].x, inv), g.x)));
+            const uint32_t b1 = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(__fmul_rn(z[i].y, inv), g.y)));
+            const uint32_t b2 = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(__fmul_rn(z[i].z, inv), g.z)));
+            const uint32_t b3 = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(__fmul_rn(z[i].w, inv), g.w)));
+            *reinterpret_cast<uint2*>(normed + size_t(r) * H + h) = make_uint2(b0 | (b1 << 16), b2 | (b3 << 16));
+        }
+    }
+}
+
+cudaError_t launch_combine_add_rmsnorm(const float* y_slots, const float* y_shared, const float* wts,
+                                       const int32_t* ub, const UnionLayout& L, int R, int H, int K,
+                                       int S, const uint16_t* residual, const float* gamma, float eps,
+                                       uint16_t* residual_out, uint16_t* normed, cudaStream_t stream) {
+    cudaError_t e = launch_pdl(combine_add_rmsnorm_kernel, dim3(R), dim3(kNormThreads), 0, stream,
+                               y_slots, y_shared, wts, ub, L, H, K, S, residual, gamma, eps,
+                               residual_out, normed);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 // Diagnostic: one block waits on a barrier nothing arrives on; the bounded
 // wait gives up after timeout_ns and records MOE_ERR_TIMEOUT.
 __global__ void wait_timeout_kernel(int32_t* err, uint64_t timeout_ns) {

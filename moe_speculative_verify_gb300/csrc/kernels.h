@@ -57,6 +57,10 @@ cudaError_t launch_ffn(int nt, int mode, const FfnMaps& mp, const FfnArgs& args,
 cudaError_t launch_combine(const float* y_slots, const float* y_shared, const float* wts,
                            const int32_t* ub, const UnionLayout& L, int R, int H, int K, int S,
                            uint16_t* out, cudaStream_t stream);
+cudaError_t launch_combine_add_rmsnorm(const float* y_slots, const float* y_shared, const float* wts,
+                                       const int32_t* ub, const UnionLayout& L, int R, int H, int K,
+                                       int S, const uint16_t* residual, const float* gamma, float eps,
+                                       uint16_t* residual_out, uint16_t* normed, cudaStream_t stream);
 cudaError_t launch_wait_timeout(int32_t* err, uint64_t timeout_ns, cudaStream_t stream);
 cudaError_t launch_greedy_verify(const void* logits, bool bf16, int V, int R, const int32_t* draft,
                                  const int32_t* n_draft, int32_t* am, int32_t* accept_len,

@@ -60,6 +60,7 @@ def lib() -> C.CDLL:
                                                                    C.c_int32, P, P, P, P,
                                                                    C.c_int32]
         L.orc_greedy_verify.argtypes = [P, C.c_int32, C.c_int32, P, P, C.c_int32, P, P, P]
+        L.orc_add_rmsnorm.argtypes = [P, P, P, C.c_float, P, C.c_int32, C.c_int32, P, P]
         L.orc_num_threads.restype = C.c_int
         L.orc_set_num_threads.argtypes = [C.c_int]
         _LIB = L
@@ -244,3 +245,16 @@ def greedy_verify(logits, draft, n_draft):
     lib().orc_greedy_verify(_p(lg), is_bf16, V, _p(_c(draft, np.int32)), _p(_c(n_draft, np.int32)),
                             n_span, _p(acc), _p(out), _p(am))
     return acc, out, am
+
+
+# ------------------------------------------------------ residual add + RMSNorm --
+def add_rmsnorm(y, residual_bf16, gamma, eps, row_valid=None):
+    """(residual_out bf16 bits [R,H], normed bf16 bits [R,H]) from fp64 y [R,H]."""
+    y = _c(y, np.float64)
+    R, H = y.shape
+    ro = np.empty((R, H), dtype=np.uint16)
+    no = np.empty((R, H), dtype=np.uint16)
+    rv = None if row_valid is None else _c(row_valid, np.uint8)
+    lib().orc_add_rmsnorm(_p(y), _p(_c(residual_bf16, np.uint16)), _p(_c(gamma, np.float32)),
+                          float(eps), _p(rv), R, H, _p(ro), _p(no))
+    return ro, no

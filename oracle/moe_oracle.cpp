@@ -593,4 +593,37 @@ void orc_greedy_verify(const void* logits, int32_t logits_is_bf16, int32_t V,
     }
 }
 
+// ------------------------------------------------ residual add + RMSNorm ----
+// The MoE output feeds the next layer through the residual stream and its
+// RMSNorm (mstar #388, commit on kernel switches: the MoE's partials reduced
+// once, fused with the next add + RMSNorm; the decoder layer's
+// residual + mlp(norm(...)) in the review thread).  READING, per valid row:
+//   z = residual + y          (y the layer's combine sum before rounding)
+//   residual_out = bf16_rne(z)
+//   normed = bf16_rne(z / sqrt(mean_h(z^2) + eps) * gamma)
+// computed in fp64 from the inputs; pad rows give +0.0 in both outputs.
+void orc_add_rmsnorm(const double* y, const uint16_t* residual, const float* gamma, float eps,
+                     const uint8_t* row_valid, int32_t R, int32_t H, uint16_t* residual_out,
+                     uint16_t* normed) {
+    std::vector<double> z(H);
+    for (int r = 0; r < R; ++r) {
+        uint16_t* ro = residual_out + size_t(r) * H;
+        uint16_t* no = normed + size_t(r) * H;
+        if (row_valid && !row_valid[r]) {
+            for (int h = 0; h < H; ++h) ro[h] = no[h] = 0;
+            continue;
+        }
+        double ss = 0.0;
+        for (int h = 0; h < H; ++h) {
+            z[h] = double(bf16_to_f32(residual[size_t(r) * H + h])) + y[size_t(r) * H + h];
+            ss += z[h] * z[h];
+        }
+        const double inv = 1.0 / std::sqrt(ss / H + double(eps));
+        for (int h = 0; h < H; ++h) {
+            ro[h] = f64_to_bf16(z[h]);
+            no[h] = f64_to_bf16(z[h] * inv * double(gamma[h]));
+        }
+    }
+}
+
 }  // extern "C"
