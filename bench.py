@@ -231,6 +231,61 @@ def run_reference(args, wl) -> None:
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ extras --
+def measure_extras(m, cfg, wl, bufs, dev, steps) -> dict:
+    """Greedy verify of one 8-row span over a GLM-sized vocabulary, and the
+    combine fused with the residual add + RMSNorm against the plain combine,
+    on the verify step's own expert outputs."""
+    out = {}
+    stream = torch.cuda.current_stream()
+    flush = bufs["flush"]
+    R, H = wl.rows, wl.shape.hidden
+
+    def timed(fn):
+        ts = []
+        for _ in range(max(3, steps)):
+            flush.zero_()
+            torch.cuda._sleep(HOST_AHEAD_CYCLES // 4)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.mean(ts[1:])
+
+    V = 151552
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    logits = torch.randn((8, V), generator=g, device=dev).to(torch.bfloat16)
+    draft = torch.randint(0, V, (8,), generator=g, device=dev, dtype=torch.int32)
+    nd = torch.full((1,), 7, dtype=torch.int32, device=dev)
+    am = torch.empty(8, dtype=torch.int32, device=dev)
+    acc = torch.empty(1, dtype=torch.int32, device=dev)
+    toks = torch.empty(8, dtype=torch.int32, device=dev)
+    ms = timed(lambda: m.moe_greedy_verify(logits, draft, nd, am, acc, toks))
+    nbytes = logits.numel() * 2
+    out["greedy_verify"] = {"rows": 8, "vocab": V, "dtype": "bf16", "us": round(ms * 1e3, 2),
+                            "gbs": round(nbytes / (ms / 1e3) / 1e9, 1)}
+    residual = torch.randn((R, H), generator=g, device=dev).to(torch.bfloat16)
+    gamma = torch.rand((H,), generator=g, device=dev) + 0.5
+    ro = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+    no = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+    ms_plain = timed(lambda: m.moe_combine(cfg, bufs["y_slots"], bufs["y_sh"], bufs["wts"],
+                                           bufs["ub"], y))
+    ms_fused = timed(lambda: m.moe_combine_add_rmsnorm(cfg, bufs["y_slots"], bufs["y_sh"],
+                                                       bufs["wts"], bufs["ub"], residual, gamma,
+                                                       1e-5, ro, no))
+    K, S = wl.shape.topk, wl.shape.n_shared
+    b_fused = R * (K + S) * H * 4 + R * H * 2 * 3 + H * 4
+    out["combine_add_rmsnorm"] = {"rows": R, "us": round(ms_fused * 1e3, 2),
+                                  "plain_combine_us": round(ms_plain * 1e3, 2),
+                                  "gbs": round(b_fused / (ms_fused / 1e3) / 1e9, 1)}
+    return out
+
+
 # -------------------------------------------------------------------- ours --
 def main() -> None:
     ap = argparse.ArgumentParser()
@@ -348,7 +403,8 @@ def main() -> None:
         alg = algorithmic(wl_m, ids.cpu().numpy(), ri["row_valid"].cpu().numpy())
         return {"ri": ri, "phase_ms": {p: statistics.mean(v) for p, v in ph.items()},
                 "step_ms": statistics.mean(tot), "step_ms_min": min(tot), "wall_s": wall,
-                "alg": alg, "clocks": clocks, "out": out}
+                "alg": alg, "clocks": clocks, "out": out,
+                "bufs": {"y_slots": y_slots, "y_sh": y_sh, "wts": wts, "ub": ub, "flush": flush}}
 
     res = measure(wl, args.steps, max(args.warmup, 3), True)
     step_ms = max_over_ranks(res["step_ms"])
@@ -383,6 +439,10 @@ def main() -> None:
                 "distinct_experts": a2["U"],
                 "phase_ms": {k: round(v, 4) for k, v in r2["phase_ms"].items()}}
             del r2
+
+    # the verify-step extras, each timed alone with events on its stream
+    if rank == 0:
+        extra.update(measure_extras(m, cfg, wl, res["bufs"], dev, args.steps))
 
     # end to end through moe_layer with host buffers
     import moe_speculative_verify_gb300 as m2
