@@ -58,9 +58,11 @@ struct FfnCfg {
     static constexpr int EPI_WARPS = 4 * CSPLIT;
     static constexpr int EPI_THREADS = 32 * EPI_WARPS;
     static constexpr int THREADS = 64 + EPI_THREADS;
-    // registers per thread for one block per SM: 64K registers over the
-    // block's warps, in steps of 8, at most 255
-    static constexpr int MAX_REGS_RAW = (65536 / THREADS) / 8 * 8;
+    // registers per thread for one block per SM: each of the four SM
+    // sub-partitions holds 16K registers and ceil(warps / 4) of the block's
+    // warps; in steps of 8, at most 255
+    static constexpr int WARPS_PER_SMSP = (THREADS / 32 + 3) / 4;
+    static constexpr int MAX_REGS_RAW = (16384 / (WARPS_PER_SMSP * 32)) / 8 * 8;
     static constexpr int MAX_REGS = MAX_REGS_RAW > 255 ? 255 : MAX_REGS_RAW;
     static constexpr int ACC_COLS = NA * NT;
     // as many tensor-memory partials as fit (at most 16): the MMA may run that
@@ -471,46 +473,49 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                     break;
                 }
                 tc_fence_after();
-                const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) +
-                                    ab * C::ACC_COLS + cg * CW;
-                float v0[CW], v1[CW];
-                tmem_ld<CW>(ta, v0);
-                if (C::NA == 2 && tl.gu) tmem_ld<CW>(ta + NT, v1);
-                tmem_wait_ld();
+                // 16 columns at a time: the TMEM loads of a chunk, then its FMAs
+#pragma unroll
+                for (int hc = 0; hc < CW / 16; ++hc) {
+                    const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) +
+                                        ab * C::ACC_COLS + cg * CW + hc * 16;
+                    float v0[16], v1[16];
+                    tmem_ld16(ta, v0);
+                    if (C::NA == 2 && tl.gu) tmem_ld16(ta + NT, v1);
+                    tmem_wait_ld();
+                    const float4* q0 =
+                        reinterpret_cast<const float4*>(s_sc + kb * NT + cg * CW + hc * 16);
+                    if (C::NA == 2 && tl.gu) {
+                        const float4* q1 = reinterpret_cast<const float4*>(
+                            s_sc + (KB + kb) * NT + cg * CW + hc * 16);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const float4 a4 = q0[v], b4 = q1[v];
+                            float* a0p = &acc0[hc * 16 + 4 * v];
+                            float* a1p = &acc1[hc * 16 + 4 * v];
+                            a0p[0] = fmaf(v0[4 * v], a4.x, a0p[0]);
+                            a0p[1] = fmaf(v0[4 * v + 1], a4.y, a0p[1]);
+                            a0p[2] = fmaf(v0[4 * v + 2], a4.z, a0p[2]);
+                            a0p[3] = fmaf(v0[4 * v + 3], a4.w, a0p[3]);
+                            a1p[0] = fmaf(v1[4 * v], b4.x, a1p[0]);
+                            a1p[1] = fmaf(v1[4 * v + 1], b4.y, a1p[1]);
+                            a1p[2] = fmaf(v1[4 * v + 2], b4.z, a1p[2]);
+                            a1p[3] = fmaf(v1[4 * v + 3], b4.w, a1p[3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const float4 a4 = q0[v];
+                            float* a0p = &acc0[hc * 16 + 4 * v];
+                            a0p[0] = fmaf(v0[4 * v], a4.x, a0p[0]);
+                            a0p[1] = fmaf(v0[4 * v + 1], a4.y, a0p[1]);
+                            a0p[2] = fmaf(v0[4 * v + 2], a4.z, a0p[2]);
+                            a0p[3] = fmaf(v0[4 * v + 3], a4.w, a0p[3]);
+                        }
+                    }
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[ab]);
-                float sc0[CW];
-                {
-                    const float4* q4 = reinterpret_cast<const float4*>(s_sc + kb * NT + cg * CW);
-#pragma unroll
-                    for (int v = 0; v < CW / 4; ++v) {
-                        const float4 t4 = q4[v];
-                        sc0[4 * v] = t4.x;
-                        sc0[4 * v + 1] = t4.y;
-                        sc0[4 * v + 2] = t4.z;
-                        sc0[4 * v + 3] = t4.w;
-                    }
-                }
-                if (C::NA == 2 && tl.gu) {
-                    const float4* q4 =
-                        reinterpret_cast<const float4*>(s_sc + (KB + kb) * NT + cg * CW);
-#pragma unroll
-                    for (int v = 0; v < CW / 4; ++v) {
-                        const float4 t4 = q4[v];
-                        acc0[4 * v] = fmaf(v0[4 * v], sc0[4 * v], acc0[4 * v]);
-                        acc0[4 * v + 1] = fmaf(v0[4 * v + 1], sc0[4 * v + 1], acc0[4 * v + 1]);
-                        acc0[4 * v + 2] = fmaf(v0[4 * v + 2], sc0[4 * v + 2], acc0[4 * v + 2]);
-                        acc0[4 * v + 3] = fmaf(v0[4 * v + 3], sc0[4 * v + 3], acc0[4 * v + 3]);
-                        acc1[4 * v] = fmaf(v1[4 * v], t4.x, acc1[4 * v]);
-                        acc1[4 * v + 1] = fmaf(v1[4 * v + 1], t4.y, acc1[4 * v + 1]);
-                        acc1[4 * v + 2] = fmaf(v1[4 * v + 2], t4.z, acc1[4 * v + 2]);
-                        acc1[4 * v + 3] = fmaf(v1[4 * v + 3], t4.w, acc1[4 * v + 3]);
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < CW; ++j) acc0[j] = fmaf(v0[j], sc0[j], acc0[j]);
-                }
                 if (++ab == C::ACC_BUFS) {
                     ab = 0;
                     aph ^= 1u;
