@@ -5,12 +5,14 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--workload verify8]
 
 One step = one pass of the whole layer (route, union, dispatch, gate/up GEMM,
 down GEMM, combine) over one batch of seeded synthetic inputs already
-resident in HBM.  The step runs through the C ABI's step entry points with a
-CUDA event between consecutive kernels on the launching stream, so every
-kernel's device time is measured live; L2 is flushed (a 256 MB write) before
-every step, outside the events.  `value` = rows processed by all ranks / max
-over ranks of the summed step time.  Under torchrun every rank runs its own
-replica (the layer has no exchange step on one GPU): scaling "weak".
+resident in HBM: one moe_layer call, its kernels chained by programmatic
+dependent launch, CUDA events at the step boundaries on the launching stream.
+L2 is flushed (a 256 MB write) before every step, outside the events.
+`value` = rows processed by all ranks / max over ranks of the step time.  A
+second pass runs the step-by-step entry points with an event between every two
+kernels: it gives each kernel's device time (`phase_ms`) and the roofline of
+the dominant kernel.  Under torchrun every rank runs its own replica (the
+layer has no exchange step on one GPU): scaling "weak".
 
 `e2e` measures the same metric through moe_layer with host buffers: per step
 the rows go from pinned host memory to the device, the layer runs, and the
@@ -41,7 +43,12 @@ import synth  # noqa: E402
 METRIC = ("MoE-layer rows/s and achieved HBM GB/s (% of 8 TB/s) at 8-row verify; "
           "fp8 TFLOPS at 4096")
 PHASES = ["router", "union", "dispatch", "ffn", "combine"]
-KERNELS_PER_STEP = 6          # router logits + select, union, dispatch, expert GEMMs, combine
+
+
+def kernels_per_step(R: int) -> int:
+    """Kernels of one moe_layer call: router logits, selection + union (one
+    kernel up to 64 rows, two above), dispatch, expert GEMMs, combine."""
+    return 5 if R <= 64 else 6
 HOST_AHEAD_CYCLES = 400_000   # GPU sleep before each step so the host enqueues it whole
 FLUSH_BYTES = 256 << 20       # > 129 MB L2
 
@@ -352,6 +359,14 @@ def main() -> None:
             m.moe_combine(cfg, y_slots, y_sh, wts, ub, out)
             mark(5)
 
+        lws = torch.zeros(m.moe_workspace_bytes(cfg, R), dtype=torch.uint8, device=dev)
+
+        def layer_step():
+            # the product call: one moe_layer (selection and union in one
+            # kernel at R <= 64)
+            m.moe_layer(cfg, ri["x"], ri["wr"], ri["bias"], W, ri["row_valid"], out, lws,
+                        topk_ids=ids, topk_w=wts)
+
         def prologue():
             # flush L2, then keep the GPU busy while the host enqueues the step
             flush.zero_()
@@ -361,9 +376,13 @@ def main() -> None:
             if record_clocks else None
         for _ in range(warmup):
             prologue()
+            layer_step()
+        for _ in range(warmup):
+            prologue()
             step()
         torch.cuda.synchronize()
         assert m.moe_get_device_error(ws) == 0
+        assert m.moe_get_device_error(lws) == 0
         # timed region: events at the step boundaries only, so consecutive
         # kernels keep overlapping their launch with the predecessor's tail
         ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -377,7 +396,7 @@ def main() -> None:
         for i in range(steps):
             prologue()
             ev0[i].record(stream)
-            step()
+            layer_step()
             ev1[i].record(stream)
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
@@ -386,9 +405,10 @@ def main() -> None:
         if world > 1:
             torch.distributed.barrier()
         clocks = clk.stop(t_start, t_end) if clk else None
-        err = m.moe_get_device_error(ws)
+        err = m.moe_get_device_error(lws)
         assert err == 0, err
         tot = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+        out_layer = out.clone()
         # breakdown pass: an event between every two kernels (this serialises
         # the kernel boundaries, so it is reported beside, not as, the step)
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
@@ -396,6 +416,8 @@ def main() -> None:
             prologue()
             step(evs[i])
         torch.cuda.synchronize()
+        assert m.moe_get_device_error(ws) == 0
+        stepwise_same = bool(torch.equal(out, out_layer))
         ph = {p: [] for p in PHASES}
         for e in evs:
             for i, p in enumerate(PHASES):
@@ -403,7 +425,7 @@ def main() -> None:
         alg = algorithmic(wl_m, ids.cpu().numpy(), ri["row_valid"].cpu().numpy())
         return {"ri": ri, "phase_ms": {p: statistics.mean(v) for p, v in ph.items()},
                 "step_ms": statistics.mean(tot), "step_ms_min": min(tot), "wall_s": wall,
-                "alg": alg, "clocks": clocks, "out": out,
+                "alg": alg, "clocks": clocks, "out": out_layer, "stepwise_same": stepwise_same,
                 "bufs": {"y_slots": y_slots, "y_sh": y_sh, "wts": wts, "ub": ub, "flush": flush}}
 
     res = measure(wl, args.steps, max(args.warmup, 3), True)
@@ -502,7 +524,10 @@ def main() -> None:
                     "algorithmic_bytes_per_step": alg["total_bytes"]},
             "fp8_tflops": round(tflops, 2),
             "phase_ms": {k: round(v, 4) for k, v in res["phase_ms"].items()},
-            "phase_note": "separate pass with an event between every two kernels",
+            "phase_note": "separate pass through the step-by-step entry points (route, union, "
+                          "dispatch, expert GEMMs, combine) with an event between every two "
+                          "kernels; the timed pass is one moe_layer call per step",
+            "stepwise_bit_identical": res["stepwise_same"],
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": round(world * R / e2e_s, 1), "unit": "rows/s",
@@ -510,7 +535,7 @@ def main() -> None:
                     "d2h_bytes_per_step": out_host.numel() * 2,
                     "note": "moe_layer, pinned host x -> device -> pinned host out, per step",
                     "bit_identical_to_step_path": e2e_same},
-            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "gpu_launches": kernels_per_step(R) * args.steps,
             "clocks": clocks,
             "also": extra,
         }

@@ -439,9 +439,23 @@ moe_status_t moe_layer(const moe_config_t* cfg, const void* x_bf16, const float*
     int32_t* ub = reinterpret_cast<int32_t*>(base + L.ubuf);
     float* y_slots = reinterpret_cast<float*>(base + L.y_slots);
     float* y_shared = reinterpret_cast<float*>(base + L.y_shared);
-    if ((st = route_impl(cfg, x_bf16, w_router, bias, row_valid, R, ids, wts, logits, s)) != MOE_OK)
-        return st;
-    if ((st = union_impl(cfg, ids, R, ub, s)) != MOE_OK) return st;
+    if (R <= moe::kRouteUnionMaxRows) {
+        // logits, then selection and union in one block
+        if ((st = cuda_status(moe::launch_router_logits(static_cast<const uint16_t*>(x_bf16),
+                                                        w_router, row_valid, R, cfg->hidden,
+                                                        cfg->n_experts, logits, s))) != MOE_OK)
+            return st;
+        if ((st = cuda_status(moe::launch_route_union(
+                 logits, bias, row_valid, R, cfg->n_experts, cfg->n_groups, cfg->topk_groups,
+                 cfg->topk, cfg->routed_scaling, ids, wts, cfg->n_shared, moe::rows_per_item(R), ub,
+                 L.un, s))) != MOE_OK)
+            return st;
+    } else {
+        if ((st = route_impl(cfg, x_bf16, w_router, bias, row_valid, R, ids, wts, logits, s)) !=
+            MOE_OK)
+            return st;
+        if ((st = union_impl(cfg, ids, R, ub, s)) != MOE_OK) return st;
+    }
     if ((st = ffn_impl(cfg, x_bf16, w, ub, R, y_slots, y_shared, ws, s)) != MOE_OK) return st;
     return combine_impl(cfg, y_slots, y_shared, wts, ub, R, out_bf16, s);
 }

@@ -6,9 +6,13 @@
 // whichever mapping carries a row; span pad ranks zero-fill their rows so no
 // NaN leaks.  mstar #388 "Speed up GLM-5.2 with fp8 kernels and one-graph
 // MTP": the MoE's partials reduced once, routed and shared experts together.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "layout.h"
+
+namespace cg = cooperative_groups;
 
 namespace moe {
 
@@ -80,15 +84,19 @@ cudaError_t launch_combine(const float* y_slots, const float* y_shared, const fl
 // Combine fused with the residual add and the RMSNorm of the next layer
 // (mstar #388 "Speed up GLM-5.2 with fp8 kernels and one-graph MTP", commit on
 // kernel switches: the MoE's partials reduced once, fused with the next
-// add + RMSNorm).  One block per row:
+// add + RMSNorm).  One cluster of kNormCluster CTAs per row, CTA c owning the
+// c-th slice of H / kNormCluster columns:
 //   acc = the fixed-order combine sum (as combine_kernel, before rounding);
 //   z = residual + acc;  residual_out = bf16_rne(z);
 //   normed = bf16_rne(z * rsqrt(sum(z^2) / H + eps) * gamma).
-// The sum of squares is reduced in a fixed order (per thread in column order,
-// xor butterfly in the warp, warps in index order), so a row's bits do not
-// depend on the batch.  Pad rows give +0.0 in both outputs.
-constexpr int kNormThreads = 256;
-constexpr int kNormMaxChunks = 16;     // H / 4 / kNormThreads, H <= 16384
+// The sum of squares is reduced in a fixed order: per thread over its columns
+// in order, xor butterfly in the warp, warps in index order, then the CTAs'
+// partial sums in rank order (read through distributed shared memory by every
+// CTA), so a row's bits do not depend on the batch.  Pad rows give +0.0 in
+// both outputs.
+constexpr int kNormThreads = 128;
+constexpr int kNormCluster = 8;
+constexpr int kNormMaxChunks = 4;      // H / 4 / kNormCluster / kNormThreads, H <= 16384
 
 __global__ void __launch_bounds__(kNormThreads) combine_add_rmsnorm_kernel(
     const float* __restrict__ y_slots, const float* __restrict__ y_shared,
@@ -96,17 +104,21 @@ __global__ void __launch_bounds__(kNormThreads) combine_add_rmsnorm_kernel(
     int S, const uint16_t* __restrict__ residual, const float* __restrict__ gamma, float eps,
     uint16_t* __restrict__ residual_out, uint16_t* __restrict__ normed) {
     __shared__ float s_warp[kNormThreads / 32];
-    __shared__ float s_inv;
+    __shared__ float s_part;
+    cg::cluster_group cl = cg::this_cluster();
     pdl_wait();
     pdl_launch_dependents();
-    const int r = blockIdx.x;
+    const int r = blockIdx.x / kNormCluster;
+    const int rank = static_cast<int>(cl.block_rank());
     const int KS = K + S;
-    const int nchunks = H / 4;
+    const int nchunks = H / 4 / kNormCluster;                 // float4 chunks of this CTA
+    const int c0 = rank * nchunks;
+    // the same for every CTA of the cluster: all leave here or none
     const bool valid = ub[L.pos + size_t(r) * KS] >= 0;
     if (!valid) {
         for (int c = threadIdx.x; c < nchunks; c += kNormThreads) {
-            reinterpret_cast<uint2*>(residual_out + size_t(r) * H)[c] = make_uint2(0u, 0u);
-            reinterpret_cast<uint2*>(normed + size_t(r) * H)[c] = make_uint2(0u, 0u);
+            reinterpret_cast<uint2*>(residual_out + size_t(r) * H)[c0 + c] = make_uint2(0u, 0u);
+            reinterpret_cast<uint2*>(normed + size_t(r) * H)[c0 + c] = make_uint2(0u, 0u);
         }
         return;
     }
@@ -117,7 +129,7 @@ __global__ void __launch_bounds__(kNormThreads) combine_add_rmsnorm_kernel(
     for (int i = 0; i < kNormMaxChunks; ++i) {
         const int c = threadIdx.x + i * kNormThreads;
         if (c < nchunks) {
-            const int h = 4 * c;
+            const int h = 4 * (c0 + c);
             float4 y[MOE_MAX_TOPK + 1];
 #pragma unroll
             for (int k = 0; k < MOE_MAX_TOPK; ++k)
@@ -168,15 +180,17 @@ __global__ void __launch_bounds__(kNormThreads) combine_add_rmsnorm_kernel(
     if (threadIdx.x == 0) {
         float t = s_warp[0];
         for (int i = 1; i < kNormThreads / 32; ++i) t = __fadd_rn(t, s_warp[i]);
-        s_inv = __frsqrt_rn(__fadd_rn(__fdiv_rn(t, static_cast<float>(H)), eps));
+        s_part = t;
     }
-    __syncthreads();
-    const float inv = s_inv;
+    cl.sync();   // every CTA's partial sum is in its shared memory
+    float t = *cl.map_shared_rank(&s_part, 0);
+    for (int i = 1; i < kNormCluster; ++i) t = __fadd_rn(t, *cl.map_shared_rank(&s_part, i));
+    const float inv = __frsqrt_rn(__fadd_rn(__fdiv_rn(t, static_cast<float>(H)), eps));
 #pragma unroll
     for (int i = 0; i < kNormMaxChunks; ++i) {
         const int c = threadIdx.x + i * kNormThreads;
         if (c < nchunks) {
-            const int h = 4 * c;
+            const int h = 4 * (c0 + c);
             const float4 g = __ldg(reinterpret_cast<const float4*>(gamma + h));
             const uint32_t b0 = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(__fmul_rn(z[i].x, inv), g.x)));
             const uint32_t b1 = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(__fmul_rn(z[i].y, inv), g.y)));
@@ -185,15 +199,20 @@ __global__ void __launch_bounds__(kNormThreads) combine_add_rmsnorm_kernel(
             *reinterpret_cast<uint2*>(normed + size_t(r) * H + h) = make_uint2(b0 | (b1 << 16), b2 | (b3 << 16));
         }
     }
+    cl.sync();   // no CTA leaves while another may still read its partial sum
 }
 
 cudaError_t launch_combine_add_rmsnorm(const float* y_slots, const float* y_shared, const float* wts,
                                        const int32_t* ub, const UnionLayout& L, int R, int H, int K,
                                        int S, const uint16_t* residual, const float* gamma, float eps,
                                        uint16_t* residual_out, uint16_t* normed, cudaStream_t stream) {
-    cudaError_t e = launch_pdl(combine_add_rmsnorm_kernel, dim3(R), dim3(kNormThreads), 0, stream,
-                               y_slots, y_shared, wts, ub, L, H, K, S, residual, gamma, eps,
-                               residual_out, normed);
+    if (H % (4 * kNormCluster) != 0 || H / 4 / kNormCluster > kNormMaxChunks * kNormThreads)
+        return cudaErrorInvalidValue;
+    cudaError_t e = launch_pdl_cluster(combine_add_rmsnorm_kernel,
+                                       dim3(static_cast<unsigned>(R) * kNormCluster),
+                                       dim3(kNormThreads), kNormCluster, 0, stream, y_slots,
+                                       y_shared, wts, ub, L, H, K, S, residual, gamma, eps,
+                                       residual_out, normed);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

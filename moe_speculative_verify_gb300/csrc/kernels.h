@@ -43,12 +43,21 @@ struct FfnArgs {
     uint64_t timeout_ns;
 };
 
+cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const uint8_t* row_valid,
+                                 int R, int H, int E, float* logits, cudaStream_t stream);
 cudaError_t launch_router(const uint16_t* x, const float* wr, const float* bias,
                           const uint8_t* row_valid, int R, int H, int E, int G, int TG, int K,
                           float scaling, int32_t* ids, float* wts, float* logits,
                           cudaStream_t stream);
 cudaError_t launch_union(const int32_t* ids, int R, int E, int K, int S, int n_tile, int32_t* ub,
                          const UnionLayout& L, cudaStream_t stream);
+// Selection and union in one launch for calls of at most kRouteUnionMaxRows
+// rows (the logits come from launch_router's first kernel).
+constexpr int kRouteUnionMaxRows = 64;
+cudaError_t launch_route_union(const float* logits, const float* bias, const uint8_t* row_valid,
+                               int R, int E, int G, int TG, int K, float scaling, int32_t* ids,
+                               float* wts, int S, int n_tile, int32_t* ub, const UnionLayout& L,
+                               cudaStream_t stream);
 cudaError_t launch_dispatch(const uint16_t* x, const int32_t* ub, const UnionLayout& L, int R,
                             int H, int KS, uint8_t* xg, float* xs, int32_t* ready, int n_ready,
                             cudaStream_t stream);

@@ -11,6 +11,7 @@
 // contraction.
 #include "common.cuh"
 #include "kernels.h"
+#include "select.cuh"
 
 namespace moe {
 
@@ -201,181 +202,33 @@ __global__ void __launch_bounds__(kTileThreads, 1) router_logits_tiled_kernel(
     }
 }
 
-// -------------------------------------------------- sigmoid with own exp ----
-// exp by Cody-Waite range reduction (Cody and Waite, "Software Manual for the
-// Elementary Functions", 1980): a = n*ln2 + r with ln2 split into a head of 16
-// significant bits (n*head exact) and an fp32 tail, then the Taylor series of
-// e^r to degree 7 in Horner form, then scaling by 2^n through the exponent
-// field.  Argument clamped to [-87, 87] so 2^n stays a normal number.
-__device__ __forceinline__ float cw_exp(float a) {
-    const float kLog2e = 0x1.715476p+0f;
-    const float kLn2Hi = 0x1.62e4p-1f;
-    const float kLn2Lo = 0x1.7f7d1cp-20f;
-    if (a != a) return a;
-    if (a > 87.0f) a = 87.0f;
-    if (a < -87.0f) a = -87.0f;
-    const float n = rintf(__fmul_rn(a, kLog2e));
-    float r = __fmaf_rn(-n, kLn2Hi, a);
-    r = __fmaf_rn(-n, kLn2Lo, r);
-    float p = 0x1.a01a02p-13f;              // 1/7!
-    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);   // 1/6!
-    p = __fmaf_rn(p, r, 0x1.111112p-7f);    // 1/5!
-    p = __fmaf_rn(p, r, 0x1.555556p-5f);    // 1/4!
-    p = __fmaf_rn(p, r, 0x1.555556p-3f);    // 1/3!
-    p = __fmaf_rn(p, r, 0x1p-1f);           // 1/2!
-    p = __fmaf_rn(p, r, 1.0f);
-    p = __fmaf_rn(p, r, 1.0f);
-    const float two_n = __int_as_float((static_cast<int>(n) + 127) << 23);
-    return __fmul_rn(p, two_n);
-}
-
-__device__ __forceinline__ float router_sigmoid(float l) {
-    return __fdiv_rn(1.0f, __fadd_rn(1.0f, cw_exp(-l)));
-}
-
-// Total order of fp32 values as unsigned keys (-0 folded onto +0).
-__device__ __forceinline__ uint32_t ordered_key(float f) {
-    if (f == 0.0f) f = 0.0f;
-    const uint32_t u = __float_as_uint(f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Larger value first; on equal values the lower index wins.
-__device__ __forceinline__ uint64_t rank_key(float v, int idx) {
-    return (static_cast<uint64_t>(ordered_key(v)) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(idx));
-}
-
-__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
-#pragma unroll
-    for (int d = 16; d >= 1; d >>= 1) {
-        const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, v, d);
-        v = o > v ? o : v;
-    }
-    return v;
-}
-
 // ------------------------------------------------------ grouped top-k ----
-// One warp per row: sigmoid scores, biased scores, group scores (sum of the
-// two largest biased scores), the topk_groups best groups, the topk best
-// experts inside them, and the normalised weights.  Lane l holds experts
-// l, l+32, l+64, ...; every reduction is over exact comparisons (no
-// arithmetic), so its order does not matter.
+// One warp per row (select.cuh); pad rows get ids -1 and weights 0.
 constexpr int kSelWarps = 8;
-constexpr int kPer = MOE_MAX_EXPERTS / 32;
 
 __global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(
     const float* __restrict__ logits, const float* __restrict__ bias,
     const uint8_t* __restrict__ row_valid, int R, int E, int G, int TG, int K, float scaling,
     int32_t* __restrict__ ids, float* __restrict__ wts) {
+    __shared__ float s_b[kSelWarps][MOE_MAX_EXPERTS];
     pdl_wait();
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x * kSelWarps + warp;
     if (r >= R) return;
-    if (row_valid != nullptr && row_valid[r] == 0) {
-        if (lane < K) {
-            ids[size_t(r) * K + lane] = -1;
-            wts[size_t(r) * K + lane] = 0.0f;
-        }
-        return;
-    }
-    const int epg = E / G;
-    float sv[kPer], bv[kPer];
-    float lg[kPer], bi[kPer];
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        const int e = lane + 32 * j;
-        lg[j] = (e < E) ? logits[size_t(r) * E + e] : 0.0f;
-        bi[j] = (e < E) ? bias[e] : 0.0f;
-    }
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        sv[j] = router_sigmoid(lg[j]);
-        bv[j] = __fadd_rn(sv[j], bi[j]);
-    }
-
-    // group scores: per group, the two largest biased scores, merged over the warp
-    float gscore_mine = -INFINITY;               // lane g keeps group g's score
-    for (int g = 0; g < G; ++g) {
-        float t1 = -INFINITY, t2 = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < kPer; ++j) {
-            const int e = lane + 32 * j;
-            if (e < E && e / epg == g) {
-                const float v = bv[j];
-                if (v > t1) {
-                    t2 = t1;
-                    t1 = v;
-                } else if (v > t2) {
-                    t2 = v;
-                }
-            }
-        }
-#pragma unroll
-        for (int d = 16; d >= 1; d >>= 1) {
-            const float o1 = __shfl_xor_sync(0xFFFFFFFFu, t1, d);
-            const float o2 = __shfl_xor_sync(0xFFFFFFFFu, t2, d);
-            const float hi = fmaxf(t1, o1), lo = fminf(t1, o1);
-            t2 = fmaxf(lo, fmaxf(t2, o2));
-            t1 = hi;
-        }
-        if (lane == g) gscore_mine = (epg >= 2) ? __fadd_rn(t1, t2) : t1;
-    }
-    // the topk_groups best groups: rank of each group among all (ties: lower id)
-    const uint64_t gkey = (lane < G) ? rank_key(gscore_mine, lane) : 0ull;
-    int grank = 0;
-    for (int g = 0; g < G; ++g) grank += (__shfl_sync(0xFFFFFFFFu, gkey, g) > gkey) ? 1 : 0;
-    const uint32_t gmask = __ballot_sync(0xFFFFFFFFu, lane < G && grank < TG);
-
-    // the topk best experts of the kept groups: K rounds of a warp-wide max of
-    // the ordered score, then the lowest id among the lanes holding it
-    uint32_t vkey[kPer];
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        const int e = lane + 32 * j;
-        vkey[j] = (e < E && ((gmask >> (e / epg)) & 1u)) ? ordered_key(bv[j]) : 0u;
-    }
-    int my_id = -1;       // lane k keeps the k-th chosen expert
-    float my_s = 0.0f;
-    for (int k = 0; k < K; ++k) {
-        uint32_t bk = 0u, bid = 0xFFFFFFFFu;
-#pragma unroll
-        for (int j = 0; j < kPer; ++j)
-            if (vkey[j] > bk) {
-                bk = vkey[j];
-                bid = static_cast<uint32_t>(lane + 32 * j);
-            }
-        const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, bk);
-        const uint32_t e = __reduce_min_sync(0xFFFFFFFFu, (bk == top) ? bid : 0xFFFFFFFFu);
-        float s_e = 0.0f;
-        if ((e & 31u) == static_cast<uint32_t>(lane)) {
-#pragma unroll
-            for (int j = 0; j < kPer; ++j)
-                if (static_cast<uint32_t>(lane + 32 * j) == e) {
-                    vkey[j] = 0u;
-                    s_e = sv[j];
-                }
-        }
-        s_e = __shfl_sync(0xFFFFFFFFu, s_e, static_cast<int>(e & 31u));
-        if (lane == k) {
-            my_id = static_cast<int>(e);
-            my_s = s_e;
-        }
-    }
-    // weights: the denominator summed in k order, then every lane its own w_k
-    float den = __shfl_sync(0xFFFFFFFFu, my_s, 0);
-    for (int k = 1; k < K; ++k) den = __fadd_rn(den, __shfl_sync(0xFFFFFFFFu, my_s, k));
+    int id = -1;
+    float w = 0.0f;
+    if (row_valid == nullptr || row_valid[r] != 0)
+        select_row(logits + size_t(r) * E, bias, E, G, TG, K, scaling, s_b[warp], lane, &id, &w);
     if (lane < K) {
-        ids[size_t(r) * K + lane] = my_id;
-        wts[size_t(r) * K + lane] = __fmul_rn(__fdiv_rn(my_s, den), scaling);
+        ids[size_t(r) * K + lane] = id;
+        wts[size_t(r) * K + lane] = w;
     }
 }
 
 // ----------------------------------------------------------- launchers ----
-cudaError_t launch_router(const uint16_t* x, const float* wr, const float* bias,
-                          const uint8_t* row_valid, int R, int H, int E, int G, int TG, int K,
-                          float scaling, int32_t* ids, float* wts, float* logits,
-                          cudaStream_t stream) {
+cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const uint8_t* row_valid,
+                                 int R, int H, int E, float* logits, cudaStream_t stream) {
     const int nchunks = (H + 1023) / 1024;
     const int threads = max(32, nchunks * 32);
     if (R <= 64) {
@@ -397,7 +250,14 @@ cudaError_t launch_router(const uint16_t* x, const float* wr, const float* bias,
                        row_valid, R, H, E, logits);
         if (e != cudaSuccess) return e;
     }
-    cudaError_t e = cudaGetLastError();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router(const uint16_t* x, const float* wr, const float* bias,
+                          const uint8_t* row_valid, int R, int H, int E, int G, int TG, int K,
+                          float scaling, int32_t* ids, float* wts, float* logits,
+                          cudaStream_t stream) {
+    cudaError_t e = launch_router_logits(x, wr, row_valid, R, H, E, logits, stream);
     if (e != cudaSuccess) return e;
     e = launch_pdl(route_select_kernel, dim3((R + kSelWarps - 1) / kSelWarps), dim3(kSelWarps * 32),
                    0, stream, logits, bias, row_valid, R, E, G, TG, K, scaling, ids, wts);

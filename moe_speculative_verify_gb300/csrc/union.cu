@@ -12,6 +12,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "layout.h"
+#include "select.cuh"
 
 namespace moe {
 
@@ -43,11 +44,17 @@ __device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
     return s_warp[warp] + incl - v;
 }
 
-__global__ void __launch_bounds__(kUnionThreads) union_kernel(const int32_t* __restrict__ ids,
-                                                              int R, int E, int K, int S,
-                                                              int n_tile, int32_t* __restrict__ ub,
-                                                              UnionLayout L) {
-    extern __shared__ uint32_t sm[];
+// Shared memory of the union build, in bytes.
+__host__ __device__ inline size_t union_smem_bytes(int R, int E) {
+    const size_t words = size_t(E) * ((R + 31) / 32);
+    return words * 4 + ((words + 1) & ~size_t(1)) * 2 + ((R + 15) & ~15) + size_t(4 * E + 8) * 4;
+}
+
+// The union of one call, built by one block of kUnionThreads threads from the
+// routed ids (global or shared memory); `sm` is union_smem_bytes of shared
+// memory, 4-byte aligned.
+__device__ void union_block(const int32_t* ids, int R, int E, int K, int S, int n_tile,
+                            int32_t* __restrict__ ub, const UnionLayout& L, uint32_t* sm) {
     const int W = (R + 31) / 32;
     uint32_t* bm = sm;                                                   // [E][W] row bitmaps
     uint16_t* wpre = reinterpret_cast<uint16_t*>(bm + size_t(E) * W);    // [E][W] rows before word
@@ -57,8 +64,6 @@ __global__ void __launch_bounds__(kUnionThreads) union_kernel(const int32_t* __r
     int* s_ioff = s_off + (E + 2);                                       // [E+1]
     __shared__ int s_warp[32];
     __shared__ int s_total, s_err, s_nvalid, s_items, s_nunion;
-    pdl_wait();
-    pdl_launch_dependents();
     const int tid = threadIdx.x;
     const int KS = K + S;
 
@@ -180,6 +185,48 @@ __global__ void __launch_bounds__(kUnionThreads) union_kernel(const int32_t* __r
     }
 }
 
+__global__ void __launch_bounds__(kUnionThreads) union_kernel(const int32_t* __restrict__ ids,
+                                                              int R, int E, int K, int S,
+                                                              int n_tile, int32_t* __restrict__ ub,
+                                                              UnionLayout L) {
+    extern __shared__ uint32_t sm[];
+    pdl_wait();
+    pdl_launch_dependents();
+    union_block(ids, R, E, K, S, n_tile, ub, L, sm);
+}
+
+// Selection and union of a small call (R <= kRouteUnionMaxRows) in one block:
+// warp w selects rows w, w + 32 (select.cuh), the ids stay in shared memory,
+// and the block builds the union from them.  Same decisions and the same
+// union buffer as route_select_kernel followed by union_kernel.
+__global__ void __launch_bounds__(kUnionThreads) route_union_kernel(
+    const float* __restrict__ logits, const float* __restrict__ bias,
+    const uint8_t* __restrict__ row_valid, int R, int E, int G, int TG, int K, float scaling,
+    int32_t* __restrict__ ids, float* __restrict__ wts, int S, int n_tile,
+    int32_t* __restrict__ ub, UnionLayout L) {
+    extern __shared__ uint32_t sm[];
+    float* s_b = reinterpret_cast<float*>(sm);                         // [32][E]
+    int32_t* s_ids = reinterpret_cast<int32_t*>(s_b + 32 * E);         // [R][K]
+    uint32_t* s_un = reinterpret_cast<uint32_t*>(s_ids + ((R * K + 3) & ~3));
+    pdl_wait();
+    pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int r = warp; r < R; r += kUnionThreads / 32) {
+        int id = -1;
+        float w = 0.0f;
+        if (row_valid == nullptr || row_valid[r] != 0)
+            select_row(logits + size_t(r) * E, bias, E, G, TG, K, scaling, s_b + warp * E, lane,
+                       &id, &w);
+        if (lane < K) {
+            s_ids[r * K + lane] = id;
+            ids[size_t(r) * K + lane] = id;
+            wts[size_t(r) * K + lane] = w;
+        }
+    }
+    __syncthreads();
+    union_block(s_ids, R, E, K, S, n_tile, ub, L, s_un);
+}
+
 // Quantise each valid row per 128 columns to e4m3 and write it to its gathered
 // positions (K routed slots, then the shared slot).  One warp per (row, block).
 __global__ void __launch_bounds__(256) dispatch_kernel(const uint16_t* __restrict__ x,
@@ -218,10 +265,7 @@ __global__ void __launch_bounds__(256) dispatch_kernel(const uint16_t* __restric
 
 cudaError_t launch_union(const int32_t* ids, int R, int E, int K, int S, int n_tile,
                          int32_t* ub, const UnionLayout& L, cudaStream_t stream) {
-    const int W = (R + 31) / 32;
-    const size_t words = size_t(E) * W;
-    const size_t smem = words * 4 + ((words + 1) & ~size_t(1)) * 2 + ((R + 15) & ~15) +
-                        size_t(4 * E + 8) * 4;
+    const size_t smem = union_smem_bytes(R, E);
     cudaError_t e = cudaFuncSetAttribute(union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -238,6 +282,22 @@ cudaError_t launch_dispatch(const uint16_t* x, const int32_t* ub, const UnionLay
     dim3 grid(R, (HB + 7) / 8);
     cudaError_t e = launch_pdl(dispatch_kernel, grid, dim3(256), 0, stream, x, ub, L, R, H, KS, xg, xs,
                                ready, n_ready);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_route_union(const float* logits, const float* bias, const uint8_t* row_valid,
+                               int R, int E, int G, int TG, int K, float scaling, int32_t* ids,
+                               float* wts, int S, int n_tile, int32_t* ub, const UnionLayout& L,
+                               cudaStream_t stream) {
+    if (R > kRouteUnionMaxRows) return cudaErrorInvalidValue;
+    const size_t smem = size_t(32) * E * 4 + size_t((R * K + 3) & ~3) * 4 + union_smem_bytes(R, E);
+    cudaError_t e = cudaFuncSetAttribute(route_union_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(route_union_kernel, dim3(1), dim3(kUnionThreads), smem, stream, logits, bias,
+                   row_valid, R, E, G, TG, K, scaling, ids, wts, S, n_tile, ub, L);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

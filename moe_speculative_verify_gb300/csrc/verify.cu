@@ -8,19 +8,24 @@
 // one-graph MTP": greedy verify runs on the device inside the step.
 //
 // Two kernels: the target's greedy token per row (argmax over the vocabulary,
-// one block per row), then the acceptance rule per span (one thread each).
+// one cluster of CTAs per row), then the acceptance rule per span (one thread each).
 // The argmax reduces 64-bit keys (ordered value, then the complement of the
 // index): the largest value wins, the lowest index wins ties, NaN never wins.
 // The key order is total, so the result does not depend on the reduction
 // order or the launch shape.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
+
+namespace cg = cooperative_groups;
 
 namespace moe {
 
 namespace {
 
-constexpr int kArgmaxThreads = 512;
+constexpr int kArgmaxThreads = 256;
+constexpr int kArgmaxCluster = 8;      // CTAs per row
 
 __device__ __forceinline__ uint64_t argmax_key(float v, uint32_t idx) {
     uint32_t hi;
@@ -36,21 +41,30 @@ __device__ __forceinline__ uint64_t argmax_key(float v, uint32_t idx) {
 
 __device__ __forceinline__ uint64_t max64(uint64_t a, uint64_t b) { return a > b ? a : b; }
 
+// A row is split over the kArgmaxCluster CTAs of one cluster, CTA c taking
+// the c-th contiguous slice (in vectors of 16 bytes when the rows allow it);
+// CTA 0 reduces the slices' keys through distributed shared memory.
 template <bool BF16, bool VEC>
 __global__ void __launch_bounds__(kArgmaxThreads) row_argmax_kernel(const void* __restrict__ logits,
                                                                    int V, int32_t* __restrict__ am) {
     __shared__ uint64_t s_red[kArgmaxThreads / 32];
+    __shared__ uint64_t s_best;
+    cg::cluster_group cl = cg::this_cluster();
     pdl_wait();
     pdl_launch_dependents();
-    const int r = blockIdx.x;
+    const int r = blockIdx.x / kArgmaxCluster;
+    const int c = static_cast<int>(cl.block_rank());
+    constexpr int PER = VEC ? (BF16 ? 8 : 4) : 1;          // elements per load
+    const int n = V / PER;                                  // loads per row
+    const int lo = static_cast<int>((int64_t(n) * c) / kArgmaxCluster);
+    const int hi = static_cast<int>((int64_t(n) * (c + 1)) / kArgmaxCluster);
     uint64_t best = 0;
     if (BF16) {
         const uint16_t* row = static_cast<const uint16_t*>(logits) + size_t(r) * V;
         if (VEC) {
-            const int nv = V / 8;
             const uint4* rv = reinterpret_cast<const uint4*>(row);
 #pragma unroll 4
-            for (int i = threadIdx.x; i < nv; i += kArgmaxThreads) {
+            for (int i = lo + threadIdx.x; i < hi; i += kArgmaxThreads) {
                 const uint4 q = __ldg(rv + i);
                 const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -60,16 +74,15 @@ __global__ void __launch_bounds__(kArgmaxThreads) row_argmax_kernel(const void* 
                 }
             }
         } else {
-            for (int i = threadIdx.x; i < V; i += kArgmaxThreads)
+            for (int i = lo + threadIdx.x; i < hi; i += kArgmaxThreads)
                 best = max64(best, argmax_key(bf16_bits_to_f32(row[i]), i));
         }
     } else {
         const float* row = static_cast<const float*>(logits) + size_t(r) * V;
         if (VEC) {
-            const int nv = V / 4;
             const float4* rv = reinterpret_cast<const float4*>(row);
 #pragma unroll 4
-            for (int i = threadIdx.x; i < nv; i += kArgmaxThreads) {
+            for (int i = lo + threadIdx.x; i < hi; i += kArgmaxThreads) {
                 const float4 q = __ldg(rv + i);
                 best = max64(best, argmax_key(q.x, 4 * i));
                 best = max64(best, argmax_key(q.y, 4 * i + 1));
@@ -77,7 +90,8 @@ __global__ void __launch_bounds__(kArgmaxThreads) row_argmax_kernel(const void* 
                 best = max64(best, argmax_key(q.w, 4 * i + 3));
             }
         } else {
-            for (int i = threadIdx.x; i < V; i += kArgmaxThreads) best = max64(best, argmax_key(row[i], i));
+            for (int i = lo + threadIdx.x; i < hi; i += kArgmaxThreads)
+                best = max64(best, argmax_key(row[i], i));
         }
     }
 #pragma unroll
@@ -88,9 +102,17 @@ __global__ void __launch_bounds__(kArgmaxThreads) row_argmax_kernel(const void* 
         best = (threadIdx.x < kArgmaxThreads / 32) ? s_red[threadIdx.x] : 0ull;
 #pragma unroll
         for (int d = 16; d >= 1; d >>= 1) best = max64(best, __shfl_xor_sync(0xFFFFFFFFu, best, d));
+        if (threadIdx.x == 0) s_best = best;
+    }
+    cl.sync();   // every slice's key is in its CTA's shared memory
+    if (c == 0 && threadIdx.x < 32) {
+        best = (threadIdx.x < kArgmaxCluster) ? *cl.map_shared_rank(&s_best, threadIdx.x) : 0ull;
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1) best = max64(best, __shfl_xor_sync(0xFFFFFFFFu, best, d));
         if (threadIdx.x == 0)
             am[r] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(best & 0xFFFFFFFFu));
     }
+    cl.sync();   // no CTA leaves while CTA 0 may still read its key
 }
 
 // Span q: draft j (1 <= j <= n_draft) is accepted while every earlier one was
@@ -120,17 +142,18 @@ cudaError_t launch_greedy_verify(const void* logits, bool bf16, int V, int R, co
     const size_t elem = bf16 ? 2 : 4;
     const bool vec = ((size_t(V) * elem) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(logits) % 16 == 0);
+    const dim3 grid(static_cast<unsigned>(R) * kArgmaxCluster), block(kArgmaxThreads);
     cudaError_t e;
     if (bf16)
-        e = vec ? launch_pdl(row_argmax_kernel<true, true>, dim3(R), dim3(kArgmaxThreads), 0, stream,
-                             logits, V, am)
-                : launch_pdl(row_argmax_kernel<true, false>, dim3(R), dim3(kArgmaxThreads), 0,
-                             stream, logits, V, am);
+        e = vec ? launch_pdl_cluster(row_argmax_kernel<true, true>, grid, block, kArgmaxCluster, 0,
+                                     stream, logits, V, am)
+                : launch_pdl_cluster(row_argmax_kernel<true, false>, grid, block, kArgmaxCluster, 0,
+                                     stream, logits, V, am);
     else
-        e = vec ? launch_pdl(row_argmax_kernel<false, true>, dim3(R), dim3(kArgmaxThreads), 0,
-                             stream, logits, V, am)
-                : launch_pdl(row_argmax_kernel<false, false>, dim3(R), dim3(kArgmaxThreads), 0,
-                             stream, logits, V, am);
+        e = vec ? launch_pdl_cluster(row_argmax_kernel<false, true>, grid, block, kArgmaxCluster, 0,
+                                     stream, logits, V, am)
+                : launch_pdl_cluster(row_argmax_kernel<false, false>, grid, block, kArgmaxCluster,
+                                     0, stream, logits, V, am);
     if (e != cudaSuccess) return e;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int n_span = R / 8;

@@ -141,6 +141,39 @@ def test_stepwise_entry_points():
     assert np.all(bf16_to_np(out)[~valid] == 0)
 
 
+@pytest.mark.parametrize("shape,R,pads", [(synth.TINY, 8, ()), (MEDIUM, 8, (2, 5)),
+                                          (MEDIUM, 37, (0, 36)), (MEDIUM, 64, (7, 23, 39, 55)),
+                                          (synth.TINY, 1, ())])
+def test_layer_routing_matches_stepwise(shape, R, pads):
+    """moe_layer selects and builds the union in one kernel at these row counts;
+    its ids, weights and output equal moe_route + moe_build_union +
+    moe_expert_ffn_fp8 + moe_combine bit for bit."""
+    wl, t, h = _make(shape, R, pads)
+    cfg = m.Config.from_shape(shape)
+    out, ids, w, _ = run_layer(cfg, t, R)
+    dev = torch.device("cuda")
+    K, H, E = shape.topk, shape.hidden, shape.n_experts
+    ids2 = torch.empty((R, K), dtype=torch.int32, device=dev)
+    w2 = torch.empty((R, K), dtype=torch.float32, device=dev)
+    logits = torch.empty((R, E), dtype=torch.float32, device=dev)
+    m.moe_route(cfg, t["x"], t["wr"], t["bias"], t["row_valid"], ids2, w2, logits)
+    ub = torch.zeros(m.moe_union_bytes(cfg, R) // 4, dtype=torch.int32, device=dev)
+    m.moe_build_union(cfg, ids2, ub)
+    ws = torch.zeros(m.moe_ffn_workspace_bytes(cfg, R), dtype=torch.uint8, device=dev)
+    ys = torch.empty((R * K, H), dtype=torch.float32, device=dev)
+    ysh = torch.empty((R, H), dtype=torch.float32, device=dev)
+    m.moe_expert_ffn_fp8(cfg, t["x"], m.Weights.from_tensors(t), ub, ys, ysh, ws)
+    out2 = torch.full((R, H), float("nan"), dtype=torch.bfloat16, device=dev)
+    m.moe_combine(cfg, ys, ysh, w2, ub, out2)
+    torch.cuda.synchronize()
+    assert m.moe_get_device_error(ws) == 0
+    assert np.array_equal(ids.cpu().numpy(), ids2.cpu().numpy())
+    assert np.array_equal(w.cpu().numpy().view(np.uint32), w2.cpu().numpy().view(np.uint32))
+    assert np.array_equal(bf16_to_np(out), bf16_to_np(out2))
+    ref_ids, _, _ = oracle.route(shape, h["x"], h["wr"], h["bias"], h["row_valid"])
+    assert np.array_equal(ids.cpu().numpy(), ref_ids)
+
+
 @pytest.mark.parametrize("shape,R", [(synth.TINY, 8), (MEDIUM, 37), (MEDIUM, 200), (synth.TINY, 600)])
 def test_fused_gemms_match_two_launches(shape, R):
     """moe_expert_gemms_fp8 (one persistent launch, down tiles gated by per-item
