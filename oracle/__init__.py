@@ -59,6 +59,8 @@ def lib() -> C.CDLL:
         L.orc_moe_layer.argtypes = [C.POINTER(_Cfg)] + [P] * 15 + [P, C.c_int32, P,
                                                                    C.c_int32, P, P, P, P,
                                                                    C.c_int32]
+        L.orc_expert_ffn_a16.argtypes = [C.POINTER(_Cfg)] + [P] * 8 + [C.c_int32, C.c_int32]
+        L.orc_moe_layer_variant.argtypes = L.orc_moe_layer.argtypes + [C.c_int32]
         L.orc_greedy_verify.argtypes = [P, C.c_int32, C.c_int32, P, P, C.c_int32, P, P, P]
         L.orc_add_rmsnorm.argtypes = [P, P, P, C.c_float, P, C.c_int32, C.c_int32, P, P]
         L.orc_num_threads.restype = C.c_int
@@ -195,13 +197,31 @@ def expert_ffn(cfg, xq, xs, wg, sg, wu, su, wd, sd, acc64: bool = True):
     return out, hq, hs
 
 
-def moe_layer(cfg, t: dict, rows=None, acc64: bool = True):
+_VARIANTS = {"fp8": 0, "w8a16": 1, "exact": 2}
+
+
+def expert_ffn_a16(cfg, x_bf16, wg, sg, wu, su, wd, sd, round16: bool = True,
+                   acc64: bool = True) -> np.ndarray:
+    """One expert on one bf16 row (uint16 [H]) with 16-bit activations: the
+    w8a16 variant (round16) or the unrounded yardstick.  Returns o [H] fp64."""
+    out = np.empty(cfg.hidden, dtype=np.float64)
+    args = [_c(x_bf16, np.uint16), _c(wg, np.uint8), _c(sg, np.float32), _c(wu, np.uint8),
+            _c(su, np.float32), _c(wd, np.uint8), _c(sd, np.float32)]
+    c = _cfg(cfg)
+    lib().orc_expert_ffn_a16(C.byref(c), *[_p(a) for a in args], _p(out), 1 if round16 else 0,
+                             1 if acc64 else 0)
+    return out
+
+
+def moe_layer(cfg, t: dict, rows=None, acc64: bool = True, variant: str = "fp8"):
     """The whole layer on host arrays.
 
     t holds x (uint16 [R,H]), wr, bias, w_gate/s_gate, w_up/s_up, w_down/s_down,
     sh_gate/sh_s_gate, sh_up/sh_s_up, sh_down/sh_s_down and optionally row_valid.
-    Returns dict(out uint16 [R,H], ids, wts, y_acc fp64 [R,H]); rows not listed in
-    `rows` are left zero.
+    variant: "fp8" (activations and h quantised per 1x128 to e4m3), "w8a16"
+    (bf16 activations, weights dequantised to bf16, h rounded to bf16) or
+    "exact" (no activation or weight rounding).  Returns dict(out uint16 [R,H],
+    ids, wts, y_acc fp64 [R,H]); rows not listed in `rows` are left zero.
     """
     x = _c(t["x"], np.uint16)
     R = x.shape[0]
@@ -221,9 +241,9 @@ def moe_layer(cfg, t: dict, rows=None, acc64: bool = True):
     wts = np.zeros((R, K), dtype=np.float32)
     y = np.zeros((R, H), dtype=np.float64)
     c = _cfg(cfg)
-    lib().orc_moe_layer(C.byref(c), _p(x), *[_p(a) for a in arrs], _p(rv), R, _p(rl),
-                        0 if rl is None else rl.size, _p(out), _p(ids), _p(wts), _p(y),
-                        1 if acc64 else 0)
+    lib().orc_moe_layer_variant(C.byref(c), _p(x), *[_p(a) for a in arrs], _p(rv), R, _p(rl),
+                                0 if rl is None else rl.size, _p(out), _p(ids), _p(wts), _p(y),
+                                1 if acc64 else 0, _VARIANTS[variant])
     return {"out": out, "ids": ids, "wts": wts, "y_acc": y}
 
 

@@ -318,6 +318,46 @@ void expert_ffn(const Cfg& c, const uint8_t* xq, const float* xs,
     if (hs_out) std::memcpy(hs_out, hs.data(), sizeof(float) * (I / QB));
 }
 
+// One expert on one row with 16-bit activations ("w8a16": mstar #388, commit
+// on kernel switches and the FlashInfer commit -- fp8 weights, bf16
+// activations at decode sizes; the activations are not quantised).  x is the
+// row's bf16 values.  round16 != 0 (the w8a16 variant, READING of "w8a16"):
+// every weight is dequantised to bf16, bf16_rne(e4m3(q) * s) from the exact
+// product, and h = silu(g) * u is rounded to bf16 before the down GEMM (the
+// down GEMM's activations are 16-bit too).  round16 == 0: weights e4m3(q) * s
+// and h exact in fp64 -- the layer without any activation or weight rounding,
+// the yardstick both variants' quantisation error is measured against.
+template <typename Acc>
+void expert_ffn_a16(const Cfg& c, const float* x, const uint8_t* wg, const float* sg,
+                    const uint8_t* wu, const float* su, const uint8_t* wd, const float* sd,
+                    double* out, bool round16) {
+    const int H = c.hidden, I = c.inter;
+    const float* lut = decode_table();
+    auto w_at = [&](const uint8_t* q, const float* sc, int ncols, int n, int k) -> double {
+        const double v = double(lut[q[size_t(n) * ncols + k]]) *
+                         double(sc[size_t(n / QB) * (ncols / QB) + k / QB]);
+        return round16 ? double(bf16_to_f32(f64_to_bf16(v))) : v;
+    };
+    std::vector<double> hv(I);
+#pragma omp parallel for schedule(static)
+    for (int n = 0; n < I; ++n) {
+        Acc g = 0, u = 0;
+        for (int k = 0; k < H; ++k) {
+            g += Acc(x[k]) * Acc(w_at(wg, sg, H, n, k));
+            u += Acc(x[k]) * Acc(w_at(wu, su, H, n, k));
+        }
+        const double gd = double(g);
+        const double hval = gd / (1.0 + std::exp(-gd)) * double(u);
+        hv[n] = round16 ? double(bf16_to_f32(f64_to_bf16(hval))) : hval;
+    }
+#pragma omp parallel for schedule(static)
+    for (int m = 0; m < H; ++m) {
+        Acc o = 0;
+        for (int k = 0; k < I; ++k) o += Acc(hv[k]) * Acc(w_at(wd, sd, I, m, k));
+        out[m] = double(o);
+    }
+}
+
 }  // namespace
 
 // =================================================================== C ABI ==
@@ -469,6 +509,20 @@ void orc_expert_ffn(const orc_config* cfg, const uint8_t* xq, const float* xs,
         expert_ffn<float>(c, xq, xs, wg, sg, wu, su, wd, sd, out, hq_out, hs_out);
 }
 
+// One expert on one bf16 row with 16-bit activations (see expert_ffn_a16):
+// round16 != 0 the w8a16 variant, 0 the unrounded yardstick.
+void orc_expert_ffn_a16(const orc_config* cfg, const uint16_t* x_bf16, const uint8_t* wg,
+                        const float* sg, const uint8_t* wu, const float* su, const uint8_t* wd,
+                        const float* sd, double* out, int32_t round16, int32_t acc64) {
+    Cfg c = to_cfg(cfg);
+    std::vector<float> xf(c.hidden);
+    for (int h = 0; h < c.hidden; ++h) xf[h] = bf16_to_f32(x_bf16[h]);
+    if (acc64)
+        expert_ffn_a16<double>(c, xf.data(), wg, sg, wu, su, wd, sd, out, round16 != 0);
+    else
+        expert_ffn_a16<float>(c, xf.data(), wg, sg, wu, su, wd, sd, out, round16 != 0);
+}
+
 // The whole layer on the rows listed in `rows` (all R rows when rows == NULL).
 // Weights: routed gate/up [E,I,H] with scales [E,I/128,H/128], down [E,H,I]
 // with scales [E,H/128,I/128]; the shared expert(s) in the same layout with
@@ -484,14 +538,17 @@ void orc_expert_ffn(const orc_config* cfg, const uint8_t* xq, const float* xs,
 //      ([P1] "Span pad ranks zero-fill ... no NaN leaks").
 // Outputs: out_bf16 [R,H]; ids/wts [R,K]; y_acc [R,H] fp64 (nullable): the
 // value before the bf16 rounding.
-void orc_moe_layer(const orc_config* cfg, const uint16_t* x, const float* wr, const float* bias,
-                   const uint8_t* w_gate, const float* s_gate, const uint8_t* w_up,
-                   const float* s_up, const uint8_t* w_down, const float* s_down,
-                   const uint8_t* sh_gate, const float* sh_s_gate, const uint8_t* sh_up,
-                   const float* sh_s_up, const uint8_t* sh_down, const float* sh_s_down,
-                   const uint8_t* row_valid, int32_t R, const int32_t* rows, int32_t n_rows,
-                   uint16_t* out_bf16, int32_t* ids_out, float* wts_out, double* y_acc,
-                   int32_t acc64) {
+// variant: 0 = fp8 (the layer above), 1 = w8a16, 2 = no activation or weight
+// rounding (see expert_ffn_a16); routing and combine are the same in all three.
+void orc_moe_layer_variant(const orc_config* cfg, const uint16_t* x, const float* wr,
+                           const float* bias, const uint8_t* w_gate, const float* s_gate,
+                           const uint8_t* w_up, const float* s_up, const uint8_t* w_down,
+                           const float* s_down, const uint8_t* sh_gate, const float* sh_s_gate,
+                           const uint8_t* sh_up, const float* sh_s_up, const uint8_t* sh_down,
+                           const float* sh_s_down, const uint8_t* row_valid, int32_t R,
+                           const int32_t* rows, int32_t n_rows, uint16_t* out_bf16,
+                           int32_t* ids_out, float* wts_out, double* y_acc, int32_t acc64,
+                           int32_t variant) {
     Cfg c = to_cfg(cfg);
     const int H = c.hidden, I = c.inter, K = c.topk;
     const size_t gsz = size_t(I) * H;                    // elements per gate/up/down
@@ -525,24 +582,47 @@ void orc_moe_layer(const orc_config* cfg, const uint16_t* x, const float* wr, co
         route_row_from_logits(c, logits.data(), bias, id, w);
         for (int h = 0; h < H; ++h) xf[h] = bf16_to_f32(xr[h]);
         quant_1x128(xf.data(), H, xq.data(), xs.data());
+        auto ffn = [&](const uint8_t* g_, const float* sg_, const uint8_t* u_, const float* su_,
+                       const uint8_t* d_, const float* sd_) {
+            if (variant == 0)
+                orc_expert_ffn(cfg, xq.data(), xs.data(), g_, sg_, u_, su_, d_, sd_, o.data(),
+                               nullptr, nullptr, acc64);
+            else if (acc64)
+                expert_ffn_a16<double>(c, xf.data(), g_, sg_, u_, su_, d_, sd_, o.data(),
+                                       variant == 1);
+            else
+                expert_ffn_a16<float>(c, xf.data(), g_, sg_, u_, su_, d_, sd_, o.data(),
+                                      variant == 1);
+        };
         for (int k = 0; k < K; ++k) {
             const size_t e = size_t(id[k]);
-            orc_expert_ffn(cfg, xq.data(), xs.data(), w_gate + e * gsz, s_gate + e * gss,
-                           w_up + e * gsz, s_up + e * gss, w_down + e * gsz, s_down + e * gss,
-                           o.data(), nullptr, nullptr, acc64);
+            ffn(w_gate + e * gsz, s_gate + e * gss, w_up + e * gsz, s_up + e * gss,
+                w_down + e * gsz, s_down + e * gss);
             for (int h = 0; h < H; ++h)
                 acc[h] = (k == 0) ? double(w[k]) * o[h] : acc[h] + double(w[k]) * o[h];
         }
         for (int sidx = 0; sidx < c.n_shared; ++sidx) {
             const size_t e = size_t(sidx);
-            orc_expert_ffn(cfg, xq.data(), xs.data(), sh_gate + e * gsz, sh_s_gate + e * gss,
-                           sh_up + e * gsz, sh_s_up + e * gss, sh_down + e * gsz,
-                           sh_s_down + e * gss, o.data(), nullptr, nullptr, acc64);
+            ffn(sh_gate + e * gsz, sh_s_gate + e * gss, sh_up + e * gsz, sh_s_up + e * gss,
+                sh_down + e * gsz, sh_s_down + e * gss);
             for (int h = 0; h < H; ++h) acc[h] = acc[h] + o[h];
         }
         for (int h = 0; h < H; ++h) yrow[h] = f64_to_bf16(acc[h]);
         if (y_acc) std::memcpy(y_acc + size_t(r) * H, acc.data(), sizeof(double) * H);
     }
+}
+
+void orc_moe_layer(const orc_config* cfg, const uint16_t* x, const float* wr, const float* bias,
+                   const uint8_t* w_gate, const float* s_gate, const uint8_t* w_up,
+                   const float* s_up, const uint8_t* w_down, const float* s_down,
+                   const uint8_t* sh_gate, const float* sh_s_gate, const uint8_t* sh_up,
+                   const float* sh_s_up, const uint8_t* sh_down, const float* sh_s_down,
+                   const uint8_t* row_valid, int32_t R, const int32_t* rows, int32_t n_rows,
+                   uint16_t* out_bf16, int32_t* ids_out, float* wts_out, double* y_acc,
+                   int32_t acc64) {
+    orc_moe_layer_variant(cfg, x, wr, bias, w_gate, s_gate, w_up, s_up, w_down, s_down, sh_gate,
+                          sh_s_gate, sh_up, sh_s_up, sh_down, sh_s_down, row_valid, R, rows,
+                          n_rows, out_bf16, ids_out, wts_out, y_acc, acc64, 0);
 }
 
 // ------------------------------------------------- greedy verify + accept ----
