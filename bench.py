@@ -293,6 +293,44 @@ def measure_extras(m, cfg, wl, bufs, dev, steps) -> dict:
     return out
 
 
+def measure_w8a16(m, cfg, W, wl, dev, steps, flush) -> dict:
+    """The layer at 1, 2, 4 and 8 rows with the w8a16 expert FFNs against the
+    fp8 ones (moe_layer_w8a16 vs moe_layer), same weights and routing mix,
+    L2 flushed before every call; microseconds per call."""
+    stream = torch.cuda.current_stream()
+    out = {}
+    for R in (1, 2, 4, 8):
+        wr = synth.Workload(f"{wl.name}_r{R}", wl.shape, rows=R, routing=wl.routing,
+                            hot_per_group=wl.hot_per_group, hot_delta=wl.hot_delta)
+        ri = synth.make_router_inputs(wr, device=dev)
+        ws = torch.zeros(m.moe_workspace_bytes(cfg, R), dtype=torch.uint8, device=dev)
+        y = torch.empty((R, wl.shape.hidden), dtype=torch.bfloat16, device=dev)
+        ids = torch.empty((R, wl.shape.topk), dtype=torch.int32, device=dev)
+        res = {}
+        for name, fn in (("fp8", m.moe_layer), ("w8a16", m.moe_layer_w8a16)):
+            ts = []
+            for i in range(max(3, steps) + 3):
+                flush.zero_()
+                torch.cuda._sleep(HOST_AHEAD_CYCLES // 4)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn(cfg, ri["x"], ri["wr"], ri["bias"], W, ri["row_valid"], y, ws, topk_ids=ids)
+                b.record(stream)
+                b.synchronize()
+                if i >= 3:
+                    ts.append(a.elapsed_time(b))
+            assert m.moe_get_device_error(ws) == 0
+            res[name] = statistics.mean(ts)
+        U = len(np.unique(ids.cpu().numpy()))
+        nbytes = (U + wl.shape.n_shared) * 3 * wl.shape.hidden * wl.shape.inter
+        out[str(R)] = {"distinct_experts": U, "fp8_us": round(res["fp8"] * 1e3, 2),
+                       "w8a16_us": round(res["w8a16"] * 1e3, 2),
+                       "w8a16_weight_gbs": round(nbytes / (res["w8a16"] / 1e3) / 1e9, 1),
+                       "w8a16_over_fp8": round(res["w8a16"] / res["fp8"], 3)}
+    return out
+
+
 # -------------------------------------------------------------------- ours --
 def main() -> None:
     ap = argparse.ArgumentParser()
@@ -465,6 +503,9 @@ def main() -> None:
     # the verify-step extras, each timed alone with events on its stream
     if rank == 0:
         extra.update(measure_extras(m, cfg, wl, res["bufs"], dev, args.steps))
+        if wl.rows <= m.W8A16_MAX_ROWS:
+            extra["w8a16_vs_fp8"] = measure_w8a16(m, cfg, W, wl, dev, args.steps,
+                                                  res["bufs"]["flush"])
 
     # end to end through moe_layer with host buffers
     import moe_speculative_verify_gb300 as m2

@@ -69,6 +69,7 @@ typedef enum {
 
 /* Compiled limits. */
 #define MOE_MAX_ROWS 4096      /* rows per call                                   */
+#define MOE_W8A16_MAX_ROWS 64  /* rows per call of the w8a16 variant              */
 #define MOE_MAX_EXPERTS 256    /* routed experts                                  */
 #define MOE_MAX_TOPK 16        /* experts per row                                 */
 #define MOE_MAX_GROUPS 32      /* expert groups                                   */
@@ -211,6 +212,25 @@ moe_status_t moe_expert_ffn_fp8(const moe_config_t* cfg, const void* x_bf16,
                                 moe_stream_t stream);
 
 /*
+ * moe_expert_ffn_w8a16 -- the expert FFNs of the union with 16-bit activations
+ * (mstar #388, commit on kernel switches and the FlashInfer commit: fp8 linears
+ * run w8a16 at decode sizes, fp8 weights with bf16 activations).  Per gathered
+ * slot (row r, expert e), with no activation quantisation:
+ *   every weight is dequantised to bf16: bf16_rne(e4m3(q) * s_block) (the
+ *     product in fp32);
+ *   g = x.Wg^T, u = x.Wu^T with x bf16 and fp32 accumulation over all of K;
+ *   h = silu(g) * u rounded to bf16;  o = h.Wd^T with fp32 accumulation.
+ * The GEMMs run on tcgen05 bf16 tensor cores (kind::f16); the dequantisation
+ * happens in shared memory, inside the GEMM kernel.
+ * Arguments, outputs and workspace as moe_expert_ffn_fp8 (the union built for
+ * the same R).  R <= MOE_W8A16_MAX_ROWS, else MOE_ERR_UNSUPPORTED.
+ */
+moe_status_t moe_expert_ffn_w8a16(const moe_config_t* cfg, const void* x_bf16,
+                                  const moe_weights_t* w, const int32_t* union_buf, int32_t R,
+                                  float* y_slots, float* y_shared, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream);
+
+/*
  * The steps of moe_expert_ffn_fp8, callable one by one (same arguments, same
  * workspace).  moe_expert_ffn_fp8 is moe_dispatch followed by
  * moe_expert_gemms_fp8; moe_gate_up_fp8 followed by moe_down_fp8 computes the
@@ -286,6 +306,16 @@ moe_status_t moe_layer(const moe_config_t* cfg, const void* x_bf16, const float*
                        const float* bias, const moe_weights_t* w, const uint8_t* row_valid,
                        int32_t R, void* out_bf16, int32_t* topk_ids_out, float* topk_w_out,
                        void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_layer_w8a16 -- moe_layer with the expert FFNs of moe_expert_ffn_w8a16
+ * (routing, union and combine unchanged).  Same arguments and workspace size;
+ * R <= MOE_W8A16_MAX_ROWS, else MOE_ERR_UNSUPPORTED.
+ */
+moe_status_t moe_layer_w8a16(const moe_config_t* cfg, const void* x_bf16, const float* w_router,
+                             const float* bias, const moe_weights_t* w, const uint8_t* row_valid,
+                             int32_t R, void* out_bf16, int32_t* topk_ids_out, float* topk_w_out,
+                             void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
  * moe_layer_noalloc -- moe_layer without a caller-provided workspace.  The

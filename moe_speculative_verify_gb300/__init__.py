@@ -23,7 +23,7 @@ __all__ = [
     "moe_diag_wait_timeout", "moe_status_string", "moe_dispatch", "moe_gate_up_fp8",
     "moe_down_fp8", "ffn_layout", "moe_layer_noalloc", "moe_expert_gemms_fp8",
     "moe_greedy_verify", "moe_combine_add_rmsnorm", "union_layout", "rows_per_item",
-    "MOE_MAX_ROWS",
+    "MOE_MAX_ROWS", "moe_expert_ffn_w8a16", "moe_layer_w8a16", "W8A16_MAX_ROWS",
 ]
 
 MOE_MAX_ROWS = 4096
@@ -101,10 +101,13 @@ def load() -> C.CDLL:
     L.moe_combine_add_rmsnorm.argtypes = [cfg, P, P, P, P, I32, P, P, C.c_float, P, P, P]
     L.moe_greedy_verify.argtypes = [P, I32, I32, I32, P, P, P, P, P, P]
     L.moe_layer_noalloc.argtypes = [cfg, P, P, P, C.POINTER(Weights), P, I32, P, P, P, P, P]
+    L.moe_expert_ffn_w8a16.argtypes = L.moe_expert_ffn_fp8.argtypes
+    L.moe_layer_w8a16.argtypes = L.moe_layer.argtypes
     L.moe_diag_wait_timeout.argtypes = [P, C.c_uint32, P]
     for n in ("moe_route", "moe_build_union", "moe_expert_ffn_fp8", "moe_combine", "moe_layer",
               "moe_get_device_error", "moe_diag_wait_timeout", "moe_dispatch", "moe_layer_noalloc", "moe_greedy_verify", "moe_combine_add_rmsnorm",
-              "moe_gate_up_fp8", "moe_down_fp8", "moe_expert_gemms_fp8"):
+              "moe_gate_up_fp8", "moe_down_fp8", "moe_expert_gemms_fp8", "moe_expert_ffn_w8a16",
+              "moe_layer_w8a16"):
         getattr(L, n).restype = C.c_int
     _LIB = L
     return L
@@ -165,6 +168,16 @@ def moe_expert_ffn_fp8(cfg: Config, x, weights: Weights, union_buf, y_slots, y_s
            "moe_expert_ffn_fp8")
 
 
+def moe_expert_ffn_w8a16(cfg: Config, x, weights: Weights, union_buf, y_slots, y_shared, ws,
+                         stream=None) -> None:
+    """The expert FFNs with bf16 activations and weights dequantised in the kernel."""
+    R = x.shape[0]
+    _check(load().moe_expert_ffn_w8a16(C.byref(cfg), _ptr(x), C.byref(weights), _ptr(union_buf),
+                                       R, _ptr(y_slots), _ptr(y_shared), _ptr(ws),
+                                       ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_expert_ffn_w8a16")
+
+
 def moe_dispatch(cfg: Config, x, union_buf, ws, stream=None) -> None:
     _check(load().moe_dispatch(C.byref(cfg), _ptr(x), _ptr(union_buf), x.shape[0], _ptr(ws),
                                ws.numel() * ws.element_size(), _stream(stream)), "moe_dispatch")
@@ -216,6 +229,17 @@ def moe_layer(cfg: Config, x, w_router, bias, weights: Weights, row_valid, out, 
            "moe_layer")
 
 
+def moe_layer_w8a16(cfg: Config, x, w_router, bias, weights: Weights, row_valid, out, ws,
+                    topk_ids=None, topk_w=None, stream=None) -> None:
+    """moe_layer with the w8a16 expert FFNs (R <= W8A16_MAX_ROWS)."""
+    R = x.shape[0]
+    _check(load().moe_layer_w8a16(C.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias),
+                                  C.byref(weights), _ptr(row_valid), R, _ptr(out),
+                                  _ptr(topk_ids), _ptr(topk_w), _ptr(ws),
+                                  ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_layer_w8a16")
+
+
 def moe_layer_noalloc(cfg: Config, x, w_router, bias, weights: Weights, row_valid, out,
                       topk_ids=None, topk_w=None, device_status=None, stream=None) -> None:
     """moe_layer with the library's own fixed scratch array (no workspace argument)."""
@@ -246,6 +270,8 @@ def moe_diag_wait_timeout(ws, timeout_us: int, stream=None) -> None:
 
 
 # ---------------------------------------------------------------- layouts --
+W8A16_MAX_ROWS = 64          # the w8a16 variant's row limit (mirrors the library)
+
 def rows_per_item(R: int) -> int:
     """Rows per GEMM work item chosen for a call with R rows (mirrors the library)."""
     return 16 if R <= 64 else (32 if R <= 512 else 64)
@@ -288,4 +314,8 @@ def ffn_layout(cfg: Config, R: int) -> dict:
     b = up(b + rows * I, 256)
     out["hs"] = b
     out["bytes"] = up(b + rows * (I // 128) * 4, 256)
+    if R <= W8A16_MAX_ROWS:
+        out["xb"] = out["xg"]
+        out["hb"] = up(out["xb"] + rows * H * 2, 256)
+        out["bytes"] = max(out["bytes"], up(out["hb"] + rows * I * 2, 256))
     return out

@@ -159,6 +159,21 @@ FfnCall ffn_call(const moe_config_t* c, int32_t R, void* ws) {
     return f;
 }
 
+// 2-D bf16 tensor [rows, cols]: 128-byte-swizzled boxes of 64 columns x
+// box_rows rows; out-of-range rows read as zero.
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+                   uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The eight tensor maps of the expert GEMMs.  Shared-expert maps fall back to
 // the routed tensors when there is no shared expert (never read then).
 bool make_maps(const moe_config_t* c, const moe_weights_t* w, const FfnCall& f, moe::FfnMaps* mp) {
@@ -228,6 +243,56 @@ moe_status_t ffn_impl(const moe_config_t* c, const void* x, const moe_weights_t*
     moe_status_t st = dispatch_impl(c, x, ub, R, ws, s);
     if (st != MOE_OK) return st;
     return gemm_impl(moe::kFfnFused, c, w, ub, R, y_slots, y_shared, ws, s);
+}
+
+// The w8a16 variant: bf16 rows gathered, then the dequantising GEMM kernel.
+moe_status_t ffn16_impl(const moe_config_t* c, const void* x, const moe_weights_t* w,
+                        const int32_t* ub, int32_t R, float* y_slots, float* y_shared, void* ws,
+                        cudaStream_t s) {
+    const FfnCall f = ffn_call(c, R, ws);
+    if (f.FL.xb < 0 || f.nt != moe::kW8A16RowsPerItem) return MOE_ERR_UNSUPPORTED;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    uint16_t* xb = reinterpret_cast<uint16_t*>(base + f.FL.xb);
+    uint16_t* hb = reinterpret_cast<uint16_t*>(base + f.FL.hb);
+    const int H = c->hidden, I = c->inter, E = c->n_experts, S = c->n_shared;
+    moe_status_t st = cuda_status(moe::launch_dispatch16(static_cast<const uint16_t*>(x), ub, f.UL,
+                                                         R, H, c->topk + S, xb, f.ready,
+                                                         f.FL.n_ready, s));
+    if (st != MOE_OK) return st;
+    const DeviceInfo dev = device_info();
+    if (dev.sms <= 0) return MOE_ERR_CUDA;
+    moe::FfnMaps mp;
+    const uint64_t srows = S ? uint64_t(S) : 1ull;
+    if (!(make_map(&mp.g, w->w_gate, uint64_t(E) * I, H, 128) &&
+          make_map(&mp.u, w->w_up, uint64_t(E) * I, H, 128) &&
+          make_map(&mp.sg, S ? w->sh_gate : w->w_gate, srows * I, H, 128) &&
+          make_map(&mp.su, S ? w->sh_up : w->w_up, srows * I, H, 128) &&
+          make_map_bf16(&mp.x, xb, f.FL.rows, H, moe::kW8A16RowsPerItem) &&
+          make_map(&mp.d, w->w_down, uint64_t(E) * H, I, 128) &&
+          make_map(&mp.sd, S ? w->sh_down : w->w_down, srows * H, I, 128) &&
+          make_map_bf16(&mp.h, hb, f.FL.rows, I, moe::kW8A16RowsPerItem)))
+        return MOE_ERR_CUDA;
+    moe::Ffn16Args a{};
+    a.ub = ub;
+    a.ul = f.UL;
+    a.s_gate = w->s_gate;
+    a.s_up = w->s_up;
+    a.sh_s_gate = S ? w->sh_s_gate : w->s_gate;
+    a.sh_s_up = S ? w->sh_s_up : w->s_up;
+    a.s_down = w->s_down;
+    a.sh_s_down = S ? w->sh_s_down : w->s_down;
+    a.hb = hb;
+    a.y_slots = y_slots;
+    a.y_shared = y_shared;
+    a.ready = f.ready;
+    a.err = f.err;
+    a.H = H;
+    a.I = I;
+    a.E = E;
+    a.K = c->topk;
+    a.KS = c->topk + S;
+    a.timeout_ns = timeout_ns(c);
+    return cuda_status(moe::launch_ffn16(mp, a, dev.sms, dev.smem_optin, s));
 }
 
 moe_status_t combine_impl(const moe_config_t* c, const float* y_slots, const float* y_shared,
@@ -317,6 +382,26 @@ moe_status_t moe_expert_ffn_fp8(const moe_config_t* cfg, const void* x_bf16,
     if (ws_bytes < moe_ffn_workspace_bytes(cfg, R)) return MOE_ERR_WORKSPACE;
     return ffn_impl(cfg, x_bf16, w, union_buf, R, y_slots, y_shared, ws,
                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_expert_ffn_w8a16(const moe_config_t* cfg, const void* x_bf16,
+                                  const moe_weights_t* w, const int32_t* union_buf, int32_t R,
+                                  float* y_slots, float* y_shared, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream) {
+    moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if ((st = check_rows(R)) != MOE_OK) return st;
+    if (R > MOE_W8A16_MAX_ROWS) return MOE_ERR_UNSUPPORTED;
+    if (R == 0) return MOE_OK;
+    if ((st = check_weights(cfg, w)) != MOE_OK) return st;
+    if (!x_bf16 || !union_buf || !y_slots || !ws) return MOE_ERR_INVALID_ARG;
+    if (cfg->n_shared > 0 && !y_shared) return MOE_ERR_INVALID_ARG;
+    if (!aligned(x_bf16, 16) || !aligned(union_buf, 16) || !aligned(y_slots, 4) ||
+        (y_shared && !aligned(y_shared, 4)) || !aligned(ws, 256))
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < moe_ffn_workspace_bytes(cfg, R)) return MOE_ERR_WORKSPACE;
+    return ffn16_impl(cfg, x_bf16, w, union_buf, R, y_slots, y_shared, ws,
+                      reinterpret_cast<cudaStream_t>(stream));
 }
 
 // Common checks of the FFN-stage entry points.
@@ -414,13 +499,15 @@ moe_status_t moe_combine_add_rmsnorm(const moe_config_t* cfg, const float* y_slo
         reinterpret_cast<cudaStream_t>(stream)));
 }
 
-moe_status_t moe_layer(const moe_config_t* cfg, const void* x_bf16, const float* w_router,
-                       const float* bias, const moe_weights_t* w, const uint8_t* row_valid,
-                       int32_t R, void* out_bf16, int32_t* topk_ids_out, float* topk_w_out,
-                       void* ws, size_t ws_bytes, moe_stream_t stream) {
+static moe_status_t layer_impl(const moe_config_t* cfg, const void* x_bf16,
+                               const float* w_router, const float* bias, const moe_weights_t* w,
+                               const uint8_t* row_valid, int32_t R, void* out_bf16,
+                               int32_t* topk_ids_out, float* topk_w_out, void* ws,
+                               size_t ws_bytes, moe_stream_t stream, bool w8a16) {
     moe_status_t st = check_cfg(cfg);
     if (st != MOE_OK) return st;
     if ((st = check_rows(R)) != MOE_OK) return st;
+    if (w8a16 && R > MOE_W8A16_MAX_ROWS) return MOE_ERR_UNSUPPORTED;
     if (R == 0) return MOE_OK;  // nothing to do; empty arrays may be NULL
     if ((st = check_weights(cfg, w)) != MOE_OK) return st;
     if (!x_bf16 || !w_router || !bias || !out_bf16 || !ws) return MOE_ERR_INVALID_ARG;
@@ -456,8 +543,26 @@ moe_status_t moe_layer(const moe_config_t* cfg, const void* x_bf16, const float*
             return st;
         if ((st = union_impl(cfg, ids, R, ub, s)) != MOE_OK) return st;
     }
-    if ((st = ffn_impl(cfg, x_bf16, w, ub, R, y_slots, y_shared, ws, s)) != MOE_OK) return st;
+    st = w8a16 ? ffn16_impl(cfg, x_bf16, w, ub, R, y_slots, y_shared, ws, s)
+               : ffn_impl(cfg, x_bf16, w, ub, R, y_slots, y_shared, ws, s);
+    if (st != MOE_OK) return st;
     return combine_impl(cfg, y_slots, y_shared, wts, ub, R, out_bf16, s);
+}
+
+moe_status_t moe_layer(const moe_config_t* cfg, const void* x_bf16, const float* w_router,
+                       const float* bias, const moe_weights_t* w, const uint8_t* row_valid,
+                       int32_t R, void* out_bf16, int32_t* topk_ids_out, float* topk_w_out,
+                       void* ws, size_t ws_bytes, moe_stream_t stream) {
+    return layer_impl(cfg, x_bf16, w_router, bias, w, row_valid, R, out_bf16, topk_ids_out,
+                      topk_w_out, ws, ws_bytes, stream, false);
+}
+
+moe_status_t moe_layer_w8a16(const moe_config_t* cfg, const void* x_bf16, const float* w_router,
+                             const float* bias, const moe_weights_t* w, const uint8_t* row_valid,
+                             int32_t R, void* out_bf16, int32_t* topk_ids_out, float* topk_w_out,
+                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+    return layer_impl(cfg, x_bf16, w_router, bias, w, row_valid, R, out_bf16, topk_ids_out,
+                      topk_w_out, ws, ws_bytes, stream, true);
 }
 
 moe_status_t moe_greedy_verify(const void* logits, int32_t logits_bf16, int32_t V, int32_t R,

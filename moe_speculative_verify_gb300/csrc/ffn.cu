@@ -106,18 +106,9 @@ __host__ __device__ inline FfnSmem ffn_smem(int nt, int n_stages, int kbmax, int
     return s;
 }
 
-// AND of `ok` over the epilogue threads, at a named barrier.
+// AND of `ok` over the epilogue threads (named barrier 1).
 __device__ __forceinline__ bool epi_bar_and(bool ok, int nthreads) {
-    int r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.b32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, %2, p;\n\t"
-        "selp.s32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(ok ? 1 : 0), "r"(nthreads)
-        : "memory");
-    return r != 0;
+    return bar_and(1, ok, nthreads);
 }
 
 __device__ __forceinline__ int ld_acquire(const int32_t* p) {
@@ -467,7 +458,8 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                 acc1[j] = 0.0f;
             }
             for (int kb = 0; kb < KB && ok; ++kb) {
-                if (!mbar_wait(&acc_full[ab], aph, p.err, p.timeout_ns)) {
+                // a failed wait is acted on by the whole warp (tcgen05.ld is warp-wide)
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&acc_full[ab], aph, p.err, p.timeout_ns))) {
                     ok = false;
                     *s_abort = 1;
                     break;

@@ -1,0 +1,531 @@
+// ffn16.cu -- w8a16 expert GEMMs: e4m3 weights dequantised to bf16 in the
+// kernel, bf16 activations, bf16 tcgen05 MMA (sm_103a).
+//
+// mstar #388 "Speed up GLM-5.2 with fp8 kernels and one-graph MTP", commit on
+// kernel switches and the FlashInfer commit: fp8 linears run w8a16 at decode
+// sizes -- fp8 weights with their 128x128 block scales, 16-bit activations
+// that are not quantised.  The weight is dequantised as bf16_rne(e4m3 * scale)
+// (one scale per 128x128 tile), the gathered rows and h stay bf16, and the
+// MMA accumulates the whole K of a tile in fp32 tensor memory.
+//
+// One persistent kernel over the tile queue of the fp8 path (gate/up tiles,
+// then down tiles, entry-major; a down tile starts once every gate/up tile of
+// its item has stored its block of h), for items of up to 16 rows.  Warp roles
+// (one CTA per SM):
+//   warp 0 lane 0: TMA producer -- e4m3 weight tiles (16 KB) into a ring of
+//                  staging buffers;
+//   warp 1 lane 0: MMA issuer -- 8 x tcgen05.mma kind::f16 (K = 16) per
+//                  128-wide K-block into the tile's accumulator (gate and up
+//                  side by side for a gate/up tile);
+//   warps 2..9   : dequant -- a staged tile to a bf16 operand tile (two
+//                  128-byte-swizzled K halves), the leader also loads the
+//                  K-block's 16 rows (bf16) next to it;
+//   warps 10..13 : epilogue -- gate/up: h = silu(g) * u rounded to bf16, row
+//                  stores; down: fp32 rows to their slot.
+// Every wait is bounded; a timeout records MOE_ERR_TIMEOUT and winds down.
+#include "common.cuh"
+#include "kernels.h"
+#include "layout.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kNT = kW8A16RowsPerItem;       // rows per item (MMA N)
+constexpr int kDqWarps = 8;
+constexpr int kEpiWarps = 4;
+constexpr int kThreads16 = 32 * (2 + kDqWarps + kEpiWarps);
+constexpr int kWBytes = 128 * 128;           // e4m3 weight tile
+constexpr int kABytes = 128 * 128 * 2;       // bf16 operand tile: two K halves of 16 KB
+constexpr int kBBytes = kNT * 128 * 2;       // bf16 rows: two K halves of kNT x 128 B
+constexpr int kSlotBytes = kABytes + kBBytes;
+constexpr int kSlots = 3;                    // operand slots (dequant -> MMA)
+constexpr int kMaxWStages = 8;
+constexpr int kAccCols = 2 * kNT;
+constexpr int kAccBufs = 4;
+constexpr int kTmemCols = 128;
+static_assert(kAccBufs * kAccCols <= kTmemCols, "tensor memory");
+static_assert(kSlotBytes % 1024 == 0, "operand slots stay 1024-byte aligned");
+
+struct Smem16 {
+    int slots, wst, bars, tmem, flag, bytes;
+};
+
+__host__ __device__ inline Smem16 smem16(int n_w) {
+    Smem16 s;
+    int b = 0;
+    s.slots = b;
+    b += kSlots * kSlotBytes;
+    s.wst = b;
+    b += n_w * kWBytes;
+    s.bars = b;
+    b += (2 * n_w + 2 * kSlots + 2 * kAccBufs + 1) * 8;
+    s.tmem = b;
+    b += 4;
+    s.flag = b;
+    b += 4;
+    s.bytes = b + 1024;
+    return s;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
+// A and B bf16 (bits 7-9 = 1, bits 10-12 = 1), both K-major, N >> 3 at bits
+// 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, one 128 x N x 16 bf16 step.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Generic-proxy shared-memory writes made visible to the async proxy (MMA).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ int ld_acquire16(const int32_t* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ bool wait_ready(const int32_t* ctr, int target, int32_t* err,
+                                           uint64_t timeout_ns, volatile int* abort_flag) {
+    if (ld_acquire16(ctr) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0; it < (1u << 28); ++it) {
+        __nanosleep(32);
+        if (ld_acquire16(ctr) >= target) return true;
+        if ((it & 31u) == 31u && (*abort_flag || globaltimer_ns() - t0 > timeout_ns)) break;
+    }
+    record_error(err, MOE_ERR_TIMEOUT);
+    return false;
+}
+
+// Four e4m3 codes (one 32-bit word, lowest byte first) times `s`, rounded to
+// bf16, as two packed bf16x2 words.
+__device__ __forceinline__ uint2 dequant4(uint32_t w, float s) {
+    uint32_t h01, h23;
+    const uint16_t lo = static_cast<uint16_t>(w & 0xFFFFu), hi = static_cast<uint16_t>(w >> 16);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"(lo));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"(hi));
+    const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+    const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+    uint2 r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r.x) : "f"(__fmul_rn(f01.y, s)), "f"(__fmul_rn(f01.x, s)));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r.y) : "f"(__fmul_rn(f23.y, s)), "f"(__fmul_rn(f23.x, s)));
+    return r;
+}
+
+struct Tile16 {
+    int item, blk;
+    bool gu;
+};
+
+__device__ __forceinline__ Tile16 tile16_of(int t, int n_gu, int mb_i, int mb_h,
+                                            const int4* __restrict__ items) {
+    Tile16 x;
+    int mb;
+    if (t < n_gu) {
+        mb = mb_i;
+        x.gu = true;
+    } else {
+        t -= n_gu;
+        mb = mb_h;
+        x.gu = false;
+    }
+    const int w = __ldg(&items[t / mb].w);
+    const int first = w >> 10, n = w & 1023;
+    const int local = t - first * mb;
+    x.blk = local / n;
+    x.item = first + (local - x.blk * n);
+    return x;
+}
+
+__global__ void __launch_bounds__(kThreads16, 1)
+    ffn16_kernel(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUtensorMap map_u,
+                 const __grid_constant__ CUtensorMap map_sg, const __grid_constant__ CUtensorMap map_su,
+                 const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_d,
+                 const __grid_constant__ CUtensorMap map_sd, const __grid_constant__ CUtensorMap map_h,
+                 const Ffn16Args p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int KB_H = p.H / kBlock, KB_I = p.I / kBlock;
+    const int MB_I = p.I / kBlock, MB_H = p.H / kBlock;
+    const int NW = p.n_wstages;
+    const Smem16 L = smem16(NW);
+    uint8_t* slots = smem + L.slots;
+    uint8_t* wst = smem + L.wst;
+    uint64_t* w_full = reinterpret_cast<uint64_t*>(smem + L.bars);
+    uint64_t* w_empty = w_full + NW;
+    uint64_t* a_full = w_empty + NW;
+    uint64_t* a_empty = a_full + kSlots;
+    uint64_t* acc_full = a_empty + kSlots;
+    uint64_t* acc_empty = acc_full + kAccBufs;
+    uint64_t* drain = acc_empty + kAccBufs;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L.tmem);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L.flag);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NW; ++s) {
+            mbar_init(&w_full[s], 1);
+            mbar_init(&w_empty[s], kDqWarps);
+        }
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(&a_full[s], kDqWarps + 1);
+            mbar_init(&a_empty[s], 1);
+        }
+        for (int b = 0; b < kAccBufs; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], kEpiWarps);
+        }
+        mbar_init(drain, 1);
+        *s_abort = 0;
+        fence_barrier_init();
+        prefetch_tensormap(&map_g);
+        prefetch_tensormap(&map_d);
+        prefetch_tensormap(&map_x);
+        prefetch_tensormap(&map_h);
+    }
+    if (warp == 1) {
+        tmem_alloc(s_tmem, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+
+    // The union buffer comes from a kernel at least two launches back: it is
+    // complete when this kernel starts.  Items must have been cut to 16 rows.
+    const int n_items = (p.ub[4] == kNT) ? p.ub[3] : 0;
+    if (threadIdx.x == 0 && p.ub[4] != kNT && p.ub[3] > 0) record_error(p.err, MOE_ERR_INVALID_ARG);
+    const int n_gu = n_items * MB_I;
+    const int n_tiles = n_gu + n_items * MB_H;
+    const int4* items = reinterpret_cast<const int4*>(p.ub + p.ul.items);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            const uint64_t pol = policy_evict_first();
+            int ws = 0;
+            uint32_t wph = 0;
+            bool ok = true;
+            bool waited = false;
+            int issued = 0;
+            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+                const Tile16 tl = tile16_of(t, n_gu, MB_I, MB_H, items);
+                const int4 it = items[tl.item];
+                const bool sh = it.x == p.E;
+                const int ex = sh ? 0 : it.x;
+                const int NS = tl.gu ? 2 * KB_H : KB_I;
+                for (int j = 0; j < NS; ++j) {
+                    // weights are inputs of the layer: the first ring of them
+                    // is requested before the wait on the previous kernel
+                    if (!waited && issued == NW) {
+                        pdl_wait();
+                        pdl_launch_dependents();
+                        waited = true;
+                    }
+                    if (*s_abort || !mbar_wait(&w_empty[ws], wph ^ 1u, p.err, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&w_full[ws], kWBytes);
+                    uint8_t* dst = wst + ws * kWBytes;
+                    if (tl.gu) {
+                        const CUtensorMap* m = (j & 1) ? (sh ? &map_su : &map_u) : (sh ? &map_sg : &map_g);
+                        tma_load_2d_hint(dst, m, &w_full[ws], (j >> 1) * kBlock,
+                                         ex * p.I + tl.blk * kBlock, pol);
+                    } else {
+                        tma_load_2d_hint(dst, sh ? &map_sd : &map_d, &w_full[ws], j * kBlock,
+                                         ex * p.H + tl.blk * kBlock, pol);
+                    }
+                    ++issued;
+                    if (++ws == NW) {
+                        ws = 0;
+                        wph ^= 1u;
+                    }
+                }
+            }
+            if (!waited) {
+                pdl_wait();
+                pdl_launch_dependents();
+            }
+            if (!ok) *s_abort = 1;
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------- MMA issuer
+            constexpr uint32_t idesc = idesc_bf16_f32(128, kNT);
+            int slot = 0, ab = 0;
+            uint32_t sph = 0, aph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+                const bool gu = t < n_gu;
+                const int NS = gu ? 2 * KB_H : KB_I;
+                if (*s_abort || !mbar_wait(&acc_empty[ab], aph ^ 1u, p.err, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t d0 = tmem + ab * kAccCols;
+                for (int j = 0; j < NS; ++j) {
+                    if (*s_abort || !mbar_wait(&a_full[slot], sph, p.err, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(slots + slot * kSlotBytes);
+                    const uint32_t b0 = a0 + kABytes;
+                    const uint32_t d = d0 + (gu ? (j & 1) * kNT : 0);
+                    const bool first = gu ? (j < 2) : (j == 0);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint32_t half = static_cast<uint32_t>(k >> 2), kk = k & 3;
+                        mma_bf16(d, sdesc_k_sw128(a0 + half * (kABytes / 2) + 32 * kk),
+                                 sdesc_k_sw128(b0 + half * (kBBytes / 2) + 32 * kk), idesc,
+                                 (first && k == 0) ? 0u : 1u);
+                    }
+                    mma_commit(&a_empty[slot]);
+                    if (++slot == kSlots) {
+                        slot = 0;
+                        sph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(&acc_full[ab]);
+                if (++ab == kAccBufs) {
+                    ab = 0;
+                    aph ^= 1u;
+                }
+            }
+            if (!ok) *s_abort = 1;
+        }
+    } else if (warp < 2 + kDqWarps) {
+        // --------------------------------------------------------- dequant
+        const int dt = threadIdx.x - 64;            // 0 .. 255
+        const bool leader = dt == 0;
+        int ws = 0, slot = 0;
+        uint32_t wph = 0, sph = 0;
+        bool ok = true;
+        pdl_wait();   // gathered rows and the counters belong to the previous kernel
+        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            const Tile16 tl = tile16_of(t, n_gu, MB_I, MB_H, items);
+            const int4 it = items[tl.item];
+            const bool sh = it.x == p.E;
+            const int ex = sh ? 0 : it.x;
+            const int NS = tl.gu ? 2 * KB_H : KB_I;
+            const int KB = tl.gu ? KB_H : KB_I;
+            const int MB = tl.gu ? MB_I : MB_H;
+            bool h_ready = tl.gu;
+            for (int j = 0; j < NS; ++j) {
+                // every wait's outcome is made uniform across the warp before use
+                bool got = !*s_abort && mbar_wait(&a_empty[slot], sph ^ 1u, p.err, p.timeout_ns);
+                if (!__all_sync(0xFFFFFFFFu, got)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* sl = slots + slot * kSlotBytes;
+                if (leader) {
+                    if (!h_ready) {
+                        // h of this item comes from this launch's gate/up tiles
+                        if (!wait_ready(p.ready + tl.item, MB_I, p.err, p.timeout_ns, s_abort)) {
+                            *s_abort = 1;
+                        }
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        h_ready = true;
+                    }
+                    const int kb = tl.gu ? (j >> 1) : j;
+                    const CUtensorMap* bm = tl.gu ? &map_x : &map_h;
+                    mbar_arrive_expect_tx(&a_full[slot], kBBytes);
+                    tma_load_2d(sl + kABytes, bm, &a_full[slot], kb * kBlock, it.y);
+                    tma_load_2d(sl + kABytes + kBBytes / 2, bm, &a_full[slot], kb * kBlock + 64, it.y);
+                }
+                got = !*s_abort && mbar_wait(&w_full[ws], wph, p.err, p.timeout_ns);
+                if (!__all_sync(0xFFFFFFFFu, got)) {
+                    ok = false;
+                    break;
+                }
+                const int kb = tl.gu ? (j >> 1) : j;
+                const float* sp = tl.gu ? ((j & 1) ? (sh ? p.sh_s_up : p.s_up) : (sh ? p.sh_s_gate : p.s_gate))
+                                        : (sh ? p.sh_s_down : p.s_down);
+                const float s = __ldg(sp + (size_t(ex) * MB + tl.blk) * KB + kb);
+                const uint8_t* src = wst + ws * kWBytes;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int i = dt + 256 * c;
+                    const int row = i >> 3, ch = i & 7, sw = row & 7;
+                    const uint4 q = *reinterpret_cast<const uint4*>(src + row * 128 + ((ch ^ sw) << 4));
+                    const uint2 o0 = dequant4(q.x, s), o1 = dequant4(q.y, s);
+                    const uint2 o2 = dequant4(q.z, s), o3 = dequant4(q.w, s);
+                    uint8_t* dst = sl + (ch >> 2) * (kABytes / 2) + row * 128;
+                    const int c0 = (ch & 3) * 2;
+                    *reinterpret_cast<uint4*>(dst + ((c0 ^ sw) << 4)) = make_uint4(o0.x, o0.y, o1.x, o1.y);
+                    *reinterpret_cast<uint4*>(dst + (((c0 + 1) ^ sw) << 4)) = make_uint4(o2.x, o2.y, o3.x, o3.y);
+                }
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&w_empty[ws]);
+                    mbar_arrive(&a_full[slot]);
+                }
+                if (++ws == NW) {
+                    ws = 0;
+                    wph ^= 1u;
+                }
+                if (++slot == kSlots) {
+                    slot = 0;
+                    sph ^= 1u;
+                }
+            }
+        }
+        if (!ok) *s_abort = 1;
+    } else {
+        // ----------------------------------------------------- epilogue
+        const int q = warp & 3;            // TMEM lane quadrant this warp may access
+        const int m = 32 * q + lane;       // output feature inside the 128-row block
+        const int et = threadIdx.x - 32 * (2 + kDqWarps);
+        int ab = 0;
+        uint32_t aph = 0;
+        bool ok = true;
+        pdl_wait();
+        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            const Tile16 tl = tile16_of(t, n_gu, MB_I, MB_H, items);
+            const int4 it = items[tl.item];
+            const int row0 = it.y, nrow = it.z;
+            // all four epilogue warps learn of a failed wait together
+            const bool got = __all_sync(0xFFFFFFFFu, mbar_wait(&acc_full[ab], aph, p.err,
+                                                                 p.timeout_ns));
+            if (!bar_and(1, got, 32 * kEpiWarps)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + ab * kAccCols;
+            float g[kNT], u[kNT];
+            tmem_ld16(ta, g);
+            if (tl.gu) tmem_ld16(ta + kNT, u);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[ab]);
+            if (++ab == kAccBufs) {
+                ab = 0;
+                aph ^= 1u;
+            }
+            if (tl.gu) {
+#pragma unroll
+                for (int c = 0; c < kNT; ++c) {
+                    if (c < nrow) {
+                        const float h = (g[c] / (1.0f + __expf(-g[c]))) * u[c];
+                        p.hb[size_t(row0 + c) * p.I + tl.blk * kBlock + m] =
+                            __bfloat16_as_ushort(__float2bfloat16_rn(h));
+                    }
+                }
+                // release this block of h to the item's down tiles
+                (void)bar_and(1, true, 32 * kEpiWarps);
+                if (et == 0) {
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    __threadfence();
+                    atomicAdd(p.ready + tl.item, 1);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kNT; ++c) {
+                    if (c < nrow) {
+                        const int slot = __ldg(p.ub + p.ul.src + row0 + c);
+                        const int r = slot / p.KS, k = slot - r * p.KS;
+                        float* dst = (k < p.K) ? p.y_slots + (size_t(r) * p.K + k) * p.H
+                                               : p.y_shared + size_t(r) * p.H;
+                        dst[tl.blk * kBlock + m] = g[c];
+                    }
+                }
+            }
+        }
+        if (!ok) *s_abort = 1;
+    }
+
+    __syncthreads();
+    if (*s_abort) {
+        // Wind down: copies already issued land within microseconds; give them
+        // a fixed budget, then let every issued MMA finish before tensor
+        // memory is released.
+        constexpr uint64_t kDrainNs = 1000000;   // 1 ms
+        if (threadIdx.x == 0) {
+            const uint64_t t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < kDrainNs) __nanosleep(1000);
+        }
+        if (threadIdx.x == 32) {
+            mma_commit(drain);
+            mbar_wait(drain, 0, nullptr, kDrainNs);
+        }
+        __syncthreads();
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// Gathered bf16 rows: each valid row copied to its K + S positions; one warp
+// per (row, 128 columns).  Clears the per-item counters of the GEMM.
+__global__ void __launch_bounds__(256) dispatch16_kernel(const uint16_t* __restrict__ x,
+                                                         const int32_t* __restrict__ ub,
+                                                         UnionLayout L, int R, int H, int KS,
+                                                         uint16_t* __restrict__ xb,
+                                                         int32_t* __restrict__ ready, int n_ready) {
+    pdl_wait();
+    pdl_launch_dependents();
+    if (blockIdx.x == 0 && blockIdx.y == 0)
+        for (int i = threadIdx.x; i < n_ready; i += blockDim.x) ready[i] = 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x;
+    const int b = blockIdx.y * 8 + warp;
+    if (b >= H / kBlock) return;
+    const int32_t* pos = ub + L.pos + size_t(r) * KS;
+    if (pos[0] < 0) return;   // pad row
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(x + size_t(r) * H + b * kBlock + 4 * lane));
+    for (int k = 0; k < KS; ++k)
+        reinterpret_cast<uint2*>(xb + size_t(pos[k]) * H + b * kBlock)[lane] = v;
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch16(const uint16_t* x, const int32_t* ub, const UnionLayout& L, int R,
+                              int H, int KS, uint16_t* xb, int32_t* ready, int n_ready,
+                              cudaStream_t stream) {
+    dim3 grid(R, (H / kBlock + 7) / 8);
+    cudaError_t e = launch_pdl(dispatch16_kernel, grid, dim3(256), 0, stream, x, ub, L, R, H, KS,
+                               xb, ready, n_ready);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ffn16(const FfnMaps& mp, Ffn16Args args, int n_sms, int smem_limit,
+                         cudaStream_t stream) {
+    int nw = kMaxWStages;
+    Smem16 L = smem16(nw);
+    while (nw > 2 && L.bytes > smem_limit) L = smem16(--nw);
+    if (L.bytes > smem_limit) return cudaErrorInvalidConfiguration;
+    args.n_wstages = nw;
+    cudaError_t e = cudaFuncSetAttribute(ffn16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         L.bytes);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(ffn16_kernel, dim3(max(1, n_sms)), dim3(kThreads16), L.bytes, stream, mp.g, mp.u,
+                   mp.sg, mp.su, mp.x, mp.d, mp.sd, mp.h, args);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -43,6 +43,32 @@ struct FfnArgs {
     uint64_t timeout_ns;
 };
 
+// Arguments of the w8a16 expert-GEMM kernel (ffn16.cu).
+struct Ffn16Args {
+    const int32_t* ub;         // union buffer
+    UnionLayout ul;
+    const float* s_gate;       // routed scales [E, I/128, H/128]
+    const float* s_up;
+    const float* sh_s_gate;    // shared-expert scales [S, I/128, H/128]
+    const float* sh_s_up;
+    const float* s_down;       // [E, H/128, I/128]
+    const float* sh_s_down;
+    uint16_t* hb;              // bf16 h [rows, I]
+    float* y_slots;            // [R*K, H]
+    float* y_shared;           // [R, H]
+    int32_t* ready;            // [max_items] gate/up blocks of h finished
+    int32_t* err;              // device error word
+    int H, I;
+    int E, K, KS;
+    int n_wstages;
+    uint64_t timeout_ns;
+};
+
+cudaError_t launch_dispatch16(const uint16_t* x, const int32_t* ub, const UnionLayout& L, int R,
+                              int H, int KS, uint16_t* xb, int32_t* ready, int n_ready,
+                              cudaStream_t stream);
+cudaError_t launch_ffn16(const FfnMaps& mp, Ffn16Args args, int n_sms, int smem_limit,
+                         cudaStream_t stream);
 cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const uint8_t* row_valid,
                                  int R, int H, int E, float* logits, cudaStream_t stream);
 cudaError_t launch_router(const uint16_t* x, const float* wr, const float* bias,

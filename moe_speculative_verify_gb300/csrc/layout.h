@@ -47,9 +47,16 @@ inline UnionLayout union_layout(int32_t E, int32_t K, int32_t S, int32_t R) {
     return L;
 }
 
+// The w8a16 variant: calls of at most kW8A16MaxRows rows, items of
+// kW8A16RowsPerItem rows (the fp8 path's item size at these row counts).
+constexpr int32_t kW8A16MaxRows = 64;
+constexpr int32_t kW8A16RowsPerItem = 16;
+
 // Scratch of the expert FFN stage (byte offsets from the workspace base).
+// The w8a16 variant's bf16 rows (xb) and bf16 h (hb) reuse the fp8 path's
+// region from xg on; they exist only for R <= kW8A16MaxRows (else -1).
 struct FfnLayout {
-    int64_t ctl, ready, xg, xs, hq, hs, bytes;
+    int64_t ctl, ready, xg, xs, hq, hs, xb, hb, bytes;
     int64_t rows;       // capacity in gathered rows
     int32_t n_ready;    // per-item counters of the fused GEMM
 };
@@ -72,6 +79,13 @@ inline FfnLayout ffn_layout(int32_t H, int32_t I, int32_t E, int32_t K, int32_t 
     L.hs = b;
     b = round_up(b + L.rows * (I / 128) * 4, 256);
     L.bytes = b;
+    L.xb = L.hb = -1;
+    if (R <= kW8A16MaxRows) {
+        L.xb = L.xg;
+        L.hb = round_up(L.xb + L.rows * H * 2, 256);
+        const int64_t end = round_up(L.hb + L.rows * I * 2, 256);
+        if (end > L.bytes) L.bytes = end;
+    }
     return L;
 }
 
