@@ -341,7 +341,8 @@ def main() -> None:
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--extra", default="verify64,decode512,prefill4096",
-                    help="other workloads measured on the same weights (summary only)")
+                    help="other workloads measured on the same weights (summary only); "
+                         "\"none\" for none")
     args = ap.parse_args()
     wl = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
@@ -487,7 +488,7 @@ def main() -> None:
 
     extra = {}
     if rank == 0 and args.extra:
-        for name in [n for n in args.extra.split(",") if n and n != wl.name]:
+        for name in [n for n in args.extra.split(",") if n not in ("", "none", wl.name)]:
             wl2 = synth.WORKLOADS[name]
             r2 = measure(wl2, 5, 3, False)
             a2 = r2["alg"]
