@@ -15,11 +15,13 @@
 //   warp 0 lane 0: TMA producer -- e4m3 weight tiles (16 KB) into a ring of
 //                  staging buffers;
 //   warp 1 lane 0: MMA issuer -- 8 x tcgen05.mma kind::f16 (K = 16) per
-//                  128-wide K-block into the tile's accumulator (gate and up
-//                  side by side for a gate/up tile);
-//   warps 2..9   : dequant -- a staged tile to a bf16 operand tile (two
-//                  128-byte-swizzled K halves), the leader also loads the
-//                  K-block's 16 rows (bf16) next to it;
+//                  128-wide K-block, A (the bf16 weight tile) from tensor
+//                  memory, B (the rows) from shared memory, into the tile's
+//                  accumulator (gate and up side by side for a gate/up tile);
+//   warps 2..9   : dequant -- a staged tile to bf16, written straight into a
+//                  tensor-memory operand slot (tcgen05.st; the dequantised
+//                  tile never touches shared memory); the leader also loads
+//                  the K-block's 16 rows (bf16) into the slot's shared part;
 //   warps 10..13 : epilogue -- gate/up: h = silu(g) * u rounded to bf16, row
 //                  stores; down: fp32 rows to their slot.
 // Every wait is bounded; a timeout records MOE_ERR_TIMEOUT and winds down.
@@ -36,15 +38,16 @@ constexpr int kDqWarps = 8;
 constexpr int kEpiWarps = 4;
 constexpr int kThreads16 = 32 * (2 + kDqWarps + kEpiWarps);
 constexpr int kWBytes = 128 * 128;           // e4m3 weight tile
-constexpr int kABytes = 128 * 128 * 2;       // bf16 operand tile: two K halves of 16 KB
 constexpr int kBBytes = kNT * 128 * 2;       // bf16 rows: two K halves of kNT x 128 B
-constexpr int kSlotBytes = kABytes + kBBytes;
-constexpr int kSlots = 3;                    // operand slots (dequant -> MMA)
-constexpr int kMaxWStages = 8;
+constexpr int kSlotBytes = kBBytes;          // shared-memory part of an operand slot
+constexpr int kSlots = 4;                    // operand slots (dequant -> MMA)
+constexpr int kMaxWStages = 12;
 constexpr int kAccCols = 2 * kNT;
 constexpr int kAccBufs = 4;
-constexpr int kTmemCols = 128;
-static_assert(kAccBufs * kAccCols <= kTmemCols, "tensor memory");
+constexpr int kACols = 64;                   // a bf16 128x128 tile in TMEM: 2 per 32-bit column
+constexpr int kAColBase = kAccBufs * kAccCols;
+constexpr int kTmemCols = 512;
+static_assert(kAColBase + kSlots * kACols <= kTmemCols, "tensor memory");
 static_assert(kSlotBytes % 1024 == 0, "operand slots stay 1024-byte aligned");
 
 struct Smem16 {
@@ -87,9 +90,34 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
-// Generic-proxy shared-memory writes made visible to the async proxy (MMA).
-__device__ __forceinline__ void fence_proxy_async_shared() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+// D[tmem] (+)= A[tmem] * B[smem]^T: A (128 x 16 bf16) read from tensor
+// memory, lane m = row m, two K elements per 32-bit column.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 32 consecutive 32-bit columns of this thread's TMEM lane (32x32b shape).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ int ld_acquire16(const int32_t* p) {
@@ -286,16 +314,15 @@ __global__ void __launch_bounds__(kThreads16, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(slots + slot * kSlotBytes);
-                    const uint32_t b0 = a0 + kABytes;
+                    const uint32_t a0 = tmem + kAColBase + slot * kACols;
+                    const uint32_t b0 = smem_u32(slots + slot * kSlotBytes);
                     const uint32_t d = d0 + (gu ? (j & 1) * kNT : 0);
                     const bool first = gu ? (j < 2) : (j == 0);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         const uint32_t half = static_cast<uint32_t>(k >> 2), kk = k & 3;
-                        mma_bf16(d, sdesc_k_sw128(a0 + half * (kABytes / 2) + 32 * kk),
-                                 sdesc_k_sw128(b0 + half * (kBBytes / 2) + 32 * kk), idesc,
-                                 (first && k == 0) ? 0u : 1u);
+                        mma_bf16_ts(d, a0 + 8 * k, sdesc_k_sw128(b0 + half * (kBBytes / 2) + 32 * kk),
+                                    idesc, (first && k == 0) ? 0u : 1u);
                     }
                     mma_commit(&a_empty[slot]);
                     if (++slot == kSlots) {
@@ -314,8 +341,13 @@ __global__ void __launch_bounds__(kThreads16, 1)
         }
     } else if (warp < 2 + kDqWarps) {
         // --------------------------------------------------------- dequant
-        const int dt = threadIdx.x - 64;            // 0 .. 255
-        const bool leader = dt == 0;
+        // Warp w converts rows 32*(w%4) .. +31 (the TMEM lanes it may access)
+        // and the K half (w-2)/4 of every staged tile: per thread 64 codes of
+        // its row, read from the swizzled stage, written as 32 bf16x2 columns.
+        const int dw = warp - 2;
+        const int qd = warp & 3, hk = dw >> 2;
+        const int row = 32 * qd + lane;
+        const bool leader = dw == 0 && lane == 0;
         int ws = 0, slot = 0;
         uint32_t wph = 0, sph = 0;
         bool ok = true;
@@ -328,58 +360,72 @@ __global__ void __launch_bounds__(kThreads16, 1)
             const int NS = tl.gu ? 2 * KB_H : KB_I;
             const int KB = tl.gu ? KB_H : KB_I;
             const int MB = tl.gu ? MB_I : MB_H;
+            const float* sg = sh ? p.sh_s_gate : p.s_gate;
+            const float* su = sh ? p.sh_s_up : p.s_up;
+            const float* sd = sh ? p.sh_s_down : p.s_down;
+            const size_t sbase = (size_t(ex) * MB + tl.blk) * KB;
+            auto scale_of = [&](int j) -> float {
+                return tl.gu ? __ldg(((j & 1) ? su : sg) + sbase + (j >> 1)) : __ldg(sd + sbase + j);
+            };
             bool h_ready = tl.gu;
+            float s_next = scale_of(0);
             for (int j = 0; j < NS; ++j) {
+                const float s = s_next;
+                if (j + 1 < NS) s_next = scale_of(j + 1);
                 // every wait's outcome is made uniform across the warp before use
                 bool got = !*s_abort && mbar_wait(&a_empty[slot], sph ^ 1u, p.err, p.timeout_ns);
                 if (!__all_sync(0xFFFFFFFFu, got)) {
                     ok = false;
                     break;
                 }
-                uint8_t* sl = slots + slot * kSlotBytes;
+                tc_fence_after();
                 if (leader) {
                     if (!h_ready) {
                         // h of this item comes from this launch's gate/up tiles
-                        if (!wait_ready(p.ready + tl.item, MB_I, p.err, p.timeout_ns, s_abort)) {
+                        if (!wait_ready(p.ready + tl.item, MB_I, p.err, p.timeout_ns, s_abort))
                             *s_abort = 1;
-                        }
                         asm volatile("fence.proxy.async.global;" ::: "memory");
                         h_ready = true;
                     }
                     const int kb = tl.gu ? (j >> 1) : j;
                     const CUtensorMap* bm = tl.gu ? &map_x : &map_h;
+                    uint8_t* sl = slots + slot * kSlotBytes;
                     mbar_arrive_expect_tx(&a_full[slot], kBBytes);
-                    tma_load_2d(sl + kABytes, bm, &a_full[slot], kb * kBlock, it.y);
-                    tma_load_2d(sl + kABytes + kBBytes / 2, bm, &a_full[slot], kb * kBlock + 64, it.y);
+                    tma_load_2d(sl, bm, &a_full[slot], kb * kBlock, it.y);
+                    tma_load_2d(sl + kBBytes / 2, bm, &a_full[slot], kb * kBlock + 64, it.y);
                 }
                 got = !*s_abort && mbar_wait(&w_full[ws], wph, p.err, p.timeout_ns);
                 if (!__all_sync(0xFFFFFFFFu, got)) {
                     ok = false;
                     break;
                 }
-                const int kb = tl.gu ? (j >> 1) : j;
-                const float* sp = tl.gu ? ((j & 1) ? (sh ? p.sh_s_up : p.s_up) : (sh ? p.sh_s_gate : p.s_gate))
-                                        : (sh ? p.sh_s_down : p.s_down);
-                const float s = __ldg(sp + (size_t(ex) * MB + tl.blk) * KB + kb);
-                const uint8_t* src = wst + ws * kWBytes;
+                const uint8_t* src = wst + ws * kWBytes + row * 128;
+                uint32_t o[32];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const int i = dt + 256 * c;
-                    const int row = i >> 3, ch = i & 7, sw = row & 7;
-                    const uint4 q = *reinterpret_cast<const uint4*>(src + row * 128 + ((ch ^ sw) << 4));
+                    const int ch = 4 * hk + c;
+                    const uint4 q = *reinterpret_cast<const uint4*>(src + ((ch ^ (row & 7)) << 4));
                     const uint2 o0 = dequant4(q.x, s), o1 = dequant4(q.y, s);
                     const uint2 o2 = dequant4(q.z, s), o3 = dequant4(q.w, s);
-                    uint8_t* dst = sl + (ch >> 2) * (kABytes / 2) + row * 128;
-                    const int c0 = (ch & 3) * 2;
-                    *reinterpret_cast<uint4*>(dst + ((c0 ^ sw) << 4)) = make_uint4(o0.x, o0.y, o1.x, o1.y);
-                    *reinterpret_cast<uint4*>(dst + (((c0 + 1) ^ sw) << 4)) = make_uint4(o2.x, o2.y, o3.x, o3.y);
+                    o[8 * c + 0] = o0.x;
+                    o[8 * c + 1] = o0.y;
+                    o[8 * c + 2] = o1.x;
+                    o[8 * c + 3] = o1.y;
+                    o[8 * c + 4] = o2.x;
+                    o[8 * c + 5] = o2.y;
+                    o[8 * c + 6] = o3.x;
+                    o[8 * c + 7] = o3.y;
                 }
-                fence_proxy_async_shared();
+                // the stage is read: hand it back before the tensor-memory store
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&w_empty[ws]);
-                    mbar_arrive(&a_full[slot]);
-                }
+                if (lane == 0) mbar_arrive(&w_empty[ws]);
+                __syncwarp();   // tcgen05.st is warp-wide: the whole warp, converged
+                tmem_st32(tmem + (static_cast<uint32_t>(32 * qd) << 16) + kAColBase +
+                              slot * kACols + 32 * hk, o);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&a_full[slot]);
                 if (++ws == NW) {
                     ws = 0;
                     wph ^= 1u;
