@@ -18,10 +18,11 @@
 //                  128-wide K-block, A (the bf16 weight tile) from tensor
 //                  memory, B (the rows) from shared memory, into the tile's
 //                  accumulator (gate and up side by side for a gate/up tile);
-//   warps 2..9   : dequant -- a staged tile to bf16, written straight into a
-//                  tensor-memory operand slot (tcgen05.st; the dequantised
-//                  tile never touches shared memory); the leader also loads
-//                  the K-block's 16 rows (bf16) into the slot's shared part;
+//   warps 2..9   : dequant, two groups of four on alternate steps -- a staged
+//                  tile to bf16, written straight into a tensor-memory
+//                  operand slot (tcgen05.st; the dequantised tile never
+//                  touches shared memory); the group's leader also loads the
+//                  K-block's 16 rows (bf16) into the slot's shared part;
 //   warps 10..13 : epilogue -- gate/up: h = silu(g) * u rounded to bf16, row
 //                  stores; down: fp32 rows to their slot.
 // Every wait is bounded; a timeout records MOE_ERR_TIMEOUT and winds down.
@@ -34,13 +35,14 @@ namespace moe {
 namespace {
 
 constexpr int kNT = kW8A16RowsPerItem;       // rows per item (MMA N)
-constexpr int kDqWarps = 8;
+constexpr int kDqWarps = 8;                  // two groups of four, alternate steps
+constexpr int kDqGroupWarps = 4;
 constexpr int kEpiWarps = 4;
 constexpr int kThreads16 = 32 * (2 + kDqWarps + kEpiWarps);
 constexpr int kWBytes = 128 * 128;           // e4m3 weight tile
 constexpr int kBBytes = kNT * 128 * 2;       // bf16 rows: two K halves of kNT x 128 B
 constexpr int kSlotBytes = kBBytes;          // shared-memory part of an operand slot
-constexpr int kSlots = 4;                    // operand slots (dequant -> MMA)
+constexpr int kSlots = 6;                    // operand slots (dequant -> MMA)
 constexpr int kMaxWStages = 12;
 constexpr int kAccCols = 2 * kNT;
 constexpr int kAccBufs = 4;
@@ -208,10 +210,10 @@ __global__ void __launch_bounds__(kThreads16, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < NW; ++s) {
             mbar_init(&w_full[s], 1);
-            mbar_init(&w_empty[s], kDqWarps);
+            mbar_init(&w_empty[s], kDqGroupWarps);
         }
         for (int s = 0; s < kSlots; ++s) {
-            mbar_init(&a_full[s], kDqWarps + 1);
+            mbar_init(&a_full[s], kDqGroupWarps + 1);
             mbar_init(&a_empty[s], 1);
         }
         for (int b = 0; b < kAccBufs; ++b) {
@@ -341,15 +343,17 @@ __global__ void __launch_bounds__(kThreads16, 1)
         }
     } else if (warp < 2 + kDqWarps) {
         // --------------------------------------------------------- dequant
-        // Warp w converts rows 32*(w%4) .. +31 (the TMEM lanes it may access)
-        // and the K half (w-2)/4 of every staged tile: per thread 64 codes of
-        // its row, read from the swizzled stage, written as 32 bf16x2 columns.
+        // Two groups of four warps take alternate steps of the CTA's step
+        // sequence, so two staged tiles are converted at once.  In a group,
+        // warp w converts rows 32*(w%4) .. +31 (the TMEM lanes it may access)
+        // of the tile: per thread the 128 codes of its row, read from the
+        // swizzled stage, written as 64 bf16x2 columns.
         const int dw = warp - 2;
-        const int qd = warp & 3, hk = dw >> 2;
+        const int grp = dw / kDqGroupWarps;
+        const int qd = warp & 3;
         const int row = 32 * qd + lane;
-        const bool leader = dw == 0 && lane == 0;
-        int ws = 0, slot = 0;
-        uint32_t wph = 0, sph = 0;
+        const bool leader = (dw % kDqGroupWarps) == 0 && lane == 0;
+        uint32_t n = 0;              // the CTA's step counter (both groups count every step)
         bool ok = true;
         pdl_wait();   // gathered rows and the counters belong to the previous kernel
         for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
@@ -368,10 +372,17 @@ __global__ void __launch_bounds__(kThreads16, 1)
                 return tl.gu ? __ldg(((j & 1) ? su : sg) + sbase + (j >> 1)) : __ldg(sd + sbase + j);
             };
             bool h_ready = tl.gu;
-            float s_next = scale_of(0);
-            for (int j = 0; j < NS; ++j) {
+            // this group's first step of the tile
+            const int j0 = static_cast<int>((static_cast<uint32_t>(grp) - n) & 1u);
+            float s_next = (j0 < NS) ? scale_of(j0) : 0.0f;
+            for (int j = j0; j < NS; j += 2) {
+                const uint32_t nj = n + static_cast<uint32_t>(j);
+                const int ws = static_cast<int>(nj % static_cast<uint32_t>(NW));
+                const uint32_t wph = (nj / static_cast<uint32_t>(NW)) & 1u;
+                const int slot = static_cast<int>(nj % kSlots);
+                const uint32_t sph = (nj / kSlots) & 1u;
                 const float s = s_next;
-                if (j + 1 < NS) s_next = scale_of(j + 1);
+                if (j + 2 < NS) s_next = scale_of(j + 2);
                 // every wait's outcome is made uniform across the warp before use
                 bool got = !*s_abort && mbar_wait(&a_empty[slot], sph ^ 1u, p.err, p.timeout_ns);
                 if (!__all_sync(0xFFFFFFFFu, got)) {
@@ -400,41 +411,41 @@ __global__ void __launch_bounds__(kThreads16, 1)
                     break;
                 }
                 const uint8_t* src = wst + ws * kWBytes + row * 128;
-                uint32_t o[32];
+                uint4 q[8];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int ch = 4 * hk + c;
-                    const uint4 q = *reinterpret_cast<const uint4*>(src + ((ch ^ (row & 7)) << 4));
-                    const uint2 o0 = dequant4(q.x, s), o1 = dequant4(q.y, s);
-                    const uint2 o2 = dequant4(q.z, s), o3 = dequant4(q.w, s);
-                    o[8 * c + 0] = o0.x;
-                    o[8 * c + 1] = o0.y;
-                    o[8 * c + 2] = o1.x;
-                    o[8 * c + 3] = o1.y;
-                    o[8 * c + 4] = o2.x;
-                    o[8 * c + 5] = o2.y;
-                    o[8 * c + 6] = o3.x;
-                    o[8 * c + 7] = o3.y;
-                }
-                // the stage is read: hand it back before the tensor-memory store
+                for (int c = 0; c < 8; ++c)
+                    q[c] = *reinterpret_cast<const uint4*>(src + ((c ^ (row & 7)) << 4));
+                // the stage is read: hand it back before converting
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&w_empty[ws]);
                 __syncwarp();   // tcgen05.st is warp-wide: the whole warp, converged
-                tmem_st32(tmem + (static_cast<uint32_t>(32 * qd) << 16) + kAColBase +
-                              slot * kACols + 32 * hk, o);
+                const uint32_t ta = tmem + (static_cast<uint32_t>(32 * qd) << 16) + kAColBase +
+                                    slot * kACols;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    uint32_t o[32];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 v = q[4 * h2 + c];
+                        const uint2 o0 = dequant4(v.x, s), o1 = dequant4(v.y, s);
+                        const uint2 o2 = dequant4(v.z, s), o3 = dequant4(v.w, s);
+                        o[8 * c + 0] = o0.x;
+                        o[8 * c + 1] = o0.y;
+                        o[8 * c + 2] = o1.x;
+                        o[8 * c + 3] = o1.y;
+                        o[8 * c + 4] = o2.x;
+                        o[8 * c + 5] = o2.y;
+                        o[8 * c + 6] = o3.x;
+                        o[8 * c + 7] = o3.y;
+                    }
+                    tmem_st32(ta + 32 * h2, o);
+                }
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&a_full[slot]);
-                if (++ws == NW) {
-                    ws = 0;
-                    wph ^= 1u;
-                }
-                if (++slot == kSlots) {
-                    slot = 0;
-                    sph ^= 1u;
-                }
             }
+            n += static_cast<uint32_t>(NS);
         }
         if (!ok) *s_abort = 1;
     } else {
