@@ -22,10 +22,11 @@
  *
  * Conventions for every entry point:
  *   - All pointers are DEVICE pointers unless stated otherwise; the caller owns
- *     every buffer and every stream.  The library allocates nothing, holds no
- *     state between calls, and never synchronises the stream except in
- *     moe_get_device_error.  Calls are asynchronous on `stream`; all but
- *     moe_layer_noalloc (see its own notes) can be captured in a CUDA graph.
+ *     every buffer and every stream.  The library allocates nothing and never
+ *     synchronises the stream except in moe_get_device_error; apart from
+ *     moe_layer_noalloc (see its own notes) it holds no state between calls.
+ *     Calls are asynchronous on `stream`; the entry points that take their
+ *     scratch from the caller can be captured in a CUDA graph.
  *   - Refusals are synchronous: a NULL required pointer, a misaligned pointer
  *     (16 bytes for bf16 / e4m3 / output arrays, 4 bytes for fp32 / int32), an
  *     unsupported shape or a short buffer returns an error code and launches
