@@ -91,6 +91,10 @@ WORKLOADS = {
                           hot_delta=1.0,
                           note="verify8's routing at 128-wide experts, for profiler captures of "
                                "the router, union, dispatch and combine kernels"),
+    "profile128": Workload("profile128", GLM52_E32, rows=128,
+                           note="128 rows on 32 experts of the GLM-5.2 shape (about 32 rows per "
+                                "expert, the 32-row tile of mixed decode batches): profiler "
+                                "captures"),
     "profile1024": Workload("profile1024", GLM52_E32, rows=1024,
                             note="1024 rows on 32 experts of the GLM-5.2 shape (256 rows per "
                                  "expert, the 64-row tile): prefill-like profiler captures"),
