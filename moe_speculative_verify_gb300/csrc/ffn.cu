@@ -434,31 +434,15 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             }
             const float* bs = tl.gu ? p.xs : p.hs;
             const int na = tl.gu ? 2 : 1;
-            // read row-major (kb fastest: coalesced), store [operand][kb][n];
-            // the loads of kSB entries are issued before any of their stores
-            constexpr int kSB = 8;
-            const int n_sc = na * NT * KB;
-            for (int i0 = et; i0 < n_sc; i0 += kSB * C::EPI_THREADS) {
-                float wv[kSB], bv[kSB];
-                int dst[kSB];
-#pragma unroll
-                for (int u = 0; u < kSB; ++u) {
-                    const int i = i0 + u * C::EPI_THREADS;
-                    dst[u] = -1;
-                    if (i < n_sc) {
-                        const int a = i / (NT * KB), rem = i - a * (NT * KB);
-                        const int n = rem / KB, kb = rem - n * KB;
-                        const float* sp = tl.gu ? ((a == 0) ? (sh ? p.sh_s_gate : p.s_gate)
-                                                            : (sh ? p.sh_s_up : p.s_up))
-                                                : (sh ? p.sh_s_down : p.s_down);
-                        wv[u] = __ldg(sp + (size_t(ex) * MB + tl.blk) * KB + kb);
-                        bv[u] = (n < nrow) ? bs[size_t(row0 + n) * KB + kb] : 0.0f;
-                        dst[u] = (a * KB + kb) * NT + n;
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kSB; ++u)
-                    if (dst[u] >= 0) s_sc[dst[u]] = wv[u] * bv[u];
+            // read row-major (kb fastest: coalesced), store [operand][kb][n]
+            for (int i = et; i < na * NT * KB; i += C::EPI_THREADS) {
+                const int a = i / (NT * KB), rem = i - a * (NT * KB);
+                const int n = rem / KB, kb = rem - n * KB;
+                const float* sp = tl.gu ? ((a == 0) ? (sh ? p.sh_s_gate : p.s_gate)
+                                                    : (sh ? p.sh_s_up : p.s_up))
+                                        : (sh ? p.sh_s_down : p.s_down);
+                const float w = sp[(size_t(ex) * MB + tl.blk) * KB + kb];
+                s_sc[(a * KB + kb) * NT + n] = (n < nrow) ? w * bs[size_t(row0 + n) * KB + kb] : 0.0f;
             }
             if (!tl.gu)
                 for (int i = et; i < NT; i += C::EPI_THREADS)

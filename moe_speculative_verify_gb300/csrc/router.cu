@@ -130,54 +130,74 @@ __global__ void __launch_bounds__(kTileThreads, 1) router_logits_tiled_kernel(
     const int r0 = blockIdx.y * kTileR, e0 = blockIdx.x * kTileE;
     const int steps = H / 128;
 
-    auto stage = [&](int i, int buf) {
-        // x tile: 32 rows x 128 bf16 = 512 x 16 bytes; w tile: 32 x 128 fp32 = 1024 x 16 bytes
-        {
-            const int row = tid >> 4, c = (tid & 15) * 8;
-            const int r = min(r0 + row, R - 1);
-            *reinterpret_cast<uint4*>(xs + (buf * kTileR + row) * 128 + c) =
-                __ldg(reinterpret_cast<const uint4*>(x + size_t(r) * H + i * 128 + c));
-        }
-        for (int q = tid; q < kTileE * 32; q += kTileThreads) {
+    // One 128-column step of x (32 rows x 128 bf16 = 512 x 16 bytes) and w (32
+    // experts x 128 fp32 = 1024 x 16 bytes) per thread: loaded into registers
+    // one step ahead, stored to the other shared buffer after the current
+    // step's arithmetic, so the loads' latency overlaps it.
+    const int xrow = tid >> 4, xc = (tid & 15) * 8;
+    const size_t xoff = size_t(min(r0 + xrow, R - 1)) * H + xc;
+    uint4 xreg;
+    float4 wreg[kTileE * 32 / kTileThreads];
+    auto load = [&](int i) {
+        xreg = __ldg(reinterpret_cast<const uint4*>(x + xoff + i * 128));
+#pragma unroll
+        for (int u = 0; u < kTileE * 32 / kTileThreads; ++u) {
+            const int q = tid + u * kTileThreads;
             const int ex = q >> 5, c = (q & 31) * 4;
             const int e = min(e0 + ex, E - 1);
-            *reinterpret_cast<float4*>(wsm + (buf * kTileE + ex) * 128 + c) =
-                __ldg(reinterpret_cast<const float4*>(wr + size_t(e) * H + i * 128 + c));
+            wreg[u] = __ldg(reinterpret_cast<const float4*>(wr + size_t(e) * H + i * 128 + c));
+        }
+    };
+    auto store = [&](int buf) {
+        *reinterpret_cast<uint4*>(xs + (buf * kTileR + xrow) * 128 + xc) = xreg;
+#pragma unroll
+        for (int u = 0; u < kTileE * 32 / kTileThreads; ++u) {
+            const int q = tid + u * kTileThreads;
+            const int ex = q >> 5, c = (q & 31) * 4;
+            *reinterpret_cast<float4*>(wsm + (buf * kTileE + ex) * 128 + c) = wreg[u];
         }
     };
 
     float p[8][8];
-    stage(0, 0);
+    load(0);
+    store(0);
     __syncthreads();
     for (int i = 0; i < steps; ++i) {
         const int buf = i & 1;
-        if (i + 1 < steps) stage(i + 1, buf ^ 1);
+        if (i + 1 < steps) load(i + 1);
         if ((i & 7) == 0) {
 #pragma unroll
             for (int a = 0; a < 8; ++a)
 #pragma unroll
                 for (int b = 0; b < 8; ++b) p[a][b] = 0.0f;
         }
-        float4 wv[8];
+        // experts in two halves of four (fewer live registers); every pair's
+        // four fmas stay in column order
 #pragma unroll
-        for (int b = 0; b < 8; ++b)
-            wv[b] = *reinterpret_cast<const float4*>(wsm + (buf * kTileE + wexp + b) * 128 + 4 * lane);
+        for (int bh = 0; bh < 8; bh += 4) {
+            float4 wv[4];
 #pragma unroll
-        for (int a = 0; a < 8; ++a) {
-            const uint2 xv =
-                *reinterpret_cast<const uint2*>(xs + (buf * kTileR + wrow + a) * 128 + 4 * lane);
-            const float x0 = bf16_bits_to_f32(xv.x & 0xFFFFu), x1 = bf16_bits_to_f32(xv.x >> 16);
-            const float x2 = bf16_bits_to_f32(xv.y & 0xFFFFu), x3 = bf16_bits_to_f32(xv.y >> 16);
+            for (int b = 0; b < 4; ++b)
+                wv[b] = *reinterpret_cast<const float4*>(wsm + (buf * kTileE + wexp + bh + b) * 128 +
+                                                         4 * lane);
 #pragma unroll
-            for (int b = 0; b < 8; ++b) {
-                float q = p[a][b];
-                q = __fmaf_rn(x0, wv[b].x, q);
-                q = __fmaf_rn(x1, wv[b].y, q);
-                q = __fmaf_rn(x2, wv[b].z, q);
-                q = __fmaf_rn(x3, wv[b].w, q);
-                p[a][b] = q;
+            for (int a = 0; a < 8; ++a) {
+                const uint2 xv =
+                    *reinterpret_cast<const uint2*>(xs + (buf * kTileR + wrow + a) * 128 + 4 * lane);
+                const float x0 = bf16_bits_to_f32(xv.x & 0xFFFFu), x1 = bf16_bits_to_f32(xv.x >> 16);
+                const float x2 = bf16_bits_to_f32(xv.y & 0xFFFFu), x3 = bf16_bits_to_f32(xv.y >> 16);
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    float q = p[a][bh + b];
+                    q = __fmaf_rn(x0, wv[b].x, q);
+                    q = __fmaf_rn(x1, wv[b].y, q);
+                    q = __fmaf_rn(x2, wv[b].z, q);
+                    q = __fmaf_rn(x3, wv[b].w, q);
+                    p[a][bh + b] = q;
+                }
             }
         }
+        if (i + 1 < steps) store(buf ^ 1);
         if ((i & 7) == 7 || i + 1 == steps) {   // end of a 1024-column chunk
             float* qw = qsm + size_t(warp) * 64 * 32;
             const bool first = (i < 8);
