@@ -108,21 +108,35 @@ __global__ void __launch_bounds__(512) router_logits_kernel(
 // Large-R variant: a block computes a tile of 32 rows x 32 experts with 16
 // warps; the warp (wr, we) owns rows 8*wr.. and experts 8*we.. (64 pairs) and
 // lane l of the warp is lane l of the reduction tree for every one of them.
-// Per 128-column step the block stages x (bf16) and w (fp32) in shared memory;
-// a thread accumulates its 64 lane partials of the current 1024-column chunk in
-// registers (fma in column order), folds them into the per-lane chunk sums in
-// shared memory at the end of each chunk (q = p for the first chunk, then
-// q = q + p), and the warp finishes every pair with the xor butterfly: the same
-// IEEE operations in the same order as the small-R kernel.
-constexpr int kTileR = 32, kTileE = 32, kTileThreads = 512;
+// Per 128-column step the block stages x (bf16) and w (fp32) in shared memory
+// through a ring of kTileStages buffers filled by cp.async (kTileStages - 1
+// steps in flight); a thread accumulates its 64 lane partials of the current
+// 1024-column chunk in registers (fma in column order), folds them into the
+// per-lane chunk sums in shared memory at the end of each chunk (q = p for the
+// first chunk, then q = q + p), and the warp finishes every pair with the xor
+// butterfly: the same IEEE operations in the same order as the small-R kernel.
+constexpr int kTileR = 32, kTileE = 32, kTileThreads = 512, kTileStages = 4;
+constexpr int kTileXBytes = kTileR * 128 * 2, kTileWBytes = kTileE * 128 * 4;
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 __global__ void __launch_bounds__(kTileThreads, 1) router_logits_tiled_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ wr,
     const uint8_t* __restrict__ row_valid, int R, int H, int E, float* __restrict__ logits) {
     extern __shared__ __align__(16) uint8_t rsm[];
-    uint16_t* xs = reinterpret_cast<uint16_t*>(rsm);                          // [2][32][128]
-    float* wsm = reinterpret_cast<float*>(rsm + 2 * kTileR * 128 * 2);        // [2][32][128]
-    float* qsm = wsm + 2 * kTileE * 128;                                      // [16 warps][64][32]
+    uint16_t* xs = reinterpret_cast<uint16_t*>(rsm);                                // [S][32][128]
+    float* wsm = reinterpret_cast<float*>(rsm + kTileStages * kTileXBytes);         // [S][32][128]
+    float* qsm = wsm + kTileStages * kTileE * 128;                                  // [16 warps][64][32]
     pdl_wait();
     pdl_launch_dependents();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -130,41 +144,33 @@ __global__ void __launch_bounds__(kTileThreads, 1) router_logits_tiled_kernel(
     const int r0 = blockIdx.y * kTileR, e0 = blockIdx.x * kTileE;
     const int steps = H / 128;
 
-    // One 128-column step of x (32 rows x 128 bf16 = 512 x 16 bytes) and w (32
-    // experts x 128 fp32 = 1024 x 16 bytes) per thread: loaded into registers
-    // one step ahead, stored to the other shared buffer after the current
-    // step's arithmetic, so the loads' latency overlaps it.
+    // Step i's tiles into ring buffer i % kTileStages: x is 512 x 16 bytes (one
+    // copy per thread), w 1024 x 16 bytes (two per thread).
     const int xrow = tid >> 4, xc = (tid & 15) * 8;
-    const size_t xoff = size_t(min(r0 + xrow, R - 1)) * H + xc;
-    uint4 xreg;
-    float4 wreg[kTileE * 32 / kTileThreads];
-    auto load = [&](int i) {
-        xreg = __ldg(reinterpret_cast<const uint4*>(x + xoff + i * 128));
+    const uint16_t* xsrc = x + size_t(min(r0 + xrow, R - 1)) * H + xc;
+    auto issue = [&](int i) {
+        if (i < steps) {
+            const int buf = i % kTileStages;
+            cp_async16(xs + (buf * kTileR + xrow) * 128 + xc, xsrc + i * 128);
 #pragma unroll
-        for (int u = 0; u < kTileE * 32 / kTileThreads; ++u) {
-            const int q = tid + u * kTileThreads;
-            const int ex = q >> 5, c = (q & 31) * 4;
-            const int e = min(e0 + ex, E - 1);
-            wreg[u] = __ldg(reinterpret_cast<const float4*>(wr + size_t(e) * H + i * 128 + c));
+            for (int u = 0; u < kTileE * 32 / kTileThreads; ++u) {
+                const int q = tid + u * kTileThreads;
+                const int ex = q >> 5, c = (q & 31) * 4;
+                const int e = min(e0 + ex, E - 1);
+                cp_async16(wsm + (buf * kTileE + ex) * 128 + c, wr + size_t(e) * H + i * 128 + c);
+            }
         }
-    };
-    auto store = [&](int buf) {
-        *reinterpret_cast<uint4*>(xs + (buf * kTileR + xrow) * 128 + xc) = xreg;
-#pragma unroll
-        for (int u = 0; u < kTileE * 32 / kTileThreads; ++u) {
-            const int q = tid + u * kTileThreads;
-            const int ex = q >> 5, c = (q & 31) * 4;
-            *reinterpret_cast<float4*>(wsm + (buf * kTileE + ex) * 128 + c) = wreg[u];
-        }
+        cp_async_commit();   // one group per step, empty past the end: uniform counting
     };
 
     float p[8][8];
-    load(0);
-    store(0);
-    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kTileStages - 1; ++i) issue(i);
     for (int i = 0; i < steps; ++i) {
-        const int buf = i & 1;
-        if (i + 1 < steps) load(i + 1);
+        const int buf = i % kTileStages;
+        cp_async_wait<kTileStages - 2>();   // this thread's copies of step i have landed
+        __syncthreads();                    // everyone's have; step i-1's buffer is free
+        issue(i + kTileStages - 1);
         if ((i & 7) == 0) {
 #pragma unroll
             for (int a = 0; a < 8; ++a)
@@ -197,7 +203,6 @@ __global__ void __launch_bounds__(kTileThreads, 1) router_logits_tiled_kernel(
                 }
             }
         }
-        if (i + 1 < steps) store(buf ^ 1);
         if ((i & 7) == 7 || i + 1 == steps) {   // end of a 1024-column chunk
             float* qw = qsm + size_t(warp) * 64 * 32;
             const bool first = (i < 8);
@@ -209,8 +214,8 @@ __global__ void __launch_bounds__(kTileThreads, 1) router_logits_tiled_kernel(
                     *slot = first ? p[a][b] : __fadd_rn(*slot, p[a][b]);
                 }
         }
-        __syncthreads();
     }
+    cp_async_wait<0>();
     const float* qw = qsm + size_t(warp) * 64 * 32;
     for (int pair = 0; pair < 64; ++pair) {
         float q = qw[pair * 32 + lane];
@@ -260,7 +265,7 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const uint8
         if (e != cudaSuccess) return e;
     } else {
         dim3 grid((E + kTileE - 1) / kTileE, (R + kTileR - 1) / kTileR);
-        const size_t smem = size_t(2) * kTileR * 128 * 2 + size_t(2) * kTileE * 128 * 4 +
+        const size_t smem = size_t(kTileStages) * (kTileXBytes + kTileWBytes) +
                             size_t(kTileThreads / 32) * 64 * 32 * 4;
         cudaError_t e = cudaFuncSetAttribute(router_logits_tiled_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
