@@ -29,7 +29,9 @@
 //   warp 0 lane 0: TMA producer -- weight tiles (evict-first) and row tiles
 //                  into an n_stages ring of shared-memory stages;
 //   warp 1 lane 0: MMA issuer -- 4 x tcgen05.mma (K = 32) per operand per
-//                  K-block into a ring of ACC_BUFS tensor-memory partials;
+//                  K-block into a ring of ACC_BUFS tensor-memory partials,
+//                  then one tcgen05.commit per K-block that frees its stages
+//                  and hands its partial to the epilogue;
 //   warps 2.. : epilogue -- 4 * NT/CW warps; warp w reads TMEM lanes
 //                  32*(w%4).. and CW columns (16, or 32 at 64-row tiles),
 //                  promotes the partials, then
@@ -76,6 +78,13 @@ struct FfnCfg {
 };
 
 constexpr int kMaxStages = 16;
+// One tcgen05.commit per K-block, onto kbrel[K-block % kKbRing]: it both frees
+// the K-block's shared-memory stages for the producer and hands its
+// accumulator to the epilogue (a commit costs about as much as four small-N
+// MMAs, so one per K-block instead of one per stage plus one per K-block).
+// The ring outlasts the producer's and the epilogue's lead over the MMA
+// (at most kMaxStages, resp. 16 K-blocks), so a parity wait never aliases.
+constexpr int kKbRing = 32;
 
 // Shared-memory carve-up, identical on host (size) and device (pointers).
 struct FfnSmem {
@@ -97,7 +106,7 @@ __host__ __device__ inline FfnSmem ffn_smem(int nt, int n_stages, int kbmax, int
     b += nt * 4;
     b = (b + 7) & ~7;
     s.bars = b;
-    b += (2 * n_stages + 2 * 16 + 1) * 8;
+    b += (n_stages + kKbRing + 16 + 1) * 8;
     s.tmem = b;
     b += 4;
     s.flag = b;
@@ -190,9 +199,8 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
     uint8_t* s_tile = smem + L.tile;                         // [NT][128]
     int* s_src = reinterpret_cast<int*>(smem + L.src);       // [NT]
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
-    uint64_t* empty = full + p.n_stages;
-    uint64_t* acc_full = empty + p.n_stages;
-    uint64_t* acc_empty = acc_full + 16;
+    uint64_t* kbrel = full + p.n_stages;       // [kKbRing] K-block done (stages free, partial ready)
+    uint64_t* acc_empty = kbrel + kKbRing;     // [16] epilogue done with a TMEM partial
     uint64_t* drain = acc_empty + 16;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L.tmem);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L.flag);
@@ -200,14 +208,9 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < p.n_stages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        for (int b = 0; b < C::ACC_BUFS; ++b) {
-            mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], C::EPI_WARPS);
-        }
+        for (int s = 0; s < p.n_stages; ++s) mbar_init(&full[s], 1);
+        for (int b = 0; b < kKbRing; ++b) mbar_init(&kbrel[b], 1);
+        for (int b = 0; b < C::ACC_BUFS; ++b) mbar_init(&acc_empty[b], C::EPI_WARPS);
         mbar_init(drain, 1);
         *s_abort = 0;
         fence_barrier_init();
@@ -274,6 +277,16 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                     phase ^= 1u;
                 }
             };
+            // used_by[s]: the CTA's K-block index that reads stage s (none yet:
+            // ~0); before a stage is refilled, that K-block must be done
+            uint32_t used_by[kMaxStages];
+            for (int q = 0; q < kMaxStages; ++q) used_by[q] = ~0u;
+            auto wait_free = [&](int s) -> bool {
+                const uint32_t jj = used_by[s];
+                return jj == ~0u ||
+                       mbar_wait(&kbrel[jj % kKbRing], (jj / kKbRing) & 1u, p.err, p.timeout_ns);
+            };
+            uint32_t kb_base = 0;   // K-blocks of the CTA's earlier tiles
             // Weights are inputs of the layer, not outputs of the previous
             // kernel: the first tile's first weight tiles are requested before
             // the wait on that kernel, its row tiles after.
@@ -285,7 +298,10 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                 tl0 = tile_of(t0, n_gu, MB_I, MB_H, items);
                 it0 = items[tl0.item];
                 pre = min(tl0.gu ? 2 * KB_H : KB_I, p.n_stages);
-                for (int j = 0; j < pre; ++j) a_load(tl0, it0, j, j);
+                for (int j = 0; j < pre; ++j) {
+                    a_load(tl0, it0, j, j);
+                    used_by[j] = static_cast<uint32_t>(tl0.gu ? (j >> 1) : j);
+                }
             }
             pdl_wait();
             pdl_launch_dependents();
@@ -318,11 +334,12 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                     int nd = 0, dst[kMaxStages];
                     if (ld_acquire(p.ready + tl.item) < MB_I) {
                         while (nd < NS && nd < p.n_stages) {
-                            if (!mbar_wait(&empty[stage], phase ^ 1u, p.err, p.timeout_ns)) {
+                            if (!wait_free(stage)) {
                                 ok = false;
                                 break;
                             }
                             a_load(tl, it, nd, stage);
+                            used_by[stage] = kb_base + static_cast<uint32_t>(nd);
                             dst[nd++] = stage;
                             ++issued;
                             next_stage();
@@ -335,15 +352,17 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                     j = nd;
                 }
                 for (; j < NS && ok; ++j) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, p.err, p.timeout_ns)) {
+                    if (!wait_free(stage)) {
                         ok = false;
                         break;
                     }
                     a_load(tl, it, j, stage);
                     b_load(tl, it, j, stage);
+                    used_by[stage] = kb_base + static_cast<uint32_t>(tl.gu ? (j >> 1) : j);
                     ++issued;
                     next_stage();
                 }
+                kb_base += static_cast<uint32_t>(tl.gu ? KB_H : KB_I);
             }
             if (!ok) *s_abort = 1;
         }
@@ -353,6 +372,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             constexpr uint32_t idesc = idesc_e4m3_f32(128, NT);
             int stage = 0, ab = 0;
             uint32_t phase = 0, aph = 0;
+            uint32_t jk = 0;   // the CTA's K-block counter
             bool ok = true;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
                 const bool gu = t < n_gu;
@@ -376,14 +396,14 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                         for (int k = 0; k < 4; ++k)
                             mma_e4m3(d, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(bb + 32 * k), idesc,
                                      k > 0);
-                        mma_commit(&empty[stage]);
                         if (++stage == p.n_stages) {
                             stage = 0;
                             phase ^= 1u;
                         }
                     }
                     if (!ok) break;
-                    mma_commit(&acc_full[ab]);
+                    mma_commit(&kbrel[jk % kKbRing]);   // stages free + partial ready
+                    ++jk;
                     if (++ab == C::ACC_BUFS) {
                         ab = 0;
                         aph ^= 1u;
@@ -400,7 +420,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
         const int m = 32 * q + lane;     // output feature inside the 128-row block
         const int et = threadIdx.x - 64; // 0 .. EPI_THREADS-1
         int ab = 0;
-        uint32_t aph = 0;
+        uint32_t je = 0;   // the CTA's K-block counter
         bool ok = true;
         pdl_wait();   // row scales and outputs belong to the previous kernel
         Tile tl_next{0, 0, true, false};
@@ -459,7 +479,8 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             }
             for (int kb = 0; kb < KB && ok; ++kb) {
                 // a failed wait is acted on by the whole warp (tcgen05.ld is warp-wide)
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&acc_full[ab], aph, p.err, p.timeout_ns))) {
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&kbrel[je % kKbRing], (je / kKbRing) & 1u,
+                                                       p.err, p.timeout_ns))) {
                     ok = false;
                     *s_abort = 1;
                     break;
@@ -508,10 +529,8 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[ab]);
-                if (++ab == C::ACC_BUFS) {
-                    ab = 0;
-                    aph ^= 1u;
-                }
+                ++je;
+                if (++ab == C::ACC_BUFS) ab = 0;
             }
             if (C::NA == 2 && tl.gu) {
                 // h = silu(g) * u; per-row amax over the 128 features
