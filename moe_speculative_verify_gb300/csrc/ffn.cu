@@ -75,15 +75,22 @@ struct FfnCfg {
                                      : (ACC_BUFS * ACC_COLS <= 128) ? 128
                                      : (ACC_BUFS * ACC_COLS <= 256) ? 256 : 512;
     static_assert(ACC_BUFS * ACC_COLS <= 512, "tensor memory");
+    static_assert(ACC_BUFS % 2 == 0, "the MMA checks TMEM partials in pairs");
 };
 
 constexpr int kMaxStages = 16;
-// One tcgen05.commit per K-block, onto kbrel[K-block % kKbRing]: it both frees
-// the K-block's shared-memory stages for the producer and hands its
-// accumulator to the epilogue (a commit costs about as much as four small-N
-// MMAs, so one per K-block instead of one per stage plus one per K-block).
-// The ring outlasts the producer's and the epilogue's lead over the MMA
-// (at most kMaxStages, resp. 16 K-blocks), so a parity wait never aliases.
+// Per K-block (not per stage) synchronisation, on two rings of barriers
+// indexed by the CTA's K-block counter j:
+//   kbfull[j % kKbRing] -- the K-block's operands have landed: the producer
+//       arms it once with the bytes of all the K-block's stages, every TMA
+//       copy of those stages completes on it;
+//   kbrel[j % kKbRing]  -- one tcgen05.commit after the K-block's MMAs: its
+//       stages are free for the producer and its partial is ready for the
+//       epilogue.
+// A barrier wait or a commit costs about as much as several small-N MMAs, so
+// the MMA thread waits once for data and commits once per K-block.  The rings
+// outlast the producer's and the epilogue's lead over the MMA (at most
+// kMaxStages, resp. 16 K-blocks), so a parity wait never aliases.
 constexpr int kKbRing = 32;
 
 // Shared-memory carve-up, identical on host (size) and device (pointers).
@@ -106,7 +113,7 @@ __host__ __device__ inline FfnSmem ffn_smem(int nt, int n_stages, int kbmax, int
     b += nt * 4;
     b = (b + 7) & ~7;
     s.bars = b;
-    b += (n_stages + kKbRing + 16 + 1) * 8;
+    b += (2 * kKbRing + 16 + 1) * 8;
     s.tmem = b;
     b += 4;
     s.flag = b;
@@ -198,18 +205,25 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
     float* s_red = reinterpret_cast<float*>(smem + L.red);   // [4][NT]
     uint8_t* s_tile = smem + L.tile;                         // [NT][128]
     int* s_src = reinterpret_cast<int*>(smem + L.src);       // [NT]
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars);
-    uint64_t* kbrel = full + p.n_stages;       // [kKbRing] K-block done (stages free, partial ready)
+    uint64_t* kbfull = reinterpret_cast<uint64_t*>(smem + L.bars);   // [kKbRing] operands landed
+    uint64_t* kbrel = kbfull + kKbRing;        // [kKbRing] K-block done (stages free, partial ready)
     uint64_t* acc_empty = kbrel + kKbRing;     // [16] epilogue done with a TMEM partial
     uint64_t* drain = acc_empty + 16;
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L.tmem);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L.flag);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // producer (thread 0): used_by[s] = the CTA's K-block index that reads
+    // stage s (none yet: ~0); before a stage is refilled, that K-block must
+    // be done, and on a wind-down its copies are waited for
+    uint32_t used_by[kMaxStages];
+    for (int q = 0; q < kMaxStages; ++q) used_by[q] = ~0u;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < p.n_stages; ++s) mbar_init(&full[s], 1);
-        for (int b = 0; b < kKbRing; ++b) mbar_init(&kbrel[b], 1);
+        for (int b = 0; b < kKbRing; ++b) {
+            mbar_init(&kbfull[b], 1);
+            mbar_init(&kbrel[b], 1);
+        }
         for (int b = 0; b < C::ACC_BUFS; ++b) mbar_init(&acc_empty[b], C::EPI_WARPS);
         mbar_init(drain, 1);
         *s_abort = 0;
@@ -251,25 +265,28 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             uint32_t phase = 0;
             // Stage j of a tile: gate/up tiles alternate gate and up weight
             // tiles per K-block (j = 2*kb + {0, 1}); down tiles one per K-block.
-            auto a_load = [&](const Tile& tl, const int4& it, int j, int s) {
+            // stage j of a tile belongs to the CTA's K-block kbj; its first
+            // stage arms the K-block's barrier with the bytes of all its stages
+            auto a_load = [&](const Tile& tl, const int4& it, int j, int s, uint32_t kbj) {
                 const bool sh = it.x == p.E;
                 const int ex = sh ? 0 : it.x;
                 uint8_t* st = st_base + s * C::STAGE_BYTES;
                 const uint64_t pol = tl.shared_w ? pol_shared : pol_once;
-                mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+                uint64_t* bar = &kbfull[kbj % kKbRing];
+                if (!tl.gu || (j & 1) == 0)
+                    mbar_arrive_expect_tx(bar, (tl.gu ? 2 : 1) * C::STAGE_BYTES);
                 if (tl.gu) {
                     const CUtensorMap* m = (j & 1) ? (sh ? &map_su : &map_u) : (sh ? &map_sg : &map_g);
-                    tma_load_2d_hint(st, m, &full[s], (j >> 1) * kBlock, ex * p.I + tl.blk * kBlock,
-                                     pol);
+                    tma_load_2d_hint(st, m, bar, (j >> 1) * kBlock, ex * p.I + tl.blk * kBlock, pol);
                 } else {
-                    tma_load_2d_hint(st, sh ? &map_sd : &map_d, &full[s], j * kBlock,
+                    tma_load_2d_hint(st, sh ? &map_sd : &map_d, bar, j * kBlock,
                                      ex * p.H + tl.blk * kBlock, pol);
                 }
             };
-            auto b_load = [&](const Tile& tl, const int4& it, int j, int s) {
+            auto b_load = [&](const Tile& tl, const int4& it, int j, int s, uint32_t kbj) {
                 const int kb = tl.gu ? (j >> 1) : j;
                 tma_load_2d(st_base + s * C::STAGE_BYTES + C::B_OFF, tl.gu ? &map_x : &map_h,
-                            &full[s], kb * kBlock, it.y);
+                            &kbfull[kbj % kKbRing], kb * kBlock, it.y);
             };
             auto next_stage = [&]() {
                 if (++stage == p.n_stages) {
@@ -277,10 +294,6 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                     phase ^= 1u;
                 }
             };
-            // used_by[s]: the CTA's K-block index that reads stage s (none yet:
-            // ~0); before a stage is refilled, that K-block must be done
-            uint32_t used_by[kMaxStages];
-            for (int q = 0; q < kMaxStages; ++q) used_by[q] = ~0u;
             auto wait_free = [&](int s) -> bool {
                 const uint32_t jj = used_by[s];
                 return jj == ~0u ||
@@ -299,8 +312,8 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                 it0 = items[tl0.item];
                 pre = min(tl0.gu ? 2 * KB_H : KB_I, p.n_stages);
                 for (int j = 0; j < pre; ++j) {
-                    a_load(tl0, it0, j, j);
                     used_by[j] = static_cast<uint32_t>(tl0.gu ? (j >> 1) : j);
+                    a_load(tl0, it0, j, j, used_by[j]);
                 }
             }
             pdl_wait();
@@ -311,7 +324,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                 ok = wait_counter(p.ready + tl0.item, MB_I, p.err, p.timeout_ns, s_abort);
                 fence_proxy_async_global();
             }
-            for (int j = 0; j < pre && ok; ++j) b_load(tl0, it0, j, j);
+            for (int j = 0; j < pre && ok; ++j) b_load(tl0, it0, j, j, used_by[j]);
             issued = static_cast<uint32_t>(pre);
             stage = pre % p.n_stages;
             phase = (pre == p.n_stages) ? 1u : 0u;
@@ -338,8 +351,8 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                                 ok = false;
                                 break;
                             }
-                            a_load(tl, it, nd, stage);
                             used_by[stage] = kb_base + static_cast<uint32_t>(nd);
+                            a_load(tl, it, nd, stage, used_by[stage]);
                             dst[nd++] = stage;
                             ++issued;
                             next_stage();
@@ -348,7 +361,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                             ok = false;
                     }
                     fence_proxy_async_global();
-                    for (int q = 0; q < nd && ok; ++q) b_load(tl, it, q, dst[q]);
+                    for (int q = 0; q < nd && ok; ++q) b_load(tl, it, q, dst[q], used_by[dst[q]]);
                     j = nd;
                 }
                 for (; j < NS && ok; ++j) {
@@ -356,9 +369,9 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                         ok = false;
                         break;
                     }
-                    a_load(tl, it, j, stage);
-                    b_load(tl, it, j, stage);
                     used_by[stage] = kb_base + static_cast<uint32_t>(tl.gu ? (j >> 1) : j);
+                    a_load(tl, it, j, stage, used_by[stage]);
+                    b_load(tl, it, j, stage, used_by[stage]);
                     ++issued;
                     next_stage();
                 }
@@ -378,17 +391,24 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                 const bool gu = t < n_gu;
                 const int KB = gu ? KB_H : KB_I;
                 for (int kb = 0; kb < KB && ok; ++kb) {
-                    if (*s_abort || !mbar_wait(&acc_empty[ab], aph ^ 1u, p.err, p.timeout_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t d0 = tmem + ab * C::ACC_COLS;
-                    for (int op = 0; op < (gu ? 2 : 1); ++op) {
-                        if (!mbar_wait(&full[stage], phase, p.err, p.timeout_ns)) {
+                    // TMEM partials are freed in order, so at even K-blocks one
+                    // wait for the odd buffer's last use covers both buffers
+                    if ((jk & 1u) == 0) {
+                        const uint32_t jn = jk + 1;
+                        const uint32_t bn = jn % C::ACC_BUFS;
+                        if (*s_abort || !mbar_wait(&acc_empty[bn], ((jn / C::ACC_BUFS) & 1u) ^ 1u,
+                                                   p.err, p.timeout_ns)) {
                             ok = false;
                             break;
                         }
-                        tc_fence_after();
+                    }
+                    if (!mbar_wait(&kbfull[jk % kKbRing], (jk / kKbRing) & 1u, p.err, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d0 = tmem + ab * C::ACC_COLS;
+                    for (int op = 0; op < (gu ? 2 : 1); ++op) {
                         const uint32_t a0 = smem_u32(st_base + stage * C::STAGE_BYTES);
                         const uint32_t bb = a0 + C::B_OFF;
                         const uint32_t d = d0 + op * NT;
@@ -401,7 +421,6 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                             phase ^= 1u;
                         }
                     }
-                    if (!ok) break;
                     mma_commit(&kbrel[jk % kKbRing]);   // stages free + partial ready
                     ++jk;
                     if (++ab == C::ACC_BUFS) {
@@ -598,13 +617,15 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
         // get one shared budget of kDrainNs (they land within microseconds).
         constexpr uint64_t kDrainNs = 2000000;   // 2 ms
         if (threadIdx.x == 0) {
+            // the K-blocks of the stages last filled (a K-block whose copies
+            // were not all requested never completes: the budget ends it)
             const uint64_t t0 = globaltimer_ns();
-            const uint32_t first = issued > static_cast<uint32_t>(p.n_stages)
-                                       ? issued - static_cast<uint32_t>(p.n_stages) : 0u;
-            for (uint32_t i = first; i < issued; ++i) {
+            for (int q = 0; q < p.n_stages && issued > 0; ++q) {
+                const uint32_t jj = used_by[q];
+                if (jj == ~0u) continue;
                 const uint64_t used = globaltimer_ns() - t0;
                 if (used >= kDrainNs) break;
-                mbar_wait(&full[i % p.n_stages], (i / p.n_stages) & 1u, nullptr, kDrainNs - used);
+                mbar_wait(&kbfull[jj % kKbRing], (jj / kKbRing) & 1u, nullptr, kDrainNs - used);
             }
             while (globaltimer_ns() - t0 < kDrainNs / 4) __nanosleep(1000);
         }
