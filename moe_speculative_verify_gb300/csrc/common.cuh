@@ -71,20 +71,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Non-blocking test: has the phase of `bar` with the given parity completed?
-// (acquire semantics when it has, like a successful wait)
-__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // Waits for the phase of `bar` with the given parity to complete, giving up
 // after `timeout_ns` of wall time or 2^30 polls, whichever comes first.  On
 // giving up it records MOE_ERR_TIMEOUT and returns false; the caller then

@@ -386,10 +386,6 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             int stage = 0, ab = 0;
             uint32_t phase = 0, aph = 0;
             uint32_t jk = 0;   // the CTA's K-block counter
-            // outcomes of the non-blocking tests of the next K-block's
-            // barriers, issued before the current K-block's MMAs so that their
-            // latency hides behind them; a blocking wait only when one failed
-            bool data_ready = false, acc_ready = false;
             bool ok = true;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
                 const bool gu = t < n_gu;
@@ -397,26 +393,18 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                 for (int kb = 0; kb < KB && ok; ++kb) {
                     // TMEM partials are freed in order, so at even K-blocks one
                     // wait for the odd buffer's last use covers both buffers
-                    const uint32_t jn = jk + 1;
-                    if ((jk & 1u) == 0 && !acc_ready) {
-                        if (*s_abort || !mbar_wait(&acc_empty[jn % C::ACC_BUFS],
-                                                   ((jn / C::ACC_BUFS) & 1u) ^ 1u, p.err,
-                                                   p.timeout_ns)) {
+                    if ((jk & 1u) == 0) {
+                        const uint32_t jn = jk + 1;
+                        const uint32_t bn = jn % C::ACC_BUFS;
+                        if (*s_abort || !mbar_wait(&acc_empty[bn], ((jn / C::ACC_BUFS) & 1u) ^ 1u,
+                                                   p.err, p.timeout_ns)) {
                             ok = false;
                             break;
                         }
                     }
-                    if (!data_ready &&
-                        !mbar_wait(&kbfull[jk % kKbRing], (jk / kKbRing) & 1u, p.err, p.timeout_ns)) {
+                    if (!mbar_wait(&kbfull[jk % kKbRing], (jk / kKbRing) & 1u, p.err, p.timeout_ns)) {
                         ok = false;
                         break;
-                    }
-                    data_ready = mbar_test(&kbfull[jn % kKbRing], (jn / kKbRing) & 1u);
-                    acc_ready = false;
-                    if ((jn & 1u) == 0) {   // the next K-block starts a pair
-                        const uint32_t jm = jn + 1;
-                        acc_ready = mbar_test(&acc_empty[jm % C::ACC_BUFS],
-                                              ((jm / C::ACC_BUFS) & 1u) ^ 1u);
                     }
                     tc_fence_after();
                     const uint32_t d0 = tmem + ab * C::ACC_COLS;
