@@ -197,6 +197,17 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
         : "memory");
 }
 
+// 8 consecutive fp32 columns of this thread's TMEM lane (32x32b shape).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // 16 consecutive fp32 columns of this thread's TMEM lane (32x32b shape).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
@@ -231,8 +242,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 
 template <int N>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N]) {
-    static_assert(N == 16 || N == 32, "16 or 32 columns");
-    if constexpr (N == 16) tmem_ld16(taddr, v);
+    static_assert(N == 8 || N == 16 || N == 32, "8, 16 or 32 columns");
+    if constexpr (N == 8) tmem_ld8(taddr, v);
+    else if constexpr (N == 16) tmem_ld16(taddr, v);
     else tmem_ld32(taddr, v);
 }
 

@@ -55,7 +55,10 @@ struct FfnCfg {
     static constexpr int B_OFF = A_BYTES;
     static constexpr int B_BYTES = NT * 128;
     static constexpr int STAGE_BYTES = B_OFF + B_BYTES;
-    static constexpr int CW = (NT >= 64) ? 32 : 16;           // columns per epilogue warp
+    // columns per epilogue warp: 16 at 16- and 64-row tiles, 8 at 32-row
+    // tiles (16 epilogue warps at 32 and 64 rows: the per-K-block promotion
+    // is spread over as many warps as the block can hold)
+    static constexpr int CW = (NT == 32) ? 8 : 16;
     static constexpr int CSPLIT = NT / CW;
     static constexpr int EPI_WARPS = 4 * CSPLIT;
     static constexpr int EPI_THREADS = 32 * EPI_WARPS;
@@ -435,7 +438,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
         // ----------------------------------------------------- epilogue
         const int ew = warp - 2;
         const int q = warp & 3;          // TMEM lane quadrant this warp may access
-        const int cg = ew >> 2;          // 16-column group
+        const int cg = ew >> 2;          // CW-column group
         const int m = 32 * q + lane;     // output feature inside the 128-row block
         const int et = threadIdx.x - 64; // 0 .. EPI_THREADS-1
         int ab = 0;
@@ -490,6 +493,9 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             if (!ok) break;
 
             constexpr int CW = C::CW;
+            // columns per TMEM load: 8 in the 18-warp blocks (96 registers a
+            // thread), else up to 16
+            constexpr int CH = (C::EPI_WARPS >= 16 || CW < 16) ? 8 : 16;
             float acc0[CW], acc1[CW];
 #pragma unroll
             for (int j = 0; j < CW; ++j) {
@@ -505,25 +511,25 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                     break;
                 }
                 tc_fence_after();
-                // 16 columns at a time: the TMEM loads of a chunk, then its FMAs
+                // CH columns at a time: the TMEM loads of a chunk, then its FMAs
 #pragma unroll
-                for (int hc = 0; hc < CW / 16; ++hc) {
+                for (int hc = 0; hc < CW / CH; ++hc) {
                     const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) +
-                                        ab * C::ACC_COLS + cg * CW + hc * 16;
-                    float v0[16], v1[16];
-                    tmem_ld16(ta, v0);
-                    if (C::NA == 2 && tl.gu) tmem_ld16(ta + NT, v1);
+                                        ab * C::ACC_COLS + cg * CW + hc * CH;
+                    float v0[CH], v1[CH];
+                    tmem_ld<CH>(ta, v0);
+                    if (C::NA == 2 && tl.gu) tmem_ld<CH>(ta + NT, v1);
                     tmem_wait_ld();
                     const float4* q0 =
-                        reinterpret_cast<const float4*>(s_sc + kb * NT + cg * CW + hc * 16);
+                        reinterpret_cast<const float4*>(s_sc + kb * NT + cg * CW + hc * CH);
                     if (C::NA == 2 && tl.gu) {
                         const float4* q1 = reinterpret_cast<const float4*>(
-                            s_sc + (KB + kb) * NT + cg * CW + hc * 16);
+                            s_sc + (KB + kb) * NT + cg * CW + hc * CH);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
+                        for (int v = 0; v < CH / 4; ++v) {
                             const float4 a4 = q0[v], b4 = q1[v];
-                            float* a0p = &acc0[hc * 16 + 4 * v];
-                            float* a1p = &acc1[hc * 16 + 4 * v];
+                            float* a0p = &acc0[hc * CH + 4 * v];
+                            float* a1p = &acc1[hc * CH + 4 * v];
                             a0p[0] = fmaf(v0[4 * v], a4.x, a0p[0]);
                             a0p[1] = fmaf(v0[4 * v + 1], a4.y, a0p[1]);
                             a0p[2] = fmaf(v0[4 * v + 2], a4.z, a0p[2]);
@@ -535,9 +541,9 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                         }
                     } else {
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
+                        for (int v = 0; v < CH / 4; ++v) {
                             const float4 a4 = q0[v];
-                            float* a0p = &acc0[hc * 16 + 4 * v];
+                            float* a0p = &acc0[hc * CH + 4 * v];
                             a0p[0] = fmaf(v0[4 * v], a4.x, a0p[0]);
                             a0p[1] = fmaf(v0[4 * v + 1], a4.y, a0p[1]);
                             a0p[2] = fmaf(v0[4 * v + 2], a4.z, a0p[2]);
