@@ -82,18 +82,16 @@ struct FfnCfg {
 };
 
 constexpr int kMaxStages = 16;
-// Synchronisation per group of two K-blocks of one tile (a tile with an odd
-// number of K-blocks ends with a group of one; a group never spans tiles, so a
-// down tile's wait for h never holds back a gate/up K-block), on two rings of
-// barriers indexed by the CTA's group counter g:
-//   kbfull[g % kKbRing] -- the group's operands have landed: the producer
-//       arms it once with the bytes of all the group's stages, every TMA copy
-//       of those stages completes on it;
-//   kbrel[g % kKbRing]  -- one tcgen05.commit after the group's MMAs: its
-//       stages are free for the producer and its partials are ready for the
+// Per K-block (not per stage) synchronisation, on two rings of barriers
+// indexed by the CTA's K-block counter j:
+//   kbfull[j % kKbRing] -- the K-block's operands have landed: the producer
+//       arms it once with the bytes of all the K-block's stages, every TMA
+//       copy of those stages completes on it;
+//   kbrel[j % kKbRing]  -- one tcgen05.commit after the K-block's MMAs: its
+//       stages are free for the producer and its partial is ready for the
 //       epilogue.
 // A barrier wait or a commit costs about as much as several small-N MMAs, so
-// the MMA thread waits once for data and commits once per group.  The rings
+// the MMA thread waits once for data and commits once per K-block.  The rings
 // outlast the producer's and the epilogue's lead over the MMA (at most
 // kMaxStages, resp. 16 K-blocks), so a parity wait never aliases.
 constexpr int kKbRing = 32;
@@ -218,9 +216,9 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L.flag);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // producer (thread 0): used_by[s] = the CTA's group index that reads
-    // stage s (none yet: ~0); before a stage is refilled, that group must be
-    // done, and on a wind-down its copies are waited for
+    // producer (thread 0): used_by[s] = the CTA's K-block index that reads
+    // stage s (none yet: ~0); before a stage is refilled, that K-block must
+    // be done, and on a wind-down its copies are waited for
     uint32_t used_by[kMaxStages];
     for (int q = 0; q < kMaxStages; ++q) used_by[q] = ~0u;
 
@@ -270,20 +268,16 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             uint32_t phase = 0;
             // Stage j of a tile: gate/up tiles alternate gate and up weight
             // tiles per K-block (j = 2*kb + {0, 1}); down tiles one per K-block.
-            // stage j of a tile belongs to the CTA's group gj; the first stage
-            // of a group arms its barrier with the bytes of all its stages
-            auto a_load = [&](const Tile& tl, const int4& it, int j, int s, uint32_t gj) {
+            // stage j of a tile belongs to the CTA's K-block kbj; its first
+            // stage arms the K-block's barrier with the bytes of all its stages
+            auto a_load = [&](const Tile& tl, const int4& it, int j, int s, uint32_t kbj) {
                 const bool sh = it.x == p.E;
                 const int ex = sh ? 0 : it.x;
                 uint8_t* st = st_base + s * C::STAGE_BYTES;
                 const uint64_t pol = tl.shared_w ? pol_shared : pol_once;
-                uint64_t* bar = &kbfull[gj % kKbRing];
-                const int spk = tl.gu ? 2 : 1;              // stages per K-block
-                if (j % (2 * spk) == 0) {
-                    const int KBt = tl.gu ? KB_H : KB_I;
-                    const int kbj = j / spk;
-                    mbar_arrive_expect_tx(bar, (kbj + 1 < KBt ? 2 : 1) * spk * C::STAGE_BYTES);
-                }
+                uint64_t* bar = &kbfull[kbj % kKbRing];
+                if (!tl.gu || (j & 1) == 0)
+                    mbar_arrive_expect_tx(bar, (tl.gu ? 2 : 1) * C::STAGE_BYTES);
                 if (tl.gu) {
                     const CUtensorMap* m = (j & 1) ? (sh ? &map_su : &map_u) : (sh ? &map_sg : &map_g);
                     tma_load_2d_hint(st, m, bar, (j >> 1) * kBlock, ex * p.I + tl.blk * kBlock, pol);
@@ -292,14 +286,10 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                                      ex * p.H + tl.blk * kBlock, pol);
                 }
             };
-            auto b_load = [&](const Tile& tl, const int4& it, int j, int s, uint32_t gj) {
+            auto b_load = [&](const Tile& tl, const int4& it, int j, int s, uint32_t kbj) {
                 const int kb = tl.gu ? (j >> 1) : j;
                 tma_load_2d(st_base + s * C::STAGE_BYTES + C::B_OFF, tl.gu ? &map_x : &map_h,
-                            &kbfull[gj % kKbRing], kb * kBlock, it.y);
-            };
-            // the group of stage j of a tile, given the groups of earlier tiles
-            auto group_of = [&](const Tile& tl, int j, uint32_t g0) -> uint32_t {
-                return g0 + static_cast<uint32_t>((tl.gu ? (j >> 1) : j) >> 1);
+                            &kbfull[kbj % kKbRing], kb * kBlock, it.y);
             };
             auto next_stage = [&]() {
                 if (++stage == p.n_stages) {
@@ -312,7 +302,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                 return jj == ~0u ||
                        mbar_wait(&kbrel[jj % kKbRing], (jj / kKbRing) & 1u, p.err, p.timeout_ns);
             };
-            uint32_t g_base = 0;   // groups of the CTA's earlier tiles
+            uint32_t kb_base = 0;   // K-blocks of the CTA's earlier tiles
             // Weights are inputs of the layer, not outputs of the previous
             // kernel: the first tile's first weight tiles are requested before
             // the wait on that kernel, its row tiles after.
@@ -325,7 +315,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                 it0 = items[tl0.item];
                 pre = min(tl0.gu ? 2 * KB_H : KB_I, p.n_stages);
                 for (int j = 0; j < pre; ++j) {
-                    used_by[j] = group_of(tl0, j, 0);
+                    used_by[j] = static_cast<uint32_t>(tl0.gu ? (j >> 1) : j);
                     a_load(tl0, it0, j, j, used_by[j]);
                 }
             }
@@ -364,7 +354,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                                 ok = false;
                                 break;
                             }
-                            used_by[stage] = group_of(tl, nd, g_base);
+                            used_by[stage] = kb_base + static_cast<uint32_t>(nd);
                             a_load(tl, it, nd, stage, used_by[stage]);
                             dst[nd++] = stage;
                             ++issued;
@@ -382,13 +372,13 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                         ok = false;
                         break;
                     }
-                    used_by[stage] = group_of(tl, j, g_base);
+                    used_by[stage] = kb_base + static_cast<uint32_t>(tl.gu ? (j >> 1) : j);
                     a_load(tl, it, j, stage, used_by[stage]);
                     b_load(tl, it, j, stage, used_by[stage]);
                     ++issued;
                     next_stage();
                 }
-                g_base += static_cast<uint32_t>(((tl.gu ? KB_H : KB_I) + 1) >> 1);
+                kb_base += static_cast<uint32_t>(tl.gu ? KB_H : KB_I);
             }
             if (!ok) *s_abort = 1;
         }
@@ -398,8 +388,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             constexpr uint32_t idesc = idesc_e4m3_f32(128, NT);
             int stage = 0, ab = 0;
             uint32_t phase = 0, aph = 0;
-            uint32_t jk = 0;   // the CTA's K-block counter (TMEM partials)
-            uint32_t jg = 0;   // the CTA's group counter (barrier rings)
+            uint32_t jk = 0;   // the CTA's K-block counter
             bool ok = true;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
                 const bool gu = t < n_gu;
@@ -416,8 +405,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                             break;
                         }
                     }
-                    if ((kb & 1) == 0 &&
-                        !mbar_wait(&kbfull[jg % kKbRing], (jg / kKbRing) & 1u, p.err, p.timeout_ns)) {
+                    if (!mbar_wait(&kbfull[jk % kKbRing], (jk / kKbRing) & 1u, p.err, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
@@ -436,10 +424,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                             phase ^= 1u;
                         }
                     }
-                    if ((kb & 1) == 1 || kb + 1 == KB) {   // the group's last K-block
-                        mma_commit(&kbrel[jg % kKbRing]);   // stages free + partials ready
-                        ++jg;
-                    }
+                    mma_commit(&kbrel[jk % kKbRing]);   // stages free + partial ready
                     ++jk;
                     if (++ab == C::ACC_BUFS) {
                         ab = 0;
@@ -457,7 +442,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
         const int m = 32 * q + lane;     // output feature inside the 128-row block
         const int et = threadIdx.x - 64; // 0 .. EPI_THREADS-1
         int ab = 0;
-        uint32_t ge = 0;   // the CTA's group counter
+        uint32_t je = 0;   // the CTA's K-block counter
         bool ok = true;
         pdl_wait();   // row scales and outputs belong to the previous kernel
         Tile tl_next{0, 0, true, false};
@@ -519,8 +504,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             }
             for (int kb = 0; kb < KB && ok; ++kb) {
                 // a failed wait is acted on by the whole warp (tcgen05.ld is warp-wide)
-                if ((kb & 1) == 0 &&
-                    !__all_sync(0xFFFFFFFFu, mbar_wait(&kbrel[ge % kKbRing], (ge / kKbRing) & 1u,
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&kbrel[je % kKbRing], (je / kKbRing) & 1u,
                                                        p.err, p.timeout_ns))) {
                     ok = false;
                     *s_abort = 1;
@@ -570,7 +554,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[ab]);
-                if ((kb & 1) == 1 || kb + 1 == KB) ++ge;
+                ++je;
                 if (++ab == C::ACC_BUFS) ab = 0;
             }
             if (C::NA == 2 && tl.gu) {
@@ -672,12 +656,11 @@ static cudaError_t launch_ffn_t(const FfnMaps& mp, FfnArgs args, int n_sms, int 
     const int kbmax = (MODE == kFfnGateUp) ? KB_H : (MODE == kFfnDown) ? KB_I : max(KB_H, KB_I);
     int stages = kMaxStages;
     FfnSmem L = ffn_smem(NT, stages, kbmax, C::STAGE_BYTES);
-    while (stages > 4 && L.bytes > smem_limit) {
+    while (stages > 2 && L.bytes > smem_limit) {
         --stages;
         L = ffn_smem(NT, stages, kbmax, C::STAGE_BYTES);
     }
-    // a group of two gate/up K-blocks occupies four stages at once
-    if (L.bytes > smem_limit || stages < 4) return cudaErrorInvalidConfiguration;
+    if (L.bytes > smem_limit) return cudaErrorInvalidConfiguration;
     args.n_stages = stages;
     cudaError_t e = cudaFuncSetAttribute(ffn_kernel<NT, MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L.bytes);
