@@ -49,6 +49,13 @@ def kernels_per_step(R: int) -> int:
     """Kernels of one moe_layer call: router logits, selection + union (one
     kernel up to 64 rows, two above), dispatch, expert GEMMs, combine."""
     return 5 if R <= 64 else 6
+# DRAM bytes (read + write) of the expert GEMM per algorithmic byte, for the
+# 16-row tile of calls of up to 64 rows: ncu on the same kernel at 8 rows on 32
+# experts of the same shape (dram__bytes_read.sum + dram__bytes_write.sum =
+# 1.0628 GB for 1.0598 GB); traffic grows with the weight bytes streamed, so a full launch's
+# traffic is this ratio times its algorithmic bytes.  Other tiles: not captured
+# at their full size here (null).
+FFN_TRAFFIC_PER_ALG_BYTE_16 = 1.0029
 HOST_AHEAD_CYCLES = 400_000   # GPU sleep before each step so the host enqueues it whole
 FLUSH_BYTES = 256 << 20       # > 129 MB L2
 
@@ -486,7 +493,12 @@ def main() -> None:
     roofline = {"kernel": {"ffn": "ffn_kernel<NT, fused> (gate/up + SiLU*mul + down)"}
                 .get(dom, dom), "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                "traffic": None, "peak_source": pk["source"],
+                "traffic": (round(dom_bytes * FFN_TRAFFIC_PER_ALG_BYTE_16)
+                            if dom == "ffn" and R <= 64 else None),
+                "traffic_source": ("ncu DRAM bytes per algorithmic byte at 8 rows on 32 experts "
+                                   "(same kernel and tile), times this launch's algorithmic bytes"
+                                   if dom == "ffn" and R <= 64 else None),
+                "peak_source": pk["source"],
                 "algorithmic_bytes_per_launch": dom_bytes}
 
     extra = {}
