@@ -18,12 +18,12 @@
 //                  128-wide K-block, A (the bf16 weight tile) from tensor
 //                  memory, B (the rows) from shared memory, into the tile's
 //                  accumulator (gate and up side by side for a gate/up tile);
-//   warps 2..13  : dequant, three groups of four taking steps in turn -- a staged
+//   warps 2..9   : dequant, two groups of four on alternate steps -- a staged
 //                  tile to bf16, written straight into a tensor-memory
 //                  operand slot (tcgen05.st; the dequantised tile never
 //                  touches shared memory); the group's leader also loads the
 //                  K-block's 16 rows (bf16) into the slot's shared part;
-//   warps 14..17 : epilogue -- gate/up: h = silu(g) * u rounded to bf16, row
+//   warps 10..13 : epilogue -- gate/up: h = silu(g) * u rounded to bf16, row
 //                  stores; down: fp32 rows to their slot.
 // Every wait is bounded; a timeout records MOE_ERR_TIMEOUT and winds down.
 #include "common.cuh"
@@ -35,14 +35,10 @@ namespace moe {
 namespace {
 
 constexpr int kNT = kW8A16RowsPerItem;       // rows per item (MMA N)
-constexpr int kDqGroups = 3;                 // dequant groups, taking steps in turn
-constexpr int kDqGroupWarps = 4;             // a group: one warp per TMEM lane quadrant
-constexpr int kDqWarps = kDqGroups * kDqGroupWarps;
+constexpr int kDqWarps = 8;                  // two groups of four, alternate steps
+constexpr int kDqGroupWarps = 4;
 constexpr int kEpiWarps = 4;
 constexpr int kThreads16 = 32 * (2 + kDqWarps + kEpiWarps);
-// registers a thread: each SM sub-partition holds 16K registers and
-// ceil(warps / 4) of the block's warps; in steps of 8
-constexpr int kMaxRegs16 = (16384 / (((kThreads16 / 32 + 3) / 4) * 32)) / 8 * 8;
 constexpr int kWBytes = 128 * 128;           // e4m3 weight tile
 constexpr int kBBytes = kNT * 128 * 2;       // bf16 rows: two K halves of kNT x 128 B
 constexpr int kSlotBytes = kBBytes;          // shared-memory part of an operand slot
@@ -185,7 +181,7 @@ __device__ __forceinline__ Tile16 tile16_of(int t, int n_gu, int mb_i, int mb_h,
     return x;
 }
 
-__global__ void __maxnreg__(kMaxRegs16)
+__global__ void __launch_bounds__(kThreads16, 1)
     ffn16_kernel(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUtensorMap map_u,
                  const __grid_constant__ CUtensorMap map_sg, const __grid_constant__ CUtensorMap map_su,
                  const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_d,
@@ -347,8 +343,8 @@ __global__ void __maxnreg__(kMaxRegs16)
         }
     } else if (warp < 2 + kDqWarps) {
         // --------------------------------------------------------- dequant
-        // kDqGroups groups of four warps take the steps of the CTA's step
-        // sequence in turn, so as many staged tiles are converted at once.  In a group,
+        // Two groups of four warps take alternate steps of the CTA's step
+        // sequence, so two staged tiles are converted at once.  In a group,
         // warp w converts rows 32*(w%4) .. +31 (the TMEM lanes it may access)
         // of the tile: per thread the 128 codes of its row, read from the
         // swizzled stage, written as 64 bf16x2 columns.
@@ -357,7 +353,7 @@ __global__ void __maxnreg__(kMaxRegs16)
         const int qd = warp & 3;
         const int row = 32 * qd + lane;
         const bool leader = (dw % kDqGroupWarps) == 0 && lane == 0;
-        uint32_t n = 0;              // the CTA's step counter (every group counts every step)
+        uint32_t n = 0;              // the CTA's step counter (both groups count every step)
         bool ok = true;
         pdl_wait();   // gathered rows and the counters belong to the previous kernel
         for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
@@ -377,17 +373,16 @@ __global__ void __maxnreg__(kMaxRegs16)
             };
             bool h_ready = tl.gu;
             // this group's first step of the tile
-            const int j0 = static_cast<int>((static_cast<uint32_t>(grp) + kDqGroups -
-                                             n % kDqGroups) % kDqGroups);
+            const int j0 = static_cast<int>((static_cast<uint32_t>(grp) - n) & 1u);
             float s_next = (j0 < NS) ? scale_of(j0) : 0.0f;
-            for (int j = j0; j < NS; j += kDqGroups) {
+            for (int j = j0; j < NS; j += 2) {
                 const uint32_t nj = n + static_cast<uint32_t>(j);
                 const int ws = static_cast<int>(nj % static_cast<uint32_t>(NW));
                 const uint32_t wph = (nj / static_cast<uint32_t>(NW)) & 1u;
                 const int slot = static_cast<int>(nj % kSlots);
                 const uint32_t sph = (nj / kSlots) & 1u;
                 const float s = s_next;
-                if (j + kDqGroups < NS) s_next = scale_of(j + kDqGroups);
+                if (j + 2 < NS) s_next = scale_of(j + 2);
                 // every wait's outcome is made uniform across the warp before use
                 bool got = !*s_abort && mbar_wait(&a_empty[slot], sph ^ 1u, p.err, p.timeout_ns);
                 if (!__all_sync(0xFFFFFFFFu, got)) {
