@@ -21,8 +21,8 @@ namespace moe {
 // per-lane partial sums of every (row, expert) pair of the tile; the block then
 // folds the chunks in ascending order per lane and finishes with the xor
 // butterfly across lanes.
-template <int RT, int EC>
-__global__ void __launch_bounds__(512) router_logits_kernel(
+template <int RT, int EC, int BS, int MAXT, int MINB>
+__global__ void __launch_bounds__(MAXT, MINB) router_logits_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ wr,
     const uint8_t* __restrict__ row_valid, int R, int H, int E, float* __restrict__ logits) {
     extern __shared__ float part[];  // [nchunks][EC][RT][32]
@@ -41,14 +41,14 @@ __global__ void __launch_bounds__(512) router_logits_kernel(
 #pragma unroll
             for (int b = 0; b < RT; ++b) p[a][b] = 0.0f;
         const int nsteps = min(8, (H - c * 1024) / 128);   // 128-column steps of this chunk
-        // Loads of four steps are issued together, then consumed in column
+        // Loads of BS steps are issued together, then consumed in column
         // order: the fma sequence per lane is unchanged.
 #pragma unroll
-        for (int s0 = 0; s0 < 8; s0 += 4) {
-            float4 w4[4][EC];
-            uint2 xv[4][RT];
+        for (int s0 = 0; s0 < 8; s0 += BS) {
+            float4 w4[BS][EC];
+            uint2 xv[BS][RT];
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
+            for (int s = 0; s < BS; ++s) {
                 if (s0 + s < nsteps) {
                     const int h = c * 1024 + (s0 + s) * 128 + 4 * lane;
 #pragma unroll
@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(512) router_logits_kernel(
                 }
             }
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
+            for (int s = 0; s < BS; ++s) {
                 if (s0 + s < nsteps) {
 #pragma unroll
                     for (int b = 0; b < RT; ++b) {
@@ -260,8 +260,14 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const uint8
         constexpr int RT = 8, EC = 1;
         dim3 grid(E / EC, (R + RT - 1) / RT);
         const size_t smem = size_t(nchunks) * EC * RT * 32 * sizeof(float);
-        cudaError_t e = launch_pdl(router_logits_kernel<RT, EC>, grid, dim3(threads), smem, stream,
-                                   x, wr, row_valid, R, H, E, logits);
+        // up to 6 chunks (hidden <= 6144): all eight steps of a chunk in one
+        // batch of loads, two blocks per SM; wider rows: batches of four
+        cudaError_t e =
+            (nchunks <= 6)
+                ? launch_pdl(router_logits_kernel<RT, EC, 8, 192, 2>, grid, dim3(threads), smem,
+                             stream, x, wr, row_valid, R, H, E, logits)
+                : launch_pdl(router_logits_kernel<RT, EC, 4, 512, 1>, grid, dim3(threads), smem,
+                             stream, x, wr, row_valid, R, H, E, logits);
         if (e != cudaSuccess) return e;
     } else {
         dim3 grid((E + kTileE - 1) / kTileE, (R + kTileR - 1) / kTileR);
