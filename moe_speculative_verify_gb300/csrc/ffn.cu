@@ -28,12 +28,12 @@
 // Warp roles (one CTA per SM):
 //   warp 0 lane 0: TMA producer -- weight tiles (evict-first) and row tiles
 //                  into an n_stages ring of shared-memory stages;
-//   warp 1 lane 0: MMA issuer -- 4 x tcgen05.mma (K = 32) per operand per
-//                  K-block into a ring of ACC_BUFS tensor-memory partials,
-//                  then one tcgen05.commit per K-block that frees its stages
-//                  and hands its partial to the epilogue;
-//   warps 2.. : epilogue -- 4 * NT/CW warps; warp w reads TMEM lanes
-//                  32*(w%4).. and CW columns (16, or 32 at 64-row tiles),
+//   warps 1, 2 lane 0: MMA issuers, alternate K-blocks -- 4 x tcgen05.mma
+//                  (K = 32) per operand per K-block into a ring of ACC_BUFS
+//                  tensor-memory partials, then one tcgen05.commit per K-block
+//                  that frees its stages and hands its partial to the epilogue;
+//   warps 3.. : epilogue -- 4 * NT/CW warps; warp w reads TMEM lanes
+//                  32*(w%4).. and CW columns (16, or 8 at 32-row tiles),
 //                  promotes the partials, then
 //                  gate/up: h = silu(g) * u, per-row 1x128 e4m3 quantisation
 //                  of h, coalesced row stores; down: fp32 rows to their slot.
@@ -62,7 +62,7 @@ struct FfnCfg {
     static constexpr int CSPLIT = NT / CW;
     static constexpr int EPI_WARPS = 4 * CSPLIT;
     static constexpr int EPI_THREADS = 32 * EPI_WARPS;
-    static constexpr int THREADS = 64 + EPI_THREADS;
+    static constexpr int THREADS = 96 + EPI_THREADS;   // producer, two MMA issuers, epilogue
     // registers per thread for one block per SM: each of the four SM
     // sub-partitions holds 16K registers and ceil(warps / 4) of the block's
     // warps; in steps of 8, at most 255
@@ -228,7 +228,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             mbar_init(&kbrel[b], 1);
         }
         for (int b = 0; b < C::ACC_BUFS; ++b) mbar_init(&acc_empty[b], C::EPI_WARPS);
-        mbar_init(drain, 1);
+        mbar_init(drain, 2);   // one commit from each MMA issuer
         *s_abort = 0;
         fence_barrier_init();
         if (MODE != kFfnDown) {
@@ -382,65 +382,62 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             }
             if (!ok) *s_abort = 1;
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 2) {
         if (lane == 0) {
-            // ------------------------------------------------- MMA issuer
+            // ------------------------------------------------ MMA issuers
+            // Two threads (warps 1 and 2) issue the MMAs of alternate
+            // K-blocks: one thread issues small-N MMAs at barely more than
+            // half the rate two can.  Each walks every K-block to keep the
+            // stage position, and for its own ones waits for the TMEM partial
+            // to be free and the operands to land, issues the MMAs and
+            // commits (a commit covers its issuing thread's MMAs only).
             constexpr uint32_t idesc = idesc_e4m3_f32(128, NT);
-            int stage = 0, ab = 0;
-            uint32_t phase = 0, aph = 0;
+            const uint32_t mine = static_cast<uint32_t>(warp - 1);
+            int stage = 0;
             uint32_t jk = 0;   // the CTA's K-block counter
             bool ok = true;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
                 const bool gu = t < n_gu;
                 const int KB = gu ? KB_H : KB_I;
-                for (int kb = 0; kb < KB && ok; ++kb) {
-                    // TMEM partials are freed in order, so at even K-blocks one
-                    // wait for the odd buffer's last use covers both buffers
-                    if ((jk & 1u) == 0) {
-                        const uint32_t jn = jk + 1;
-                        const uint32_t bn = jn % C::ACC_BUFS;
-                        if (*s_abort || !mbar_wait(&acc_empty[bn], ((jn / C::ACC_BUFS) & 1u) ^ 1u,
-                                                   p.err, p.timeout_ns)) {
-                            ok = false;
-                            break;
-                        }
-                    }
-                    if (!mbar_wait(&kbfull[jk % kKbRing], (jk / kKbRing) & 1u, p.err, p.timeout_ns)) {
+                const int nst = gu ? 2 : 1;
+                for (int kb = 0; kb < KB && ok; ++kb, ++jk) {
+                    const int s0 = stage;
+                    stage += nst;
+                    if (stage >= p.n_stages) stage -= p.n_stages;
+                    if ((jk & 1u) != mine) continue;
+                    const uint32_t ab = jk % C::ACC_BUFS;
+                    if (*s_abort ||
+                        !mbar_wait(&acc_empty[ab], ((jk / C::ACC_BUFS) & 1u) ^ 1u, p.err,
+                                   p.timeout_ns) ||
+                        !mbar_wait(&kbfull[jk % kKbRing], (jk / kKbRing) & 1u, p.err, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t d0 = tmem + ab * C::ACC_COLS;
-                    for (int op = 0; op < (gu ? 2 : 1); ++op) {
-                        const uint32_t a0 = smem_u32(st_base + stage * C::STAGE_BYTES);
+                    int st = s0;
+                    for (int op = 0; op < nst; ++op) {
+                        const uint32_t a0 = smem_u32(st_base + st * C::STAGE_BYTES);
                         const uint32_t bb = a0 + C::B_OFF;
                         const uint32_t d = d0 + op * NT;
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
                             mma_e4m3(d, sdesc_k_sw128(a0 + 32 * k), sdesc_k_sw128(bb + 32 * k), idesc,
                                      k > 0);
-                        if (++stage == p.n_stages) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
+                        if (++st == p.n_stages) st = 0;
                     }
                     mma_commit(&kbrel[jk % kKbRing]);   // stages free + partial ready
-                    ++jk;
-                    if (++ab == C::ACC_BUFS) {
-                        ab = 0;
-                        aph ^= 1u;
-                    }
                 }
             }
             if (!ok) *s_abort = 1;
         }
     } else {
         // ----------------------------------------------------- epilogue
-        const int ew = warp - 2;
+        const int ew = warp - 3;
         const int q = warp & 3;          // TMEM lane quadrant this warp may access
         const int cg = ew >> 2;          // CW-column group
         const int m = 32 * q + lane;     // output feature inside the 128-row block
-        const int et = threadIdx.x - 64; // 0 .. EPI_THREADS-1
+        const int et = threadIdx.x - 96; // 0 .. EPI_THREADS-1
         int ab = 0;
         uint32_t je = 0;   // the CTA's K-block counter
         bool ok = true;
@@ -635,6 +632,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             }
             while (globaltimer_ns() - t0 < kDrainNs / 4) __nanosleep(1000);
         }
+        if (threadIdx.x == 64) mma_commit(drain);
         if (threadIdx.x == 32) {
             mma_commit(drain);
             mbar_wait(drain, 0, nullptr, kDrainNs);
