@@ -77,13 +77,19 @@ __device__ void union_block(const int32_t* ids, int R, int E, int K, int S, int 
     // 1. row validity: all -1 (pad), or K distinct ids in [0, E)
     for (int r = tid; r < R; r += kUnionThreads) {
         const int32_t* row = ids + size_t(r) * K;
+        int rid[MOE_MAX_TOPK];
+#pragma unroll
+        for (int k = 0; k < MOE_MAX_TOPK; ++k) rid[k] = (k < K) ? row[k] : 0;
         bool pad = true, ok = true;
-        for (int k = 0; k < K; ++k) {
-            const int e = row[k];
+#pragma unroll
+        for (int k = 0; k < MOE_MAX_TOPK; ++k) {
+            if (k >= K) break;
+            const int e = rid[k];
             if (e != -1) pad = false;
             if (e < 0 || e >= E) ok = false;
+#pragma unroll
             for (int j = 0; j < k; ++j)
-                if (row[j] == e) ok = false;
+                if (rid[j] == e) ok = false;
         }
         if (!pad && !ok) atomicExch(&s_err, MOE_ERR_INVALID_ARG);
         const bool v = !pad && ok;
@@ -100,14 +106,31 @@ __device__ void union_block(const int32_t* ids, int R, int E, int K, int S, int 
     }
     __syncthreads();
 
-    // 3. per-expert counts and per-word prefix counts
-    for (int e = tid; e < E; e += kUnionThreads) {
-        int c = 0;
-        for (int w = 0; w < W; ++w) {
-            wpre[size_t(e) * W + w] = static_cast<uint16_t>(c);
-            c += __popc(bm[size_t(e) * W + w]);
+    // 3. per-expert counts and per-word prefix counts: one warp per expert,
+    //    lane l taking a contiguous run of the expert's words (a thread per
+    //    expert would put a whole warp on one shared-memory bank: experts are
+    //    W words apart), then an exclusive scan over the lanes
+    {
+        const int warp = tid >> 5, lane = tid & 31;
+        const int per = (W + 31) / 32;
+        const int w0 = min(W, lane * per), w1 = min(W, w0 + per);
+        for (int e = warp; e < E; e += kUnionThreads / 32) {
+            const uint32_t* bme = bm + size_t(e) * W;
+            int c = 0;
+            for (int w = w0; w < w1; ++w) c += __popc(bme[w]);
+            int incl = c;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+                if (lane >= d) incl += o;
+            }
+            int run = incl - c;
+            for (int w = w0; w < w1; ++w) {
+                wpre[size_t(e) * W + w] = static_cast<uint16_t>(run);
+                run += __popc(bme[w]);
+            }
+            if (lane == 31) s_cnt[e] = incl;
         }
-        s_cnt[e] = c;
     }
     if (tid == 0) s_cnt[E] = S ? s_nvalid : 0;
     __syncthreads();
