@@ -45,7 +45,7 @@
 
 namespace moe {
 
-constexpr int kIssuers = 3;   // MMA-issuing threads (warps 1 .. kIssuers), K-blocks in turn
+constexpr int kIssuers = 2;   // MMA-issuing threads (warps 1 .. kIssuers), K-blocks in turn
 
 template <int NT, int MODE>
 struct FfnCfg {
