@@ -45,11 +45,10 @@ METRIC = ("MoE-layer rows/s and achieved HBM GB/s (% of 8 TB/s) at 8-row verify;
 PHASES = ["router", "union", "dispatch", "ffn", "combine"]
 
 
-def kernels_per_step(R: int, n_shared: int) -> int:
-    """Kernels of one moe_layer call: the shared expert's L2 prefetch (when
-    there is a shared expert), router logits, selection + union (one kernel up
-    to 64 rows, two above), dispatch, expert GEMMs, combine."""
-    return (5 if R <= 64 else 6) + (1 if n_shared > 0 else 0)
+def kernels_per_step(R: int) -> int:
+    """Kernels of one moe_layer call: router logits, selection + union (one
+    kernel up to 64 rows, two above), dispatch, expert GEMMs, combine."""
+    return 5 if R <= 64 else 6
 # DRAM bytes (read + write) of the expert GEMM per algorithmic byte, for the
 # 16-row tile of calls of up to 64 rows: ncu on the same kernel at 8 rows on 32
 # experts of the same shape (dram__bytes_read.sum + dram__bytes_write.sum =
@@ -593,7 +592,7 @@ def main() -> None:
                     "d2h_bytes_per_step": out_host.numel() * 2,
                     "note": "moe_layer, pinned host x -> device -> pinned host out, per step",
                     "bit_identical_to_step_path": e2e_same},
-            "gpu_launches": kernels_per_step(R, wl.shape.n_shared) * args.steps,
+            "gpu_launches": kernels_per_step(R) * args.steps,
             "clocks": clocks,
             "also": extra,
         }

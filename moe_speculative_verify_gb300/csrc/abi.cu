@@ -526,14 +526,6 @@ static moe_status_t layer_impl(const moe_config_t* cfg, const void* x_bf16,
     int32_t* ub = reinterpret_cast<int32_t*>(base + L.ubuf);
     float* y_slots = reinterpret_cast<float*>(base + L.y_slots);
     float* y_shared = reinterpret_cast<float*>(base + L.y_shared);
-    if (cfg->n_shared > 0) {
-        // the shared expert's weights into L2 while the routing runs
-        const DeviceInfo dev = device_info();
-        const size_t per = size_t(cfg->n_shared) * cfg->inter * cfg->hidden;
-        if ((st = cuda_status(moe::launch_prefetch_l2(w->sh_gate, per, w->sh_up, per, w->sh_down,
-                                                      per, dev.sms, s))) != MOE_OK)
-            return st;
-    }
     if (R <= moe::kRouteUnionMaxRows) {
         // logits, then selection and union in one block
         if ((st = cuda_status(moe::launch_router_logits(static_cast<const uint16_t*>(x_bf16),

@@ -84,10 +84,6 @@ cudaError_t launch_route_union(const float* logits, const float* bias, const uin
                                int R, int E, int G, int TG, int K, float scaling, int32_t* ids,
                                float* wts, int S, int n_tile, int32_t* ub, const UnionLayout& L,
                                cudaStream_t stream);
-// Bulk L2 prefetch of up to three device ranges (16-byte aligned, sizes
-// multiples of 16), spread over n_sms blocks.
-cudaError_t launch_prefetch_l2(const void* a, size_t na, const void* b, size_t nb, const void* c,
-                               size_t nc, int n_sms, cudaStream_t stream);
 cudaError_t launch_dispatch(const uint16_t* x, const int32_t* ub, const UnionLayout& L, int R,
                             int H, int KS, uint8_t* xg, float* xs, int32_t* ready, int n_ready,
                             cudaStream_t stream);

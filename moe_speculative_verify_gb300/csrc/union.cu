@@ -325,52 +325,4 @@ cudaError_t launch_route_union(const float* logits, const float* bias, const uin
     return cudaGetLastError();
 }
 
-// Shared-expert weights into L2 ahead of the expert GEMM.  The shared expert
-// does not depend on the routing, and the GEMM processes its tiles first, so
-// its weights are requested while the routing kernels run (HBM is nearly idle
-// then): bulk L2 prefetches of kPrefetchChunk bytes, spread over the grid.
-constexpr uint32_t kPrefetchChunk = 64 * 1024;
-
-__global__ void __launch_bounds__(128) prefetch_l2_kernel(const uint8_t* __restrict__ a, size_t na,
-                                                          const uint8_t* __restrict__ b, size_t nb,
-                                                          const uint8_t* __restrict__ c, size_t nc) {
-    pdl_wait();
-    pdl_launch_dependents();
-    const size_t ca = (na + kPrefetchChunk - 1) / kPrefetchChunk;
-    const size_t cb = (nb + kPrefetchChunk - 1) / kPrefetchChunk;
-    const size_t cc = (nc + kPrefetchChunk - 1) / kPrefetchChunk;
-    const size_t total = ca + cb + cc;
-    for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-         i += size_t(gridDim.x) * blockDim.x) {
-        const uint8_t* base;
-        size_t n, k = i;
-        if (k < ca) {
-            base = a;
-            n = na;
-        } else if ((k -= ca) < cb) {
-            base = b;
-            n = nb;
-        } else {
-            k -= cb;
-            base = c;
-            n = nc;
-        }
-        const size_t off = k * kPrefetchChunk;
-        const uint32_t len = static_cast<uint32_t>(min(size_t(kPrefetchChunk), n - off));
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + off), "r"(len)
-                     : "memory");
-    }
-}
-
-cudaError_t launch_prefetch_l2(const void* a, size_t na, const void* b, size_t nb, const void* c,
-                               size_t nc, int n_sms, cudaStream_t stream) {
-    // sizes are whole 16-byte multiples from 16-byte aligned bases (the
-    // boundary checks of the weights guarantee both)
-    cudaError_t e = launch_pdl(prefetch_l2_kernel, dim3(max(1, n_sms)), dim3(128), 0, stream,
-                               static_cast<const uint8_t*>(a), na, static_cast<const uint8_t*>(b),
-                               nb, static_cast<const uint8_t*>(c), nc);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
-}
-
 }  // namespace moe
