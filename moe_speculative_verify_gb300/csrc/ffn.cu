@@ -28,11 +28,11 @@
 // Warp roles (one CTA per SM):
 //   warp 0 lane 0: TMA producer -- weight tiles (evict-first) and row tiles
 //                  into an n_stages ring of shared-memory stages;
-//   warps 1..kIssuers lane 0: MMA issuers, K-blocks in turn -- 4 x tcgen05.mma
+//   warps 1, 2 lane 0: MMA issuers, alternate K-blocks -- 4 x tcgen05.mma
 //                  (K = 32) per operand per K-block into a ring of ACC_BUFS
 //                  tensor-memory partials, then one tcgen05.commit per K-block
 //                  that frees its stages and hands its partial to the epilogue;
-//   later warps: epilogue -- 4 * NT/CW warps; warp w reads TMEM lanes
+//   warps 3.. : epilogue -- 4 * NT/CW warps; warp w reads TMEM lanes
 //                  32*(w%4).. and CW columns (16, or 8 at 32-row tiles),
 //                  promotes the partials, then
 //                  gate/up: h = silu(g) * u, per-row 1x128 e4m3 quantisation
@@ -44,8 +44,6 @@
 #include "layout.h"
 
 namespace moe {
-
-constexpr int kIssuers = 2;   // MMA-issuing threads (warps 1 .. kIssuers), K-blocks in turn
 
 template <int NT, int MODE>
 struct FfnCfg {
@@ -64,7 +62,7 @@ struct FfnCfg {
     static constexpr int CSPLIT = NT / CW;
     static constexpr int EPI_WARPS = 4 * CSPLIT;
     static constexpr int EPI_THREADS = 32 * EPI_WARPS;
-    static constexpr int THREADS = 32 * (1 + kIssuers) + EPI_THREADS;   // producer, MMA issuers, epilogue
+    static constexpr int THREADS = 96 + EPI_THREADS;   // producer, two MMA issuers, epilogue
     // registers per thread for one block per SM: each of the four SM
     // sub-partitions holds 16K registers and ceil(warps / 4) of the block's
     // warps; in steps of 8, at most 255
@@ -230,7 +228,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             mbar_init(&kbrel[b], 1);
         }
         for (int b = 0; b < C::ACC_BUFS; ++b) mbar_init(&acc_empty[b], C::EPI_WARPS);
-        mbar_init(drain, kIssuers);   // one commit from each MMA issuer
+        mbar_init(drain, 2);   // one commit from each MMA issuer
         *s_abort = 0;
         fence_barrier_init();
         if (MODE != kFfnDown) {
@@ -384,12 +382,12 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             }
             if (!ok) *s_abort = 1;
         }
-    } else if (warp <= kIssuers) {
+    } else if (warp == 1 || warp == 2) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuers
-            // kIssuers threads (warps 1 ..) issue the MMAs of the K-blocks in
-            // turn: one thread issues small-N MMAs at barely more than half
-            // the rate two can.  Each walks every K-block to keep the
+            // Two threads (warps 1 and 2) issue the MMAs of alternate
+            // K-blocks: one thread issues small-N MMAs at barely more than
+            // half the rate two can.  Each walks every K-block to keep the
             // stage position, and for its own ones waits for the TMEM partial
             // to be free and the operands to land, issues the MMAs and
             // commits (a commit covers its issuing thread's MMAs only).
@@ -406,7 +404,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                     const int s0 = stage;
                     stage += nst;
                     if (stage >= p.n_stages) stage -= p.n_stages;
-                    if (jk % kIssuers != mine) continue;
+                    if ((jk & 1u) != mine) continue;
                     const uint32_t ab = jk % C::ACC_BUFS;
                     if (*s_abort ||
                         !mbar_wait(&acc_empty[ab], ((jk / C::ACC_BUFS) & 1u) ^ 1u, p.err,
@@ -435,11 +433,11 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
         }
     } else {
         // ----------------------------------------------------- epilogue
-        const int ew = warp - (1 + kIssuers);
+        const int ew = warp - 3;
         const int q = warp & 3;          // TMEM lane quadrant this warp may access
         const int cg = ew >> 2;          // CW-column group
         const int m = 32 * q + lane;     // output feature inside the 128-row block
-        const int et = threadIdx.x - 32 * (1 + kIssuers); // 0 .. EPI_THREADS-1
+        const int et = threadIdx.x - 96; // 0 .. EPI_THREADS-1
         int ab = 0;
         uint32_t je = 0;   // the CTA's K-block counter
         bool ok = true;
@@ -634,7 +632,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             }
             while (globaltimer_ns() - t0 < kDrainNs / 4) __nanosleep(1000);
         }
-        if (warp >= 2 && warp <= kIssuers && lane == 0) mma_commit(drain);
+        if (threadIdx.x == 64) mma_commit(drain);
         if (threadIdx.x == 32) {
             mma_commit(drain);
             mbar_wait(drain, 0, nullptr, kDrainNs);
