@@ -103,7 +103,21 @@ typedef struct {
  *   sh_*         : the shared expert, same layouts with S in place of E
  *                  (ignored when n_shared == 0).
  * Device memory, read only; 16-byte aligned codes, 4-byte aligned scales.
+ *
+ * layout says how the codes of each [rows, cols] matrix lie in memory (the
+ * scales are always as above):
+ *   MOE_LAYOUT_ROW_MAJOR (0): row-major, cols contiguous, as listed above;
+ *   MOE_LAYOUT_TILED (1): the 128x128 blocks that the scales cover, each
+ *     stored as 16 KB of its own (its 128 rows of 128 codes one after the
+ *     other), blocks in row-block-major order: block (rb, kb) of matrix n at
+ *     byte ((n * rows/128 + rb) * cols/128 + kb) * 16384.  The expert GEMMs
+ *     stream every block once, along K, so this layout turns each of their
+ *     weight streams into sequential 16 KB reads.  moe_tile_weights converts.
+ * A zero-initialised layout field selects the row-major layout.
  */
+#define MOE_LAYOUT_ROW_MAJOR 0
+#define MOE_LAYOUT_TILED 1
+
 typedef struct {
     const uint8_t* w_gate;
     const uint8_t* w_up;
@@ -117,6 +131,7 @@ typedef struct {
     const float* sh_s_gate;
     const float* sh_s_up;
     const float* sh_s_down;
+    int32_t layout;   /* MOE_LAYOUT_ROW_MAJOR or MOE_LAYOUT_TILED (all six code tensors) */
 } moe_weights_t;
 
 /*
@@ -348,6 +363,24 @@ moe_status_t moe_layer_noalloc(const moe_config_t* cfg, const void* x_bf16,
                                const uint8_t* row_valid, int32_t R, void* out_bf16,
                                int32_t* topk_ids_out, float* topk_w_out, int32_t* device_status,
                                moe_stream_t stream);
+
+/*
+ * moe_tile_weights -- copy n row-major e4m3 matrices [rows, cols] into the
+ * MOE_LAYOUT_TILED layout (see moe_weights_t): a pure permutation of bytes,
+ * done once when the weights are loaded.  For a set of expert weights call it
+ * once per code tensor: w_gate and w_up with (E, I, H), w_down with (E, H, I),
+ * and the shared expert's with S in place of E.  The layout is this library's
+ * (for its HBM streams); the block-scaled e4m3 format itself is unchanged.
+ *
+ *   src  uint8 [n, rows, cols] device, 16-byte aligned (read only)
+ *   dst  uint8, n*rows*cols bytes, device, 16-byte aligned, not overlapping src
+ *   rows, cols  multiples of 128 (1 .. 16384 / 128 blocks each); n >= 0
+ *
+ * Asynchronous on stream.  MOE_ERR_INVALID_ARG: NULL or misaligned pointer,
+ * overlap, n < 0, rows or cols not a positive multiple of 128 or above 16384.
+ */
+moe_status_t moe_tile_weights(const uint8_t* src, uint8_t* dst, int64_t n, int32_t rows,
+                              int32_t cols, moe_stream_t stream);
 
 /*
  * moe_greedy_verify -- greedy verify and acceptance of speculative spans on

@@ -24,7 +24,12 @@ __all__ = [
     "moe_down_fp8", "ffn_layout", "moe_layer_noalloc", "moe_expert_gemms_fp8",
     "moe_greedy_verify", "moe_combine_add_rmsnorm", "union_layout", "rows_per_item",
     "MOE_MAX_ROWS", "moe_expert_ffn_w8a16", "moe_layer_w8a16", "W8A16_MAX_ROWS",
+    "moe_tile_weights", "tile_weights", "LAYOUT_ROW_MAJOR", "LAYOUT_TILED",
 ]
+
+LAYOUT_ROW_MAJOR = 0
+LAYOUT_TILED = 1
+CODE_KEYS = ("w_gate", "w_up", "w_down", "sh_gate", "sh_up", "sh_down")
 
 MOE_MAX_ROWS = 4096
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
@@ -52,17 +57,20 @@ class Config(C.Structure):
 class Weights(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in (
         "w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down",
-        "sh_gate", "sh_up", "sh_down", "sh_s_gate", "sh_s_up", "sh_s_down")]
+        "sh_gate", "sh_up", "sh_down", "sh_s_gate", "sh_s_up", "sh_s_down")] + [
+        ("layout", C.c_int32)]
 
     @classmethod
-    def from_tensors(cls, t: dict) -> "Weights":
-        """From a dict with w_gate/s_gate/... and sh_gate/sh_s_gate/... tensors."""
+    def from_tensors(cls, t: dict, layout: int = LAYOUT_ROW_MAJOR) -> "Weights":
+        """From a dict with w_gate/s_gate/... and sh_gate/sh_s_gate/... tensors
+        whose code tensors are in the given layout (tile_weights makes a tiled
+        dict)."""
         def p(k):
             v = t.get(k)
             return None if v is None else v.data_ptr()
         return cls(p("w_gate"), p("w_up"), p("w_down"), p("s_gate"), p("s_up"), p("s_down"),
                    p("sh_gate"), p("sh_up"), p("sh_down"), p("sh_s_gate"), p("sh_s_up"),
-                   p("sh_s_down"))
+                   p("sh_s_down"), layout)
 
 
 _LIB: Optional[C.CDLL] = None
@@ -98,6 +106,7 @@ def load() -> C.CDLL:
     L.moe_expert_gemms_fp8.argtypes = [cfg, C.POINTER(Weights), P, I32, P, P, P, SZ, P]
     L.moe_layer.argtypes = [cfg, P, P, P, C.POINTER(Weights), P, I32, P, P, P, P, SZ, P]
     L.moe_get_device_error.argtypes = [P, I32, P]
+    L.moe_tile_weights.argtypes = [P, P, C.c_int64, I32, I32, P]
     L.moe_combine_add_rmsnorm.argtypes = [cfg, P, P, P, P, I32, P, P, C.c_float, P, P, P]
     L.moe_greedy_verify.argtypes = [P, I32, I32, I32, P, P, P, P, P, P]
     L.moe_layer_noalloc.argtypes = [cfg, P, P, P, C.POINTER(Weights), P, I32, P, P, P, P, P]
@@ -257,6 +266,33 @@ def moe_greedy_verify(logits, draft, n_draft, argmax_out, accept_len, out_tokens
     _check(load().moe_greedy_verify(_ptr(logits), 1 if logits.dtype == torch.bfloat16 else 0, V, R,
                                     _ptr(draft), _ptr(n_draft), _ptr(argmax_out), _ptr(accept_len),
                                     _ptr(out_tokens), _stream(stream)), "moe_greedy_verify")
+
+
+def moe_tile_weights(src, dst, stream=None) -> None:
+    """src: uint8 [n, rows, cols] row-major codes on the device; dst: a device
+    uint8 tensor of the same number of bytes, written in the tiled layout."""
+    n, rows, cols = src.shape
+    if dst.numel() != src.numel() or dst.dtype != torch.uint8 or src.dtype != torch.uint8:
+        raise MoeError(1, "moe_tile_weights")
+    _check(load().moe_tile_weights(_ptr(src), _ptr(dst), n, rows, cols, _stream(stream)),
+           "moe_tile_weights")
+
+
+def tile_weights(t: dict, stream=None) -> dict:
+    """A copy of the weight dict t whose six code tensors are in the tiled
+    layout (new tensors of the same shapes, bytes permuted by
+    moe_tile_weights); the scales and any other entries are shared with t.
+    Pass the result to Weights.from_tensors(..., layout=LAYOUT_TILED)."""
+    out = dict(t)
+    for k in CODE_KEYS:
+        v = t.get(k)
+        if v is None:
+            continue
+        src = v.view(torch.uint8).contiguous()
+        dst = torch.empty_like(src)
+        moe_tile_weights(src, dst, stream)
+        out[k] = dst.view(v.dtype)
+    return out
 
 
 def moe_get_device_error(ws, clear: bool = True, stream=None) -> int:

@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libmoe_verify.so")
 SOURCES = ["abi.cu", "router.cu", "union.cu", "ffn.cu", "ffn16.cu", "combine.cu", "noalloc.cu",
-           "verify.cu"]
+           "verify.cu", "tile.cu"]
 HEADERS = ["common.cuh", "kernels.h", "layout.h", "select.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -100,6 +100,8 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, ui
 
 moe_status_t check_weights(const moe_config_t* c, const moe_weights_t* w) {
     if (w == nullptr) return MOE_ERR_INVALID_ARG;
+    if (w->layout != MOE_LAYOUT_ROW_MAJOR && w->layout != MOE_LAYOUT_TILED)
+        return MOE_ERR_INVALID_ARG;
     const void* codes[3] = {w->w_gate, w->w_up, w->w_down};
     const float* scales[3] = {w->s_gate, w->s_up, w->s_down};
     for (int i = 0; i < 3; ++i) {
@@ -174,18 +176,28 @@ bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Weight codes of matrices stacked to [rows, cols] (rows = matrices x their
+// rows): 128x128 boxes, in either layout.  A tiled tensor is a column of
+// 16 KB blocks, so its map is [rows * cols/128, 128]: block (rb, kb) of the
+// stack is the box at row (rb * cols/128 + kb) * 128.
+bool make_wmap(CUtensorMap* m, const void* base, int layout, uint64_t rows, uint64_t cols) {
+    return layout == MOE_LAYOUT_TILED ? make_map(m, base, rows * (cols / 128), 128, 128)
+                                      : make_map(m, base, rows, cols, 128);
+}
+
 // The eight tensor maps of the expert GEMMs.  Shared-expert maps fall back to
 // the routed tensors when there is no shared expert (never read then).
 bool make_maps(const moe_config_t* c, const moe_weights_t* w, const FfnCall& f, moe::FfnMaps* mp) {
     const int H = c->hidden, I = c->inter, E = c->n_experts, S = c->n_shared;
     const uint64_t srows = S ? uint64_t(S) : 1ull;
-    return make_map(&mp->g, w->w_gate, uint64_t(E) * I, H, 128) &&
-           make_map(&mp->u, w->w_up, uint64_t(E) * I, H, 128) &&
-           make_map(&mp->sg, S ? w->sh_gate : w->w_gate, srows * I, H, 128) &&
-           make_map(&mp->su, S ? w->sh_up : w->w_up, srows * I, H, 128) &&
+    const int lo = w->layout;
+    return make_wmap(&mp->g, w->w_gate, lo, uint64_t(E) * I, H) &&
+           make_wmap(&mp->u, w->w_up, lo, uint64_t(E) * I, H) &&
+           make_wmap(&mp->sg, S ? w->sh_gate : w->w_gate, lo, srows * I, H) &&
+           make_wmap(&mp->su, S ? w->sh_up : w->w_up, lo, srows * I, H) &&
            make_map(&mp->x, f.xg, f.FL.rows, H, f.nt) &&
-           make_map(&mp->d, w->w_down, uint64_t(E) * H, I, 128) &&
-           make_map(&mp->sd, S ? w->sh_down : w->w_down, srows * H, I, 128) &&
+           make_wmap(&mp->d, w->w_down, lo, uint64_t(E) * H, I) &&
+           make_wmap(&mp->sd, S ? w->sh_down : w->w_down, lo, srows * H, I) &&
            make_map(&mp->h, f.hq, f.FL.rows, I, f.nt);
 }
 
@@ -213,6 +225,7 @@ moe::FfnArgs ffn_args(const moe_config_t* c, const moe_weights_t* w, const int32
     a.E = c->n_experts;
     a.K = c->topk;
     a.KS = c->topk + S;
+    a.tiled = w->layout == MOE_LAYOUT_TILED;
     a.timeout_ns = timeout_ns(c);
     return a;
 }
@@ -263,13 +276,14 @@ moe_status_t ffn16_impl(const moe_config_t* c, const void* x, const moe_weights_
     if (dev.sms <= 0) return MOE_ERR_CUDA;
     moe::FfnMaps mp;
     const uint64_t srows = S ? uint64_t(S) : 1ull;
-    if (!(make_map(&mp.g, w->w_gate, uint64_t(E) * I, H, 128) &&
-          make_map(&mp.u, w->w_up, uint64_t(E) * I, H, 128) &&
-          make_map(&mp.sg, S ? w->sh_gate : w->w_gate, srows * I, H, 128) &&
-          make_map(&mp.su, S ? w->sh_up : w->w_up, srows * I, H, 128) &&
+    const int lo = w->layout;
+    if (!(make_wmap(&mp.g, w->w_gate, lo, uint64_t(E) * I, H) &&
+          make_wmap(&mp.u, w->w_up, lo, uint64_t(E) * I, H) &&
+          make_wmap(&mp.sg, S ? w->sh_gate : w->w_gate, lo, srows * I, H) &&
+          make_wmap(&mp.su, S ? w->sh_up : w->w_up, lo, srows * I, H) &&
           make_map_bf16(&mp.x, xb, f.FL.rows, H, moe::kW8A16RowsPerItem) &&
-          make_map(&mp.d, w->w_down, uint64_t(E) * H, I, 128) &&
-          make_map(&mp.sd, S ? w->sh_down : w->w_down, srows * H, I, 128) &&
+          make_wmap(&mp.d, w->w_down, lo, uint64_t(E) * H, I) &&
+          make_wmap(&mp.sd, S ? w->sh_down : w->w_down, lo, srows * H, I) &&
           make_map_bf16(&mp.h, hb, f.FL.rows, I, moe::kW8A16RowsPerItem)))
         return MOE_ERR_CUDA;
     moe::Ffn16Args a{};
@@ -291,6 +305,7 @@ moe_status_t ffn16_impl(const moe_config_t* c, const void* x, const moe_weights_
     a.E = E;
     a.K = c->topk;
     a.KS = c->topk + S;
+    a.tiled = w->layout == MOE_LAYOUT_TILED;
     a.timeout_ns = timeout_ns(c);
     return cuda_status(moe::launch_ffn16(mp, a, dev.sms, dev.smem_optin, s));
 }
@@ -579,6 +594,20 @@ moe_status_t moe_greedy_verify(const void* logits, int32_t logits_bf16, int32_t 
     return cuda_status(moe::launch_greedy_verify(logits, logits_bf16 != 0, V, R, draft, n_draft,
                                                  argmax_out, accept_len, out_tokens,
                                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_tile_weights(const uint8_t* src, uint8_t* dst, int64_t n, int32_t rows,
+                              int32_t cols, moe_stream_t stream) {
+    if (n < 0 || rows <= 0 || cols <= 0 || rows % 128 || cols % 128 || rows > 16384 ||
+        cols > 16384)
+        return MOE_ERR_INVALID_ARG;
+    if (n == 0) return MOE_OK;
+    if (!src || !dst || !aligned(src, 16) || !aligned(dst, 16)) return MOE_ERR_INVALID_ARG;
+    const uintptr_t bytes = uintptr_t(n) * uintptr_t(rows) * uintptr_t(cols);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(src), b = reinterpret_cast<uintptr_t>(dst);
+    if (a < b + bytes && b < a + bytes) return MOE_ERR_INVALID_ARG;
+    return cuda_status(moe::launch_tile_weights(src, dst, n, rows, cols,
+                                                reinterpret_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_get_device_error(void* ws, int32_t clear, moe_stream_t stream) {

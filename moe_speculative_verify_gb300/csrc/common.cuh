@@ -110,6 +110,14 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
         : "memory");
 }
 
+// Box coordinates (x, y) of the 128x128 weight block at K-block kb of the
+// 128-row block that starts at row `row` of a stack of code matrices with kbn
+// K-blocks per row: row-major (x = kb * 128, y = row), or tiled, where the
+// stack is a column of 16 KB blocks in row-block-major order.
+__device__ __forceinline__ int2 wbox(int tiled, int row, int kb, int kbn) {
+    return tiled ? make_int2(0, ((row >> 7) * kbn + kb) << 7) : make_int2(kb << 7, row);
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));

@@ -280,10 +280,11 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                     mbar_arrive_expect_tx(bar, (tl.gu ? 2 : 1) * C::STAGE_BYTES);
                 if (tl.gu) {
                     const CUtensorMap* m = (j & 1) ? (sh ? &map_su : &map_u) : (sh ? &map_sg : &map_g);
-                    tma_load_2d_hint(st, m, bar, (j >> 1) * kBlock, ex * p.I + tl.blk * kBlock, pol);
+                    const int2 c = wbox(p.tiled, ex * p.I + tl.blk * kBlock, j >> 1, p.H / kBlock);
+                    tma_load_2d_hint(st, m, bar, c.x, c.y, pol);
                 } else {
-                    tma_load_2d_hint(st, sh ? &map_sd : &map_d, bar, j * kBlock,
-                                     ex * p.H + tl.blk * kBlock, pol);
+                    const int2 c = wbox(p.tiled, ex * p.H + tl.blk * kBlock, j, p.I / kBlock);
+                    tma_load_2d_hint(st, sh ? &map_sd : &map_d, bar, c.x, c.y, pol);
                 }
             };
             auto b_load = [&](const Tile& tl, const int4& it, int j, int s, uint32_t kbj) {

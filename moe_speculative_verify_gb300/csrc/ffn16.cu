@@ -276,11 +276,13 @@ __global__ void __launch_bounds__(kThreads16, 1)
                     uint8_t* dst = wst + ws * kWBytes;
                     if (tl.gu) {
                         const CUtensorMap* m = (j & 1) ? (sh ? &map_su : &map_u) : (sh ? &map_sg : &map_g);
-                        tma_load_2d_hint(dst, m, &w_full[ws], (j >> 1) * kBlock,
-                                         ex * p.I + tl.blk * kBlock, pol);
+                        const int2 c = wbox(p.tiled, ex * p.I + tl.blk * kBlock, j >> 1,
+                                            p.H / kBlock);
+                        tma_load_2d_hint(dst, m, &w_full[ws], c.x, c.y, pol);
                     } else {
-                        tma_load_2d_hint(dst, sh ? &map_sd : &map_d, &w_full[ws], j * kBlock,
-                                         ex * p.H + tl.blk * kBlock, pol);
+                        const int2 c = wbox(p.tiled, ex * p.H + tl.blk * kBlock, j,
+                                            p.I / kBlock);
+                        tma_load_2d_hint(dst, sh ? &map_sd : &map_d, &w_full[ws], c.x, c.y, pol);
                     }
                     ++issued;
                     if (++ws == NW) {

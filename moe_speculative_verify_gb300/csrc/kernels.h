@@ -40,6 +40,7 @@ struct FfnArgs {
     int H, I;
     int E, K, KS;
     int n_stages;
+    int tiled;                 // weight codes in 16 KB blocks (else row-major)
     uint64_t timeout_ns;
 };
 
@@ -61,6 +62,7 @@ struct Ffn16Args {
     int H, I;
     int E, K, KS;
     int n_wstages;
+    int tiled;                 // weight codes in 16 KB blocks (else row-major)
     uint64_t timeout_ns;
 };
 
@@ -84,6 +86,9 @@ cudaError_t launch_route_union(const float* logits, const float* bias, const uin
                                int R, int E, int G, int TG, int K, float scaling, int32_t* ids,
                                float* wts, int S, int n_tile, int32_t* ub, const UnionLayout& L,
                                cudaStream_t stream);
+// Row-major [n, rows, cols] e4m3 codes into 16 KB 128x128 blocks (tile.cu).
+cudaError_t launch_tile_weights(const uint8_t* src, uint8_t* dst, int64_t n, int rows, int cols,
+                                cudaStream_t stream);
 cudaError_t launch_dispatch(const uint16_t* x, const int32_t* ub, const UnionLayout& L, int R,
                             int H, int KS, uint8_t* xg, float* xs, int32_t* ready, int n_ready,
                             cudaStream_t stream);

@@ -21,15 +21,17 @@ def bf16_to_np(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().view(torch.int16).numpy().view(np.uint16)
 
 
-def run_layer(cfg, t, R, ws=None, out_fill=float("nan")):
+def run_layer(cfg, t, R, ws=None, out_fill=float("nan"), layout=m.LAYOUT_ROW_MAJOR):
+    """moe_layer on the dict t; with layout=LAYOUT_TILED t's code tensors must
+    already be tiled (m.tile_weights)."""
     dev = t["x"].device
     if ws is None:
         ws = torch.zeros(m.moe_workspace_bytes(cfg, R), dtype=torch.uint8, device=dev)
     out = torch.full((R, cfg.hidden), out_fill, dtype=torch.bfloat16, device=dev)
     ids = torch.empty((R, cfg.topk), dtype=torch.int32, device=dev)
     w = torch.empty((R, cfg.topk), dtype=torch.float32, device=dev)
-    m.moe_layer(cfg, t["x"], t["wr"], t["bias"], m.Weights.from_tensors(t), t.get("row_valid"),
-                out, ws, topk_ids=ids, topk_w=w)
+    m.moe_layer(cfg, t["x"], t["wr"], t["bias"], m.Weights.from_tensors(t, layout),
+                t.get("row_valid"), out, ws, topk_ids=ids, topk_w=w)
     torch.cuda.synchronize()
     err = m.moe_get_device_error(ws)
     assert err == 0, m.STATUS.get(err, err)

@@ -104,6 +104,23 @@ def test_union_and_layer_refusals(lib):
     assert lib.moe_diag_wait_timeout(FAKE, 0, None) == 1
 
 
+def test_tile_weights_refusals(lib):
+    f = lib.moe_tile_weights
+    assert f(FAKE, FAKE + 4096, 2, 256, 256, None) == 1          # overlapping
+    assert f(FAKE + 8, FAKE << 1, 1, 256, 256, None) == 1        # src not 16-byte aligned
+    assert f(FAKE, (FAKE << 1) + 4, 1, 256, 256, None) == 1      # dst not 16-byte aligned
+    assert f(FAKE, FAKE << 1, 1, 200, 256, None) == 1            # rows not a multiple of 128
+    assert f(FAKE, FAKE << 1, 1, 256, 16384 + 128, None) == 1    # cols above 16384
+    assert f(FAKE, FAKE << 1, -1, 256, 256, None) == 1
+    assert f(None, FAKE << 1, 1, 256, 256, None) == 1
+    assert f(FAKE, FAKE << 1, 0, 256, 256, None) == 0            # nothing to do
+    cfg = _cfg()
+    wsb = m.moe_workspace_bytes(cfg, 8)
+    bad = m.Weights(*([FAKE] * 12), 2)                           # unknown layout
+    assert lib.moe_layer(C.byref(cfg), FAKE, FAKE, FAKE, C.byref(bad), None, 8, FAKE, None, None,
+                         FAKE, wsb, None) == 1
+
+
 def test_sizes(lib):
     cfg = _cfg()
     for R in (1, 8, 64, 512, 4096):
