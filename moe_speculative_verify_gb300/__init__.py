@@ -340,8 +340,9 @@ def ffn_layout(cfg: Config, R: int) -> dict:
     H, I, E, K, S = cfg.hidden, cfg.inter, cfg.n_experts, cfg.topk, cfg.n_shared
     rows = up(R * (K + S), 64) + 64
     n_ready = R * (K + S) // 16 + min(E, R * K) + S + 1
-    out = {"rows": rows, "ctl": 0, "ready": 256, "n_ready": n_ready}
-    b = up(256 + n_ready * 4, 256)
+    out = {"rows": rows, "ctl": 0, "ready": 256, "n_ready": n_ready,
+           "sched": 256 + n_ready * 4}
+    b = up(256 + (n_ready + 2) * 4, 256)     # per-item counters, then 2 scheduler words
     out["xg"] = b
     b = up(b + rows * H, 256)
     out["xs"] = b

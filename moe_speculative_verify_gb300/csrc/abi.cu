@@ -139,6 +139,7 @@ struct FfnCall {
     UnionLayout UL;
     int32_t* err;
     int32_t* ready;
+    int32_t* sched;
     uint8_t* xg;
     float* xs;
     uint8_t* hq;
@@ -153,6 +154,7 @@ FfnCall ffn_call(const moe_config_t* c, int32_t R, void* ws) {
     uint8_t* base = static_cast<uint8_t*>(ws);
     f.err = reinterpret_cast<int32_t*>(base + f.FL.ctl);
     f.ready = reinterpret_cast<int32_t*>(base + f.FL.ready);
+    f.sched = reinterpret_cast<int32_t*>(base + f.FL.sched);
     f.xg = base + f.FL.xg;
     f.xs = reinterpret_cast<float*>(base + f.FL.xs);
     f.hq = base + f.FL.hq;
@@ -219,6 +221,7 @@ moe::FfnArgs ffn_args(const moe_config_t* c, const moe_weights_t* w, const int32
     a.y_slots = y_slots;
     a.y_shared = y_shared;
     a.ready = f.ready;
+    a.sched = f.sched;
     a.err = f.err;
     a.H = c->hidden;
     a.I = c->inter;
@@ -235,7 +238,7 @@ moe_status_t dispatch_impl(const moe_config_t* c, const void* x, const int32_t* 
     const FfnCall f = ffn_call(c, R, ws);
     return cuda_status(moe::launch_dispatch(static_cast<const uint16_t*>(x), ub, f.UL, R, c->hidden,
                                             c->topk + c->n_shared, f.xg, f.xs, f.ready,
-                                            f.FL.n_ready, s));
+                                            f.FL.n_ready + moe::kSchedWords, s));
 }
 
 // One of the three expert-GEMM modes (gate/up, down, or both fused).
@@ -270,7 +273,7 @@ moe_status_t ffn16_impl(const moe_config_t* c, const void* x, const moe_weights_
     const int H = c->hidden, I = c->inter, E = c->n_experts, S = c->n_shared;
     moe_status_t st = cuda_status(moe::launch_dispatch16(static_cast<const uint16_t*>(x), ub, f.UL,
                                                          R, H, c->topk + S, xb, f.ready,
-                                                         f.FL.n_ready, s));
+                                                         f.FL.n_ready + moe::kSchedWords, s));
     if (st != MOE_OK) return st;
     const DeviceInfo dev = device_info();
     if (dev.sms <= 0) return MOE_ERR_CUDA;

@@ -96,9 +96,27 @@ constexpr int kMaxStages = 16;
 // kMaxStages, resp. 16 K-blocks), so a parity wait never aliases.
 constexpr int kKbRing = 32;
 
+// Tiles are handed out at run time: a CTA's first tile is its block index,
+// every further one comes from a global counter (claimed by the producer one
+// tile ahead), so CTAs that finish early take more of the small down tiles and
+// all end within about one tile of each other.  The producer writes the CTA's
+// k-th tile into entry k % kTq of a shared-memory queue and completes
+// tq_full[k % kTq]; the MMA issuers and the epilogue read the entries in
+// order.  No role trails the producer by more than kMaxStages + 16 tiles
+// (every tile has at least one stage and one K-block), so an entry is read
+// before it is rewritten.
+constexpr int kTq = 64;
+
+struct TileEntry {
+    int t;               // tile index (>= the tile count: no more tiles)
+    int item, blk;       // the Tile fields
+    int flags;           // 1: gate/up tile, 2: shared weight tile
+    int4 it;             // the item record
+};
+
 // Shared-memory carve-up, identical on host (size) and device (pointers).
 struct FfnSmem {
-    int stages, sc, red, tile, src, bars, tmem, flag, bytes;
+    int stages, sc, red, tile, src, tq, bars, tmem, flag, bytes;
 };
 
 __host__ __device__ inline FfnSmem ffn_smem(int nt, int n_stages, int kbmax, int stage_bytes) {
@@ -114,9 +132,11 @@ __host__ __device__ inline FfnSmem ffn_smem(int nt, int n_stages, int kbmax, int
     b += nt * 128;
     s.src = b;
     b += nt * 4;
-    b = (b + 7) & ~7;
+    b = (b + 15) & ~15;
+    s.tq = b;
+    b += kTq * static_cast<int>(sizeof(TileEntry));
     s.bars = b;
-    b += (2 * kKbRing + 16 + 1) * 8;
+    b += (2 * kKbRing + 16 + 1 + kTq) * 8;
     s.tmem = b;
     b += 4;
     s.flag = b;
@@ -212,6 +232,8 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
     uint64_t* kbrel = kbfull + kKbRing;        // [kKbRing] K-block done (stages free, partial ready)
     uint64_t* acc_empty = kbrel + kKbRing;     // [16] epilogue done with a TMEM partial
     uint64_t* drain = acc_empty + 16;
+    uint64_t* tq_full = drain + 1;             // [kTq] tile-queue entry written
+    TileEntry* tq = reinterpret_cast<TileEntry*>(smem + L.tq);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L.tmem);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L.flag);
 
@@ -229,6 +251,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
         }
         for (int b = 0; b < C::ACC_BUFS; ++b) mbar_init(&acc_empty[b], C::EPI_WARPS);
         mbar_init(drain, 2);   // one commit from each MMA issuer
+        for (int b = 0; b < kTq; ++b) mbar_init(&tq_full[b], 1);
         *s_abort = 0;
         fence_barrier_init();
         if (MODE != kFfnDown) {
@@ -303,6 +326,15 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                 return jj == ~0u ||
                        mbar_wait(&kbrel[jj % kKbRing], (jj / kKbRing) & 1u, p.err, p.timeout_ns);
             };
+            auto publish = [&](uint32_t k, int t, const Tile& tl, const int4& it) {
+                TileEntry& en = tq[k % kTq];
+                en.t = t;
+                en.item = tl.item;
+                en.blk = tl.blk;
+                en.flags = (tl.gu ? 1 : 0) | (tl.shared_w ? 2 : 0);
+                en.it = it;
+                mbar_arrive(&tq_full[k % kTq]);
+            };
             uint32_t kb_base = 0;   // K-blocks of the CTA's earlier tiles
             // Weights are inputs of the layer, not outputs of the previous
             // kernel: the first tile's first weight tiles are requested before
@@ -320,6 +352,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                     a_load(tl0, it0, j, j, used_by[j]);
                 }
             }
+            publish(0, t0, tl0, it0);
             pdl_wait();
             pdl_launch_dependents();
             bool ok = true;
@@ -332,20 +365,22 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             issued = static_cast<uint32_t>(pre);
             stage = pre % p.n_stages;
             phase = (pre == p.n_stages) ? 1u : 0u;
-            // the next tile and its item are fetched one tile ahead
+            // the next tile is claimed, and its item fetched, one tile ahead
             Tile tl_next = tl0;
             int4 it_next = it0;
-            for (int t = t0; t < n_tiles && ok && !*s_abort; t += gridDim.x) {
+            uint32_t kq = 0;   // queue entry of the current tile
+            for (int t = t0; t < n_tiles && ok && !*s_abort; ++kq) {
                 const Tile tl = tl_next;
                 const int4 it = it_next;
-                const int tn = t + gridDim.x;
+                const int tn = atomicAdd(p.sched, 1) + static_cast<int>(gridDim.x);
                 if (tn < n_tiles) {
                     tl_next = tile_of(tn, n_gu, MB_I, MB_H, items);
                     it_next = items[tl_next.item];
                 }
+                publish(kq + 1, tn, tl_next, it_next);
                 const int NS = tl.gu ? 2 * KB_H : KB_I;
-                int j = (t == t0) ? pre : 0;
-                if (kFused && !tl.gu && t != t0) {
+                int j = (kq == 0) ? pre : 0;
+                if (kFused && !tl.gu && kq != 0) {
                     // h of this item comes from other tiles of this launch: request
                     // up to a ring of weight tiles, then wait for h, then its rows.
                     int nd = 0, dst[kMaxStages];
@@ -380,6 +415,16 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                     next_stage();
                 }
                 kb_base += static_cast<uint32_t>(tl.gu ? KB_H : KB_I);
+                t = tn;
+            }
+            // This CTA claims no more tiles; the last CTA to get here resets
+            // the counter (and this count) for the next launch on the
+            // workspace.
+            __threadfence();
+            if (atomicAdd(p.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+                __threadfence();
+                atomicExch(p.sched, 0);
+                atomicExch(p.sched + 1, 0);
             }
             if (!ok) *s_abort = 1;
         }
@@ -397,7 +442,14 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             int stage = 0;
             uint32_t jk = 0;   // the CTA's K-block counter
             bool ok = true;
-            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            for (uint32_t kq = 0; ok; ++kq) {
+                if (*s_abort ||
+                    !mbar_wait(&tq_full[kq % kTq], (kq / kTq) & 1u, p.err, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                const int t = tq[kq % kTq].t;
+                if (t >= n_tiles) break;
                 const bool gu = t < n_gu;
                 const int KB = gu ? KB_H : KB_I;
                 const int nst = gu ? 2 : 1;
@@ -443,27 +495,22 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
         uint32_t je = 0;   // the CTA's K-block counter
         bool ok = true;
         pdl_wait();   // row scales and outputs belong to the previous kernel
-        Tile tl_next{0, 0, true, false};
-        int4 it_next = make_int4(0, 0, 0, 0);
-        if (blockIdx.x < n_tiles) {
-            tl_next = tile_of(blockIdx.x, n_gu, MB_I, MB_H, items);
-            it_next = items[tl_next.item];
-        }
-        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
-            const Tile tl = tl_next;
-            const int4 it = it_next;
-            if (t + gridDim.x < n_tiles) {
-                tl_next = tile_of(t + gridDim.x, n_gu, MB_I, MB_H, items);
-                it_next = items[tl_next.item];
-            }
+        for (uint32_t kq = 0;; ++kq) {
+            // the tile's queue entry, then: the previous tile's readers are
+            // done with the scale / tile buffers
+            if (ok && !mbar_wait(&tq_full[kq % kTq], (kq / kTq) & 1u, p.err, p.timeout_ns))
+                ok = false;
+            ok = epi_bar_and(ok, C::EPI_THREADS);
+            if (!ok) break;
+            const TileEntry en = tq[kq % kTq];
+            if (en.t >= n_tiles) break;
+            const Tile tl{en.item, en.blk, (en.flags & 1) != 0, (en.flags & 2) != 0};
+            const int4 it = en.it;
             const bool sh = it.x == p.E;
             const int ex = sh ? 0 : it.x;
             const int row0 = it.y, nrow = it.z;
             const int KB = tl.gu ? KB_H : KB_I;
             const int MB = tl.gu ? MB_I : MB_H;
-            // previous tile's readers are done with the scale / tile buffers
-            ok = epi_bar_and(ok, C::EPI_THREADS);
-            if (!ok) break;
             if (kFused && !tl.gu) {
                 // h and its scales come from this launch's gate/up tiles
                 if (et == 0 && !wait_counter(p.ready + tl.item, MB_I, p.err, p.timeout_ns, s_abort))

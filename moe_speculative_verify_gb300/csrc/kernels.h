@@ -36,6 +36,7 @@ struct FfnArgs {
     float* y_slots;            // [R*K, H]
     float* y_shared;           // [R, H]
     int32_t* ready;            // [max_items] gate/up blocks of h finished (fused mode)
+    int32_t* sched;            // [2] tile counter, CTAs done claiming (zero between launches)
     int32_t* err;              // device error word
     int H, I;
     int E, K, KS;

@@ -55,8 +55,12 @@ constexpr int32_t kW8A16RowsPerItem = 16;
 // Scratch of the expert FFN stage (byte offsets from the workspace base).
 // The w8a16 variant's bf16 rows (xb) and bf16 h (hb) reuse the fp8 path's
 // region from xg on; they exist only for R <= kW8A16MaxRows (else -1).
+// Words of the expert GEMM's tile scheduler (counter, CTAs done) after the
+// per-item counters; the dispatch kernels zero both regions.
+constexpr int32_t kSchedWords = 2;
+
 struct FfnLayout {
-    int64_t ctl, ready, xg, xs, hq, hs, xb, hb, bytes;
+    int64_t ctl, ready, sched, xg, xs, hq, hs, xb, hb, bytes;
     int64_t rows;       // capacity in gathered rows
     int32_t n_ready;    // per-item counters of the fused GEMM
 };
@@ -69,7 +73,8 @@ inline FfnLayout ffn_layout(int32_t H, int32_t I, int32_t E, int32_t K, int32_t 
     L.ctl = b;
     b += 256;
     L.ready = b;
-    b = round_up(b + int64_t(L.n_ready) * 4, 256);
+    L.sched = b + int64_t(L.n_ready) * 4;   // right after ready: zeroed with it
+    b = round_up(L.sched + kSchedWords * 4, 256);
     L.xg = b;
     b = round_up(b + L.rows * H, 256);
     L.xs = b;

@@ -106,11 +106,21 @@ __device__ void union_block(const int32_t* ids, int R, int E, int K, int S, int 
     }
     __syncthreads();
 
-    // 3. per-expert counts and per-word prefix counts: one warp per expert,
+    // 3. per-expert counts and per-word prefix counts.  Up to 128 rows (a few
+    //    words per expert): a thread per expert.  More: one warp per expert,
     //    lane l taking a contiguous run of the expert's words (a thread per
     //    expert would put a whole warp on one shared-memory bank: experts are
     //    W words apart), then an exclusive scan over the lanes
-    {
+    if (W <= 4) {
+        for (int e = tid; e < E; e += kUnionThreads) {
+            int c = 0;
+            for (int w = 0; w < W; ++w) {
+                wpre[size_t(e) * W + w] = static_cast<uint16_t>(c);
+                c += __popc(bm[size_t(e) * W + w]);
+            }
+            s_cnt[e] = c;
+        }
+    } else {
         const int warp = tid >> 5, lane = tid & 31;
         const int per = (W + 31) / 32;
         const int w0 = min(W, lane * per), w1 = min(W, w0 + per);
