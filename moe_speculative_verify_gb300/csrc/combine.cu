@@ -75,7 +75,6 @@ cudaError_t launch_combine(const float* y_slots, const float* y_shared, const fl
                            const int32_t* ub, const UnionLayout& L, int R, int H, int K, int S,
                            uint16_t* out, cudaStream_t stream) {
     dim3 grid(R, (H / 4 + 255) / 256);
-    prefer_max_shared(reinterpret_cast<const void*>(combine_kernel));
     cudaError_t e = launch_pdl(combine_kernel, grid, dim3(256), 0, stream, y_slots, y_shared, wts, ub,
                                L, R, H, K, S, out);
     if (e != cudaSuccess) return e;

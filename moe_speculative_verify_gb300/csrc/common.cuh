@@ -312,13 +312,12 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) {
     return __uint_as_float(b16 << 16);
 }
 
-// Host: ask for the largest shared-memory carveout for `kernel` (once per
-// kernel and device).  An SM reconfigures its L1 / shared split only when it
-// is empty, so a kernel whose split differs from the expert GEMM's cannot
-// share SMs with it: the kernels right before and after the GEMM (dispatch,
-// combine) take the GEMM's split, so the GEMM's 200+ KB blocks join SMs where
-// dispatch blocks still run and the combine's blocks join SMs the GEMM has
-// left.  (Not for the router: its x reads want the large L1.)
+// Host: every kernel of the library asks for the largest shared-memory
+// carveout (once per kernel and device).  An SM reconfigures its L1 / shared
+// split only when it is empty, so consecutive kernels with different splits
+// cannot share an SM; with one split for all, a dependent kernel's blocks
+// (the expert GEMM's 200+ KB ones included) join SMs where the predecessor's
+// blocks still run, which is what programmatic dependent launch overlaps.
 inline void prefer_max_shared(const void* kernel) {
     static std::mutex mu;
     static std::set<std::pair<const void*, int>> done;
@@ -335,6 +334,7 @@ inline void prefer_max_shared(const void* kernel) {
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t stream, Args&&... args) {
+    prefer_max_shared(reinterpret_cast<const void*>(kernel));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -352,6 +352,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, int cluster,
                                       size_t smem, cudaStream_t stream, Args&&... args) {
+    prefer_max_shared(reinterpret_cast<const void*>(kernel));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;

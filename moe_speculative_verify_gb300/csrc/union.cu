@@ -328,7 +328,6 @@ cudaError_t launch_dispatch(const uint16_t* x, const int32_t* ub, const UnionLay
                             cudaStream_t stream) {
     const int HB = H / kBlock;
     dim3 grid(R, (HB + 7) / 8);
-    prefer_max_shared(reinterpret_cast<const void*>(dispatch_kernel));
     cudaError_t e = launch_pdl(dispatch_kernel, grid, dim3(256), 0, stream, x, ub, L, R, H, KS, xg, xs,
                                ready, n_ready);
     if (e != cudaSuccess) return e;
