@@ -9,8 +9,6 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <mutex>
-#include <set>
 #include <utility>
 
 #include "moe_verify.h"
@@ -312,29 +310,10 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) {
     return __uint_as_float(b16 << 16);
 }
 
-// Host: every kernel of the library asks for the largest shared-memory
-// carveout (once per kernel and device).  An SM reconfigures its L1 / shared
-// split only when it is empty, so consecutive kernels with different splits
-// cannot share an SM; with one split for all, a dependent kernel's blocks
-// (the expert GEMM's 200+ KB ones included) join SMs where the predecessor's
-// blocks still run, which is what programmatic dependent launch overlaps.
-inline void prefer_max_shared(const void* kernel) {
-    static std::mutex mu;
-    static std::set<std::pair<const void*, int>> done;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!done.insert({kernel, dev}).second) return;
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
-        (void)cudaGetLastError();   // a hint only: clear the error, launch as is
-}
-
 // Host: launch `kernel` on `stream` with programmatic stream serialisation.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t stream, Args&&... args) {
-    prefer_max_shared(reinterpret_cast<const void*>(kernel));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -352,7 +331,6 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, int cluster,
                                       size_t smem, cudaStream_t stream, Args&&... args) {
-    prefer_max_shared(reinterpret_cast<const void*>(kernel));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;

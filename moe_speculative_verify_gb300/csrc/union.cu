@@ -239,24 +239,16 @@ __global__ void __launch_bounds__(kUnionThreads) route_union_kernel(
     int32_t* __restrict__ ub, UnionLayout L) {
     extern __shared__ uint32_t sm[];
     float* s_b = reinterpret_cast<float*>(sm);                         // [32][E]
-    float* s_bias = s_b + 32 * E;                                      // [E]
-    uint8_t* s_rv = reinterpret_cast<uint8_t*>(s_bias + E);            // [kRouteUnionMaxRows]
-    int32_t* s_ids = reinterpret_cast<int32_t*>(s_rv + kRouteUnionMaxRows);   // [R][K]
+    int32_t* s_ids = reinterpret_cast<int32_t*>(s_b + 32 * E);         // [R][K]
     uint32_t* s_un = reinterpret_cast<uint32_t*>(s_ids + ((R * K + 3) & ~3));
-    // bias and row_valid are inputs of the layer, not outputs of the previous
-    // kernel: staged before the wait on the logits
-    for (int e = threadIdx.x; e < E; e += kUnionThreads) s_bias[e] = bias[e];
-    for (int r = threadIdx.x; r < R; r += kUnionThreads)
-        s_rv[r] = (row_valid == nullptr || row_valid[r] != 0) ? 1 : 0;
     pdl_wait();
     pdl_launch_dependents();
-    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int r = warp; r < R; r += kUnionThreads / 32) {
         int id = -1;
         float w = 0.0f;
-        if (s_rv[r])
-            select_row(logits + size_t(r) * E, s_bias, E, G, TG, K, scaling, s_b + warp * E, lane,
+        if (row_valid == nullptr || row_valid[r] != 0)
+            select_row(logits + size_t(r) * E, bias, E, G, TG, K, scaling, s_b + warp * E, lane,
                        &id, &w);
         if (lane < K) {
             s_ids[r * K + lane] = id;
@@ -276,34 +268,27 @@ __global__ void __launch_bounds__(256) dispatch_kernel(const uint16_t* __restric
                                                        uint8_t* __restrict__ xg,
                                                        float* __restrict__ xs,
                                                        int32_t* __restrict__ ready, int n_ready) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = blockIdx.x;
-    const int HB = H / kBlock;
-    const int b = blockIdx.y * 8 + warp;
-    // x is an input of the layer: read and quantised before the wait on the
-    // union, which only says where the codes go
-    const bool live = b < HB;   // warp-uniform
-    uint32_t q = 0;
-    float sc = 1.0f;
-    if (live) {
-        const uint2 xv =
-            __ldg(reinterpret_cast<const uint2*>(x + size_t(r) * H + b * kBlock + 4 * lane));
-        const float f0 = bf16_bits_to_f32(xv.x & 0xFFFFu), f1 = bf16_bits_to_f32(xv.x >> 16);
-        const float f2 = bf16_bits_to_f32(xv.y & 0xFFFFu), f3 = bf16_bits_to_f32(xv.y >> 16);
-        float amax = fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3)));
-#pragma unroll
-        for (int d = 16; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, d));
-        sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
-        q = to_e4m3x4(__fdiv_rn(f0, sc), __fdiv_rn(f1, sc), __fdiv_rn(f2, sc), __fdiv_rn(f3, sc));
-    }
     pdl_wait();
     pdl_launch_dependents();
     // the fused expert GEMM's per-item counters start at zero every call
     if (blockIdx.x == 0 && blockIdx.y == 0)
         for (int i = threadIdx.x; i < n_ready; i += blockDim.x) ready[i] = 0;
-    if (!live) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x;
+    const int HB = H / kBlock;
+    const int b = blockIdx.y * 8 + warp;
+    if (b >= HB) return;
     const int32_t* pos = ub + L.pos + size_t(r) * KS;
     if (pos[0] < 0) return;  // pad row
+    const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + size_t(r) * H + b * kBlock + 4 * lane));
+    const float f0 = bf16_bits_to_f32(xv.x & 0xFFFFu), f1 = bf16_bits_to_f32(xv.x >> 16);
+    const float f2 = bf16_bits_to_f32(xv.y & 0xFFFFu), f3 = bf16_bits_to_f32(xv.y >> 16);
+    float amax = fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3)));
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, d));
+    const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+    const uint32_t q = to_e4m3x4(__fdiv_rn(f0, sc), __fdiv_rn(f1, sc), __fdiv_rn(f2, sc),
+                                 __fdiv_rn(f3, sc));
     for (int k = 0; k < KS; ++k) {
         const int p = pos[k];
         reinterpret_cast<uint32_t*>(xg + size_t(p) * H + b * kBlock)[lane] = q;
@@ -339,8 +324,7 @@ cudaError_t launch_route_union(const float* logits, const float* bias, const uin
                                float* wts, int S, int n_tile, int32_t* ub, const UnionLayout& L,
                                cudaStream_t stream) {
     if (R > kRouteUnionMaxRows) return cudaErrorInvalidValue;
-    const size_t smem = size_t(32) * E * 4 + size_t(E) * 4 + kRouteUnionMaxRows +
-                        size_t((R * K + 3) & ~3) * 4 + union_smem_bytes(R, E);
+    const size_t smem = size_t(32) * E * 4 + size_t((R * K + 3) & ~3) * 4 + union_smem_bytes(R, E);
     cudaError_t e = cudaFuncSetAttribute(route_union_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
