@@ -58,135 +58,6 @@ __device__ __forceinline__ uint64_t rank_key(float v, int idx) {
 
 constexpr int kSelPer = MOE_MAX_EXPERTS / 32;   // experts per lane
 
-// The float an ordered key came from (key 0: no value, -inf).
-__device__ __forceinline__ float key_value(uint32_t k) {
-    if (k == 0u) return -INFINITY;
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
-__device__ __forceinline__ void cmp_swap_desc(uint64_t& a, uint64_t& b) {
-    const uint64_t hi = a > b ? a : b, lo = a > b ? b : a;
-    a = hi;
-    b = lo;
-}
-
-// Sort 8 keys descending (Batcher's odd-even merge sort, 19 comparators).
-__device__ __forceinline__ void sort8_desc(uint64_t* v) {
-    cmp_swap_desc(v[0], v[1]); cmp_swap_desc(v[2], v[3]);
-    cmp_swap_desc(v[4], v[5]); cmp_swap_desc(v[6], v[7]);
-    cmp_swap_desc(v[0], v[2]); cmp_swap_desc(v[1], v[3]);
-    cmp_swap_desc(v[4], v[6]); cmp_swap_desc(v[5], v[7]);
-    cmp_swap_desc(v[1], v[2]); cmp_swap_desc(v[5], v[6]);
-    cmp_swap_desc(v[0], v[4]); cmp_swap_desc(v[1], v[5]);
-    cmp_swap_desc(v[2], v[6]); cmp_swap_desc(v[3], v[7]);
-    cmp_swap_desc(v[2], v[4]); cmp_swap_desc(v[3], v[5]);
-    cmp_swap_desc(v[1], v[2]); cmp_swap_desc(v[3], v[4]);
-    cmp_swap_desc(v[5], v[6]);
-}
-
-// Rows whose groups are 32 experts wide (E = 32 G, as in GLM-5.2 and
-// DeepSeek-V3 layers) with K <= 8: lane l holds expert l + 32 j, the lane-l
-// member of group j, so the group scores are warp reductions, every lane
-// holds every group score, and the K experts come from one warp-wide merge of
-// sorted 8-key lists instead of K rounds of warp maxima.  The decisions are
-// those of the general path below, by construction: the same keys in the same
-// total orders (group scores: the two largest non-NaN biased scores, ties
-// counted twice; groups: score, then lower group id; experts: biased-score
-// key, then lower expert id).
-__device__ __forceinline__ void select_row_g32(const float* __restrict__ lrow,
-                                               const float* __restrict__ bias, int E, int G,
-                                               int TG, int K, float scaling, float* sb, int lane,
-                                               int* out_id, float* out_w) {
-    uint32_t vkey[kSelPer];   // biased-score key of expert lane + 32 j (0: none)
-    uint32_t gkey[kSelPer];   // the same with NaN left out (for the group scores)
-    {
-        float lg[kSelPer], bi[kSelPer];
-#pragma unroll
-        for (int j = 0; j < kSelPer; ++j) {
-            const int e = lane + 32 * j;
-            lg[j] = (j < G) ? lrow[e] : 0.0f;
-            bi[j] = (j < G) ? bias[e] : 0.0f;
-        }
-#pragma unroll
-        for (int j = 0; j < kSelPer; ++j) {
-            const float sv = router_sigmoid(lg[j]);
-            const float b = __fadd_rn(sv, bi[j]);
-            if (j < G) sb[lane + 32 * j] = sv;
-            vkey[j] = (j < G) ? ordered_key(b) : 0u;
-            gkey[j] = (j < G && b == b) ? ordered_key(b) : 0u;
-        }
-    }
-    __syncwarp();
-    // group scores (every lane gets all of them)
-    float gs[kSelPer];
-#pragma unroll
-    for (int j = 0; j < kSelPer; ++j) {
-        gs[j] = -INFINITY;
-        if (j < G) {
-            const uint32_t m1 = __reduce_max_sync(0xFFFFFFFFu, gkey[j]);
-            const int n1 = __popc(__ballot_sync(0xFFFFFFFFu, gkey[j] == m1));
-            const uint32_t m2 =
-                (n1 >= 2) ? m1 : __reduce_max_sync(0xFFFFFFFFu, gkey[j] == m1 ? 0u : gkey[j]);
-            gs[j] = __fadd_rn(key_value(m1), key_value(m2));
-        }
-    }
-    // the kept groups: rank below TG by (score, then lower id)
-    uint32_t gmask = 0u;
-#pragma unroll
-    for (int j = 0; j < kSelPer; ++j) {
-        if (j >= G) continue;
-        const uint64_t kj = rank_key(gs[j], j);
-        int rank = 0;
-#pragma unroll
-        for (int o = 0; o < kSelPer; ++o)
-            if (o < G && rank_key(gs[o], o) > kj) ++rank;
-        if (rank < TG) gmask |= 1u << j;
-    }
-    // candidates: (key, then lower id) as one 64-bit key, 0 for none
-    uint64_t c[kSelPer];
-#pragma unroll
-    for (int j = 0; j < kSelPer; ++j) {
-        const bool cand = j < G && ((gmask >> j) & 1u) && vkey[j] != 0u;
-        c[j] = cand ? ((static_cast<uint64_t>(vkey[j]) << 32) |
-                       (0xFFFFFFFFu - static_cast<uint32_t>(lane + 32 * j)))
-                    : 0ull;
-    }
-    sort8_desc(c);
-    // butterfly: each step keeps the 8 largest of the lane's and the
-    // partner's lists (a bitonic merge), so every lane ends with the warp's
-    for (int d = 1; d < 32; d <<= 1) {
-        uint64_t o[kSelPer];
-#pragma unroll
-        for (int i = 0; i < kSelPer; ++i) o[i] = __shfl_xor_sync(0xFFFFFFFFu, c[i], d);
-#pragma unroll
-        for (int i = 0; i < kSelPer; ++i) {
-            const uint64_t b = o[kSelPer - 1 - i];
-            c[i] = c[i] > b ? c[i] : b;
-        }
-        cmp_swap_desc(c[0], c[4]); cmp_swap_desc(c[1], c[5]);
-        cmp_swap_desc(c[2], c[6]); cmp_swap_desc(c[3], c[7]);
-        cmp_swap_desc(c[0], c[2]); cmp_swap_desc(c[1], c[3]);
-        cmp_swap_desc(c[4], c[6]); cmp_swap_desc(c[5], c[7]);
-        cmp_swap_desc(c[0], c[1]); cmp_swap_desc(c[2], c[3]);
-        cmp_swap_desc(c[4], c[5]); cmp_swap_desc(c[6], c[7]);
-    }
-    uint64_t mine = 0ull;
-#pragma unroll
-    for (int i = 0; i < kSelPer; ++i)
-        if (i == lane) mine = c[i];
-    int my_id = -1;
-    float my_s = 0.0f;
-    if (lane < K) {
-        my_id = (mine == 0ull) ? -1 : static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(mine));
-        my_s = (my_id >= 0) ? sb[my_id] : 0.0f;
-    }
-    float den = __shfl_sync(0xFFFFFFFFu, my_s, 0);
-    for (int k = 1; k < K; ++k) den = __fadd_rn(den, __shfl_sync(0xFFFFFFFFu, my_s, k));
-    *out_id = my_id;
-    *out_w = __fmul_rn(__fdiv_rn(my_s, den), scaling);
-    __syncwarp();   // sb may be reused for the warp's next row
-}
-
 // One warp selects the experts of one valid row.  `lrow` is the row's E
 // logits, `sb` a shared-memory scratch of E floats owned by this warp.  On
 // return lane k < K holds the k-th chosen expert (biased score descending,
@@ -202,10 +73,6 @@ __device__ __forceinline__ void select_row(const float* __restrict__ lrow,
                                            const float* __restrict__ bias, int E, int G, int TG,
                                            int K, float scaling, float* sb, int lane, int* out_id,
                                            float* out_w) {
-    if (E == 32 * G && K <= kSelPer) {
-        select_row_g32(lrow, bias, E, G, TG, K, scaling, sb, lane, out_id, out_w);
-        return;
-    }
     const int epg = E / G;
     float sv[kSelPer];
     uint32_t vkey[kSelPer];
