@@ -83,7 +83,6 @@ struct FfnCfg {
 
 constexpr int kMaxStages = 16;
 constexpr int kStagesNt16 = 8;   // ring depth at 16-row tiles (see launch_ffn_t)
-constexpr int kClaimLead = 4;    // stages before a tile's end at which the next is claimed
 // Per K-block (not per stage) synchronisation, on two rings of barriers
 // indexed by the CTA's K-block counter j:
 //   kbfull[j % kKbRing] -- the K-block's operands have landed: the producer
@@ -367,16 +366,19 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             issued = static_cast<uint32_t>(pre);
             stage = pre % p.n_stages;
             phase = (pre == p.n_stages) ? 1u : 0u;
-            // The next tile is claimed kClaimLead stages before the current
-            // tile's last stage is requested (the atomic's round trip hides
-            // behind those requests), then fetched and published once the
-            // current tile is requested in full.
+            // the next tile is claimed, and its item fetched, one tile ahead
             Tile tl_next = tl0;
             int4 it_next = it0;
             uint32_t kq = 0;   // queue entry of the current tile
             for (int t = t0; t < n_tiles && ok && !*s_abort; ++kq) {
                 const Tile tl = tl_next;
                 const int4 it = it_next;
+                const int tn = atomicAdd(p.sched, 1) + static_cast<int>(gridDim.x);
+                if (tn < n_tiles) {
+                    tl_next = tile_of(tn, n_gu, MB_I, MB_H, items);
+                    it_next = items[tl_next.item];
+                }
+                publish(kq + 1, tn, tl_next, it_next);
                 const int NS = tl.gu ? 2 * KB_H : KB_I;
                 int j = (kq == 0) ? pre : 0;
                 if (kFused && !tl.gu && kq != 0) {
@@ -402,10 +404,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                     for (int q = 0; q < nd && ok; ++q) b_load(tl, it, q, dst[q], used_by[dst[q]]);
                     j = nd;
                 }
-                const int jc = max(j, NS - kClaimLead);
-                int claim = -1;
                 for (; j < NS && ok; ++j) {
-                    if (j == jc) claim = atomicAdd(p.sched, 1);
                     if (!wait_free(stage)) {
                         ok = false;
                         break;
@@ -416,13 +415,6 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                     ++issued;
                     next_stage();
                 }
-                const int tn = (claim >= 0 ? claim : atomicAdd(p.sched, 1)) +
-                               static_cast<int>(gridDim.x);
-                if (tn < n_tiles) {
-                    tl_next = tile_of(tn, n_gu, MB_I, MB_H, items);
-                    it_next = items[tl_next.item];
-                }
-                publish(kq + 1, tn, tl_next, it_next);
                 kb_base += static_cast<uint32_t>(tl.gu ? KB_H : KB_I);
                 t = tn;
             }
