@@ -522,15 +522,40 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             }
             const float* bs = tl.gu ? p.xs : p.hs;
             const int na = tl.gu ? 2 : 1;
-            // read row-major (kb fastest: coalesced), store [operand][kb][n]
-            for (int i = et; i < na * NT * KB; i += C::EPI_THREADS) {
-                const int a = i / (NT * KB), rem = i - a * (NT * KB);
-                const int n = rem / KB, kb = rem - n * KB;
-                const float* sp = tl.gu ? ((a == 0) ? (sh ? p.sh_s_gate : p.s_gate)
-                                                    : (sh ? p.sh_s_up : p.s_up))
-                                        : (sh ? p.sh_s_down : p.s_down);
-                const float w = sp[(size_t(ex) * MB + tl.blk) * KB + kb];
-                s_sc[(a * KB + kb) * NT + n] = (n < nrow) ? w * bs[size_t(row0 + n) * KB + kb] : 0.0f;
+            // the row block's weight block scales, one per K-block (operand 0:
+            // gate or down, 1: up)
+            const size_t wrow = (size_t(ex) * MB + tl.blk) * KB;
+            const float* sw0 = (tl.gu ? (sh ? p.sh_s_gate : p.s_gate) : (sh ? p.sh_s_down : p.s_down)) + wrow;
+            const float* sw1 = (sh ? p.sh_s_up : p.s_up) + wrow;
+            // table [operand][kb][n] = weight block scale x row scale; rows are
+            // read kb fastest (coalesced), four K-blocks per 16-byte load when
+            // the rows allow it.  Row scales are read with plain loads: h's
+            // come from this launch (acquired above).
+            if ((KB & 3) == 0 &&
+                ((reinterpret_cast<uintptr_t>(sw0) | reinterpret_cast<uintptr_t>(sw1) |
+                  reinterpret_cast<uintptr_t>(bs)) & 15) == 0) {
+                const int K4 = KB >> 2;
+                for (int i = et; i < na * NT * K4; i += C::EPI_THREADS) {
+                    const int a = i / (NT * K4), rem = i - a * (NT * K4);
+                    const int n = rem / K4, k4 = rem - n * K4;
+                    const float4 w = __ldg(reinterpret_cast<const float4*>(a ? sw1 : sw0) + k4);
+                    float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    if (n < nrow) x = reinterpret_cast<const float4*>(bs + size_t(row0 + n) * KB)[k4];
+                    float* d = s_sc + (a * KB + 4 * k4) * NT + n;
+                    const bool live = n < nrow;
+                    d[0] = live ? w.x * x.x : 0.0f;
+                    d[NT] = live ? w.y * x.y : 0.0f;
+                    d[2 * NT] = live ? w.z * x.z : 0.0f;
+                    d[3 * NT] = live ? w.w * x.w : 0.0f;
+                }
+            } else {
+                for (int i = et; i < na * NT * KB; i += C::EPI_THREADS) {
+                    const int a = i / (NT * KB), rem = i - a * (NT * KB);
+                    const int n = rem / KB, kb = rem - n * KB;
+                    const float w = (a ? sw1 : sw0)[kb];
+                    s_sc[(a * KB + kb) * NT + n] =
+                        (n < nrow) ? w * bs[size_t(row0 + n) * KB + kb] : 0.0f;
+                }
             }
             if (!tl.gu)
                 for (int i = et; i < NT; i += C::EPI_THREADS)
@@ -610,7 +635,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                 for (int j = 0; j < CW; ++j) {
                     const int c = cg * CW + j;
                     const float g = acc0[j];
-                    h[j] = (c < nrow) ? (g / (1.0f + __expf(-g))) * acc1[j] : 0.0f;
+                    h[j] = (c < nrow) ? __fdividef(g, 1.0f + __expf(-g)) * acc1[j] : 0.0f;
                     float a = fabsf(h[j]);
 #pragma unroll
                     for (int d = 16; d >= 1; d >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, d));
