@@ -216,6 +216,11 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                const FfnArgs p) {
     using C = FfnCfg<NT, MODE>;
     constexpr bool kFused = (MODE == kFfnFused);
+    // Measured per tile width: the scale table from 16-byte loads is faster
+    // at 16- and 32-row tiles and slower at 64 (code generation), SiLU with
+    // the fast division faster at every width.
+    constexpr bool kVecTable = NT <= 32;
+    constexpr bool kFastSilu = true;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -531,7 +536,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             // read kb fastest (coalesced), four K-blocks per 16-byte load when
             // the rows allow it.  Row scales are read with plain loads: h's
             // come from this launch (acquired above).
-            if ((KB & 3) == 0 &&
+            if (kVecTable && (KB & 3) == 0 &&
                 ((reinterpret_cast<uintptr_t>(sw0) | reinterpret_cast<uintptr_t>(sw1) |
                   reinterpret_cast<uintptr_t>(bs)) & 15) == 0) {
                 const int K4 = KB >> 2;
@@ -635,7 +640,9 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                 for (int j = 0; j < CW; ++j) {
                     const int c = cg * CW + j;
                     const float g = acc0[j];
-                    h[j] = (c < nrow) ? __fdividef(g, 1.0f + __expf(-g)) * acc1[j] : 0.0f;
+                    const float sg = kFastSilu ? __fdividef(g, 1.0f + __expf(-g))
+                                               : g / (1.0f + __expf(-g));
+                    h[j] = (c < nrow) ? sg * acc1[j] : 0.0f;
                     float a = fabsf(h[j]);
 #pragma unroll
                     for (int d = 16; d >= 1; d >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, d));
