@@ -217,8 +217,10 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
     using C = FfnCfg<NT, MODE>;
     constexpr bool kFused = (MODE == kFfnFused);
     // Measured per tile width: the scale table from 16-byte loads is faster
-    // at 16- and 32-row tiles and slower at 64 (code generation).
+    // at 16- and 32-row tiles and slower at 64 (code generation), SiLU with
+    // the fast division faster at every width.
     constexpr bool kVecTable = NT <= 32;
+    constexpr bool kFastSilu = true;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -638,7 +640,8 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                 for (int j = 0; j < CW; ++j) {
                     const int c = cg * CW + j;
                     const float g = acc0[j];
-                    const float sg = __fdividef(g, 1.0f + __expf(-g));   // SiLU (tolerance-level)
+                    const float sg = kFastSilu ? __fdividef(g, 1.0f + __expf(-g))
+                                               : g / (1.0f + __expf(-g));
                     h[j] = (c < nrow) ? sg * acc1[j] : 0.0f;
                     float a = fabsf(h[j]);
 #pragma unroll
