@@ -596,13 +596,6 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                     tmem_ld<CH>(ta, v0);
                     if (C::NA == 2 && tl.gu) tmem_ld<CH>(ta + NT, v1);
                     tmem_wait_ld();
-                    if (hc == CW / CH - 1) {
-                        // the partial's last columns are in registers: hand
-                        // it back to the MMA before the FMAs
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&acc_empty[ab]);
-                    }
                     const float4* q0 =
                         reinterpret_cast<const float4*>(s_sc + kb * NT + cg * CW + hc * CH);
                     if (C::NA == 2 && tl.gu) {
@@ -634,6 +627,9 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                         }
                     }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[ab]);
                 ++je;
                 if (++ab == C::ACC_BUFS) ab = 0;
             }
