@@ -563,8 +563,17 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                 }
             }
             if (!tl.gu)
-                for (int i = et; i < NT; i += C::EPI_THREADS)
-                    s_src[i] = (i < nrow) ? p.ub[p.ul.src + row0 + i] : -1;
+                // each gathered row's output row: y_slots row r*K + k (>= 0)
+                // or y_shared row r (stored as -1 - r)
+                for (int i = et; i < NT; i += C::EPI_THREADS) {
+                    int d = -1;
+                    if (i < nrow) {
+                        const int slot = p.ub[p.ul.src + row0 + i];
+                        const int r = slot / p.KS, k = slot - r * p.KS;
+                        d = (k < p.K) ? r * p.K + k : -1 - r;
+                    }
+                    s_src[i] = d;
+                }
             ok = epi_bar_and(ok, C::EPI_THREADS);
             if (!ok) break;
 
@@ -681,10 +690,9 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                 for (int j = 0; j < CW; ++j) {
                     const int c = cg * CW + j;
                     if (ok && c < nrow) {
-                        const int slot = s_src[c];
-                        const int r = slot / p.KS, k = slot - r * p.KS;
-                        float* dst = (k < p.K) ? p.y_slots + (size_t(r) * p.K + k) * p.H
-                                               : p.y_shared + size_t(r) * p.H;
+                        const int d = s_src[c];
+                        float* dst = (d >= 0) ? p.y_slots + size_t(d) * p.H
+                                              : p.y_shared + size_t(-1 - d) * p.H;
                         dst[tl.blk * kBlock + m] = acc0[j];
                     }
                 }
