@@ -532,53 +532,34 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             const size_t wrow = (size_t(ex) * MB + tl.blk) * KB;
             const float* sw0 = (tl.gu ? (sh ? p.sh_s_gate : p.s_gate) : (sh ? p.sh_s_down : p.s_down)) + wrow;
             const float* sw1 = (sh ? p.sh_s_up : p.s_up) + wrow;
-            // table [operand][kb][n] = weight block scale x row scale.  Thread
-            // et takes one K-block column (et mod the column count: rows are
-            // read kb fastest, coalesced) and every per-th row from
-            // et / columns, so a tile costs each thread one division, and a
-            // row scale is loaded once for both operands.  Four K-blocks per
-            // 16-byte load when the rows allow it.  Row scales are read with
-            // plain loads: h's come from this launch (acquired above).
+            // table [operand][kb][n] = weight block scale x row scale; rows are
+            // read kb fastest (coalesced), four K-blocks per 16-byte load when
+            // the rows allow it.  Row scales are read with plain loads: h's
+            // come from this launch (acquired above).
             if (kVecTable && (KB & 3) == 0 &&
                 ((reinterpret_cast<uintptr_t>(sw0) | reinterpret_cast<uintptr_t>(sw1) |
                   reinterpret_cast<uintptr_t>(bs)) & 15) == 0) {
                 const int K4 = KB >> 2;
-                const int per = C::EPI_THREADS / K4;
-                const int k4 = et % K4, n0 = et / K4;
-                if (n0 < per) {
-                    const float4 w0 = __ldg(reinterpret_cast<const float4*>(sw0) + k4);
-                    const float4 w1 =
-                        (na == 2) ? __ldg(reinterpret_cast<const float4*>(sw1) + k4) : w0;
-                    for (int n = n0; n < NT; n += per) {
-                        const bool live = n < nrow;
-                        float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                        if (live) x = reinterpret_cast<const float4*>(bs + size_t(row0 + n) * KB)[k4];
-                        float* d = s_sc + 4 * k4 * NT + n;
-                        d[0] = live ? w0.x * x.x : 0.0f;
-                        d[NT] = live ? w0.y * x.y : 0.0f;
-                        d[2 * NT] = live ? w0.z * x.z : 0.0f;
-                        d[3 * NT] = live ? w0.w * x.w : 0.0f;
-                        if (na == 2) {
-                            d += KB * NT;
-                            d[0] = live ? w1.x * x.x : 0.0f;
-                            d[NT] = live ? w1.y * x.y : 0.0f;
-                            d[2 * NT] = live ? w1.z * x.z : 0.0f;
-                            d[3 * NT] = live ? w1.w * x.w : 0.0f;
-                        }
-                    }
+                for (int i = et; i < na * NT * K4; i += C::EPI_THREADS) {
+                    const int a = i / (NT * K4), rem = i - a * (NT * K4);
+                    const int n = rem / K4, k4 = rem - n * K4;
+                    const float4 w = __ldg(reinterpret_cast<const float4*>(a ? sw1 : sw0) + k4);
+                    float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    if (n < nrow) x = reinterpret_cast<const float4*>(bs + size_t(row0 + n) * KB)[k4];
+                    float* d = s_sc + (a * KB + 4 * k4) * NT + n;
+                    const bool live = n < nrow;
+                    d[0] = live ? w.x * x.x : 0.0f;
+                    d[NT] = live ? w.y * x.y : 0.0f;
+                    d[2 * NT] = live ? w.z * x.z : 0.0f;
+                    d[3 * NT] = live ? w.w * x.w : 0.0f;
                 }
             } else {
-                // KB <= 128 <= EPI_THREADS (hidden and inter are at most 16384)
-                const int per = C::EPI_THREADS / KB;
-                const int kb = et % KB, n0 = et / KB;
-                if (n0 < per) {
-                    const float w0 = sw0[kb], w1 = (na == 2) ? sw1[kb] : 0.0f;
-                    for (int n = n0; n < NT; n += per) {
-                        const bool live = n < nrow;
-                        const float x = live ? bs[size_t(row0 + n) * KB + kb] : 0.0f;
-                        s_sc[kb * NT + n] = live ? w0 * x : 0.0f;
-                        if (na == 2) s_sc[(KB + kb) * NT + n] = live ? w1 * x : 0.0f;
-                    }
+                for (int i = et; i < na * NT * KB; i += C::EPI_THREADS) {
+                    const int a = i / (NT * KB), rem = i - a * (NT * KB);
+                    const int n = rem / KB, kb = rem - n * KB;
+                    const float w = (a ? sw1 : sw0)[kb];
+                    s_sc[(a * KB + kb) * NT + n] =
+                        (n < nrow) ? w * bs[size_t(row0 + n) * KB + kb] : 0.0f;
                 }
             }
             if (!tl.gu)
