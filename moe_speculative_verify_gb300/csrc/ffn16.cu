@@ -377,10 +377,12 @@ __global__ void __launch_bounds__(kThreads16, 1)
             // this group's first step of the tile
             const int j0 = static_cast<int>((static_cast<uint32_t>(grp) - n) & 1u);
             float s_next = (j0 < NS) ? scale_of(j0) : 0.0f;
-            for (int j = j0; j < NS; j += 2) {
-                const uint32_t nj = n + static_cast<uint32_t>(j);
-                const int ws = static_cast<int>(nj % static_cast<uint32_t>(NW));
-                const uint32_t wph = (nj / static_cast<uint32_t>(NW)) & 1u;
+            // weight stage and phase of the group's step: divided out once
+            // per tile, then advanced two steps at a time
+            uint32_t nj = n + static_cast<uint32_t>(j0);
+            int ws = static_cast<int>(nj % static_cast<uint32_t>(NW));
+            uint32_t wph = (nj / static_cast<uint32_t>(NW)) & 1u;
+            for (int j = j0; j < NS; j += 2, nj += 2) {
                 const int slot = static_cast<int>(nj % kSlots);
                 const uint32_t sph = (nj / kSlots) & 1u;
                 const float s = s_next;
@@ -446,6 +448,11 @@ __global__ void __launch_bounds__(kThreads16, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&a_full[slot]);
+                ws += 2;   // NW >= 2
+                if (ws >= NW) {
+                    ws -= NW;
+                    wph ^= 1u;
+                }
             }
             n += static_cast<uint32_t>(NS);
         }
