@@ -518,14 +518,12 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             const int KB = tl.gu ? KB_H : KB_I;
             const int MB = tl.gu ? MB_I : MB_H;
             if (kFused && !tl.gu) {
-                // h and its scales come from this launch's gate/up tiles: one
-                // thread acquires the item's counter (its last read is an
-                // acquire at GPU scope), and the barrier orders every other
-                // thread's reads of the scales after it
+                // h and its scales come from this launch's gate/up tiles
                 if (et == 0 && !wait_counter(p.ready + tl.item, MB_I, p.err, p.timeout_ns, s_abort))
                     ok = false;
                 ok = epi_bar_and(ok, C::EPI_THREADS);
                 if (!ok) break;
+                (void)ld_acquire(p.ready + tl.item);
             }
             const float* bs = tl.gu ? p.xs : p.hs;
             const int na = tl.gu ? 2 : 1;
