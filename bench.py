@@ -52,11 +52,11 @@ def kernels_per_step(R: int) -> int:
 # DRAM bytes (read + write) of the expert GEMM per algorithmic byte, for the
 # 16-row tile of calls of up to 64 rows: ncu on the same kernel (tiled weight
 # codes, run-time tile scheduler) at 8 rows on 32 experts of the same shape
-# (dram__bytes_read.sum + dram__bytes_write.sum = 1.0631 GB for 1.0598 GB);
+# (dram__bytes_read.sum + dram__bytes_write.sum = 1.0629 GB for 1.0598 GB);
 # traffic grows with the weight bytes streamed, so a full launch's traffic is
 # this ratio times its algorithmic bytes.  Other tiles: not captured at their
 # full size here (null).
-FFN_TRAFFIC_PER_ALG_BYTE_16 = 1.0031
+FFN_TRAFFIC_PER_ALG_BYTE_16 = 1.0030
 HOST_AHEAD_CYCLES = 400_000   # GPU sleep before each step so the host enqueues it whole
 FLUSH_BYTES = 256 << 20       # > 129 MB L2
 
