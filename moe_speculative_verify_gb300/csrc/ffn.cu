@@ -216,7 +216,11 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                const FfnArgs p) {
     using C = FfnCfg<NT, MODE>;
     constexpr bool kFused = (MODE == kFfnFused);
-    constexpr bool kFastSilu = true;   // SiLU with the fast division (measured faster)
+    // Measured per tile width: the scale table from 16-byte loads is faster
+    // at 16- and 32-row tiles and slower at 64 (code generation), SiLU with
+    // the fast division faster at every width.
+    constexpr bool kVecTable = NT <= 32;
+    constexpr bool kFastSilu = true;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -528,39 +532,34 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             const size_t wrow = (size_t(ex) * MB + tl.blk) * KB;
             const float* sw0 = (tl.gu ? (sh ? p.sh_s_gate : p.s_gate) : (sh ? p.sh_s_down : p.s_down)) + wrow;
             const float* sw1 = (sh ? p.sh_s_up : p.s_up) + wrow;
-            // table [operand][kb][n] = weight block scale x row scale, four
-            // K-blocks per 16-byte load when the rows allow it.  Consecutive
-            // threads take consecutive rows n (conflict-free shared-memory
-            // stores; NT is a compile-time power of two, so no division).
-            // Row scales are read with plain loads: h's come from this launch
-            // (acquired above).
-            if ((KB & 3) == 0 &&
+            // table [operand][kb][n] = weight block scale x row scale; rows are
+            // read kb fastest (coalesced), four K-blocks per 16-byte load when
+            // the rows allow it.  Row scales are read with plain loads: h's
+            // come from this launch (acquired above).
+            if (kVecTable && (KB & 3) == 0 &&
                 ((reinterpret_cast<uintptr_t>(sw0) | reinterpret_cast<uintptr_t>(sw1) |
                   reinterpret_cast<uintptr_t>(bs)) & 15) == 0) {
                 const int K4 = KB >> 2;
-                for (int a = 0; a < na; ++a) {
-                    const float4* w4 = reinterpret_cast<const float4*>(a ? sw1 : sw0);
-                    for (int i = et; i < K4 * NT; i += C::EPI_THREADS) {
-                        const int n = i % NT, k4 = i / NT;
-                        const bool live = n < nrow;
-                        const float4 w = __ldg(w4 + k4);
-                        float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                        if (live) x = reinterpret_cast<const float4*>(bs + size_t(row0 + n) * KB)[k4];
-                        float* d = s_sc + (a * KB + 4 * k4) * NT + n;
-                        d[0] = live ? w.x * x.x : 0.0f;
-                        d[NT] = live ? w.y * x.y : 0.0f;
-                        d[2 * NT] = live ? w.z * x.z : 0.0f;
-                        d[3 * NT] = live ? w.w * x.w : 0.0f;
-                    }
+                for (int i = et; i < na * NT * K4; i += C::EPI_THREADS) {
+                    const int a = i / (NT * K4), rem = i - a * (NT * K4);
+                    const int n = rem / K4, k4 = rem - n * K4;
+                    const float4 w = __ldg(reinterpret_cast<const float4*>(a ? sw1 : sw0) + k4);
+                    float4 x = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    if (n < nrow) x = reinterpret_cast<const float4*>(bs + size_t(row0 + n) * KB)[k4];
+                    float* d = s_sc + (a * KB + 4 * k4) * NT + n;
+                    const bool live = n < nrow;
+                    d[0] = live ? w.x * x.x : 0.0f;
+                    d[NT] = live ? w.y * x.y : 0.0f;
+                    d[2 * NT] = live ? w.z * x.z : 0.0f;
+                    d[3 * NT] = live ? w.w * x.w : 0.0f;
                 }
             } else {
-                for (int a = 0; a < na; ++a) {
-                    const float* w1p = a ? sw1 : sw0;
-                    for (int i = et; i < KB * NT; i += C::EPI_THREADS) {
-                        const int n = i % NT, kb = i / NT;
-                        s_sc[(a * KB + kb) * NT + n] =
-                            (n < nrow) ? w1p[kb] * bs[size_t(row0 + n) * KB + kb] : 0.0f;
-                    }
+                for (int i = et; i < na * NT * KB; i += C::EPI_THREADS) {
+                    const int a = i / (NT * KB), rem = i - a * (NT * KB);
+                    const int n = rem / KB, kb = rem - n * KB;
+                    const float w = (a ? sw1 : sw0)[kb];
+                    s_sc[(a * KB + kb) * NT + n] =
+                        (n < nrow) ? w * bs[size_t(row0 + n) * KB + kb] : 0.0f;
                 }
             }
             if (!tl.gu)
