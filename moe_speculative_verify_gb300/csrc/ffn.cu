@@ -554,31 +554,12 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                     d[3 * NT] = live ? w.w * x.w : 0.0f;
                 }
             } else {
-                // four entries' loads in flight before their stores
-                const int total = na * NT * KB;
-                for (int i0 = et; i0 < total; i0 += 4 * C::EPI_THREADS) {
-                    float wv[4], xv[4];
-                    int at[4];
-                    bool live[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int i = i0 + u * C::EPI_THREADS;
-                        at[u] = -1;
-                        live[u] = false;
-                        wv[u] = 0.0f;
-                        xv[u] = 0.0f;
-                        if (i < total) {
-                            const int a = i / (NT * KB), rem = i - a * (NT * KB);
-                            const int n = rem / KB, kb = rem - n * KB;
-                            at[u] = (a * KB + kb) * NT + n;
-                            live[u] = n < nrow;
-                            wv[u] = (a ? sw1 : sw0)[kb];
-                            if (live[u]) xv[u] = bs[size_t(row0 + n) * KB + kb];
-                        }
-                    }
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        if (at[u] >= 0) s_sc[at[u]] = live[u] ? wv[u] * xv[u] : 0.0f;
+                for (int i = et; i < na * NT * KB; i += C::EPI_THREADS) {
+                    const int a = i / (NT * KB), rem = i - a * (NT * KB);
+                    const int n = rem / KB, kb = rem - n * KB;
+                    const float w = (a ? sw1 : sw0)[kb];
+                    s_sc[(a * KB + kb) * NT + n] =
+                        (n < nrow) ? w * bs[size_t(row0 + n) * KB + kb] : 0.0f;
                 }
             }
             if (!tl.gu)
