@@ -248,9 +248,10 @@ moe_status_t moe_expert_ffn_w8a16(const moe_config_t* cfg, const void* x_bf16,
 
 /*
  * The steps of moe_expert_ffn_fp8, callable one by one (same arguments, same
- * workspace).  moe_expert_ffn_fp8 is moe_dispatch followed by
- * moe_expert_gemms_fp8; moe_gate_up_fp8 followed by moe_down_fp8 computes the
- * same values as moe_expert_gemms_fp8 in two launches.
+ * workspace).  moe_expert_ffn_fp8 (and moe_layer) is moe_dispatch followed by
+ * moe_expert_gemms_fp8 for R <= 64 and by moe_gate_up_fp8 + moe_down_fp8 above
+ * (measured faster there); moe_gate_up_fp8 followed by moe_down_fp8 computes
+ * the same values as moe_expert_gemms_fp8 in two launches.
  *   moe_dispatch          quantise each valid row per 1x128 and write it to its
  *                         K+S gathered positions (workspace); clears the fused
  *                         GEMM's per-item counters;
