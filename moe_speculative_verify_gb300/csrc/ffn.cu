@@ -216,10 +216,10 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                const FfnArgs p) {
     using C = FfnCfg<NT, MODE>;
     constexpr bool kFused = (MODE == kFfnFused);
-    // Measured per tile width: the scale table from 16-byte loads is faster
-    // at 16- and 32-row tiles and slower at 64 (code generation), SiLU with
-    // the fast division faster at every width.
-    constexpr bool kVecTable = NT <= 32;
+    // Measured: the scale table from 16-byte loads is faster in every kernel
+    // but the fused one at 64-row tiles (code generation), SiLU with the fast
+    // division faster at every width.
+    constexpr bool kVecTable = NT <= 32 || MODE != kFfnFused;
     constexpr bool kFastSilu = true;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
