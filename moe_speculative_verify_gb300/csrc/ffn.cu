@@ -82,7 +82,7 @@ struct FfnCfg {
 };
 
 constexpr int kMaxStages = 16;
-constexpr int kStagesNt16 = 8;   // ring depth at 16-row tiles (see launch_ffn_t)
+constexpr int kStagesNt16 = 8;   // ring depth where the weight stream counts (see launch_ffn_t)
 // Per K-block (not per stage) synchronisation, on two rings of barriers
 // indexed by the CTA's K-block counter j:
 //   kbfull[j % kKbRing] -- the K-block's operands have landed: the producer
@@ -764,11 +764,11 @@ static cudaError_t launch_ffn_t(const FfnMaps& mp, FfnArgs args, int n_sms, int 
     using C = FfnCfg<NT, MODE>;
     const int KB_H = args.H / kBlock, KB_I = args.I / kBlock;
     const int kbmax = (MODE == kFfnGateUp) ? KB_H : (MODE == kFfnDown) ? KB_I : max(KB_H, KB_I);
-    // At 16-row tiles the weight stream is the bound, and HBM streams 16 KB
-    // tiles fastest with about 8 of them in flight per SM (a TMA probe: 7.2
-    // TB/s at 6-8, 6.5 at 12); wider tiles keep every stage that fits, for
-    // the MMA's and the epilogue's slack.
-    int stages = (NT == 16) ? kStagesNt16 : kMaxStages;
+    // HBM streams 16 KB tiles fastest with about 8 of them in flight per SM
+    // (a TMA probe: 7.2 TB/s at 6-8, 6.5 at 12).  Measured: 8 stages are
+    // faster at 16-row tiles and in the separate gate/up and down kernels;
+    // the fused kernel at 32 and 64 rows keeps every stage that fits.
+    int stages = (NT == 16 || MODE != kFfnFused) ? kStagesNt16 : kMaxStages;
     FfnSmem L = ffn_smem(NT, stages, kbmax, C::STAGE_BYTES);
     while (stages > 2 && L.bytes > smem_limit) {
         --stages;
