@@ -36,33 +36,43 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
         return;
     }
     const float* w = wts + size_t(r) * K;
-    // every slot's row is requested before the fixed-order accumulation
-    float4 y[MOE_MAX_TOPK + 1];
-    float wk[MOE_MAX_TOPK];
+    // the shared row first, then the K slots in k order, four rows requested
+    // at a time (few registers: more blocks per SM keep more rows in flight)
+    float4 ysh = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (S) ysh = __ldg(reinterpret_cast<const float4*>(y_shared + size_t(r) * H + h));
+    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+    for (int k0 = 0; k0 < K; k0 += 4) {
+        float4 y[4];
+        float wk[4];
 #pragma unroll
-    for (int k = 0; k < MOE_MAX_TOPK; ++k) {
-        if (k < K) {
-            y[k] = __ldg(reinterpret_cast<const float4*>(y_slots + (size_t(r) * K + k) * H + h));
-            wk[k] = w[k];
+        for (int u = 0; u < 4; ++u) {
+            if (k0 + u < K) {
+                y[u] = __ldg(reinterpret_cast<const float4*>(y_slots + (size_t(r) * K + k0 + u) * H + h));
+                wk[u] = w[k0 + u];
+            }
         }
-    }
-    if (S) y[MOE_MAX_TOPK] = __ldg(reinterpret_cast<const float4*>(y_shared + size_t(r) * H + h));
-    float a0 = __fmul_rn(wk[0], y[0].x), a1 = __fmul_rn(wk[0], y[0].y),
-          a2 = __fmul_rn(wk[0], y[0].z), a3 = __fmul_rn(wk[0], y[0].w);
 #pragma unroll
-    for (int k = 1; k < MOE_MAX_TOPK; ++k) {
-        if (k < K) {
-            a0 = __fmaf_rn(wk[k], y[k].x, a0);
-            a1 = __fmaf_rn(wk[k], y[k].y, a1);
-            a2 = __fmaf_rn(wk[k], y[k].z, a2);
-            a3 = __fmaf_rn(wk[k], y[k].w, a3);
+        for (int u = 0; u < 4; ++u) {
+            const int k = k0 + u;
+            if (k >= K) break;
+            if (k == 0) {
+                a0 = __fmul_rn(wk[u], y[u].x);
+                a1 = __fmul_rn(wk[u], y[u].y);
+                a2 = __fmul_rn(wk[u], y[u].z);
+                a3 = __fmul_rn(wk[u], y[u].w);
+            } else {
+                a0 = __fmaf_rn(wk[u], y[u].x, a0);
+                a1 = __fmaf_rn(wk[u], y[u].y, a1);
+                a2 = __fmaf_rn(wk[u], y[u].z, a2);
+                a3 = __fmaf_rn(wk[u], y[u].w, a3);
+            }
         }
     }
     if (S) {
-        a0 = __fadd_rn(a0, y[MOE_MAX_TOPK].x);
-        a1 = __fadd_rn(a1, y[MOE_MAX_TOPK].y);
-        a2 = __fadd_rn(a2, y[MOE_MAX_TOPK].z);
-        a3 = __fadd_rn(a3, y[MOE_MAX_TOPK].w);
+        a0 = __fadd_rn(a0, ysh.x);
+        a1 = __fadd_rn(a1, ysh.y);
+        a2 = __fadd_rn(a2, ysh.z);
+        a3 = __fadd_rn(a3, ysh.w);
     }
     const uint32_t b0 = __bfloat16_as_ushort(__float2bfloat16_rn(a0));
     const uint32_t b1 = __bfloat16_as_ushort(__float2bfloat16_rn(a1));
