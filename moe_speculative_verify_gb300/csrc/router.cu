@@ -177,30 +177,26 @@ __global__ void __launch_bounds__(kTileThreads, 1) router_logits_tiled_kernel(
 #pragma unroll
                 for (int b = 0; b < 8; ++b) p[a][b] = 0.0f;
         }
-        // experts in two halves of four (fewer live registers); every pair's
-        // four fmas stay in column order
+        // all eight experts' columns held, each row's x read and widened
+        // once; every pair's four fmas stay in column order
+        float4 wv[8];
 #pragma unroll
-        for (int bh = 0; bh < 8; bh += 4) {
-            float4 wv[4];
+        for (int b = 0; b < 8; ++b)
+            wv[b] = *reinterpret_cast<const float4*>(wsm + (buf * kTileE + wexp + b) * 128 + 4 * lane);
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
-                wv[b] = *reinterpret_cast<const float4*>(wsm + (buf * kTileE + wexp + bh + b) * 128 +
-                                                         4 * lane);
+        for (int a = 0; a < 8; ++a) {
+            const uint2 xv =
+                *reinterpret_cast<const uint2*>(xs + (buf * kTileR + wrow + a) * 128 + 4 * lane);
+            const float x0 = bf16_bits_to_f32(xv.x & 0xFFFFu), x1 = bf16_bits_to_f32(xv.x >> 16);
+            const float x2 = bf16_bits_to_f32(xv.y & 0xFFFFu), x3 = bf16_bits_to_f32(xv.y >> 16);
 #pragma unroll
-            for (int a = 0; a < 8; ++a) {
-                const uint2 xv =
-                    *reinterpret_cast<const uint2*>(xs + (buf * kTileR + wrow + a) * 128 + 4 * lane);
-                const float x0 = bf16_bits_to_f32(xv.x & 0xFFFFu), x1 = bf16_bits_to_f32(xv.x >> 16);
-                const float x2 = bf16_bits_to_f32(xv.y & 0xFFFFu), x3 = bf16_bits_to_f32(xv.y >> 16);
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    float q = p[a][bh + b];
-                    q = __fmaf_rn(x0, wv[b].x, q);
-                    q = __fmaf_rn(x1, wv[b].y, q);
-                    q = __fmaf_rn(x2, wv[b].z, q);
-                    q = __fmaf_rn(x3, wv[b].w, q);
-                    p[a][bh + b] = q;
-                }
+            for (int b = 0; b < 8; ++b) {
+                float q = p[a][b];
+                q = __fmaf_rn(x0, wv[b].x, q);
+                q = __fmaf_rn(x1, wv[b].y, q);
+                q = __fmaf_rn(x2, wv[b].z, q);
+                q = __fmaf_rn(x3, wv[b].w, q);
+                p[a][b] = q;
             }
         }
         if ((i & 7) == 7 || i + 1 == steps) {   // end of a 1024-column chunk
