@@ -121,6 +121,19 @@ def test_tile_weights_refusals(lib):
                          FAKE, wsb, None) == 1
 
 
+def test_ffn_layout_mirror_matches_library(lib):
+    """The binding's mirror of the FFN workspace carve-up (which the GPU tests
+    use to read regions of the workspace) ends where the library's size query
+    says, for every tile width, with and without a shared expert."""
+    import dataclasses
+    for sh in (synth.GLM52, synth.TINY, dataclasses.replace(synth.TINY, n_shared=0)):
+        cfg = m.Config.from_shape(sh)
+        for R in (1, 8, 63, 64, 65, 512, 513, 4096):
+            lay = m.ffn_layout(cfg, R)
+            assert lay["bytes"] == m.moe_ffn_workspace_bytes(cfg, R), (sh, R)
+            assert lay["ready"] < lay["sched"] < lay["xg"] < lay["xs"] < lay["hq"] < lay["hs"]
+
+
 def test_sizes(lib):
     cfg = _cfg()
     for R in (1, 8, 64, 512, 4096):
