@@ -25,6 +25,7 @@ workload, and prints the same line with "impl": "reference".
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -51,25 +52,57 @@ def kernels_per_step(R: int) -> int:
     kernel up to 64 rows, two above), dispatch, expert GEMMs (one fused launch
     up to 64 rows, gate/up and down above), combine."""
     return 5 if R <= 64 else 7
-# DRAM bytes (read + write) of the expert GEMM per algorithmic byte, for the
-# 16-row tile of calls of up to 64 rows: ncu on the same kernel (tiled weight
-# codes, run-time tile scheduler) at 8 rows on 32 experts of the same shape
-# (dram__bytes_read.sum + dram__bytes_write.sum = 1.0629 GB for 1.0598 GB);
-# traffic grows with the weight bytes streamed, so a full launch's traffic is
-# this ratio times its algorithmic bytes.  Other tiles: not captured at their
-# full size here (null).
-FFN_TRAFFIC_PER_ALG_BYTE_16 = 1.0030
+# DRAM bytes (read + write) of the fused expert GEMM per algorithmic byte at
+# the 16-row tile (calls of up to 64 rows), from one ncu capture of that kernel
+# at 8 rows on 32 experts of the same shape (dram__bytes_read.sum +
+# dram__bytes_write.sum over the launch's algorithmic bytes); traffic grows
+# with the weight bytes streamed, so a full launch's traffic is this ratio
+# times its algorithmic bytes.  The capture holds only for the kernel source it
+# was taken on: `kernel_sha16` is the hash of that source (ffn_source_sha16()),
+# and a bench run on other source reports the traffic as null.
+FFN_TRAFFIC = {"per_alg_byte": 1.0030, "profile": "profiles/ffn_fused_profile8.md",
+               "kernel_sha16": None}
+FFN_SOURCES = ("moe_speculative_verify_gb300/csrc/ffn.cu",
+               "moe_speculative_verify_gb300/csrc/common.cuh")
 HOST_AHEAD_CYCLES = 400_000   # GPU sleep before each step so the host enqueues it whole
 FLUSH_BYTES = 256 << 20       # > 129 MB L2
 
 
+def ffn_source_sha16() -> str:
+    """Hash of the expert GEMM's source files (what a profile was taken on)."""
+    h = hashlib.sha256()
+    for f in FFN_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def peaks():
+    """Roofline denominators: measured HBM copy GB/s and dense bf16 TFLOP/s
+    (burst); fp8 dense is taken as 2x bf16, the nominal ratio of the two
+    tensor rates (4.5 vs 2.25 PFLOP/s)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
-                "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+        out = {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+               "source": "measured"}
+    else:
+        out = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+    out["fp8_tflops"] = 2.0 * out["bf16_tflops"]
+    return out
+
+
+def fp8_roofline(flops: float, nbytes: float, ms: float, pk: dict) -> dict:
+    """fp8 tensor-pipe figures of a phase: achieved TFLOP/s, its fraction of
+    the fp8 dense peak, and its fraction of the intensity-bound ceiling
+    min(peak, AI * HBM bandwidth) with AI = flops / algorithmic bytes."""
+    tf = flops / (ms / 1e3) / 1e12
+    ai = flops / nbytes
+    ceiling = min(pk["fp8_tflops"], ai * pk["hbm_gbs"] / 1e3)
+    return {"tflops": round(tf, 1), "fp8_peak_tflops": round(pk["fp8_tflops"], 1),
+            "fp8_frac_of_peak": round(tf / pk["fp8_tflops"], 4),
+            "ai_flop_per_byte": round(ai, 1), "ai_ceiling_tflops": round(ceiling, 1),
+            "frac_of_ai_ceiling": round(tf / ceiling, 4)}
 
 
 # ------------------------------------------------------------------ ranks --
@@ -505,30 +538,48 @@ def main() -> None:
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     ffn_name = ("ffn_kernel<NT, fused> (gate/up + SiLU*mul + down)" if R <= 64 else
                 "ffn_kernel<NT, gate/up> + ffn_kernel<NT, down> (the two launches together)")
+    sha = ffn_source_sha16()
+    traffic, traffic_src = None, None
+    if dom == "ffn" and R <= 64:
+        if FFN_TRAFFIC["kernel_sha16"] == sha:
+            traffic = round(dom_bytes * FFN_TRAFFIC["per_alg_byte"])
+            traffic_src = (f"{FFN_TRAFFIC['profile']}: ncu DRAM read + write per algorithmic "
+                           f"byte of the same kernel and tile at 8 rows on 32 experts "
+                           f"({FFN_TRAFFIC['per_alg_byte']}), times this launch's algorithmic "
+                           f"bytes; kernel source {sha}")
+        else:
+            traffic_src = (f"null: the kernel source ({sha}) differs from the one profiled in "
+                           f"{FFN_TRAFFIC['profile']} ({FFN_TRAFFIC['kernel_sha16']})")
     roofline = {"kernel": {"ffn": ffn_name}
                 .get(dom, dom), "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                "traffic": (round(dom_bytes * FFN_TRAFFIC_PER_ALG_BYTE_16)
-                            if dom == "ffn" and R <= 64 else None),
-                "traffic_source": ("ncu DRAM bytes per algorithmic byte at 8 rows on 32 experts "
-                                   "(same kernel and tile), times this launch's algorithmic bytes"
-                                   if dom == "ffn" and R <= 64 else None),
-                "peak_source": pk["source"],
+                "traffic": traffic, "traffic_source": traffic_src,
+                "peak_source": pk["source"], "kernel_source_sha16": sha,
                 "algorithmic_bytes_per_launch": dom_bytes}
 
     extra = {}
     if rank == 0 and args.extra:
         for name in [n for n in args.extra.split(",") if n not in ("", "none", wl.name)]:
             wl2 = synth.WORKLOADS[name]
-            r2 = measure(wl2, 5, 3, False)
+            r2 = measure(wl2, max(20, args.steps), 3, False)
             a2 = r2["alg"]
+            ffn_ms = r2["phase_ms"]["ffn"]
             extra[name] = {
                 "rows": wl2.rows, "rows_per_s": round(wl2.rows / (r2["step_ms"] / 1e3), 1),
-                "ms_per_step": round(r2["step_ms"], 4),
+                "ms_per_step": round(r2["step_ms"], 4), "steps": max(20, args.steps),
                 "hbm_gbs": round(a2["total_bytes"] / (r2["step_ms"] / 1e3) / 1e9, 1),
+                "hbm_frac_of_measured": round(a2["total_bytes"] / (r2["step_ms"] / 1e3) / 1e9
+                                              / pk["hbm_gbs"], 4),
                 "fp8_tflops": round(a2["flops"] / (r2["step_ms"] / 1e3) / 1e12, 1),
                 "distinct_experts": a2["U"],
-                "phase_ms": {k: round(v, 4) for k, v in r2["phase_ms"].items()}}
+                "phase_ms": {k: round(v, 4) for k, v in r2["phase_ms"].items()},
+                "ffn_gbs": round(a2["bytes"]["ffn"] / (ffn_ms / 1e3) / 1e9, 1),
+                # fp8 MMA throughput of the expert GEMMs alone (their event-timed
+                # phase) and of the whole step, against the fp8 dense peak
+                # (2 x the measured bf16 burst, the nominal fp8 : bf16 ratio)
+                # and against min(peak, AI x measured HBM)
+                "ffn_fp8": fp8_roofline(a2["flops"], a2["bytes"]["ffn"], ffn_ms, pk),
+                "step_fp8": fp8_roofline(a2["flops"], a2["total_bytes"], r2["step_ms"], pk)}
             del r2
 
     # the verify-step extras, each timed alone with events on its stream

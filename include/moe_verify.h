@@ -183,7 +183,7 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x_bf16, const float*
  *   [0] U  number of distinct routed experts hit    [1] R_v valid rows
  *   [2] T  gathered slots = R_v * KS                [3] GEMM work items
  *   [4] rows per work item                          [5] error code (0 = OK)
- *   [6], [7] reserved
+ *   [6] R, the row count it was built for           [7] shape word (E << 8) | (K << 1) | S
  *   counts  [E+1]   at word 8: slots per expert; counts[E] = R_v * S
  *   offsets [E+2]   exclusive prefix of counts (experts ascending, shared last)
  *   ulist   [E+1]   the U experts hit, ascending, then E (the shared entry)
@@ -193,6 +193,14 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x_bf16, const float*
  *   items   [.. *4] work items (entry, first gathered row, row count, 0)
  * Inside an expert, slots are placed in (row, k) order; shared rows in row
  * order.  Word offsets of each array follow from E, K, S and R as listed.
+ *
+ * Every call that reads a union (moe_dispatch, the expert GEMM calls,
+ * moe_expert_ffn_fp8 / _w8a16, moe_combine, moe_combine_add_rmsnorm) first
+ * compares words [6] and [7] with its own R and shape.  A union built for
+ * another call is not indexed: the call computes nothing and records
+ * MOE_ERR_INVALID_ARG -- in the workspace error word (read it with
+ * moe_get_device_error) for the calls that take a workspace, in the union's
+ * own word [5] for the two combine calls (the only union word they write).
  */
 size_t moe_union_bytes(const moe_config_t* cfg, int32_t max_rows);
 moe_status_t moe_build_union(const moe_config_t* cfg, const int32_t* topk_ids, int32_t R,
@@ -319,6 +327,17 @@ moe_status_t moe_combine_add_rmsnorm(const moe_config_t* cfg, const float* y_slo
  *   ws            at least moe_workspace_bytes(cfg, R) bytes, 256-byte aligned.
  */
 size_t moe_workspace_bytes(const moe_config_t* cfg, int32_t max_rows);
+
+/*
+ * moe_workspace_size -- the same size as a status-returning query: *bytes is
+ * set to moe_workspace_bytes(cfg, max_rows), which also covers the union
+ * buffer (moe_union_bytes) and the FFN workspace (moe_ffn_workspace_bytes) of
+ * a call of up to max_rows rows, so one buffer of this size serves any entry
+ * point.  MOE_ERR_INVALID_ARG for a NULL pointer, a malformed shape or
+ * max_rows < 0; MOE_ERR_UNSUPPORTED beyond the compiled limits (*bytes = 0).
+ */
+moe_status_t moe_workspace_size(const moe_config_t* cfg, int32_t max_rows, size_t* bytes);
+
 moe_status_t moe_layer(const moe_config_t* cfg, const void* x_bf16, const float* w_router,
                        const float* bias, const moe_weights_t* w, const uint8_t* row_valid,
                        int32_t R, void* out_bf16, int32_t* topk_ids_out, float* topk_w_out,
@@ -349,8 +368,11 @@ moe_status_t moe_layer_w8a16(const moe_config_t* cfg, const void* x_bf16, const 
  * cudaMalloc, cudaFree or allocating library call.
  *
  * The first call on a device looks up the array's device address with that
- * device current (cudaGetSymbolAddress) and caches it; make that first call
- * outside any stream capture.  Every call shares the one array and leaves its
+ * device current (cudaGetSymbolAddress) and caches it per device and CUDA
+ * context; make that first call outside any stream capture.  A call made in
+ * another context than the cached one (a context of the caller's own, or the
+ * primary context created again after cudaDeviceReset) looks the address up
+ * again, so make the first call after such a change outside capture too.  Every call shares the one array and leaves its
  * contents behind; the call clears the error word at its head itself.  Calls
  * that overlap on the GPU (concurrent streams, or several host threads) race on
  * the array and corrupt each other: serialise them.

@@ -25,6 +25,7 @@ __all__ = [
     "moe_greedy_verify", "moe_combine_add_rmsnorm", "union_layout", "rows_per_item",
     "MOE_MAX_ROWS", "moe_expert_ffn_w8a16", "moe_layer_w8a16", "W8A16_MAX_ROWS",
     "moe_tile_weights", "tile_weights", "LAYOUT_ROW_MAJOR", "LAYOUT_TILED",
+    "moe_workspace_size",
 ]
 
 LAYOUT_ROW_MAJOR = 0
@@ -96,6 +97,7 @@ def load() -> C.CDLL:
     for n in ("moe_union_bytes", "moe_ffn_workspace_bytes", "moe_workspace_bytes"):
         getattr(L, n).restype = SZ
         getattr(L, n).argtypes = [cfg, I32]
+    L.moe_workspace_size.argtypes = [cfg, I32, C.POINTER(SZ)]
     L.moe_route.argtypes = [cfg, P, P, P, P, I32, P, P, P, P]
     L.moe_build_union.argtypes = [cfg, P, I32, P, SZ, P]
     L.moe_expert_ffn_fp8.argtypes = [cfg, P, C.POINTER(Weights), P, I32, P, P, P, SZ, P]
@@ -116,7 +118,7 @@ def load() -> C.CDLL:
     for n in ("moe_route", "moe_build_union", "moe_expert_ffn_fp8", "moe_combine", "moe_layer",
               "moe_get_device_error", "moe_diag_wait_timeout", "moe_dispatch", "moe_layer_noalloc", "moe_greedy_verify", "moe_combine_add_rmsnorm",
               "moe_gate_up_fp8", "moe_down_fp8", "moe_expert_gemms_fp8", "moe_expert_ffn_w8a16",
-              "moe_layer_w8a16"):
+              "moe_layer_w8a16", "moe_workspace_size"):
         getattr(L, n).restype = C.c_int
     _LIB = L
     return L
@@ -151,6 +153,13 @@ def moe_ffn_workspace_bytes(cfg: Config, max_rows: int) -> int:
 
 def moe_workspace_bytes(cfg: Config, max_rows: int) -> int:
     return load().moe_workspace_bytes(C.byref(cfg), max_rows)
+
+
+def moe_workspace_size(cfg: Config, max_rows: int) -> int:
+    """Bytes of one buffer that serves every entry point at up to max_rows rows."""
+    n = C.c_size_t(0)
+    _check(load().moe_workspace_size(C.byref(cfg), max_rows, C.byref(n)), "moe_workspace_size")
+    return n.value
 
 
 def moe_route(cfg: Config, x, w_router, bias, row_valid, topk_ids, topk_w, logits,

@@ -203,7 +203,7 @@ bool make_maps(const moe_config_t* c, const moe_weights_t* w, const FfnCall& f, 
            make_map(&mp->h, f.hq, f.FL.rows, I, f.nt);
 }
 
-moe::FfnArgs ffn_args(const moe_config_t* c, const moe_weights_t* w, const int32_t* ub,
+moe::FfnArgs ffn_args(const moe_config_t* c, const moe_weights_t* w, const int32_t* ub, int32_t R,
                       const FfnCall& f, float* y_slots, float* y_shared) {
     const int S = c->n_shared;
     moe::FfnArgs a{};
@@ -223,6 +223,8 @@ moe::FfnArgs ffn_args(const moe_config_t* c, const moe_weights_t* w, const int32
     a.ready = f.ready;
     a.sched = f.sched;
     a.err = f.err;
+    a.R = R;
+    a.ushape = moe::union_shape_word(c->n_experts, c->topk, c->n_shared);
     a.H = c->hidden;
     a.I = c->inter;
     a.E = c->n_experts;
@@ -236,9 +238,10 @@ moe::FfnArgs ffn_args(const moe_config_t* c, const moe_weights_t* w, const int32
 moe_status_t dispatch_impl(const moe_config_t* c, const void* x, const int32_t* ub, int32_t R,
                            void* ws, cudaStream_t s) {
     const FfnCall f = ffn_call(c, R, ws);
-    return cuda_status(moe::launch_dispatch(static_cast<const uint16_t*>(x), ub, f.UL, R, c->hidden,
-                                            c->topk + c->n_shared, f.xg, f.xs, f.ready,
-                                            f.FL.n_ready + moe::kSchedWords, s));
+    return cuda_status(moe::launch_dispatch(
+        static_cast<const uint16_t*>(x), ub, f.UL, R, c->hidden, c->topk + c->n_shared,
+        moe::union_shape_word(c->n_experts, c->topk, c->n_shared), f.xg, f.xs, f.ready,
+        f.FL.n_ready + moe::kSchedWords, f.err, s));
 }
 
 // One of the three expert-GEMM modes (gate/up, down, or both fused).
@@ -249,7 +252,7 @@ moe_status_t gemm_impl(int mode, const moe_config_t* c, const moe_weights_t* w, 
     if (dev.sms <= 0) return MOE_ERR_CUDA;
     moe::FfnMaps mp;
     if (!make_maps(c, w, f, &mp)) return MOE_ERR_CUDA;
-    return cuda_status(moe::launch_ffn(f.nt, mode, mp, ffn_args(c, w, ub, f, y_slots, y_shared),
+    return cuda_status(moe::launch_ffn(f.nt, mode, mp, ffn_args(c, w, ub, R, f, y_slots, y_shared),
                                        dev.sms, dev.smem_optin, s));
 }
 
@@ -280,9 +283,10 @@ moe_status_t ffn16_impl(const moe_config_t* c, const void* x, const moe_weights_
     uint16_t* xb = reinterpret_cast<uint16_t*>(base + f.FL.xb);
     uint16_t* hb = reinterpret_cast<uint16_t*>(base + f.FL.hb);
     const int H = c->hidden, I = c->inter, E = c->n_experts, S = c->n_shared;
-    moe_status_t st = cuda_status(moe::launch_dispatch16(static_cast<const uint16_t*>(x), ub, f.UL,
-                                                         R, H, c->topk + S, xb, f.ready,
-                                                         f.FL.n_ready + moe::kSchedWords, s));
+    moe_status_t st = cuda_status(moe::launch_dispatch16(
+        static_cast<const uint16_t*>(x), ub, f.UL, R, H, c->topk + S,
+        moe::union_shape_word(E, c->topk, S), xb, f.ready, f.FL.n_ready + moe::kSchedWords, f.err,
+        s));
     if (st != MOE_OK) return st;
     const DeviceInfo dev = device_info();
     if (dev.sms <= 0) return MOE_ERR_CUDA;
@@ -312,6 +316,8 @@ moe_status_t ffn16_impl(const moe_config_t* c, const void* x, const moe_weights_
     a.y_shared = y_shared;
     a.ready = f.ready;
     a.err = f.err;
+    a.R = R;
+    a.ushape = moe::union_shape_word(E, c->topk, S);
     a.H = H;
     a.I = I;
     a.E = E;
@@ -326,8 +332,9 @@ moe_status_t combine_impl(const moe_config_t* c, const float* y_slots, const flo
                           const float* wts, const int32_t* ub, int32_t R, void* out,
                           cudaStream_t s) {
     const UnionLayout UL = moe::union_layout(c->n_experts, c->topk, c->n_shared, R);
-    return cuda_status(moe::launch_combine(y_slots, y_shared, wts, ub, UL, R, c->hidden, c->topk,
-                                           c->n_shared, static_cast<uint16_t*>(out), s));
+    return cuda_status(moe::launch_combine(y_slots, y_shared, wts, const_cast<int32_t*>(ub), UL, R,
+                                           c->n_experts, c->hidden, c->topk, c->n_shared,
+                                           static_cast<uint16_t*>(out), s));
 }
 
 }  // namespace
@@ -363,6 +370,16 @@ size_t moe_workspace_bytes(const moe_config_t* cfg, int32_t max_rows) {
     return size_t(moe::layer_layout(cfg->hidden, cfg->inter, cfg->n_experts, cfg->topk,
                                     cfg->n_shared, max_rows)
                       .bytes);
+}
+
+moe_status_t moe_workspace_size(const moe_config_t* cfg, int32_t max_rows, size_t* bytes) {
+    if (bytes == nullptr) return MOE_ERR_INVALID_ARG;
+    *bytes = 0;
+    moe_status_t st = check_cfg(cfg);
+    if (st != MOE_OK) return st;
+    if ((st = check_rows(max_rows)) != MOE_OK) return st;
+    *bytes = moe_workspace_bytes(cfg, max_rows);
+    return MOE_OK;
 }
 
 moe_status_t moe_route(const moe_config_t* cfg, const void* x_bf16, const float* w_router,
@@ -520,7 +537,8 @@ moe_status_t moe_combine_add_rmsnorm(const moe_config_t* cfg, const float* y_slo
         return MOE_ERR_INVALID_ARG;
     const UnionLayout UL = moe::union_layout(cfg->n_experts, cfg->topk, cfg->n_shared, R);
     return cuda_status(moe::launch_combine_add_rmsnorm(
-        y_slots, y_shared, topk_w, union_buf, UL, R, cfg->hidden, cfg->topk, cfg->n_shared,
+        y_slots, y_shared, topk_w, const_cast<int32_t*>(union_buf), UL, R, cfg->n_experts,
+        cfg->hidden, cfg->topk, cfg->n_shared,
         static_cast<const uint16_t*>(residual_bf16), gamma, eps,
         static_cast<uint16_t*>(residual_out_bf16), static_cast<uint16_t*>(normed_bf16),
         reinterpret_cast<cudaStream_t>(stream)));

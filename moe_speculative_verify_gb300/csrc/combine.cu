@@ -16,16 +16,26 @@ namespace cg = cooperative_groups;
 
 namespace moe {
 
+// A union built for another call (row count or shape) is not read: the kernel
+// writes nothing and records MOE_ERR_INVALID_ARG in the union's word [5].
+__device__ __forceinline__ bool combine_union_ok(int32_t* ub, int R, int E, int K, int S) {
+    if (union_fits(ub, R, union_shape_word(E, K, S))) return true;
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+        atomicCAS(ub + 5, 0, MOE_ERR_INVALID_ARG);
+    return false;
+}
+
 // One thread per (row, 4 columns).  acc = w0*o0, then fma over k = 1..K-1,
 // then + shared, rounded once to bf16.  No atomics: the order is fixed.
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y_slots,
                                                       const float* __restrict__ y_shared,
                                                       const float* __restrict__ wts,
-                                                      const int32_t* __restrict__ ub,
-                                                      UnionLayout L, int R, int H, int K, int S,
-                                                      uint16_t* __restrict__ out) {
+                                                      int32_t* __restrict__ ub,
+                                                      UnionLayout L, int R, int E, int H, int K,
+                                                      int S, uint16_t* __restrict__ out) {
     pdl_wait();
     pdl_launch_dependents();
+    if (!combine_union_ok(ub, R, E, K, S)) return;
     const int r = blockIdx.x;
     const int h = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
     if (h >= H) return;
@@ -82,11 +92,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
 }
 
 cudaError_t launch_combine(const float* y_slots, const float* y_shared, const float* wts,
-                           const int32_t* ub, const UnionLayout& L, int R, int H, int K, int S,
+                           int32_t* ub, const UnionLayout& L, int R, int E, int H, int K, int S,
                            uint16_t* out, cudaStream_t stream) {
     dim3 grid(R, (H / 4 + 255) / 256);
     cudaError_t e = launch_pdl(combine_kernel, grid, dim3(256), 0, stream, y_slots, y_shared, wts, ub,
-                               L, R, H, K, S, out);
+                               L, R, E, H, K, S, out);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -110,14 +120,16 @@ constexpr int kNormMaxChunks = 4;      // H / 4 / kNormCluster / kNormThreads, H
 
 __global__ void __launch_bounds__(kNormThreads) combine_add_rmsnorm_kernel(
     const float* __restrict__ y_slots, const float* __restrict__ y_shared,
-    const float* __restrict__ wts, const int32_t* __restrict__ ub, UnionLayout L, int H, int K,
-    int S, const uint16_t* __restrict__ residual, const float* __restrict__ gamma, float eps,
+    const float* __restrict__ wts, int32_t* __restrict__ ub, UnionLayout L, int R, int E, int H,
+    int K, int S, const uint16_t* __restrict__ residual, const float* __restrict__ gamma, float eps,
     uint16_t* __restrict__ residual_out, uint16_t* __restrict__ normed) {
     __shared__ float s_warp[kNormThreads / 32];
     __shared__ float s_part;
     cg::cluster_group cl = cg::this_cluster();
     pdl_wait();
     pdl_launch_dependents();
+    // the same words for every CTA of every cluster: all leave here or none
+    if (!combine_union_ok(ub, R, E, K, S)) return;
     const int r = blockIdx.x / kNormCluster;
     const int rank = static_cast<int>(cl.block_rank());
     const int KS = K + S;
@@ -213,16 +225,17 @@ __global__ void __launch_bounds__(kNormThreads) combine_add_rmsnorm_kernel(
 }
 
 cudaError_t launch_combine_add_rmsnorm(const float* y_slots, const float* y_shared, const float* wts,
-                                       const int32_t* ub, const UnionLayout& L, int R, int H, int K,
-                                       int S, const uint16_t* residual, const float* gamma, float eps,
-                                       uint16_t* residual_out, uint16_t* normed, cudaStream_t stream) {
+                                       int32_t* ub, const UnionLayout& L, int R, int E, int H,
+                                       int K, int S, const uint16_t* residual, const float* gamma,
+                                       float eps, uint16_t* residual_out, uint16_t* normed,
+                                       cudaStream_t stream) {
     if (H % (4 * kNormCluster) != 0 || H / 4 / kNormCluster > kNormMaxChunks * kNormThreads)
         return cudaErrorInvalidValue;
     cudaError_t e = launch_pdl_cluster(combine_add_rmsnorm_kernel,
                                        dim3(static_cast<unsigned>(R) * kNormCluster),
                                        dim3(kNormThreads), kNormCluster, 0, stream, y_slots,
-                                       y_shared, wts, ub, L, H, K, S, residual, gamma, eps,
-                                       residual_out, normed);
+                                       y_shared, wts, ub, L, R, E, H, K, S, residual, gamma,
+                                       eps, residual_out, normed);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

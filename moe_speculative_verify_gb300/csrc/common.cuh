@@ -279,6 +279,17 @@ __device__ __forceinline__ bool bar_and(int id, bool ok, int nthreads) {
     return r != 0;
 }
 
+// Words [6] and [7] of a union buffer name the call it was built for: the row
+// count R and the shape word below.  Every kernel that reads a union compares
+// both with its own call before it indexes anything whose offset depends on R.
+__host__ __device__ inline int32_t union_shape_word(int E, int K, int S) {
+    return (E << 8) | (K << 1) | S;
+}
+
+__device__ __forceinline__ bool union_fits(const int32_t* ub, int R, int32_t shape_word) {
+    return ub[6] == R && ub[7] == shape_word;
+}
+
 __device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31u) == 0u; }
 
 // ------------------------------------------- programmatic dependent launch ----

@@ -282,8 +282,10 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
     // The union buffer comes from a kernel at least two launches back: it is
     // complete when this kernel starts (see pdl_wait).  Items must have been
     // cut to this kernel's row tile.
-    const int n_items = (p.ub[4] == NT) ? p.ub[3] : 0;
-    if (threadIdx.x == 0 && p.ub[4] != NT && p.ub[3] > 0) record_error(p.err, MOE_ERR_INVALID_ARG);
+    // a union built for another call (row count, shape or row tile) runs nothing
+    const bool fits = union_fits(p.ub, p.R, p.ushape) && p.ub[4] == NT;
+    const int n_items = fits ? p.ub[3] : 0;
+    if (threadIdx.x == 0 && !fits) record_error(p.err, MOE_ERR_INVALID_ARG);
     const int n_gu = (MODE == kFfnDown) ? 0 : n_items * MB_I;
     const int n_tiles = n_gu + ((MODE == kFfnGateUp) ? 0 : n_items * MB_H);
     const int4* items = reinterpret_cast<const int4*>(p.ub + p.ul.items);

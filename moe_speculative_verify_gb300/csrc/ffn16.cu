@@ -239,8 +239,10 @@ __global__ void __launch_bounds__(kThreads16, 1)
 
     // The union buffer comes from a kernel at least two launches back: it is
     // complete when this kernel starts.  Items must have been cut to 16 rows.
-    const int n_items = (p.ub[4] == kNT) ? p.ub[3] : 0;
-    if (threadIdx.x == 0 && p.ub[4] != kNT && p.ub[3] > 0) record_error(p.err, MOE_ERR_INVALID_ARG);
+    // a union built for another call (row count, shape or row tile) runs nothing
+    const bool fits = union_fits(p.ub, p.R, p.ushape) && p.ub[4] == kNT;
+    const int n_items = fits ? p.ub[3] : 0;
+    if (threadIdx.x == 0 && !fits) record_error(p.err, MOE_ERR_INVALID_ARG);
     const int n_gu = n_items * MB_I;
     const int n_tiles = n_gu + n_items * MB_H;
     const int4* items = reinterpret_cast<const int4*>(p.ub + p.ul.items);
@@ -549,12 +551,19 @@ __global__ void __launch_bounds__(kThreads16, 1)
 __global__ void __launch_bounds__(256) dispatch16_kernel(const uint16_t* __restrict__ x,
                                                          const int32_t* __restrict__ ub,
                                                          UnionLayout L, int R, int H, int KS,
+                                                         int32_t ushape,
                                                          uint16_t* __restrict__ xb,
-                                                         int32_t* __restrict__ ready, int n_ready) {
+                                                         int32_t* __restrict__ ready, int n_ready,
+                                                         int32_t* __restrict__ err) {
     pdl_wait();
     pdl_launch_dependents();
     if (blockIdx.x == 0 && blockIdx.y == 0)
         for (int i = threadIdx.x; i < n_ready; i += blockDim.x) ready[i] = 0;
+    if (!union_fits(ub, R, ushape)) {   // built for another call
+        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+            record_error(err, MOE_ERR_INVALID_ARG);
+        return;
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x;
     const int b = blockIdx.y * 8 + warp;
@@ -569,11 +578,11 @@ __global__ void __launch_bounds__(256) dispatch16_kernel(const uint16_t* __restr
 }  // namespace
 
 cudaError_t launch_dispatch16(const uint16_t* x, const int32_t* ub, const UnionLayout& L, int R,
-                              int H, int KS, uint16_t* xb, int32_t* ready, int n_ready,
-                              cudaStream_t stream) {
+                              int H, int KS, int32_t ushape, uint16_t* xb, int32_t* ready,
+                              int n_ready, int32_t* err, cudaStream_t stream) {
     dim3 grid(R, (H / kBlock + 7) / 8);
     cudaError_t e = launch_pdl(dispatch16_kernel, grid, dim3(256), 0, stream, x, ub, L, R, H, KS,
-                               xb, ready, n_ready);
+                               ushape, xb, ready, n_ready, err);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

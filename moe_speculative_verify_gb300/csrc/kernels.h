@@ -38,6 +38,8 @@ struct FfnArgs {
     int32_t* ready;            // [max_items] gate/up blocks of h finished (fused mode)
     int32_t* sched;            // [2] tile counter, CTAs done claiming (zero between launches)
     int32_t* err;              // device error word
+    int R;                     // rows of the call
+    int32_t ushape;            // union_shape_word of the call
     int H, I;
     int E, K, KS;
     int n_stages;
@@ -60,6 +62,8 @@ struct Ffn16Args {
     float* y_shared;           // [R, H]
     int32_t* ready;            // [max_items] gate/up blocks of h finished
     int32_t* err;              // device error word
+    int R;                     // rows of the call
+    int32_t ushape;            // union_shape_word of the call
     int H, I;
     int E, K, KS;
     int n_wstages;
@@ -68,8 +72,8 @@ struct Ffn16Args {
 };
 
 cudaError_t launch_dispatch16(const uint16_t* x, const int32_t* ub, const UnionLayout& L, int R,
-                              int H, int KS, uint16_t* xb, int32_t* ready, int n_ready,
-                              cudaStream_t stream);
+                              int H, int KS, int32_t ushape, uint16_t* xb, int32_t* ready,
+                              int n_ready, int32_t* err, cudaStream_t stream);
 cudaError_t launch_ffn16(const FfnMaps& mp, Ffn16Args args, int n_sms, int smem_limit,
                          cudaStream_t stream);
 cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const uint8_t* row_valid,
@@ -91,17 +95,19 @@ cudaError_t launch_route_union(const float* logits, const float* bias, const uin
 cudaError_t launch_tile_weights(const uint8_t* src, uint8_t* dst, int64_t n, int rows, int cols,
                                 cudaStream_t stream);
 cudaError_t launch_dispatch(const uint16_t* x, const int32_t* ub, const UnionLayout& L, int R,
-                            int H, int KS, uint8_t* xg, float* xs, int32_t* ready, int n_ready,
-                            cudaStream_t stream);
+                            int H, int KS, int32_t ushape, uint8_t* xg, float* xs, int32_t* ready,
+                            int n_ready, int32_t* err, cudaStream_t stream);
 cudaError_t launch_ffn(int nt, int mode, const FfnMaps& mp, const FfnArgs& args, int n_sms,
                        int smem_limit, cudaStream_t stream);
+// The combine kernels record a union built for another call in its word [5].
 cudaError_t launch_combine(const float* y_slots, const float* y_shared, const float* wts,
-                           const int32_t* ub, const UnionLayout& L, int R, int H, int K, int S,
+                           int32_t* ub, const UnionLayout& L, int R, int E, int H, int K, int S,
                            uint16_t* out, cudaStream_t stream);
 cudaError_t launch_combine_add_rmsnorm(const float* y_slots, const float* y_shared, const float* wts,
-                                       const int32_t* ub, const UnionLayout& L, int R, int H, int K,
-                                       int S, const uint16_t* residual, const float* gamma, float eps,
-                                       uint16_t* residual_out, uint16_t* normed, cudaStream_t stream);
+                                       int32_t* ub, const UnionLayout& L, int R, int E, int H,
+                                       int K, int S, const uint16_t* residual, const float* gamma,
+                                       float eps, uint16_t* residual_out, uint16_t* normed,
+                                       cudaStream_t stream);
 cudaError_t launch_wait_timeout(int32_t* err, uint64_t timeout_ns, cudaStream_t stream);
 cudaError_t launch_greedy_verify(const void* logits, bool bf16, int V, int R, const int32_t* draft,
                                  const int32_t* n_draft, int32_t* am, int32_t* accept_len,

@@ -11,6 +11,8 @@
 // experts, top-8, one shared expert).
 #include <mutex>
 
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "layout.h"
 
@@ -25,21 +27,53 @@ static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
-void* g_addr[kMaxDevices] = {};
+// Per device: the context the address was looked up in, and the address.  A
+// context of its own (a driver context made current by the caller) or the
+// primary context created again after cudaDeviceReset loads the library's
+// device code anew, so the array may sit elsewhere: the address is looked up
+// again whenever the current context is not the one it was found in.
+struct ScratchAddr {
+    CUcontext ctx = nullptr;
+    void* addr = nullptr;
+};
+ScratchAddr g_addr[kMaxDevices];
 
-// Device address of the scratch array on the current device, looked up once
-// per device (with that device current) and cached.
+PFN_cuCtxGetCurrent_v4000 ctx_get_current() {
+    static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    });
+    return fn;
+}
+
+// Device address of the scratch array on the current device, looked up with
+// that device current and cached per (device, context).
 moe_status_t scratch_address(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    auto get_ctx = ctx_get_current();
+    CUcontext ctx = nullptr;
+    if (get_ctx == nullptr || get_ctx(&ctx) != CUDA_SUCCESS) return MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mu);
-    if (g_addr[dev] == nullptr) {
+    ScratchAddr& a = g_addr[dev];
+    if (ctx == nullptr || a.addr == nullptr || a.ctx != ctx) {
+        // (with no context current yet, the lookup makes the device's
+        // primary context current)
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || p == nullptr)
             return MOE_ERR_CUDA;
-        g_addr[dev] = p;
+        if (ctx == nullptr && (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr))
+            return MOE_ERR_CUDA;
+        a.ctx = ctx;
+        a.addr = p;
     }
-    *out = g_addr[dev];
+    *out = a.addr;
     return MOE_OK;
 }
 

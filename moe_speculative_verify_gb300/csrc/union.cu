@@ -167,8 +167,8 @@ __device__ void union_block(const int32_t* ids, int R, int E, int K, int S, int 
         ub[3] = s_items;
         ub[4] = n_tile;
         ub[5] = s_err;
-        ub[6] = 0;
-        ub[7] = 0;
+        ub[6] = R;
+        ub[7] = union_shape_word(E, K, S);
     }
     for (int e = tid; e <= E; e += kUnionThreads) ub[L.counts + e] = s_cnt[e];
     for (int e = tid; e <= E + 1; e += kUnionThreads) ub[L.offsets + e] = s_off[e];
@@ -264,15 +264,22 @@ __global__ void __launch_bounds__(kUnionThreads) route_union_kernel(
 // positions (K routed slots, then the shared slot).  One warp per (row, block).
 __global__ void __launch_bounds__(256) dispatch_kernel(const uint16_t* __restrict__ x,
                                                        const int32_t* __restrict__ ub, UnionLayout L,
-                                                       int R, int H, int KS,
+                                                       int R, int H, int KS, int32_t ushape,
                                                        uint8_t* __restrict__ xg,
                                                        float* __restrict__ xs,
-                                                       int32_t* __restrict__ ready, int n_ready) {
+                                                       int32_t* __restrict__ ready, int n_ready,
+                                                       int32_t* __restrict__ err) {
     pdl_wait();
     pdl_launch_dependents();
     // the fused expert GEMM's per-item counters start at zero every call
     if (blockIdx.x == 0 && blockIdx.y == 0)
         for (int i = threadIdx.x; i < n_ready; i += blockDim.x) ready[i] = 0;
+    // a union built for another call: its positions may lie outside xg
+    if (!union_fits(ub, R, ushape)) {
+        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+            record_error(err, MOE_ERR_INVALID_ARG);
+        return;
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = blockIdx.x;
     const int HB = H / kBlock;
@@ -309,12 +316,12 @@ cudaError_t launch_union(const int32_t* ids, int R, int E, int K, int S, int n_t
 }
 
 cudaError_t launch_dispatch(const uint16_t* x, const int32_t* ub, const UnionLayout& L, int R,
-                            int H, int KS, uint8_t* xg, float* xs, int32_t* ready, int n_ready,
-                            cudaStream_t stream) {
+                            int H, int KS, int32_t ushape, uint8_t* xg, float* xs, int32_t* ready,
+                            int n_ready, int32_t* err, cudaStream_t stream) {
     const int HB = H / kBlock;
     dim3 grid(R, (HB + 7) / 8);
-    cudaError_t e = launch_pdl(dispatch_kernel, grid, dim3(256), 0, stream, x, ub, L, R, H, KS, xg, xs,
-                               ready, n_ready);
+    cudaError_t e = launch_pdl(dispatch_kernel, grid, dim3(256), 0, stream, x, ub, L, R, H, KS,
+                               ushape, xg, xs, ready, n_ready, err);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

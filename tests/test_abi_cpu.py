@@ -26,12 +26,42 @@ def _declared():
                                  text, re.M)))
 
 
+# The boundary's entry points as the hot-path scope lists them; the header
+# declares each of them (plus the stepwise calls and the extensions).
+SCOPE_ENTRY_POINTS = {"moe_route", "moe_build_union", "moe_expert_ffn_fp8", "moe_combine",
+                      "moe_layer", "moe_workspace_size", "moe_get_device_error",
+                      "moe_status_string"}
+
+
 def test_exports_every_declared_symbol(lib):
     names = _declared()
-    assert {"moe_route", "moe_build_union", "moe_expert_ffn_fp8", "moe_combine",
-            "moe_layer"} <= set(names)
+    assert SCOPE_ENTRY_POINTS <= set(names)
     for n in names:
         assert hasattr(lib, n), n
+
+
+def test_workspace_size_query(lib):
+    cfg = _cfg()
+    for R in (0, 1, 8, 64, 65, 512, 4096):
+        assert m.moe_workspace_size(cfg, R) == m.moe_workspace_bytes(cfg, R)
+        # one buffer of that size also holds a union and an FFN workspace
+        assert m.moe_workspace_size(cfg, R) >= m.moe_union_bytes(cfg, R)
+        assert m.moe_workspace_size(cfg, R) >= m.moe_ffn_workspace_bytes(cfg, R)
+    n = C.c_size_t(77)
+    assert lib.moe_workspace_size(C.byref(cfg), m.MOE_MAX_ROWS + 1, C.byref(n)) == 2
+    assert n.value == 0
+    assert lib.moe_workspace_size(C.byref(cfg), -1, C.byref(n)) == 1
+    assert lib.moe_workspace_size(C.byref(_cfg(hidden=100)), 8, C.byref(n)) == 1
+    assert lib.moe_workspace_size(None, 8, C.byref(n)) == 1
+    assert lib.moe_workspace_size(C.byref(cfg), 8, None) == 1
+
+
+def test_noalloc_row_limit_at_glm_shape(lib):
+    """The no-allocation entry point's fixed 32 MiB array holds the workspace of
+    up to 109 rows at the GLM-5.2 shape, and not of 110 (the limit stated beside
+    the entry point)."""
+    cfg = _cfg()
+    assert m.moe_workspace_bytes(cfg, 109) <= 32 << 20 < m.moe_workspace_bytes(cfg, 110)
 
 
 def test_status_strings(lib):

@@ -76,3 +76,23 @@ def test_glm_workload(weights, name):
     if name == "verify8":
         U = len(np.unique(gid))
         assert 30 <= U <= 48, U
+
+
+@pytest.mark.parametrize("name", ["verify8", "prefill4096"])
+def test_glm_tiled_layout_bit_identical(weights, name):
+    """The layout the bench gives the layer -- weight codes in 16 KB 128x128
+    blocks (moe_tile_weights) -- gives the same output bits as the row-major
+    codes at the full shape, on the verify and the prefill row tile."""
+    dev_w, _ = weights
+    wl = synth.WORKLOADS[name]
+    t = dict(synth.make_router_inputs(wl, device="cuda"))
+    t.update(dev_w)
+    cfg = m.Config.from_shape(wl.shape)
+    out_rm, ids_rm, w_rm, _ = run_layer(cfg, t, wl.rows)
+    tt = m.tile_weights(t)
+    out_t, ids_t, w_t, _ = run_layer(cfg, tt, wl.rows, layout=m.LAYOUT_TILED)
+    assert torch.equal(ids_t, ids_rm)
+    assert torch.equal(w_t, w_rm)
+    assert torch.equal(out_t.view(torch.int16), out_rm.view(torch.int16))
+    del tt
+    torch.cuda.empty_cache()

@@ -7,15 +7,18 @@ its rows, their validity and every weight from device memory at kernel time;
 the row count fixes the launch shapes.  A graph captured once at R = 8 and
 replayed with other inputs and other pad patterns gives the same bits as
 eager calls with those inputs (kernels chained by programmatic dependent
-launch inside the graph).
+launch inside the graph), and every replay matches the oracle on those
+inputs: routing ids and weights bit for bit, the output within the parity
+tolerance, pad rows +0.0.
 """
 import numpy as np
 import pytest
 import torch
 
 import moe_speculative_verify_gb300 as m
+import oracle
 import synth
-from gpu_helpers import MEDIUM, bf16_to_np
+from gpu_helpers import MEDIUM, TOL, bf16_bits_to_f64, bf16_to_np, rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -24,13 +27,16 @@ pytestmark = pytest.mark.gpu
 def _built():
     m.build()
     m.load()
+    oracle.lib()
     torch.cuda.set_device(0)
 
 
 def test_one_graph_any_occupancy():
     shape, R = MEDIUM, 8
     wl = synth.Workload("graph", shape, rows=R)
-    t = {k: v.cuda() for k, v in synth.make_layer(wl, device="cpu").items()}
+    t_cpu = synth.make_layer(wl, device="cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    host = synth.to_numpy(t_cpu)
     cfg = m.Config.from_shape(shape)
     W = m.Weights.from_tensors(t)
     ws = torch.zeros(m.moe_workspace_bytes(cfg, R), dtype=torch.uint8, device="cuda")
@@ -38,9 +44,10 @@ def test_one_graph_any_occupancy():
     valid = torch.ones(R, dtype=torch.uint8, device="cuda")
     out = torch.empty((R, shape.hidden), dtype=torch.bfloat16, device="cuda")
     ids = torch.empty((R, shape.topk), dtype=torch.int32, device="cuda")
+    wts = torch.empty((R, shape.topk), dtype=torch.float32, device="cuda")
 
     def layer():
-        m.moe_layer(cfg, x, t["wr"], t["bias"], W, valid, out, ws, topk_ids=ids)
+        m.moe_layer(cfg, x, t["wr"], t["bias"], W, valid, out, ws, topk_ids=ids, topk_w=wts)
 
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -65,6 +72,19 @@ def test_one_graph_any_occupancy():
         torch.cuda.synchronize()
         got = bf16_to_np(out).copy()
         got_ids = ids.cpu().numpy().copy()
+        got_w = wts.cpu().numpy().copy()
+        # the replay against the oracle on the inputs it read at kernel time
+        h = dict(host)
+        h["x"] = synth.to_numpy({"x": xv})["x"]
+        h["row_valid"] = vmask
+        ref = oracle.moe_layer(shape, h)
+        assert np.array_equal(got_ids, ref["ids"])
+        assert np.array_equal(got_w.view(np.uint32), ref["wts"].view(np.uint32))
+        v = vmask != 0
+        if v.any():
+            y = bf16_bits_to_f64(got)
+            assert np.all(np.isfinite(y))
+            assert rel_fro(y[v], ref["y_acc"][v]) <= TOL
         out.fill_(float("nan"))
         layer()                                  # eager, same inputs
         torch.cuda.synchronize()

@@ -3,10 +3,13 @@
 Such a caller (a plugin whose host framework owns all device memory, code that
 must not call cudaMalloc) gets the layer with the library's own fixed scratch
 array instead of a workspace.  The test calls it through the C ABI twice in a
-row, on two shapes one after the other (so the array holds the previous call's
-leftovers each time), and checks it against moe_layer with a workspace: the
-same routing ids and weights, the same output within the parity tolerance,
-pads zero-filled, and a clean device status.  It also checks that a row count
+row, on three cases one after the other (so the array holds the previous
+call's leftovers each time) -- 8 and 37 rows (selection and union in one
+kernel, one fused GEMM launch) and 100 rows (separate selection and union
+kernels, gate/up and down GEMMs as two launches, whose tile scheduler words
+stay in the array between calls) -- and checks it against moe_layer with a
+workspace: the same routing ids and weights, the same output within the
+parity tolerance, pads zero-filled, and a clean device status.  It also checks that a row count
 whose workspace would not fit in the array is refused.
 
 This file is collected last on purpose.
@@ -37,7 +40,7 @@ def _layer(shape, rows, pads):
 
 
 def test_noalloc_matches_moe_layer_twice():
-    for shape, R, pads in ((synth.TINY, 8, ()), (MEDIUM, 37, (0, 36))):
+    for shape, R, pads in ((synth.TINY, 8, ()), (MEDIUM, 37, (0, 36)), (MEDIUM, 100, (5, 99))):
         t = _layer(shape, R, pads)
         cfg = m.Config.from_shape(shape)
         ref_out, ref_ids, ref_w, _ = run_layer(cfg, t, R)
