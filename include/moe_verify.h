@@ -45,6 +45,14 @@
  *   - For a fixed R the kernel configuration is fixed, and no reduction depends
  *     on which slot of the batch a row occupies: a row's outputs are bit-
  *     identical wherever it sits and whatever its neighbours hold.
+ *   - The expert GEMM kernels are persistent (one CTA per SM) and their CTAs
+ *     wait on one another: a down tile starts once the gate/up tiles of its
+ *     rows have stored their h, and the first tile of every CTA is fixed by
+ *     its index.  They expect every SM to be free for them; while kernels of
+ *     other streams hold SMs, some of their CTAs start late and the others
+ *     wait.  Every such wait is bounded by wait_timeout_us: past it the call
+ *     stops and records MOE_ERR_TIMEOUT (read with moe_get_device_error); it
+ *     never hangs.
  */
 #ifndef MOE_VERIFY_H
 #define MOE_VERIFY_H
