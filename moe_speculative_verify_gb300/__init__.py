@@ -319,7 +319,7 @@ W8A16_MAX_ROWS = 64          # the w8a16 variant's row limit (mirrors the librar
 
 def rows_per_item(R: int) -> int:
     """Rows per GEMM work item chosen for a call with R rows (mirrors the library)."""
-    return 16 if R <= 64 else (32 if R <= 512 else 64)
+    return 16 if R <= 64 else (32 if R <= 256 else 64)
 
 
 def union_layout(cfg: Config, R: int) -> dict:

@@ -59,28 +59,44 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
+// Tests the phase; with HINT_NS > 0 a thread whose phase is not yet complete
+// may be suspended for up to HINT_NS nanoseconds (it resumes as soon as the
+// phase completes), so a waiting warp stops taking issue slots from the
+// warps that work.
+template <uint32_t HINT_NS = 0>
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
+    if constexpr (HINT_NS > 0) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity), "n"(HINT_NS)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+    }
     return ok != 0;
 }
 
 // Waits for the phase of `bar` with the given parity to complete, giving up
 // after `timeout_ns` of wall time or 2^30 polls, whichever comes first.  On
 // giving up it records MOE_ERR_TIMEOUT and returns false; the caller then
-// stops its role and winds down.
+// stops its role and winds down.  HINT_NS as in mbar_try_wait.
+template <uint32_t HINT_NS = 0>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* err,
                                           uint64_t timeout_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<HINT_NS>(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 0; it < (1u << 30); ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait<HINT_NS>(bar, parity)) return true;
         if ((it & 63u) == 63u && globaltimer_ns() - t0 > timeout_ns) break;
     }
     record_error(err, MOE_ERR_TIMEOUT);
@@ -258,6 +274,19 @@ __device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N]) {
 
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Two IEEE fp32 fmas in one packed instruction: d0 = fma(a0, b0, d0) and
+// d1 = fma(a1, b1, d1), each rounded once as fmaf would round it.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\t"
+        "mov.b64 pb, {%4, %5};\n\t"
+        "mov.b64 pd, {%0, %1};\n\t"
+        "fma.rn.f32x2 pd, pa, pb, pd;\n\t"
+        "mov.b64 {%0, %1}, pd;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 // Named barrier over `nthreads` threads (multiple of 32), id 1..15.

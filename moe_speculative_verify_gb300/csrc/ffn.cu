@@ -78,6 +78,11 @@ struct FfnCfg {
                                      : (ACC_BUFS * ACC_COLS <= 128) ? 128
                                      : (ACC_BUFS * ACC_COLS <= 256) ? 256 : 512;
     static_assert(ACC_BUFS * ACC_COLS <= 512, "tensor memory");
+    // suspend-time hint of the role loops' barrier waits: at 32- and 64-row
+    // tiles waiting warps then leave their issue slots to the epilogue warps
+    // (measured: decode512's GEMMs 1.259 -> 1.220 ms, prefill4096's 4.09 ->
+    // 4.02); at 16-row tiles, where the HBM stream bounds the kernel, none
+    static constexpr uint32_t WAIT_HINT_NS = (NT >= 32) ? 20000u : 0u;
     static_assert(ACC_BUFS % 2 == 0, "the MMA checks TMEM partials in pairs");
 };
 
@@ -333,7 +338,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             auto wait_free = [&](int s) -> bool {
                 const uint32_t jj = used_by[s];
                 return jj == ~0u ||
-                       mbar_wait(&kbrel[jj % kKbRing], (jj / kKbRing) & 1u, p.err, p.timeout_ns);
+                       mbar_wait<C::WAIT_HINT_NS>(&kbrel[jj % kKbRing], (jj / kKbRing) & 1u, p.err, p.timeout_ns);
             };
             auto publish = [&](uint32_t k, int t, const Tile& tl, const int4& it) {
                 TileEntry& en = tq[k % kTq];
@@ -453,7 +458,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             bool ok = true;
             for (uint32_t kq = 0; ok; ++kq) {
                 if (*s_abort ||
-                    !mbar_wait(&tq_full[kq % kTq], (kq / kTq) & 1u, p.err, p.timeout_ns)) {
+                    !mbar_wait<C::WAIT_HINT_NS>(&tq_full[kq % kTq], (kq / kTq) & 1u, p.err, p.timeout_ns)) {
                     ok = false;
                     break;
                 }
@@ -469,9 +474,9 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                     if ((jk & 1u) != mine) continue;
                     const uint32_t ab = jk % C::ACC_BUFS;
                     if (*s_abort ||
-                        !mbar_wait(&acc_empty[ab], ((jk / C::ACC_BUFS) & 1u) ^ 1u, p.err,
+                        !mbar_wait<C::WAIT_HINT_NS>(&acc_empty[ab], ((jk / C::ACC_BUFS) & 1u) ^ 1u, p.err,
                                    p.timeout_ns) ||
-                        !mbar_wait(&kbfull[jk % kKbRing], (jk / kKbRing) & 1u, p.err, p.timeout_ns)) {
+                        !mbar_wait<C::WAIT_HINT_NS>(&kbfull[jk % kKbRing], (jk / kKbRing) & 1u, p.err, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
@@ -507,7 +512,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
         for (uint32_t kq = 0;; ++kq) {
             // the tile's queue entry, then: the previous tile's readers are
             // done with the scale / tile buffers
-            if (ok && !mbar_wait(&tq_full[kq % kTq], (kq / kTq) & 1u, p.err, p.timeout_ns))
+            if (ok && !mbar_wait<C::WAIT_HINT_NS>(&tq_full[kq % kTq], (kq / kTq) & 1u, p.err, p.timeout_ns))
                 ok = false;
             ok = epi_bar_and(ok, C::EPI_THREADS);
             if (!ok) break;
@@ -606,7 +611,6 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             constexpr int CW = C::CW;
             // columns per TMEM load: 8 in the 18-warp blocks (96 registers a
             // thread), else up to 16
-            constexpr int CH = (C::EPI_WARPS >= 16 || CW < 16) ? 8 : 16;
             float acc0[CW], acc1[CW];
 #pragma unroll
             for (int j = 0; j < CW; ++j) {
@@ -615,56 +619,50 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             }
             for (int kb = 0; kb < KB && ok; ++kb) {
                 // a failed wait is acted on by the whole warp (tcgen05.ld is warp-wide)
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&kbrel[je % kKbRing], (je / kKbRing) & 1u,
-                                                       p.err, p.timeout_ns))) {
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait<C::WAIT_HINT_NS>(
+                                                 &kbrel[je % kKbRing], (je / kKbRing) & 1u, p.err,
+                                                 p.timeout_ns))) {
                     ok = false;
                     *s_abort = 1;
                     break;
                 }
                 tc_fence_after();
-                // CH columns at a time: the TMEM loads of a chunk, then its FMAs
-#pragma unroll
-                for (int hc = 0; hc < CW / CH; ++hc) {
-                    const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) +
-                                        ab * C::ACC_COLS + cg * CW + hc * CH;
-                    float v0[CH], v1[CH];
-                    tmem_ld<CH>(ta, v0);
-                    if (C::NA == 2 && tl.gu) tmem_ld<CH>(ta + NT, v1);
-                    tmem_wait_ld();
-                    const float4* q0 =
-                        reinterpret_cast<const float4*>(s_sc + kb * NT + cg * CW + hc * CH);
-                    if (C::NA == 2 && tl.gu) {
-                        const float4* q1 = reinterpret_cast<const float4*>(
-                            s_sc + (KB + kb) * NT + cg * CW + hc * CH);
-#pragma unroll
-                        for (int v = 0; v < CH / 4; ++v) {
-                            const float4 a4 = q0[v], b4 = q1[v];
-                            float* a0p = &acc0[hc * CH + 4 * v];
-                            float* a1p = &acc1[hc * CH + 4 * v];
-                            a0p[0] = fmaf(v0[4 * v], a4.x, a0p[0]);
-                            a0p[1] = fmaf(v0[4 * v + 1], a4.y, a0p[1]);
-                            a0p[2] = fmaf(v0[4 * v + 2], a4.z, a0p[2]);
-                            a0p[3] = fmaf(v0[4 * v + 3], a4.w, a0p[3]);
-                            a1p[0] = fmaf(v1[4 * v], b4.x, a1p[0]);
-                            a1p[1] = fmaf(v1[4 * v + 1], b4.y, a1p[1]);
-                            a1p[2] = fmaf(v1[4 * v + 2], b4.z, a1p[2]);
-                            a1p[3] = fmaf(v1[4 * v + 3], b4.w, a1p[3]);
-                        }
-                    } else {
-#pragma unroll
-                        for (int v = 0; v < CH / 4; ++v) {
-                            const float4 a4 = q0[v];
-                            float* a0p = &acc0[hc * CH + 4 * v];
-                            a0p[0] = fmaf(v0[4 * v], a4.x, a0p[0]);
-                            a0p[1] = fmaf(v0[4 * v + 1], a4.y, a0p[1]);
-                            a0p[2] = fmaf(v0[4 * v + 2], a4.z, a0p[2]);
-                            a0p[3] = fmaf(v0[4 * v + 3], a4.w, a0p[3]);
-                        }
-                    }
-                }
+                // the warp's CW columns of the partial(s) in one round trip to
+                // tensor memory; the partial is handed back to the MMA as soon
+                // as it sits in registers, before the FMAs
+                const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) +
+                                    ab * C::ACC_COLS + cg * CW;
+                float v0[CW], v1[CW];
+                tmem_ld<CW>(ta, v0);
+                if (C::NA == 2 && tl.gu) tmem_ld<CW>(ta + NT, v1);
+                tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[ab]);
+                // acc = fma(partial, weight scale x row scale, acc), two
+                // columns per packed instruction (each an IEEE fma)
+                const float4* q0 = reinterpret_cast<const float4*>(s_sc + kb * NT + cg * CW);
+                if (C::NA == 2 && tl.gu) {
+                    const float4* q1 = reinterpret_cast<const float4*>(s_sc + (KB + kb) * NT + cg * CW);
+#pragma unroll
+                    for (int v = 0; v < CW / 4; ++v) {
+                        const float4 a4 = q0[v], b4 = q1[v];
+                        float* a0p = &acc0[4 * v];
+                        float* a1p = &acc1[4 * v];
+                        fma2(a0p[0], a0p[1], v0[4 * v], v0[4 * v + 1], a4.x, a4.y);
+                        fma2(a0p[2], a0p[3], v0[4 * v + 2], v0[4 * v + 3], a4.z, a4.w);
+                        fma2(a1p[0], a1p[1], v1[4 * v], v1[4 * v + 1], b4.x, b4.y);
+                        fma2(a1p[2], a1p[3], v1[4 * v + 2], v1[4 * v + 3], b4.z, b4.w);
+                    }
+                } else {
+#pragma unroll
+                    for (int v = 0; v < CW / 4; ++v) {
+                        const float4 a4 = q0[v];
+                        float* a0p = &acc0[4 * v];
+                        fma2(a0p[0], a0p[1], v0[4 * v], v0[4 * v + 1], a4.x, a4.y);
+                        fma2(a0p[2], a0p[3], v0[4 * v + 2], v0[4 * v + 3], a4.z, a4.w);
+                    }
+                }
                 ++je;
                 if (++ab == C::ACC_BUFS) ab = 0;
             }
@@ -678,9 +676,12 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                     const float sg = kFastSilu ? __fdividef(g, 1.0f + __expf(-g))
                                                : g / (1.0f + __expf(-g));
                     h[j] = (c < nrow) ? sg * acc1[j] : 0.0f;
-                    float a = fabsf(h[j]);
-#pragma unroll
-                    for (int d = 16; d >= 1; d >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, d));
+                    // amax over the warp's 32 features in one instruction:
+                    // non-negative floats order as their bit patterns (a NaN
+                    // counts as 0, as fmaxf would skip it)
+                    const float ah = fabsf(h[j]);
+                    const float a = __uint_as_float(__reduce_max_sync(
+                        0xFFFFFFFFu, (ah == ah) ? __float_as_uint(ah) : 0u));
                     if (lane == 0) s_red[q * NT + c] = a;
                 }
                 ok = epi_bar_and(ok, C::EPI_THREADS);

@@ -16,10 +16,14 @@ struct UnionLayout {
 inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 
 // Rows per GEMM work item: the MMA N dimension, fixed by the row count of the
-// call (a graph captured at R always replays the same kernels).
+// call (a graph captured at R always replays the same kernels).  Above 256
+// rows the 64-row tile: experts hit by hundreds of rows (Zipf-skewed decode
+// batches) are cut into half as many items, each of which streams the
+// expert's weights to its SM again (measured at 512 rows: layer 1.331 ->
+// 1.284 ms against 32-row tiles).
 inline int rows_per_item(int32_t R) {
     if (R <= 64) return 16;
-    if (R <= 512) return 32;
+    if (R <= 256) return 32;
     return 64;
 }
 
