@@ -134,7 +134,7 @@ __host__ __device__ inline FfnSmem ffn_smem(int nt, int n_stages, int kbmax, int
     s.sc = b;
     b += 2 * kbmax * nt * 4;
     s.red = b;
-    b += 4 * nt * 4;
+    b += 5 * nt * 4;
     s.tile = b;
     b += nt * 128;
     s.src = b;
@@ -237,7 +237,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
     uint8_t* st_base = smem + L.stages;
     // per-tile scale table: weight block scale x row scale, [operand][kb][n]
     float* s_sc = reinterpret_cast<float*>(smem + L.sc);
-    float* s_red = reinterpret_cast<float*>(smem + L.red);   // [4][NT]
+    float* s_red = reinterpret_cast<float*>(smem + L.red);   // [4][NT] amax parts, [NT] h scales
     uint8_t* s_tile = smem + L.tile;                         // [NT][128]
     int* s_src = reinterpret_cast<int*>(smem + L.src);       // [NT]
     uint64_t* kbfull = reinterpret_cast<uint64_t*>(smem + L.bars);   // [kKbRing] operands landed
@@ -306,7 +306,9 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             // Stage j of a tile: gate/up tiles alternate gate and up weight
             // tiles per K-block (j = 2*kb + {0, 1}); down tiles one per K-block.
             // stage j of a tile belongs to the CTA's K-block kbj; its first
-            // stage arms the K-block's barrier with the bytes of all its stages
+            // stage arms the K-block's barrier with the bytes of all its
+            // stages.  A gate/up K-block's row tile is loaded once, into its
+            // gate stage, and both of its MMAs read it there.
             auto a_load = [&](const Tile& tl, const int4& it, int j, int s, uint32_t kbj) {
                 const bool sh = it.x == p.E;
                 const int ex = sh ? 0 : it.x;
@@ -314,7 +316,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                 const uint64_t pol = tl.shared_w ? pol_shared : pol_once;
                 uint64_t* bar = &kbfull[kbj % kKbRing];
                 if (!tl.gu || (j & 1) == 0)
-                    mbar_arrive_expect_tx(bar, (tl.gu ? 2 : 1) * C::STAGE_BYTES);
+                    mbar_arrive_expect_tx(bar, tl.gu ? 2 * C::A_BYTES + C::B_BYTES : C::STAGE_BYTES);
                 if (tl.gu) {
                     const CUtensorMap* m = (j & 1) ? (sh ? &map_su : &map_u) : (sh ? &map_sg : &map_g);
                     const int2 c = wbox(p.tiled, ex * p.I + tl.blk * kBlock, j >> 1, p.H / kBlock);
@@ -325,6 +327,7 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                 }
             };
             auto b_load = [&](const Tile& tl, const int4& it, int j, int s, uint32_t kbj) {
+                if (tl.gu && (j & 1)) return;   // the up stage reads the gate stage's rows
                 const int kb = tl.gu ? (j >> 1) : j;
                 tma_load_2d(st_base + s * C::STAGE_BYTES + C::B_OFF, tl.gu ? &map_x : &map_h,
                             &kbfull[kbj % kKbRing], kb * kBlock, it.y);
@@ -483,9 +486,10 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                     tc_fence_after();
                     const uint32_t d0 = tmem + ab * C::ACC_COLS;
                     int st = s0;
+                    // the K-block's row tile sits in its first stage
+                    const uint32_t bb = smem_u32(st_base + s0 * C::STAGE_BYTES) + C::B_OFF;
                     for (int op = 0; op < nst; ++op) {
                         const uint32_t a0 = smem_u32(st_base + st * C::STAGE_BYTES);
-                        const uint32_t bb = a0 + C::B_OFF;
                         const uint32_t d = d0 + op * NT;
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
@@ -686,14 +690,20 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                 }
                 ok = epi_bar_and(ok, C::EPI_THREADS);
                 if (!ok) break;
+                // each row's scale once: amax over the four lane quarters, / 448
+                if (et < NT) {
+                    const float amax = fmaxf(fmaxf(s_red[et], s_red[NT + et]),
+                                             fmaxf(s_red[2 * NT + et], s_red[3 * NT + et]));
+                    const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+                    s_red[4 * NT + et] = sc;
+                    if (et < nrow) p.hs[size_t(row0 + et) * MB + tl.blk] = sc;
+                }
+                ok = epi_bar_and(ok, C::EPI_THREADS);
+                if (!ok) break;
 #pragma unroll
                 for (int j = 0; j < CW; ++j) {
                     const int c = cg * CW + j;
-                    const float amax = fmaxf(fmaxf(s_red[c], s_red[NT + c]),
-                                             fmaxf(s_red[2 * NT + c], s_red[3 * NT + c]));
-                    const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
-                    s_tile[c * 128 + m] = to_e4m3(__fdiv_rn(h[j], sc));
-                    if (m == 0 && c < nrow) p.hs[size_t(row0 + c) * MB + tl.blk] = sc;
+                    s_tile[c * 128 + m] = to_e4m3(__fdiv_rn(h[j], s_red[4 * NT + c]));
                 }
                 ok = epi_bar_and(ok, C::EPI_THREADS);
                 if (!ok) break;
