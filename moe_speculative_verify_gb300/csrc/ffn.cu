@@ -88,7 +88,8 @@ struct FfnCfg {
 
 constexpr int kMaxStages = 16;
 constexpr int kStagesNt16 = 8;   // ring depth where the weight stream counts (see launch_ffn_t)
-constexpr int kStagesWide = 6;   // ring depth of the separate kernels at 64-row tiles
+constexpr int kStagesWide = 6;        // ring depth of the separate kernels at 64-row tiles ...
+constexpr int kStagesWideDecode = 7;  // ... and in calls of at most 512 rows
 // Per K-block (not per stage) synchronisation, on two rings of barriers
 // indexed by the CTA's K-block counter j:
 //   kbfull[j % kKbRing] -- the K-block's operands have landed: the producer
@@ -781,11 +782,12 @@ static cudaError_t launch_ffn_t(const FfnMaps& mp, FfnArgs args, int n_sms, int 
     // HBM streams 16 KB tiles fastest with about 8 of them in flight per SM
     // (a TMA probe: 7.2 TB/s at 6-8, 6.5 at 12).  Measured: 8 stages are
     // faster at 16-row tiles and in the separate gate/up and down kernels at
-    // 32 rows, 6 in those at 64 rows; the fused kernel at 32 and 64 rows keeps
-    // every stage that fits.
+    // 32 rows; in those at 64 rows 7 up to 512 rows (decode512's GEMMs 1.141
+    // -> 1.125 ms) and 6 above (prefill4096's 3.92 -> 3.82 ms); the fused
+    // kernel at 32 and 64 rows keeps every stage that fits.
     int stages = kMaxStages;
     if (NT == 16 || (MODE != kFfnFused && NT == 32)) stages = kStagesNt16;
-    if (MODE != kFfnFused && NT == 64) stages = kStagesWide;
+    if (MODE != kFfnFused && NT == 64) stages = (args.R <= 512) ? kStagesWideDecode : kStagesWide;
     FfnSmem L = ffn_smem(NT, stages, kbmax, C::STAGE_BYTES);
     while (stages > 2 && L.bytes > smem_limit) {
         --stages;

@@ -105,18 +105,30 @@ __global__ void __launch_bounds__(MAXT, MINB) router_logits_kernel(
     }
 }
 
-// Large-R variant: a block computes a tile of 32 rows x 32 experts with 16
-// warps; the warp (wr, we) owns rows 8*wr.. and experts 8*we.. (64 pairs) and
-// lane l of the warp is lane l of the reduction tree for every one of them.
-// Per 128-column step the block stages x (bf16) and w (fp32) in shared memory
+// Large-R variant: a block computes a tile of 32 rows x 32 experts; the warp
+// (wr, we) owns rows 8*wr.. and PE experts from PE*we.. (8*PE pairs) and lane
+// l of the warp is lane l of the reduction tree for every one of them.  Per
+// 128-column step the block stages x (bf16) and w (fp32) in shared memory
 // through a ring of kTileStages buffers filled by cp.async (kTileStages - 1
-// steps in flight); a thread accumulates its 64 lane partials of the current
+// steps in flight); a thread accumulates its lane partials of the current
 // 1024-column chunk in registers (fma in column order), folds them into the
 // per-lane chunk sums in shared memory at the end of each chunk (q = p for the
 // first chunk, then q = q + p), and the warp finishes every pair with the xor
 // butterfly: the same IEEE operations in the same order as the small-R kernel.
-constexpr int kTileR = 32, kTileE = 32, kTileThreads = 512, kTileStages = 4;
+// A larger PE reads each x and w value from shared memory for more fmas:
+// measured at 4096 rows, 16 experts a thread (8 warps, 220 registers) took
+// the prefill layer from 4.597 to 4.522 ms against 8 (16 warps).
+constexpr int kTileR = 32, kTileE = 32, kTileStages = 4;
 constexpr int kTileXBytes = kTileR * 128 * 2, kTileWBytes = kTileE * 128 * 4;
+constexpr int kTilePE = 16;   // experts per thread
+
+template <int PE>
+struct RouterTile {
+    static constexpr int WARPS = 4 * (kTileE / PE);
+    static constexpr int THREADS = 32 * WARPS;
+    static constexpr size_t SMEM = size_t(kTileStages) * (kTileXBytes + kTileWBytes) +
+                                   size_t(WARPS) * 8 * PE * 32 * 4;
+};
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
@@ -130,31 +142,38 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__global__ void __launch_bounds__(kTileThreads, 1) router_logits_tiled_kernel(
+template <int PE>
+__global__ void __launch_bounds__(RouterTile<PE>::THREADS, 1) router_logits_tiled_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ wr,
     const uint8_t* __restrict__ row_valid, int R, int H, int E, float* __restrict__ logits) {
+    constexpr int NTH = RouterTile<PE>::THREADS;
+    constexpr int EG = kTileE / PE;   // expert groups of the warp grid
     extern __shared__ __align__(16) uint8_t rsm[];
     uint16_t* xs = reinterpret_cast<uint16_t*>(rsm);                                // [S][32][128]
     float* wsm = reinterpret_cast<float*>(rsm + kTileStages * kTileXBytes);         // [S][32][128]
-    float* qsm = wsm + kTileStages * kTileE * 128;                                  // [16 warps][64][32]
+    float* qsm = wsm + kTileStages * kTileE * 128;                                  // [warps][8*PE][32]
     pdl_wait();
     pdl_launch_dependents();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wrow = (warp >> 2) * 8, wexp = (warp & 3) * 8;
+    const int wrow = (warp / EG) * 8, wexp = (warp % EG) * PE;
     const int r0 = blockIdx.y * kTileR, e0 = blockIdx.x * kTileE;
     const int steps = H / 128;
 
-    // Step i's tiles into ring buffer i % kTileStages: x is 512 x 16 bytes (one
-    // copy per thread), w 1024 x 16 bytes (two per thread).
-    const int xrow = tid >> 4, xc = (tid & 15) * 8;
-    const uint16_t* xsrc = x + size_t(min(r0 + xrow, R - 1)) * H + xc;
+    // Step i's tiles into ring buffer i % kTileStages: x is 512 x 16 bytes, w
+    // 1024 x 16 bytes, spread over the block's threads.
     auto issue = [&](int i) {
         if (i < steps) {
             const int buf = i % kTileStages;
-            cp_async16(xs + (buf * kTileR + xrow) * 128 + xc, xsrc + i * 128);
 #pragma unroll
-            for (int u = 0; u < kTileE * 32 / kTileThreads; ++u) {
-                const int q = tid + u * kTileThreads;
+            for (int u = 0; u < kTileR * 16 / NTH; ++u) {
+                const int q = tid + u * NTH;
+                const int xrow = q >> 4, xc = (q & 15) * 8;
+                cp_async16(xs + (buf * kTileR + xrow) * 128 + xc,
+                           x + size_t(min(r0 + xrow, R - 1)) * H + i * 128 + xc);
+            }
+#pragma unroll
+            for (int u = 0; u < kTileE * 32 / NTH; ++u) {
+                const int q = tid + u * NTH;
                 const int ex = q >> 5, c = (q & 31) * 4;
                 const int e = min(e0 + ex, E - 1);
                 cp_async16(wsm + (buf * kTileE + ex) * 128 + c, wr + size_t(e) * H + i * 128 + c);
@@ -163,7 +182,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) router_logits_tiled_kernel(
         cp_async_commit();   // one group per step, empty past the end: uniform counting
     };
 
-    float p[8][8];
+    float p[8][PE];
 #pragma unroll
     for (int i = 0; i < kTileStages - 1; ++i) issue(i);
     for (int i = 0; i < steps; ++i) {
@@ -175,13 +194,13 @@ __global__ void __launch_bounds__(kTileThreads, 1) router_logits_tiled_kernel(
 #pragma unroll
             for (int a = 0; a < 8; ++a)
 #pragma unroll
-                for (int b = 0; b < 8; ++b) p[a][b] = 0.0f;
+                for (int b = 0; b < PE; ++b) p[a][b] = 0.0f;
         }
-        // all eight experts' columns held, each row's x read and widened
-        // once; every pair's four fmas stay in column order
-        float4 wv[8];
+        // all PE experts' columns held, each row's x read and widened once;
+        // every pair's four fmas stay in column order
+        float4 wv[PE];
 #pragma unroll
-        for (int b = 0; b < 8; ++b)
+        for (int b = 0; b < PE; ++b)
             wv[b] = *reinterpret_cast<const float4*>(wsm + (buf * kTileE + wexp + b) * 128 + 4 * lane);
 #pragma unroll
         for (int a = 0; a < 8; ++a) {
@@ -190,7 +209,7 @@ __global__ void __launch_bounds__(kTileThreads, 1) router_logits_tiled_kernel(
             const float x0 = bf16_bits_to_f32(xv.x & 0xFFFFu), x1 = bf16_bits_to_f32(xv.x >> 16);
             const float x2 = bf16_bits_to_f32(xv.y & 0xFFFFu), x3 = bf16_bits_to_f32(xv.y >> 16);
 #pragma unroll
-            for (int b = 0; b < 8; ++b) {
+            for (int b = 0; b < PE; ++b) {
                 float q = p[a][b];
                 q = __fmaf_rn(x0, wv[b].x, q);
                 q = __fmaf_rn(x1, wv[b].y, q);
@@ -200,24 +219,24 @@ __global__ void __launch_bounds__(kTileThreads, 1) router_logits_tiled_kernel(
             }
         }
         if ((i & 7) == 7 || i + 1 == steps) {   // end of a 1024-column chunk
-            float* qw = qsm + size_t(warp) * 64 * 32;
+            float* qw = qsm + size_t(warp) * 8 * PE * 32;
             const bool first = (i < 8);
 #pragma unroll
             for (int a = 0; a < 8; ++a)
 #pragma unroll
-                for (int b = 0; b < 8; ++b) {
-                    float* slot = qw + (a * 8 + b) * 32 + lane;
+                for (int b = 0; b < PE; ++b) {
+                    float* slot = qw + (a * PE + b) * 32 + lane;
                     *slot = first ? p[a][b] : __fadd_rn(*slot, p[a][b]);
                 }
         }
     }
     cp_async_wait<0>();
-    const float* qw = qsm + size_t(warp) * 64 * 32;
-    for (int pair = 0; pair < 64; ++pair) {
+    const float* qw = qsm + size_t(warp) * 8 * PE * 32;
+    for (int pair = 0; pair < 8 * PE; ++pair) {
         float q = qw[pair * 32 + lane];
 #pragma unroll
         for (int d = 16; d >= 1; d >>= 1) q = __fadd_rn(q, __shfl_xor_sync(0xFFFFFFFFu, q, d));
-        const int r = r0 + wrow + pair / 8, e = e0 + wexp + pair % 8;
+        const int r = r0 + wrow + pair / PE, e = e0 + wexp + pair % PE;
         if (lane == 0 && r < R && e < E && (row_valid == nullptr || row_valid[r] != 0))
             logits[size_t(r) * E + e] = q;
     }
@@ -267,14 +286,13 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const uint8
         if (e != cudaSuccess) return e;
     } else {
         dim3 grid((E + kTileE - 1) / kTileE, (R + kTileR - 1) / kTileR);
-        const size_t smem = size_t(kTileStages) * (kTileXBytes + kTileWBytes) +
-                            size_t(kTileThreads / 32) * 64 * 32 * 4;
-        cudaError_t e = cudaFuncSetAttribute(router_logits_tiled_kernel,
+        using T = RouterTile<kTilePE>;
+        cudaError_t e = cudaFuncSetAttribute(router_logits_tiled_kernel<kTilePE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+                                             static_cast<int>(T::SMEM));
         if (e != cudaSuccess) return e;
-        e = launch_pdl(router_logits_tiled_kernel, grid, dim3(kTileThreads), smem, stream, x, wr,
-                       row_valid, R, H, E, logits);
+        e = launch_pdl(router_logits_tiled_kernel<kTilePE>, grid, dim3(T::THREADS), T::SMEM, stream,
+                       x, wr, row_valid, R, H, E, logits);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
