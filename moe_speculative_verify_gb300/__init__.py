@@ -65,13 +65,17 @@ class Weights(C.Structure):
     def from_tensors(cls, t: dict, layout: int = LAYOUT_ROW_MAJOR) -> "Weights":
         """From a dict with w_gate/s_gate/... and sh_gate/sh_s_gate/... tensors
         whose code tensors are in the given layout (tile_weights makes a tiled
-        dict)."""
+        dict).  The result holds references to those tensors, so the device
+        memory its pointers name stays allocated while it exists."""
         def p(k):
             v = t.get(k)
             return None if v is None else v.data_ptr()
-        return cls(p("w_gate"), p("w_up"), p("w_down"), p("s_gate"), p("s_up"), p("s_down"),
-                   p("sh_gate"), p("sh_up"), p("sh_down"), p("sh_s_gate"), p("sh_s_up"),
-                   p("sh_s_down"), layout)
+        w = cls(p("w_gate"), p("w_up"), p("w_down"), p("s_gate"), p("s_up"), p("s_down"),
+                p("sh_gate"), p("sh_up"), p("sh_down"), p("sh_s_gate"), p("sh_s_up"),
+                p("sh_s_down"), layout)
+        w._tensors = [t[k] for k in CODE_KEYS + ("s_gate", "s_up", "s_down", "sh_s_gate",
+                                                 "sh_s_up", "sh_s_down") if t.get(k) is not None]
+        return w
 
 
 _LIB: Optional[C.CDLL] = None
