@@ -14,10 +14,14 @@
 // (one CTA per SM):
 //   warp 0 lane 0: TMA producer -- e4m3 weight tiles (16 KB) into a ring of
 //                  staging buffers;
-//   warp 1 lane 0: MMA issuer -- 8 x tcgen05.mma kind::f16 (K = 16) per
-//                  128-wide K-block, A (the bf16 weight tile) from tensor
-//                  memory, B (the rows) from shared memory, into the tile's
-//                  accumulator (gate and up side by side for a gate/up tile);
+//   warps 1, 14 lane 0: MMA issuers, alternate steps -- 8 x tcgen05.mma
+//                  kind::f16 (K = 16) per 128-wide K-block, A (the bf16 weight
+//                  tile) from tensor memory, B (the rows) from shared memory,
+//                  into the tile's accumulator: gate (even steps) and up (odd)
+//                  side by side for a gate/up tile; for a down tile with an even
+//                  number of K-blocks the even and odd K-blocks into the two
+//                  halves, which the epilogue adds (one issuer for an odd
+//                  number);
 //   warps 2..9   : dequant, two groups of four on alternate steps -- a staged
 //                  tile to bf16, written straight into a tensor-memory
 //                  operand slot (tcgen05.st; the dequantised tile never
@@ -38,7 +42,11 @@ constexpr int kNT = kW8A16RowsPerItem;       // rows per item (MMA N)
 constexpr int kDqWarps = 8;                  // two groups of four, alternate steps
 constexpr int kDqGroupWarps = 4;
 constexpr int kEpiWarps = 4;
-constexpr int kThreads16 = 32 * (2 + kDqWarps + kEpiWarps);
+// warp 0 producer, warp 1 MMA issuer, dequant warps, epilogue warps, second
+// MMA issuer (measured: one thread issuing these small-N MMAs was busy 60 % of
+// the kernel, ~107 cycles per MMA, and set the pace)
+constexpr int kMma2Warp = 2 + kDqWarps + kEpiWarps;
+constexpr int kThreads16 = 32 * (3 + kDqWarps + kEpiWarps);
 constexpr int kWBytes = 128 * 128;           // e4m3 weight tile
 constexpr int kBBytes = kNT * 128 * 2;       // bf16 rows: two K halves of kNT x 128 B
 constexpr int kSlotBytes = kBBytes;          // shared-memory part of an operand slot
@@ -206,10 +214,10 @@ __global__ void __launch_bounds__(kThreads16, 1)
             mbar_init(&a_empty[s], 1);
         }
         for (int b = 0; b < kAccBufs; ++b) {
-            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_full[b], 2);   // one commit from each MMA issuer
             mbar_init(&acc_empty[b], kEpiWarps);
         }
-        mbar_init(drain, 1);
+        mbar_init(drain, 2);
         *s_abort = 0;
         fence_barrier_init();
         prefetch_tensormap(&map_g);
@@ -288,10 +296,13 @@ __global__ void __launch_bounds__(kThreads16, 1)
             }
             if (!ok) *s_abort = 1;
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == kMma2Warp) {
         if (lane == 0) {
-            // ------------------------------------------------- MMA issuer
+            // ------------------------------------------------ MMA issuers
+            // Both walk every step (slot positions); each waits for, issues
+            // and commits its own steps (a commit covers its thread's MMAs).
             constexpr uint32_t idesc = idesc_bf16_f32(128, kNT);
+            const int mine = (warp == 1) ? 0 : 1;
             int slot = 0, ab = 0;
             uint32_t sph = 0, aph = 0;
             bool ok = true;
@@ -303,27 +314,32 @@ __global__ void __launch_bounds__(kThreads16, 1)
                     break;
                 }
                 const uint32_t d0 = tmem + ab * kAccCols;
+                // steps split by parity over the two halves of the accumulator
+                const bool split = gu || (NS % 2) == 0;
                 for (int j = 0; j < NS; ++j) {
-                    if (*s_abort || !mbar_wait(&a_full[slot], sph, p.err, p.timeout_ns)) {
+                    const int s_cur = slot;
+                    const uint32_t ph = sph;
+                    if (++slot == kSlots) {
+                        slot = 0;
+                        sph ^= 1u;
+                    }
+                    if (split ? ((j & 1) != mine) : (mine != 0)) continue;
+                    if (*s_abort || !mbar_wait(&a_full[s_cur], ph, p.err, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = tmem + kAColBase + slot * kACols;
-                    const uint32_t b0 = smem_u32(slots + slot * kSlotBytes);
-                    const uint32_t d = d0 + (gu ? (j & 1) * kNT : 0);
-                    const bool first = gu ? (j < 2) : (j == 0);
+                    const uint32_t a0 = tmem + kAColBase + s_cur * kACols;
+                    const uint32_t b0 = smem_u32(slots + s_cur * kSlotBytes);
+                    const uint32_t d = d0 + (split ? (j & 1) * kNT : 0);
+                    const bool first = split ? (j < 2) : (j == 0);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         const uint32_t half = static_cast<uint32_t>(k >> 2), kk = k & 3;
                         mma_bf16_ts(d, a0 + 8 * k, sdesc_k_sw128(b0 + half * (kBBytes / 2) + 32 * kk),
                                     idesc, (first && k == 0) ? 0u : 1u);
                     }
-                    mma_commit(&a_empty[slot]);
-                    if (++slot == kSlots) {
-                        slot = 0;
-                        sph ^= 1u;
-                    }
+                    mma_commit(&a_empty[s_cur]);
                 }
                 if (!ok) break;
                 mma_commit(&acc_full[ab]);
@@ -470,9 +486,11 @@ __global__ void __launch_bounds__(kThreads16, 1)
             }
             tc_fence_after();
             const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + ab * kAccCols;
+            // gate and up, or a down tile's even- and odd-K-block halves
+            const bool split = tl.gu || (KB_I % 2) == 0;
             float g[kNT], u[kNT];
             tmem_ld16(ta, g);
-            if (tl.gu) tmem_ld16(ta + kNT, u);
+            if (split) tmem_ld16(ta + kNT, u);
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
@@ -505,7 +523,7 @@ __global__ void __launch_bounds__(kThreads16, 1)
                         const int r = slot / p.KS, k = slot - r * p.KS;
                         float* dst = (k < p.K) ? p.y_slots + (size_t(r) * p.K + k) * p.H
                                                : p.y_shared + size_t(r) * p.H;
-                        dst[tl.blk * kBlock + m] = g[c];
+                        dst[tl.blk * kBlock + m] = split ? __fadd_rn(g[c], u[c]) : g[c];
                     }
                 }
             }
@@ -523,6 +541,7 @@ __global__ void __launch_bounds__(kThreads16, 1)
             const uint64_t t0 = globaltimer_ns();
             while (globaltimer_ns() - t0 < kDrainNs) __nanosleep(1000);
         }
+        if (threadIdx.x == 32 * kMma2Warp) mma_commit(drain);
         if (threadIdx.x == 32) {
             mma_commit(drain);
             mbar_wait(drain, 0, nullptr, kDrainNs);
