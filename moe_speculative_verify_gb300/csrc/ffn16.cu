@@ -39,14 +39,20 @@ namespace moe {
 namespace {
 
 constexpr int kNT = kW8A16RowsPerItem;       // rows per item (MMA N)
-constexpr int kDqWarps = 8;                  // two groups of four, alternate steps
 constexpr int kDqGroupWarps = 4;
+// three groups of four, each taking every third step (measured: with two
+// groups the MMA issuers waited for converted tiles 45 % of the kernel)
+constexpr int kDqGroups = 3;
+constexpr int kDqWarps = kDqGroups * kDqGroupWarps;
 constexpr int kEpiWarps = 4;
 // warp 0 producer, warp 1 MMA issuer, dequant warps, epilogue warps, second
 // MMA issuer (measured: one thread issuing these small-N MMAs was busy 60 % of
 // the kernel, ~107 cycles per MMA, and set the pace)
 constexpr int kMma2Warp = 2 + kDqWarps + kEpiWarps;
 constexpr int kThreads16 = 32 * (3 + kDqWarps + kEpiWarps);
+// registers a thread for one block per SM: each SM sub-partition holds 16K
+// registers and ceil(warps / 4) of the block's warps; in steps of 8
+constexpr int kMaxRegs16 = (16384 / (((kThreads16 / 32 + 3) / 4) * 32)) / 8 * 8;
 constexpr int kWBytes = 128 * 128;           // e4m3 weight tile
 constexpr int kBBytes = kNT * 128 * 2;       // bf16 rows: two K halves of kNT x 128 B
 constexpr int kSlotBytes = kBBytes;          // shared-memory part of an operand slot
@@ -178,7 +184,7 @@ __device__ __forceinline__ Tile16 tile16_of(int t, int n_gu, int mb_i, int mb_h,
     return x;
 }
 
-__global__ void __launch_bounds__(kThreads16, 1)
+__global__ void __maxnreg__(kMaxRegs16)
     ffn16_kernel(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUtensorMap map_u,
                  const __grid_constant__ CUtensorMap map_sg, const __grid_constant__ CUtensorMap map_su,
                  const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_d,
@@ -352,8 +358,9 @@ __global__ void __launch_bounds__(kThreads16, 1)
         }
     } else if (warp < 2 + kDqWarps) {
         // --------------------------------------------------------- dequant
-        // Two groups of four warps take alternate steps of the CTA's step
-        // sequence, so two staged tiles are converted at once.  In a group,
+        // kDqGroups groups of four warps take turns over the CTA's step
+        // sequence (group g the steps g, g + kDqGroups, ...), so that many
+        // staged tiles are converted at once.  In a group,
         // warp w converts rows 32*(w%4) .. +31 (the TMEM lanes it may access)
         // of the tile: per thread the 128 codes of its row, read from the
         // swizzled stage, written as 64 bf16x2 columns.
@@ -362,7 +369,7 @@ __global__ void __launch_bounds__(kThreads16, 1)
         const int qd = warp & 3;
         const int row = 32 * qd + lane;
         const bool leader = (dw % kDqGroupWarps) == 0 && lane == 0;
-        uint32_t n = 0;              // the CTA's step counter (both groups count every step)
+        uint32_t n = 0;              // the CTA's step counter (every group counts every step)
         bool ok = true;
         pdl_wait();   // gathered rows and the counters belong to the previous kernel
         for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
@@ -382,18 +389,18 @@ __global__ void __launch_bounds__(kThreads16, 1)
             };
             bool h_ready = tl.gu;
             // this group's first step of the tile
-            const int j0 = static_cast<int>((static_cast<uint32_t>(grp) - n) & 1u);
+            const int j0 = (grp - static_cast<int>(n % kDqGroups) + kDqGroups) % kDqGroups;
             float s_next = (j0 < NS) ? scale_of(j0) : 0.0f;
             // weight stage and phase of the group's step: divided out once
-            // per tile, then advanced two steps at a time
+            // per tile, then advanced kDqGroups steps at a time
             uint32_t nj = n + static_cast<uint32_t>(j0);
             int ws = static_cast<int>(nj % static_cast<uint32_t>(NW));
             uint32_t wph = (nj / static_cast<uint32_t>(NW)) & 1u;
-            for (int j = j0; j < NS; j += 2, nj += 2) {
+            for (int j = j0; j < NS; j += kDqGroups, nj += kDqGroups) {
                 const int slot = static_cast<int>(nj % kSlots);
                 const uint32_t sph = (nj / kSlots) & 1u;
                 const float s = s_next;
-                if (j + 2 < NS) s_next = scale_of(j + 2);
+                if (j + kDqGroups < NS) s_next = scale_of(j + kDqGroups);
                 // every wait's outcome is made uniform across the warp before use
                 bool got = !*s_abort && mbar_wait(&a_empty[slot], sph ^ 1u, p.err, p.timeout_ns);
                 if (!__all_sync(0xFFFFFFFFu, got)) {
@@ -455,7 +462,7 @@ __global__ void __launch_bounds__(kThreads16, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&a_full[slot]);
-                ws += 2;   // NW >= 2
+                ws += kDqGroups;   // NW >= kDqGroups
                 if (ws >= NW) {
                     ws -= NW;
                     wph ^= 1u;
@@ -599,7 +606,7 @@ cudaError_t launch_ffn16(const FfnMaps& mp, Ffn16Args args, int n_sms, int smem_
                          cudaStream_t stream) {
     int nw = kMaxWStages;
     Smem16 L = smem16(nw);
-    while (nw > 2 && L.bytes > smem_limit) L = smem16(--nw);
+    while (nw > kDqGroups && L.bytes > smem_limit) L = smem16(--nw);
     if (L.bytes > smem_limit) return cudaErrorInvalidConfiguration;
     args.n_wstages = nw;
     cudaError_t e = cudaFuncSetAttribute(ffn16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
