@@ -153,9 +153,13 @@ __device__ __forceinline__ uint2 dequant4(uint32_t w, float s) {
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"(hi));
     const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
     const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+    // code x scale, two per packed instruction (each an IEEE fp32 product)
+    float p0, p1, p2, p3;
+    mul2(p0, p1, f01.x, f01.y, s, s);
+    mul2(p2, p3, f23.x, f23.y, s, s);
     uint2 r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r.x) : "f"(__fmul_rn(f01.y, s)), "f"(__fmul_rn(f01.x, s)));
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r.y) : "f"(__fmul_rn(f23.y, s)), "f"(__fmul_rn(f23.x, s)));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r.x) : "f"(p1), "f"(p0));
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r.y) : "f"(p3), "f"(p2));
     return r;
 }
 
