@@ -220,6 +220,7 @@ moe::FfnArgs ffn_args(const moe_config_t* c, const moe_weights_t* w, const int32
     a.hs = f.hs;
     a.y_slots = y_slots;
     a.y_shared = y_shared;
+    a.out_vec = aligned(y_slots, 16) && (y_shared == nullptr || aligned(y_shared, 16));
     a.ready = f.ready;
     a.sched = f.sched;
     a.err = f.err;

@@ -55,6 +55,13 @@ struct FfnCfg {
     static constexpr int B_OFF = A_BYTES;
     static constexpr int B_BYTES = NT * 128;
     static constexpr int STAGE_BYTES = B_OFF + B_BYTES;
+    // a down tile's rows leave through shared memory as 16-byte stores at
+    // 16-row tiles (measured in one run: verify8's GEMM 0.2264 -> 0.2253 ms,
+    // verify64's 0.874 -> 0.872; at 64-row tiles the extra barrier cost more
+    // than the scattered stores, +0.8 %)
+    static constexpr bool STAGED_OUT = (NT == 16 && MODE != kFfnGateUp);
+    // shared-memory tile at a tile's end: h codes, and a down tile's fp32 rows
+    static constexpr int TILE_BYTES = STAGED_OUT ? NT * 128 * 4 : NT * 128;
     // columns per epilogue warp: 16 at 16- and 64-row tiles, 8 at 32-row
     // tiles (16 epilogue warps at 32 and 64 rows: the per-K-block promotion
     // is spread over as many warps as the block can hold)
@@ -127,7 +134,10 @@ struct FfnSmem {
     int stages, sc, red, tile, src, tq, bars, tmem, flag, bytes;
 };
 
-__host__ __device__ inline FfnSmem ffn_smem(int nt, int n_stages, int kbmax, int stage_bytes) {
+// tile_bytes: the h tile of a gate/up tile (nt x 128 e4m3 codes) or, in a
+// kernel with down tiles, the fp32 output tile (nt x 128 x 4 bytes).
+__host__ __device__ inline FfnSmem ffn_smem(int nt, int n_stages, int kbmax, int stage_bytes,
+                                             int tile_bytes) {
     FfnSmem s;
     int b = 0;
     s.stages = b;
@@ -137,7 +147,7 @@ __host__ __device__ inline FfnSmem ffn_smem(int nt, int n_stages, int kbmax, int
     s.red = b;
     b += 5 * nt * 4;
     s.tile = b;
-    b += nt * 128;
+    b += tile_bytes;
     s.src = b;
     b += nt * 4;
     b = (b + 15) & ~15;
@@ -234,12 +244,12 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
     const int KB_H = p.H / kBlock, KB_I = p.I / kBlock;   // K-blocks of gate/up, of down
     const int MB_I = p.I / kBlock, MB_H = p.H / kBlock;   // output blocks of gate/up, of down
     const int KBMAX = (MODE == kFfnGateUp) ? KB_H : (MODE == kFfnDown) ? KB_I : max(KB_H, KB_I);
-    const FfnSmem L = ffn_smem(NT, p.n_stages, KBMAX, C::STAGE_BYTES);
+    const FfnSmem L = ffn_smem(NT, p.n_stages, KBMAX, C::STAGE_BYTES, C::TILE_BYTES);
     uint8_t* st_base = smem + L.stages;
     // per-tile scale table: weight block scale x row scale, [operand][kb][n]
     float* s_sc = reinterpret_cast<float*>(smem + L.sc);
     float* s_red = reinterpret_cast<float*>(smem + L.red);   // [4][NT] amax parts, [NT] h scales
-    uint8_t* s_tile = smem + L.tile;                         // [NT][128]
+    uint8_t* s_tile = smem + L.tile;                         // [NT][128] codes or fp32
     int* s_src = reinterpret_cast<int*>(smem + L.src);       // [NT]
     uint64_t* kbfull = reinterpret_cast<uint64_t*>(smem + L.bars);   // [kKbRing] operands landed
     uint64_t* kbrel = kbfull + kKbRing;        // [kKbRing] K-block done (stages free, partial ready)
@@ -723,6 +733,22 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
                         atomicAdd(p.ready + tl.item, 1);
                     }
                 }
+            } else if (C::STAGED_OUT && p.out_vec) {
+                // the tile's rows through shared memory, then out as 16-byte
+                // stores, a row's 512 bytes by 32 consecutive threads
+                float* stg = reinterpret_cast<float*>(s_tile);   // [NT][128]
+#pragma unroll
+                for (int j = 0; j < CW; ++j) stg[(cg * CW + j) * kBlock + m] = acc0[j];
+                ok = epi_bar_and(ok, C::EPI_THREADS);
+                if (!ok) break;
+                for (int i = et; i < nrow * 32; i += C::EPI_THREADS) {
+                    const int c = i >> 5, v = i & 31;
+                    const int d = s_src[c];
+                    float* dst = (d >= 0) ? p.y_slots + size_t(d) * p.H
+                                          : p.y_shared + size_t(-1 - d) * p.H;
+                    reinterpret_cast<float4*>(dst + tl.blk * kBlock)[v] =
+                        reinterpret_cast<const float4*>(stg + c * kBlock)[v];
+                }
             } else {
 #pragma unroll
                 for (int j = 0; j < CW; ++j) {
@@ -788,10 +814,10 @@ static cudaError_t launch_ffn_t(const FfnMaps& mp, FfnArgs args, int n_sms, int 
     int stages = kMaxStages;
     if (NT == 16 || (MODE != kFfnFused && NT == 32)) stages = kStagesNt16;
     if (MODE != kFfnFused && NT == 64) stages = (args.R <= 512) ? kStagesWideDecode : kStagesWide;
-    FfnSmem L = ffn_smem(NT, stages, kbmax, C::STAGE_BYTES);
+    FfnSmem L = ffn_smem(NT, stages, kbmax, C::STAGE_BYTES, C::TILE_BYTES);
     while (stages > 2 && L.bytes > smem_limit) {
         --stages;
-        L = ffn_smem(NT, stages, kbmax, C::STAGE_BYTES);
+        L = ffn_smem(NT, stages, kbmax, C::STAGE_BYTES, C::TILE_BYTES);
     }
     if (L.bytes > smem_limit) return cudaErrorInvalidConfiguration;
     args.n_stages = stages;

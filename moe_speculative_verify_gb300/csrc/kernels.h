@@ -35,6 +35,7 @@ struct FfnArgs {
     float* hs;                 // h scales [rows, I/128]
     float* y_slots;            // [R*K, H]
     float* y_shared;           // [R, H]
+    int out_vec;               // y_slots and y_shared 16-byte aligned: rows stored 16 bytes at a time
     int32_t* ready;            // [max_items] gate/up blocks of h finished (fused mode)
     int32_t* sched;            // [2] tile counter, CTAs done claiming (zero between launches)
     int32_t* err;              // device error word
