@@ -316,6 +316,7 @@ moe_status_t ffn16_impl(const moe_config_t* c, const void* x, const moe_weights_
     a.y_slots = y_slots;
     a.y_shared = y_shared;
     a.ready = f.ready;
+    a.sched = f.sched;
     a.err = f.err;
     a.R = R;
     a.ushape = moe::union_shape_word(E, c->topk, S);

@@ -8,12 +8,13 @@
 // (one scale per 128x128 tile), the gathered rows and h stay bf16, and the
 // MMA accumulates the whole K of a tile in fp32 tensor memory.
 //
-// One persistent kernel over the tile queue of the fp8 path (gate/up tiles,
+// One persistent kernel over the tile order of the fp8 path (gate/up tiles,
 // then down tiles, entry-major; a down tile starts once every gate/up tile of
-// its item has stored its block of h), for items of up to 16 rows.  Warp roles
-// (one CTA per SM):
-//   warp 0 lane 0: TMA producer -- e4m3 weight tiles (16 KB) into a ring of
-//                  staging buffers;
+// its item has stored its block of h), for items of up to 16 rows, the tiles
+// handed out at run time as in the fp8 GEMM.  Warp roles (one CTA per SM):
+//   warp 0 lane 0: TMA producer -- claims the CTA's tiles and publishes them
+//                  to the other roles; e4m3 weight tiles (16 KB) into a ring
+//                  of staging buffers;
 //   warps 1, 14 lane 0: MMA issuers, alternate steps -- 8 x tcgen05.mma
 //                  kind::f16 (K = 16) per 128-wide K-block, A (the bf16 weight
 //                  tile) from tensor memory, B (the rows) from shared memory,
@@ -22,12 +23,12 @@
 //                  number of K-blocks the even and odd K-blocks into the two
 //                  halves, which the epilogue adds (one issuer for an odd
 //                  number);
-//   warps 2..9   : dequant, two groups of four on alternate steps -- a staged
+//   warps 2..13  : dequant, three groups of four taking turns -- a staged
 //                  tile to bf16, written straight into a tensor-memory
 //                  operand slot (tcgen05.st; the dequantised tile never
 //                  touches shared memory); the group's leader also loads the
 //                  K-block's 16 rows (bf16) into the slot's shared part;
-//   warps 10..13 : epilogue -- gate/up: h = silu(g) * u rounded to bf16, row
+//   warps 14..17 : epilogue -- gate/up: h = silu(g) * u rounded to bf16, row
 //                  stores; down: fp32 rows to their slot.
 // Every wait is bounded; a timeout records MOE_ERR_TIMEOUT and winds down.
 #include "common.cuh"
@@ -66,8 +67,22 @@ constexpr int kTmemCols = 512;
 static_assert(kAColBase + kSlots * kACols <= kTmemCols, "tensor memory");
 static_assert(kSlotBytes % 1024 == 0, "operand slots stay 1024-byte aligned");
 
+// Tiles are handed out at run time, as in the fp8 GEMM: a CTA's first tile
+// is its block index, every further one the producer claims from a global
+// counter one tile ahead and publishes into entry k % kTq16 of a shared-memory
+// queue (completing tq_full[k % kTq16]); the other roles read the entries in
+// order.  No role trails the producer by more than the weight ring, the
+// operand slots and the accumulators together (every tile has at least one
+// step), far below kTq16, so an entry is read before it is rewritten.
+constexpr int kTq16 = 64;
+
+struct TileEntry16 {
+    int t;               // tile index (>= the tile count: no more tiles)
+    int item, blk, gu;
+};
+
 struct Smem16 {
-    int slots, wst, bars, tmem, flag, bytes;
+    int slots, wst, tq, bars, tmem, flag, bytes;
 };
 
 __host__ __device__ inline Smem16 smem16(int n_w) {
@@ -77,8 +92,10 @@ __host__ __device__ inline Smem16 smem16(int n_w) {
     b += kSlots * kSlotBytes;
     s.wst = b;
     b += n_w * kWBytes;
+    s.tq = b;
+    b += kTq16 * static_cast<int>(sizeof(TileEntry16));
     s.bars = b;
-    b += (2 * n_w + 2 * kSlots + 2 * kAccBufs + 1) * 8;
+    b += (2 * n_w + 2 * kSlots + 2 * kAccBufs + 1 + kTq16) * 8;
     s.tmem = b;
     b += 4;
     s.flag = b;
@@ -210,6 +227,8 @@ __global__ void __maxnreg__(kMaxRegs16)
     uint64_t* acc_full = a_empty + kSlots;
     uint64_t* acc_empty = acc_full + kAccBufs;
     uint64_t* drain = acc_empty + kAccBufs;
+    uint64_t* tq_full = drain + 1;             // [kTq16] tile-queue entry written
+    TileEntry16* tq = reinterpret_cast<TileEntry16*>(smem + L.tq);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L.tmem);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L.flag);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -228,6 +247,7 @@ __global__ void __maxnreg__(kMaxRegs16)
             mbar_init(&acc_empty[b], kEpiWarps);
         }
         mbar_init(drain, 2);
+        for (int b = 0; b < kTq16; ++b) mbar_init(&tq_full[b], 1);
         *s_abort = 0;
         fence_barrier_init();
         prefetch_tensormap(&map_g);
@@ -261,22 +281,24 @@ __global__ void __maxnreg__(kMaxRegs16)
             int ws = 0;
             uint32_t wph = 0;
             bool ok = true;
-            bool waited = false;
-            int issued = 0;
-            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            auto publish = [&](uint32_t k, int t) {
+                TileEntry16& en = tq[k % kTq16];
+                en.t = t;
+                if (t < n_tiles) {
+                    const Tile16 tl = tile16_of(t, n_gu, MB_I, MB_H, items);
+                    en.item = tl.item;
+                    en.blk = tl.blk;
+                    en.gu = tl.gu ? 1 : 0;
+                }
+                mbar_arrive(&tq_full[k % kTq16]);
+            };
+            // one tile's weight steps j0 .. j1-1 into the ring
+            auto load_steps = [&](int t, int j0, int j1) {
                 const Tile16 tl = tile16_of(t, n_gu, MB_I, MB_H, items);
                 const int4 it = items[tl.item];
                 const bool sh = it.x == p.E;
                 const int ex = sh ? 0 : it.x;
-                const int NS = tl.gu ? 2 * KB_H : KB_I;
-                for (int j = 0; j < NS; ++j) {
-                    // weights are inputs of the layer: the first ring of them
-                    // is requested before the wait on the previous kernel
-                    if (!waited && issued == NW) {
-                        pdl_wait();
-                        pdl_launch_dependents();
-                        waited = true;
-                    }
+                for (int j = j0; j < j1; ++j) {
                     if (*s_abort || !mbar_wait(&w_empty[ws], wph ^ 1u, p.err, p.timeout_ns)) {
                         ok = false;
                         break;
@@ -293,16 +315,40 @@ __global__ void __maxnreg__(kMaxRegs16)
                                             p.I / kBlock);
                         tma_load_2d_hint(dst, sh ? &map_sd : &map_d, &w_full[ws], c.x, c.y, pol);
                     }
-                    ++issued;
                     if (++ws == NW) {
                         ws = 0;
                         wph ^= 1u;
                     }
                 }
+            };
+            const int t0 = blockIdx.x;
+            publish(0, t0);
+            // weights are inputs of the layer: the first tile's first ring of
+            // them is requested before the wait on the previous kernel (the
+            // tile counter is that kernel's output: tiles are claimed after)
+            int pre = 0;
+            if (t0 < n_tiles) {
+                const int NS0 = (t0 < n_gu) ? 2 * KB_H : KB_I;
+                pre = NS0 < NW ? NS0 : NW;
+                load_steps(t0, 0, pre);
             }
-            if (!waited) {
-                pdl_wait();
-                pdl_launch_dependents();
+            pdl_wait();
+            pdl_launch_dependents();
+            uint32_t kq = 0;
+            for (int t = t0; t < n_tiles && ok && !*s_abort; ++kq) {
+                const int tn = atomicAdd(p.sched, 1) + static_cast<int>(gridDim.x);
+                publish(kq + 1, tn);
+                const int NS = (t < n_gu) ? 2 * KB_H : KB_I;
+                load_steps(t, (kq == 0) ? pre : 0, NS);
+                t = tn;
+            }
+            // This CTA claims no more tiles; the last CTA to get here resets
+            // the counter (and this count) for the next launch on the workspace.
+            __threadfence();
+            if (atomicAdd(p.sched + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+                __threadfence();
+                atomicExch(p.sched, 0);
+                atomicExch(p.sched + 1, 0);
             }
             if (!ok) *s_abort = 1;
         }
@@ -316,8 +362,15 @@ __global__ void __maxnreg__(kMaxRegs16)
             int slot = 0, ab = 0;
             uint32_t sph = 0, aph = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-                const bool gu = t < n_gu;
+            for (uint32_t kq = 0; ok; ++kq) {
+                if (*s_abort ||
+                    !mbar_wait(&tq_full[kq % kTq16], (kq / kTq16) & 1u, p.err, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                const TileEntry16 en = tq[kq % kTq16];
+                if (en.t >= n_tiles) break;
+                const bool gu = en.gu != 0;
                 const int NS = gu ? 2 * KB_H : KB_I;
                 if (*s_abort || !mbar_wait(&acc_empty[ab], aph ^ 1u, p.err, p.timeout_ns)) {
                     ok = false;
@@ -376,8 +429,16 @@ __global__ void __maxnreg__(kMaxRegs16)
         uint32_t n = 0;              // the CTA's step counter (every group counts every step)
         bool ok = true;
         pdl_wait();   // gathered rows and the counters belong to the previous kernel
-        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-            const Tile16 tl = tile16_of(t, n_gu, MB_I, MB_H, items);
+        for (uint32_t kq = 0; ok; ++kq) {
+            bool got = !*s_abort &&
+                       mbar_wait(&tq_full[kq % kTq16], (kq / kTq16) & 1u, p.err, p.timeout_ns);
+            if (!__all_sync(0xFFFFFFFFu, got)) {
+                ok = false;
+                break;
+            }
+            const TileEntry16 en = tq[kq % kTq16];
+            if (en.t >= n_tiles) break;
+            const Tile16 tl{en.item, en.blk, en.gu != 0};
             const int4 it = items[tl.item];
             const bool sh = it.x == p.E;
             const int ex = sh ? 0 : it.x;
@@ -484,8 +545,16 @@ __global__ void __maxnreg__(kMaxRegs16)
         uint32_t aph = 0;
         bool ok = true;
         pdl_wait();
-        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-            const Tile16 tl = tile16_of(t, n_gu, MB_I, MB_H, items);
+        for (uint32_t kq = 0; ok; ++kq) {
+            const bool got_t = __all_sync(0xFFFFFFFFu, !*s_abort &&
+                mbar_wait(&tq_full[kq % kTq16], (kq / kTq16) & 1u, p.err, p.timeout_ns));
+            if (!bar_and(1, got_t, 32 * kEpiWarps)) {
+                ok = false;
+                break;
+            }
+            const TileEntry16 en = tq[kq % kTq16];
+            if (en.t >= n_tiles) break;
+            const Tile16 tl{en.item, en.blk, en.gu != 0};
             const int4 it = items[tl.item];
             const int row0 = it.y, nrow = it.z;
             // all four epilogue warps learn of a failed wait together

@@ -62,6 +62,7 @@ struct Ffn16Args {
     float* y_slots;            // [R*K, H]
     float* y_shared;           // [R, H]
     int32_t* ready;            // [max_items] gate/up blocks of h finished
+    int32_t* sched;            // [2] tile counter, CTAs done claiming (zero between launches)
     int32_t* err;              // device error word
     int R;                     // rows of the call
     int32_t ushape;            // union_shape_word of the call
