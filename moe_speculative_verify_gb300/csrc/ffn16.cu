@@ -15,7 +15,7 @@
 //   warp 0 lane 0: TMA producer -- claims the CTA's tiles and publishes them
 //                  to the other roles; e4m3 weight tiles (16 KB) into a ring
 //                  of staging buffers;
-//   warps 1, 14 lane 0: MMA issuers, alternate steps -- 8 x tcgen05.mma
+//   warps 1, 18 lane 0: MMA issuers, alternate steps -- 8 x tcgen05.mma
 //                  kind::f16 (K = 16) per 128-wide K-block, A (the bf16 weight
 //                  tile) from tensor memory, B (the rows) from shared memory,
 //                  into the tile's accumulator: gate (even steps) and up (odd)
