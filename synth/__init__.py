@@ -98,6 +98,13 @@ WORKLOADS = {
     "profile1024": Workload("profile1024", GLM52_E32, rows=1024,
                             note="1024 rows on 32 experts of the GLM-5.2 shape (256 rows per "
                                  "expert, the 64-row tile): prefill-like profiler captures"),
+    "profile512": Workload("profile512", GLM52_E32, rows=512,
+                           note="512 rows on 32 experts of the GLM-5.2 shape (128 rows per "
+                                "expert, the 64-row tile with the deeper ring of calls of at "
+                                "most 512 rows): decode-batch-like profiler captures"),
+    "profile4096r": Workload("profile4096r", GLM52_ROUTER, rows=4096,
+                             note="prefill4096's routing at 128-wide experts: the large-R "
+                                  "router at its real size, for profiler captures"),
 }
 
 
