@@ -92,3 +92,56 @@ def test_one_graph_any_occupancy():
         assert np.array_equal(got_ids, ids.cpu().numpy())
         assert np.all(got[vmask == 0] == 0)
         assert m.moe_get_device_error(ws) == 0
+
+
+def test_one_graph_any_occupancy_two_gemm_launches():
+    """The same at 100 rows, where the layer runs the selection and the union
+    as two kernels and the expert GEMMs as a gate/up and a down launch."""
+    shape, R = MEDIUM, 100
+    wl = synth.Workload("graph100", shape, rows=R)
+    t_cpu = synth.make_layer(wl, device="cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    host = synth.to_numpy(t_cpu)
+    cfg = m.Config.from_shape(shape)
+    W = m.Weights.from_tensors(t)
+    ws = torch.zeros(m.moe_workspace_bytes(cfg, R), dtype=torch.uint8, device="cuda")
+    x = t["x"].clone()
+    valid = torch.ones(R, dtype=torch.uint8, device="cuda")
+    out = torch.empty((R, shape.hidden), dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty((R, shape.topk), dtype=torch.int32, device="cuda")
+
+    def layer():
+        m.moe_layer(cfg, x, t["wr"], t["bias"], W, valid, out, ws, topk_ids=ids)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer()
+    rng = np.random.default_rng(41)
+    for vmask in (np.ones(R, np.uint8), (rng.random(R) < 0.7).astype(np.uint8)):
+        xv = torch.from_numpy(rng.normal(0, 1, (R, shape.hidden)).astype(np.float32))
+        xv = xv.to(torch.bfloat16).cuda()
+        xv[torch.from_numpy(vmask == 0).cuda()] = float("nan")
+        x.copy_(xv)
+        valid.copy_(torch.from_numpy(vmask))
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert m.moe_get_device_error(ws) == 0
+        got = bf16_to_np(out).copy()
+        h = dict(host)
+        h["x"] = synth.to_numpy({"x": xv})["x"]
+        h["row_valid"] = vmask
+        rows = np.unique(np.linspace(0, R - 1, 16).astype(int))
+        ref = oracle.moe_layer(shape, h, rows=rows)
+        ref_ids, _, _ = oracle.route(shape, h["x"], h["wr"], h["bias"], vmask)
+        assert np.array_equal(ids.cpu().numpy(), ref_ids)
+        v = vmask != 0
+        vr = [r for r in rows if v[r]]
+        y = bf16_bits_to_f64(got)
+        assert rel_fro(y[vr], ref["y_acc"][vr]) <= TOL
+        assert np.all(got[~v] == 0)

@@ -226,7 +226,7 @@ def test_pads_nan_zero_filled():
     assert np.array_equal(o[keep], bf16_to_np(out2)[keep])
 
 
-@pytest.mark.parametrize("shape,R", [(synth.TINY, 8), (MEDIUM, 64), (MEDIUM, 200)])
+@pytest.mark.parametrize("shape,R", [(synth.TINY, 8), (MEDIUM, 64), (MEDIUM, 200), (MEDIUM, 300)])
 def test_row_slot_bit_identity(shape, R):
     """The same row gives the same bits wherever it sits in the batch
     (openinfer #610, "Gates": same rows through both mappings bit-identical)."""
@@ -242,9 +242,11 @@ def test_row_slot_bit_identity(shape, R):
     assert np.array_equal(ids2.cpu().numpy(), ids.cpu().numpy()[pc])
 
 
-@pytest.mark.parametrize("R", [1, 13, 65, 100, 513, 600])
+@pytest.mark.parametrize("R", [1, 13, 64, 65, 100, 256, 257, 512, 513, 600])
 def test_row_counts_and_tiles(R):
-    """Every row-tile variant with ragged tails; several items per expert."""
+    """Every row-tile variant with ragged tails, on both sides of each switch
+    (16 rows up to 64, 32 up to 256, 64 above, the deeper ring up to 512);
+    several items per expert."""
     shape = synth.TINY
     wl, t, h = _make(shape, R, seed=R)
     cfg = m.Config.from_shape(shape)
