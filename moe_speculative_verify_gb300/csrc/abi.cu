@@ -118,12 +118,36 @@ moe_status_t check_weights(const moe_config_t* c, const moe_weights_t* w) {
     return MOE_OK;
 }
 
+// The large-R router's maps: x bf16 [R, H] and w fp32 [E, H], boxes of
+// kRouterStageCols columns x 32 rows, unswizzled; rows and columns past the
+// end read as zero.
+bool make_router_maps(const void* x, const float* wr, int R, int H, int E, moe::RouterMaps* m) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint32_t box[2] = {cuuint32_t(moe::kRouterStageCols), 32};
+    const cuuint32_t es[2] = {1, 1};
+    const cuuint64_t xd[2] = {cuuint64_t(H), cuuint64_t(R)}, xs[1] = {cuuint64_t(H) * 2};
+    const cuuint64_t wd[2] = {cuuint64_t(H), cuuint64_t(E)}, wst[1] = {cuuint64_t(H) * 4};
+    return fn(&m->x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), xd, xs, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+               CUDA_SUCCESS &&
+           fn(&m->w, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(wr), wd, wst, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+               CUDA_SUCCESS;
+}
+
 moe_status_t route_impl(const moe_config_t* c, const void* x, const float* wr, const float* bias,
                         const uint8_t* valid, int32_t R, int32_t* ids, float* wts, float* logits,
-                        cudaStream_t s) {
+                        int32_t* err, cudaStream_t s) {
+    moe::RouterMaps maps;
+    if (R > moe::kRouteUnionMaxRows && !make_router_maps(x, wr, R, c->hidden, c->n_experts, &maps))
+        return MOE_ERR_CUDA;
     return cuda_status(moe::launch_router(static_cast<const uint16_t*>(x), wr, bias, valid, R,
                                           c->hidden, c->n_experts, c->n_groups, c->topk_groups,
-                                          c->topk, c->routed_scaling, ids, wts, logits, s));
+                                          c->topk, c->routed_scaling, ids, wts, logits, &maps,
+                                          device_info().sms, err, timeout_ns(c), s));
 }
 
 moe_status_t union_impl(const moe_config_t* c, const int32_t* ids, int32_t R, int32_t* ub,
@@ -396,7 +420,7 @@ moe_status_t moe_route(const moe_config_t* cfg, const void* x_bf16, const float*
         !aligned(topk_ids, 4) || !aligned(topk_w, 4) || !aligned(logits, 4))
         return MOE_ERR_INVALID_ARG;
     return route_impl(cfg, x_bf16, w_router, bias, row_valid, R, topk_ids, topk_w, logits,
-                      reinterpret_cast<cudaStream_t>(stream));
+                      nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_build_union(const moe_config_t* cfg, const int32_t* topk_ids, int32_t R,
@@ -575,9 +599,9 @@ static moe_status_t layer_impl(const moe_config_t* cfg, const void* x_bf16,
     float* y_shared = reinterpret_cast<float*>(base + L.y_shared);
     if (R <= moe::kRouteUnionMaxRows) {
         // logits, then selection and union in one block
-        if ((st = cuda_status(moe::launch_router_logits(static_cast<const uint16_t*>(x_bf16),
-                                                        w_router, row_valid, R, cfg->hidden,
-                                                        cfg->n_experts, logits, s))) != MOE_OK)
+        if ((st = cuda_status(moe::launch_router_logits(
+                 static_cast<const uint16_t*>(x_bf16), w_router, row_valid, R, cfg->hidden,
+                 cfg->n_experts, logits, nullptr, 0, nullptr, 0, s))) != MOE_OK)
             return st;
         if ((st = cuda_status(moe::launch_route_union(
                  logits, bias, row_valid, R, cfg->n_experts, cfg->n_groups, cfg->topk_groups,
@@ -585,8 +609,8 @@ static moe_status_t layer_impl(const moe_config_t* cfg, const void* x_bf16,
                  L.un, s))) != MOE_OK)
             return st;
     } else {
-        if ((st = route_impl(cfg, x_bf16, w_router, bias, row_valid, R, ids, wts, logits, s)) !=
-            MOE_OK)
+        if ((st = route_impl(cfg, x_bf16, w_router, bias, row_valid, R, ids, wts, logits,
+                             static_cast<int32_t*>(ws), s)) != MOE_OK)
             return st;
         if ((st = union_impl(cfg, ids, R, ub, s)) != MOE_OK) return st;
     }

@@ -105,140 +105,253 @@ __global__ void __launch_bounds__(MAXT, MINB) router_logits_kernel(
     }
 }
 
-// Large-R variant: a block computes a tile of 32 rows x 32 experts; the warp
-// (wr, we) owns rows 8*wr.. and PE experts from PE*we.. (8*PE pairs) and lane
-// l of the warp is lane l of the reduction tree for every one of them.  Per
-// 128-column step the block stages x (bf16) and w (fp32) in shared memory
-// through a ring of kTileStages buffers filled by cp.async (kTileStages - 1
-// steps in flight); a thread accumulates its lane partials of the current
-// 1024-column chunk in registers (fma in column order), folds them into the
-// per-lane chunk sums in shared memory at the end of each chunk (q = p for the
-// first chunk, then q = q + p), and the warp finishes every pair with the xor
-// butterfly: the same IEEE operations in the same order as the small-R kernel.
-// A larger PE reads each x and w value from shared memory for more fmas:
-// measured at 4096 rows, 16 experts a thread (8 warps, 220 registers) took
-// the prefill layer from 4.597 to 4.522 ms against 8 (16 warps).
-constexpr int kTileR = 32, kTileE = 32, kTileStages = 4;
-constexpr int kTileXBytes = kTileR * 128 * 2, kTileWBytes = kTileE * 128 * 4;
-constexpr int kTilePE = 16;   // experts per thread
+// Large-R variant, persistent (one CTA per SM): tiles of kLR rows x kLE
+// experts, tile t at rows (t / n_eb) * kLR and experts (t % n_eb) * kLE, taken
+// by the CTAs in turn.  Warp w owns the tile's rows (w / 4) * 16 .. +15 and
+// experts (w % 4) * 8 .. +7, and lane l of the warp is lane l of the reduction
+// tree for those 128 (row, expert) pairs.
+//
+// Per stage of kLCols columns, x [kLR][kLCols] bf16 and w [kLE][kLCols] fp32
+// arrive by TMA in a ring of kLStages stages (one barrier each); the last warp
+// to finish reading a stage (one acquire-release atomic per warp and stage)
+// issues the copies of the stage kLStages later into it, so the warps drift
+// apart instead of meeting at every stage.  A thread forms its lane partials
+// of the current 1024-column chunk in registers (fma in column order) and
+// folds them at the chunk's end into the chunk sums held in tensor memory
+// (q = p for the first chunk, q = q + p after): shared memory carries only x
+// and w.  The last chunk's sums stay in registers and the warp finishes the
+// tree by recursive halving: at distance d = 16 .. 1 each lane keeps half of
+// its values and adds its partner's copy of them, which are the xor
+// butterfly's additions (v[l] + v[l ^ d], IEEE addition commutes) with every
+// value summed in one lane only; lane l ends with pairs 4l .. 4l + 3.  The
+// same IEEE operations in the same order as the small-R kernel.
+constexpr int kLR = 32, kLE = 32;
+constexpr int kLRT = 16, kLPE = 8, kLNP = kLRT * kLPE;   // rows, experts, pairs of a thread
+constexpr int kLWarps = (kLR / kLRT) * (kLE / kLPE);
+constexpr int kLCols = kRouterStageCols;                 // columns per stage
+constexpr int kLBlk = kLCols / 128;                      // 128-column blocks per stage
+constexpr int kLStages = 1024 / kLCols;                  // 192 KB of stages
+constexpr int kLXBytes = kLR * kLCols * 2, kLWBytes = kLE * kLCols * 4;
+constexpr int kLStageBytes = kLXBytes + kLWBytes;
+constexpr uint32_t kLTmemCols = (kLWarps / 4) * kLNP;    // warps per lane quarter x pairs
+constexpr size_t kLSmem = size_t(kLStages) * kLStageBytes + 256;
+static_assert(kLBlk >= 1 && 8 % kLBlk == 0, "a stage holds whole blocks of one chunk");
 
-template <int PE>
-struct RouterTile {
-    static constexpr int WARPS = 4 * (kTileE / PE);
-    static constexpr int THREADS = 32 * WARPS;
-    static constexpr size_t SMEM = size_t(kTileStages) * (kTileXBytes + kTileWBytes) +
-                                   size_t(WARPS) * 8 * PE * 32 * 4;
-};
-
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+__device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+        "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
+        "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]),
+        "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]),
+        "f"(v[29]), "f"(v[30]), "f"(v[31])
+        : "memory");
 }
 
-template <int PE>
-__global__ void __launch_bounds__(RouterTile<PE>::THREADS, 1) router_logits_tiled_kernel(
-    const uint16_t* __restrict__ x, const float* __restrict__ wr,
-    const uint8_t* __restrict__ row_valid, int R, int H, int E, float* __restrict__ logits) {
-    constexpr int NTH = RouterTile<PE>::THREADS;
-    constexpr int EG = kTileE / PE;   // expert groups of the warp grid
-    extern __shared__ __align__(16) uint8_t rsm[];
-    uint16_t* xs = reinterpret_cast<uint16_t*>(rsm);                                // [S][32][128]
-    float* wsm = reinterpret_cast<float*>(rsm + kTileStages * kTileXBytes);         // [S][32][128]
-    float* qsm = wsm + kTileStages * kTileE * 128;                                  // [warps][8*PE][32]
-    pdl_wait();
-    pdl_launch_dependents();
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// One recursive-halving level over the first N values at xor distance D.
+template <int M, int N, int D>
+__device__ __forceinline__ void halve(float (&v)[M], int lane) {
+    const bool upper = (lane & D) != 0;
+#pragma unroll
+    for (int j = 0; j < N / 2; ++j) {
+        const float send = upper ? v[j] : v[j + N / 2];
+        const float keep = upper ? v[j + N / 2] : v[j];
+        v[j] = __fadd_rn(keep, __shfl_xor_sync(0xFFFFFFFFu, send, D));
+    }
+}
+
+__global__ void __launch_bounds__(kLWarps * 32, 1) router_logits_tma_kernel(
+    const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
+    const uint8_t* __restrict__ row_valid, int R, int H, int E, float* __restrict__ logits,
+    int32_t* err, uint64_t timeout_ns) {
+    extern __shared__ __align__(1024) uint8_t lsm[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(lsm + kLStages * kLStageBytes);
+    uint32_t* cnt = reinterpret_cast<uint32_t*>(full + kLStages);   // warps done per stage
+    int32_t* last = reinterpret_cast<int32_t*>(cnt + kLStages);      // last stage load issued
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(last + kLStages);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int wrow = (warp / EG) * 8, wexp = (warp % EG) * PE;
-    const int r0 = blockIdx.y * kTileR, e0 = blockIdx.x * kTileE;
-    const int steps = H / 128;
+    const int n_eb = (E + kLE - 1) / kLE;
+    const int n_tiles = ((R + kLR - 1) / kLR) * n_eb;
+    const int NB = H / 128;                       // 128-column blocks
+    const int NSt = (NB + kLBlk - 1) / kLBlk;     // stages per tile
+    const int my_tiles =
+        static_cast<int>(blockIdx.x) < n_tiles ? (n_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int G = my_tiles * NSt;   // this CTA's stage loads, over all its tiles
 
-    // Step i's tiles into ring buffer i % kTileStages: x is 512 x 16 bytes, w
-    // 1024 x 16 bytes, spread over the block's threads.
-    auto issue = [&](int i) {
-        if (i < steps) {
-            const int buf = i % kTileStages;
-#pragma unroll
-            for (int u = 0; u < kTileR * 16 / NTH; ++u) {
-                const int q = tid + u * NTH;
-                const int xrow = q >> 4, xc = (q & 15) * 8;
-                cp_async16(xs + (buf * kTileR + xrow) * 128 + xc,
-                           x + size_t(min(r0 + xrow, R - 1)) * H + i * 128 + xc);
-            }
-#pragma unroll
-            for (int u = 0; u < kTileE * 32 / NTH; ++u) {
-                const int q = tid + u * NTH;
-                const int ex = q >> 5, c = (q & 31) * 4;
-                const int e = min(e0 + ex, E - 1);
-                cp_async16(wsm + (buf * kTileE + ex) * 128 + c, wr + size_t(e) * H + i * 128 + c);
-            }
-        }
-        cp_async_commit();   // one group per step, empty past the end: uniform counting
+    // load g into ring slot g % kLStages (one thread); columns past H read as 0
+    auto issue = [&](int g) {
+        const int st = g % kLStages, s = g % NSt;
+        const int t = blockIdx.x + (g / NSt) * gridDim.x;
+        uint8_t* base = lsm + st * kLStageBytes;
+        last[st] = g;
+        mbar_arrive_expect_tx(&full[st], kLStageBytes);
+        tma_load_2d(base, &xmap, &full[st], s * kLCols, (t / n_eb) * kLR);
+        tma_load_2d(base + kLXBytes, &wmap, &full[st], s * kLCols, (t % n_eb) * kLE);
     };
 
-    float p[8][PE];
-#pragma unroll
-    for (int i = 0; i < kTileStages - 1; ++i) issue(i);
-    for (int i = 0; i < steps; ++i) {
-        const int buf = i % kTileStages;
-        cp_async_wait<kTileStages - 2>();   // this thread's copies of step i have landed
-        __syncthreads();                    // everyone's have; step i-1's buffer is free
-        issue(i + kTileStages - 1);
-        if ((i & 7) == 0) {
-#pragma unroll
-            for (int a = 0; a < 8; ++a)
-#pragma unroll
-                for (int b = 0; b < PE; ++b) p[a][b] = 0.0f;
+    if (tid == 0) {
+        prefetch_tensormap(&xmap);
+        prefetch_tensormap(&wmap);
+        for (int i = 0; i < kLStages; ++i) {
+            mbar_init(&full[i], 1);
+            cnt[i] = 0;
+            last[i] = -1;
         }
-        // all PE experts' columns held, each row's x read and widened once;
-        // every pair's four fmas stay in column order
-        float4 wv[PE];
+        *s_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, kLTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    pdl_wait();   // x may be written by the previous kernel
+    pdl_launch_dependents();
+    if (tid == 0)
+        for (int g = 0; g < kLStages && g < G; ++g) issue(g);
+
+    const int wrow = (warp / (kLE / kLPE)) * kLRT, wexp = (warp % (kLE / kLPE)) * kLPE;
+    const uint32_t tq = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) +
+                        static_cast<uint32_t>(warp >> 2) * kLNP;
+    bool ok = true;
+    int g = 0;
+    for (int ti = 0; ti < my_tiles && ok; ++ti) {
+        const int t = blockIdx.x + ti * gridDim.x;
+        float p[kLNP];   // pair k = 8 * row + expert of the warp's 16 x 8
+        for (int s = 0; s < NSt; ++s, ++g) {
+            const int st = g % kLStages;
+            const uint32_t par = (g / kLStages) & 1;
+            // the outcome is made uniform across the warp before use
+            bool got = mbar_try_wait(&full[st], par);
+            if (!got) got = !*s_abort && mbar_wait(&full[st], par, err, timeout_ns);
+            if (!__all_sync(0xFFFFFFFFu, got)) {
+                ok = false;
+                break;
+            }
+            const uint16_t* xs = reinterpret_cast<const uint16_t*>(lsm + st * kLStageBytes);
+            const float* ws = reinterpret_cast<const float*>(lsm + st * kLStageBytes + kLXBytes);
 #pragma unroll
-        for (int b = 0; b < PE; ++b)
-            wv[b] = *reinterpret_cast<const float4*>(wsm + (buf * kTileE + wexp + b) * 128 + 4 * lane);
+            for (int i = 0; i < kLBlk; ++i) {
+                const int blk = s * kLBlk + i;
+                if (blk < NB) {
+                    if ((blk & 7) == 0) {
 #pragma unroll
-        for (int a = 0; a < 8; ++a) {
-            const uint2 xv =
-                *reinterpret_cast<const uint2*>(xs + (buf * kTileR + wrow + a) * 128 + 4 * lane);
-            const float x0 = bf16_bits_to_f32(xv.x & 0xFFFFu), x1 = bf16_bits_to_f32(xv.x >> 16);
-            const float x2 = bf16_bits_to_f32(xv.y & 0xFFFFu), x3 = bf16_bits_to_f32(xv.y >> 16);
+                        for (int k = 0; k < kLNP; ++k) p[k] = 0.0f;
+                    }
+                    float4 wv[8];
 #pragma unroll
-            for (int b = 0; b < PE; ++b) {
-                float q = p[a][b];
-                q = __fmaf_rn(x0, wv[b].x, q);
-                q = __fmaf_rn(x1, wv[b].y, q);
-                q = __fmaf_rn(x2, wv[b].z, q);
-                q = __fmaf_rn(x3, wv[b].w, q);
-                p[a][b] = q;
+                    for (int b = 0; b < 8; ++b)
+                        wv[b] = *reinterpret_cast<const float4*>(ws + (wexp + b) * kLCols + i * 128 +
+                                                                 4 * lane);
+#pragma unroll
+                    for (int a = 0; a < kLRT; ++a) {
+                        const uint2 xv = *reinterpret_cast<const uint2*>(
+                            xs + (wrow + a) * kLCols + i * 128 + 4 * lane);
+                        const float x0 = bf16_bits_to_f32(xv.x & 0xFFFFu);
+                        const float x1 = bf16_bits_to_f32(xv.x >> 16);
+                        const float x2 = bf16_bits_to_f32(xv.y & 0xFFFFu);
+                        const float x3 = bf16_bits_to_f32(xv.y >> 16);
+#pragma unroll
+                        for (int b = 0; b < 8; ++b) {
+                            float q = p[a * 8 + b];
+                            q = __fmaf_rn(x0, wv[b].x, q);
+                            q = __fmaf_rn(x1, wv[b].y, q);
+                            q = __fmaf_rn(x2, wv[b].z, q);
+                            q = __fmaf_rn(x3, wv[b].w, q);
+                            p[a * 8 + b] = q;
+                        }
+                    }
+                }
+            }
+            // the slot is free once every warp has read it: the last one
+            // refills it with load g + kLStages
+            __syncwarp();
+            if (lane == 0) {
+                uint32_t before;
+                asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
+                             : "=r"(before)
+                             : "r"(smem_u32(&cnt[st]))
+                             : "memory");
+                if (before == kLWarps - 1) {
+                    cnt[st] = 0;
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    if (g + kLStages < G) issue(g + kLStages);
+                }
+            }
+            // a chunk's end before the tile's last block: q = p (first chunk)
+            // or q = q + p, 32 pairs at a time
+            const int lastblk = min(s * kLBlk + kLBlk, NB) - 1;
+            if ((lastblk & 7) == 7 && lastblk != NB - 1) {
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < kLNP / 32; ++j) {
+                    if (lastblk >= 8) {
+                        float q[32];
+                        tmem_ld32(tq + 32 * j, q);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) p[32 * j + i] = __fadd_rn(q[i], p[32 * j + i]);
+                    }
+                    tmem_st32f(tq + 32 * j, p + 32 * j);
+                }
+                tmem_wait_st();
             }
         }
-        if ((i & 7) == 7 || i + 1 == steps) {   // end of a 1024-column chunk
-            float* qw = qsm + size_t(warp) * 8 * PE * 32;
-            const bool first = (i < 8);
+        if (!ok) break;
+        if (NB > 8) {   // the last chunk: q + p, kept in registers
+            __syncwarp();
 #pragma unroll
-            for (int a = 0; a < 8; ++a)
+            for (int j = 0; j < kLNP / 32; ++j) {
+                float q[32];
+                tmem_ld32(tq + 32 * j, q);
+                tmem_wait_ld();
 #pragma unroll
-                for (int b = 0; b < PE; ++b) {
-                    float* slot = qw + (a * PE + b) * 32 + lane;
-                    *slot = first ? p[a][b] : __fadd_rn(*slot, p[a][b]);
-                }
+                for (int i = 0; i < 32; ++i) p[32 * j + i] = __fadd_rn(q[i], p[32 * j + i]);
+            }
+        }
+        halve<kLNP, kLNP, 16>(p, lane);
+        halve<kLNP, kLNP / 2, 8>(p, lane);
+        halve<kLNP, kLNP / 4, 4>(p, lane);
+        halve<kLNP, kLNP / 8, 2>(p, lane);
+        halve<kLNP, kLNP / 16, 1>(p, lane);
+        // lane l holds pairs 4l .. 4l + 3: row l / 2, experts 4 * (l % 2) ..
+        const int r = (t / n_eb) * kLR + wrow + (lane >> 1);
+        const int e = (t % n_eb) * kLE + wexp + 4 * (lane & 1);
+        if (r < R && (row_valid == nullptr || row_valid[r] != 0)) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (e + j < E) logits[size_t(r) * E + e + j] = p[j];
         }
     }
-    cp_async_wait<0>();
-    const float* qw = qsm + size_t(warp) * 8 * PE * 32;
-    for (int pair = 0; pair < 8 * PE; ++pair) {
-        float q = qw[pair * 32 + lane];
-#pragma unroll
-        for (int d = 16; d >= 1; d >>= 1) q = __fadd_rn(q, __shfl_xor_sync(0xFFFFFFFFu, q, d));
-        const int r = r0 + wrow + pair / PE, e = e0 + wexp + pair % PE;
-        if (lane == 0 && r < R && e < E && (row_valid == nullptr || row_valid[r] != 0))
-            logits[size_t(r) * E + e] = q;
+    if (!ok) *s_abort = 1;
+
+    __syncthreads();
+    if (*s_abort && tid == 0) {
+        // let every copy issued land before the CTA exits (bounded)
+        constexpr uint64_t kDrainNs = 2000000;
+        const uint64_t t0 = globaltimer_ns();
+        for (int i = 0; i < kLStages; ++i) {
+            if (last[i] < 0) continue;
+            const uint64_t used = globaltimer_ns() - t0;
+            if (used >= kDrainNs) break;
+            mbar_wait(&full[i], (last[i] / kLStages) & 1, nullptr, kDrainNs - used);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kLTmemCols);
     }
 }
 
@@ -268,7 +381,9 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(
 
 // ----------------------------------------------------------- launchers ----
 cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const uint8_t* row_valid,
-                                 int R, int H, int E, float* logits, cudaStream_t stream) {
+                                 int R, int H, int E, float* logits, const RouterMaps* maps,
+                                 int n_sms, int32_t* err, uint64_t timeout_ns,
+                                 cudaStream_t stream) {
     const int nchunks = (H + 1023) / 1024;
     const int threads = max(32, nchunks * 32);
     if (R <= 64) {
@@ -285,14 +400,15 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const uint8
                              stream, x, wr, row_valid, R, H, E, logits);
         if (e != cudaSuccess) return e;
     } else {
-        dim3 grid((E + kTileE - 1) / kTileE, (R + kTileR - 1) / kTileR);
-        using T = RouterTile<kTilePE>;
-        cudaError_t e = cudaFuncSetAttribute(router_logits_tiled_kernel<kTilePE>,
+        if (maps == nullptr) return cudaErrorInvalidValue;
+        const int n_tiles = ((R + kLR - 1) / kLR) * ((E + kLE - 1) / kLE);
+        cudaError_t e = cudaFuncSetAttribute(router_logits_tma_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(T::SMEM));
+                                             static_cast<int>(kLSmem));
         if (e != cudaSuccess) return e;
-        e = launch_pdl(router_logits_tiled_kernel<kTilePE>, grid, dim3(T::THREADS), T::SMEM, stream,
-                       x, wr, row_valid, R, H, E, logits);
+        e = launch_pdl(router_logits_tma_kernel, dim3(min(n_tiles, max(n_sms, 1))),
+                       dim3(kLWarps * 32), kLSmem, stream, maps->x, maps->w, row_valid, R, H, E,
+                       logits, err, timeout_ns);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
@@ -301,8 +417,10 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const uint8
 cudaError_t launch_router(const uint16_t* x, const float* wr, const float* bias,
                           const uint8_t* row_valid, int R, int H, int E, int G, int TG, int K,
                           float scaling, int32_t* ids, float* wts, float* logits,
+                          const RouterMaps* maps, int n_sms, int32_t* err, uint64_t timeout_ns,
                           cudaStream_t stream) {
-    cudaError_t e = launch_router_logits(x, wr, row_valid, R, H, E, logits, stream);
+    cudaError_t e = launch_router_logits(x, wr, row_valid, R, H, E, logits, maps, n_sms, err,
+                                         timeout_ns, stream);
     if (e != cudaSuccess) return e;
     e = launch_pdl(route_select_kernel, dim3((R + kSelWarps - 1) / kSelWarps), dim3(kSelWarps * 32),
                    0, stream, logits, bias, row_valid, R, E, G, TG, K, scaling, ids, wts);
