@@ -112,10 +112,13 @@ __global__ void __launch_bounds__(MAXT, MINB) router_logits_kernel(
 // tree for those 128 (row, expert) pairs.
 //
 // Per stage of kLCols columns, x [kLR][kLCols] bf16 and w [kLE][kLCols] fp32
-// arrive by TMA in a ring of kLStages stages (one barrier each); the last warp
-// to finish reading a stage (one acquire-release atomic per warp and stage)
-// issues the copies of the stage kLStages later into it, so the warps drift
-// apart instead of meeting at every stage.  A thread forms its lane partials
+// arrive by TMA in a ring of kLStages slots (a full and an empty barrier
+// each).  Warpgroup 0 is the producer: its thread 0 waits for a slot's empty
+// phase and refills it; the 8 consumer warps of warpgroups 1 and 2 only wait
+// for full slots and arrive on empty ones (no round trip), so they drift apart
+// instead of meeting at every stage.  The producer warpgroup gives up its
+// registers (setmaxnreg: 40 a thread) to the consumers (232), whose 16 x 8
+// pair tiles need them: 4 x 32 x 40 + 8 x 32 x 232 = 384 x 168, the launch's.  A thread forms its lane partials
 // of the current 1024-column chunk in registers (fma in column order) and
 // folds them at the chunk's end into the chunk sums held in tensor memory
 // (q = p for the first chunk, q = q + p after): shared memory carries only x
@@ -127,7 +130,12 @@ __global__ void __launch_bounds__(MAXT, MINB) router_logits_kernel(
 // same IEEE operations in the same order as the small-R kernel.
 constexpr int kLR = 32, kLE = 32;
 constexpr int kLRT = 16, kLPE = 8, kLNP = kLRT * kLPE;   // rows, experts, pairs of a thread
-constexpr int kLWarps = (kLR / kLRT) * (kLE / kLPE);
+constexpr int kLWarps = (kLR / kLRT) * (kLE / kLPE);       // consumer warps
+constexpr int kLThreads = 32 * (4 + kLWarps);              // + the producer warpgroup
+constexpr int kLProdRegs = 40, kLConsRegs = 232, kLLaunchRegs = 65536 / kLThreads / 8 * 8;
+static_assert(kLWarps == 8, "two consumer warpgroups");
+static_assert(128 * kLProdRegs + 32 * kLWarps * kLConsRegs <= kLThreads * kLLaunchRegs,
+              "register split within the launch's registers");
 constexpr int kLCols = kRouterStageCols;                 // columns per stage
 constexpr int kLBlk = kLCols / 128;                      // 128-column blocks per stage
 constexpr int kLStages = 1024 / kLCols;                  // 192 KB of stages
@@ -166,14 +174,14 @@ __device__ __forceinline__ void halve(float (&v)[M], int lane) {
     }
 }
 
-__global__ void __launch_bounds__(kLWarps * 32, 1) router_logits_tma_kernel(
+__global__ void __launch_bounds__(kLThreads, 1) router_logits_tma_kernel(
     const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
     const uint8_t* __restrict__ row_valid, int R, int H, int E, float* __restrict__ logits,
     int32_t* err, uint64_t timeout_ns) {
     extern __shared__ __align__(1024) uint8_t lsm[];
     uint64_t* full = reinterpret_cast<uint64_t*>(lsm + kLStages * kLStageBytes);
-    uint32_t* cnt = reinterpret_cast<uint32_t*>(full + kLStages);   // warps done per stage
-    int32_t* last = reinterpret_cast<int32_t*>(cnt + kLStages);      // last stage load issued
+    uint64_t* empty = full + kLStages;                               // consumers done with it
+    int32_t* last = reinterpret_cast<int32_t*>(empty + kLStages);    // last stage load issued
     uint32_t* tslot = reinterpret_cast<uint32_t*>(last + kLStages);
     volatile int* s_abort = reinterpret_cast<volatile int*>(tslot + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -201,7 +209,7 @@ __global__ void __launch_bounds__(kLWarps * 32, 1) router_logits_tma_kernel(
         prefetch_tensormap(&wmap);
         for (int i = 0; i < kLStages; ++i) {
             mbar_init(&full[i], 1);
-            cnt[i] = 0;
+            mbar_init(&empty[i], kLWarps);
             last[i] = -1;
         }
         *s_abort = 0;
@@ -217,120 +225,133 @@ __global__ void __launch_bounds__(kLWarps * 32, 1) router_logits_tma_kernel(
     const uint32_t tmem = *tslot;
     pdl_wait();   // x may be written by the previous kernel
     pdl_launch_dependents();
-    if (tid == 0)
-        for (int g = 0; g < kLStages && g < G; ++g) issue(g);
 
-    const int wrow = (warp / (kLE / kLPE)) * kLRT, wexp = (warp % (kLE / kLPE)) * kLPE;
-    const uint32_t tq = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) +
-                        static_cast<uint32_t>(warp >> 2) * kLNP;
     bool ok = true;
-    int g = 0;
-    for (int ti = 0; ti < my_tiles && ok; ++ti) {
-        const int t = blockIdx.x + ti * gridDim.x;
-        float p[kLNP];   // pair k = 8 * row + expert of the warp's 16 x 8
-        for (int s = 0; s < NSt; ++s, ++g) {
-            const int st = g % kLStages;
-            const uint32_t par = (g / kLStages) & 1;
-            // the outcome is made uniform across the warp before use
-            bool got = mbar_try_wait(&full[st], par);
-            if (!got) got = !*s_abort && mbar_wait(&full[st], par, err, timeout_ns);
-            if (!__all_sync(0xFFFFFFFFu, got)) {
-                ok = false;
-                break;
-            }
-            const uint16_t* xs = reinterpret_cast<const uint16_t*>(lsm + st * kLStageBytes);
-            const float* ws = reinterpret_cast<const float*>(lsm + st * kLStageBytes + kLXBytes);
-#pragma unroll
-            for (int i = 0; i < kLBlk; ++i) {
-                const int blk = s * kLBlk + i;
-                if (blk < NB) {
-                    if ((blk & 7) == 0) {
-#pragma unroll
-                        for (int k = 0; k < kLNP; ++k) p[k] = 0.0f;
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLProdRegs));
+        if (tid == 0) {
+            // every stage load in order; slot reuse waits for its empty phase
+            for (int n = 0; n < G && ok; ++n) {
+                const int st = n % kLStages;
+                if (n >= kLStages) {
+                    const uint32_t par = ((n / kLStages) - 1) & 1;
+                    uint64_t t0 = 0;
+                    for (uint32_t it = 0; !mbar_try_wait<20000>(&empty[st], par); ++it) {
+                        if (it == 0) t0 = globaltimer_ns();
+                        if (*s_abort || globaltimer_ns() - t0 > timeout_ns || it >= (1u << 30)) {
+                            if (!*s_abort) record_error(err, MOE_ERR_TIMEOUT);
+                            ok = false;
+                            break;
+                        }
                     }
-                    float4 wv[8];
-#pragma unroll
-                    for (int b = 0; b < 8; ++b)
-                        wv[b] = *reinterpret_cast<const float4*>(ws + (wexp + b) * kLCols + i * 128 +
-                                                                 4 * lane);
-#pragma unroll
-                    for (int a = 0; a < kLRT; ++a) {
-                        const uint2 xv = *reinterpret_cast<const uint2*>(
-                            xs + (wrow + a) * kLCols + i * 128 + 4 * lane);
-                        const float x0 = bf16_bits_to_f32(xv.x & 0xFFFFu);
-                        const float x1 = bf16_bits_to_f32(xv.x >> 16);
-                        const float x2 = bf16_bits_to_f32(xv.y & 0xFFFFu);
-                        const float x3 = bf16_bits_to_f32(xv.y >> 16);
-#pragma unroll
-                        for (int b = 0; b < 8; ++b) {
-                            float q = p[a * 8 + b];
-                            q = __fmaf_rn(x0, wv[b].x, q);
-                            q = __fmaf_rn(x1, wv[b].y, q);
-                            q = __fmaf_rn(x2, wv[b].z, q);
-                            q = __fmaf_rn(x3, wv[b].w, q);
-                            p[a * 8 + b] = q;
+                    if (!ok) break;
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                }
+                issue(n);
+            }
+        }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kLConsRegs));
+        const int cw = warp - 4;   // consumer warp
+        const int wrow = (cw / (kLE / kLPE)) * kLRT, wexp = (cw % (kLE / kLPE)) * kLPE;
+        const uint32_t tq = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) +
+                            static_cast<uint32_t>(cw >> 2) * kLNP;
+        int g = 0;
+        for (int ti = 0; ti < my_tiles && ok; ++ti) {
+            const int t = blockIdx.x + ti * gridDim.x;
+            float p[kLNP];   // pair k = 8 * row + expert of the warp's 16 x 8
+            for (int s = 0; s < NSt; ++s, ++g) {
+                const int st = g % kLStages;
+                const uint32_t par = (g / kLStages) & 1;
+                // the outcome is made uniform across the warp before use
+                bool got = mbar_try_wait(&full[st], par);
+                if (!got) got = !*s_abort && mbar_wait(&full[st], par, err, timeout_ns);
+                if (!__all_sync(0xFFFFFFFFu, got)) {
+                    ok = false;
+                    break;
+                }
+                const uint16_t* xs = reinterpret_cast<const uint16_t*>(lsm + st * kLStageBytes);
+                const float* ws = reinterpret_cast<const float*>(lsm + st * kLStageBytes + kLXBytes);
+    #pragma unroll
+                for (int i = 0; i < kLBlk; ++i) {
+                    const int blk = s * kLBlk + i;
+                    if (blk < NB) {
+                        if ((blk & 7) == 0) {
+    #pragma unroll
+                            for (int k = 0; k < kLNP; ++k) p[k] = 0.0f;
+                        }
+                        float4 wv[8];
+    #pragma unroll
+                        for (int b = 0; b < 8; ++b)
+                            wv[b] = *reinterpret_cast<const float4*>(ws + (wexp + b) * kLCols + i * 128 +
+                                                                     4 * lane);
+    #pragma unroll
+                        for (int a = 0; a < kLRT; ++a) {
+                            const uint2 xv = *reinterpret_cast<const uint2*>(
+                                xs + (wrow + a) * kLCols + i * 128 + 4 * lane);
+                            const float x0 = bf16_bits_to_f32(xv.x & 0xFFFFu);
+                            const float x1 = bf16_bits_to_f32(xv.x >> 16);
+                            const float x2 = bf16_bits_to_f32(xv.y & 0xFFFFu);
+                            const float x3 = bf16_bits_to_f32(xv.y >> 16);
+    #pragma unroll
+                            for (int b = 0; b < 8; ++b) {
+                                float q = p[a * 8 + b];
+                                q = __fmaf_rn(x0, wv[b].x, q);
+                                q = __fmaf_rn(x1, wv[b].y, q);
+                                q = __fmaf_rn(x2, wv[b].z, q);
+                                q = __fmaf_rn(x3, wv[b].w, q);
+                                p[a * 8 + b] = q;
+                            }
                         }
                     }
                 }
-            }
-            // the slot is free once every warp has read it: the last one
-            // refills it with load g + kLStages
-            __syncwarp();
-            if (lane == 0) {
-                uint32_t before;
-                asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
-                             : "=r"(before)
-                             : "r"(smem_u32(&cnt[st]))
-                             : "memory");
-                if (before == kLWarps - 1) {
-                    cnt[st] = 0;
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    if (g + kLStages < G) issue(g + kLStages);
-                }
-            }
-            // a chunk's end before the tile's last block: q = p (first chunk)
-            // or q = q + p, 32 pairs at a time
-            const int lastblk = min(s * kLBlk + kLBlk, NB) - 1;
-            if ((lastblk & 7) == 7 && lastblk != NB - 1) {
+                // this warp is done with the slot
                 __syncwarp();
-#pragma unroll
-                for (int j = 0; j < kLNP / 32; ++j) {
-                    if (lastblk >= 8) {
-                        float q[32];
-                        tmem_ld32(tq + 32 * j, q);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) p[32 * j + i] = __fadd_rn(q[i], p[32 * j + i]);
+                if (lane == 0) mbar_arrive(&empty[st]);
+                // a chunk's end before the tile's last block: q = p (first chunk)
+                // or q = q + p, 32 pairs at a time
+                const int lastblk = min(s * kLBlk + kLBlk, NB) - 1;
+                if ((lastblk & 7) == 7 && lastblk != NB - 1) {
+                    __syncwarp();
+    #pragma unroll
+                    for (int j = 0; j < kLNP / 32; ++j) {
+                        if (lastblk >= 8) {
+                            float q[32];
+                            tmem_ld32(tq + 32 * j, q);
+                            tmem_wait_ld();
+    #pragma unroll
+                            for (int i = 0; i < 32; ++i) p[32 * j + i] = __fadd_rn(q[i], p[32 * j + i]);
+                        }
+                        tmem_st32f(tq + 32 * j, p + 32 * j);
                     }
-                    tmem_st32f(tq + 32 * j, p + 32 * j);
+                    tmem_wait_st();
                 }
-                tmem_wait_st();
             }
-        }
-        if (!ok) break;
-        if (NB > 8) {   // the last chunk: q + p, kept in registers
-            __syncwarp();
-#pragma unroll
-            for (int j = 0; j < kLNP / 32; ++j) {
-                float q[32];
-                tmem_ld32(tq + 32 * j, q);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) p[32 * j + i] = __fadd_rn(q[i], p[32 * j + i]);
+            if (!ok) break;
+            if (NB > 8) {   // the last chunk: q + p, kept in registers
+                __syncwarp();
+    #pragma unroll
+                for (int j = 0; j < kLNP / 32; ++j) {
+                    float q[32];
+                    tmem_ld32(tq + 32 * j, q);
+                    tmem_wait_ld();
+    #pragma unroll
+                    for (int i = 0; i < 32; ++i) p[32 * j + i] = __fadd_rn(q[i], p[32 * j + i]);
+                }
             }
-        }
-        halve<kLNP, kLNP, 16>(p, lane);
-        halve<kLNP, kLNP / 2, 8>(p, lane);
-        halve<kLNP, kLNP / 4, 4>(p, lane);
-        halve<kLNP, kLNP / 8, 2>(p, lane);
-        halve<kLNP, kLNP / 16, 1>(p, lane);
-        // lane l holds pairs 4l .. 4l + 3: row l / 2, experts 4 * (l % 2) ..
-        const int r = (t / n_eb) * kLR + wrow + (lane >> 1);
-        const int e = (t % n_eb) * kLE + wexp + 4 * (lane & 1);
-        if (r < R && (row_valid == nullptr || row_valid[r] != 0)) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (e + j < E) logits[size_t(r) * E + e + j] = p[j];
+            halve<kLNP, kLNP, 16>(p, lane);
+            halve<kLNP, kLNP / 2, 8>(p, lane);
+            halve<kLNP, kLNP / 4, 4>(p, lane);
+            halve<kLNP, kLNP / 8, 2>(p, lane);
+            halve<kLNP, kLNP / 16, 1>(p, lane);
+            // lane l holds pairs 4l .. 4l + 3: row l / 2, experts 4 * (l % 2) ..
+            const int r = (t / n_eb) * kLR + wrow + (lane >> 1);
+            const int e = (t % n_eb) * kLE + wexp + 4 * (lane & 1);
+            if (r < R && (row_valid == nullptr || row_valid[r] != 0)) {
+    #pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (e + j < E) logits[size_t(r) * E + e + j] = p[j];
+            }
         }
     }
     if (!ok) *s_abort = 1;
@@ -406,8 +427,12 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const uint8
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kLSmem));
         if (e != cudaSuccess) return e;
+        // the warpgroups' register split needs the launch's full share
+        cudaFuncAttributes fa;
+        if ((e = cudaFuncGetAttributes(&fa, router_logits_tma_kernel)) != cudaSuccess) return e;
+        if (fa.numRegs < kLLaunchRegs) return cudaErrorInvalidConfiguration;
         e = launch_pdl(router_logits_tma_kernel, dim3(min(n_tiles, max(n_sms, 1))),
-                       dim3(kLWarps * 32), kLSmem, stream, maps->x, maps->w, row_valid, R, H, E,
+                       dim3(kLThreads), kLSmem, stream, maps->x, maps->w, row_valid, R, H, E,
                        logits, err, timeout_ns);
         if (e != cudaSuccess) return e;
     }
