@@ -172,6 +172,12 @@ typedef struct {
  *     listed by b descending;
  *   w_k = (s_k / (s_0 + ... + s_{K-1})) * routed_scaling, the sum in k order.
  *   Pad rows: ids -1, weights 0, logits untouched.
+ * Above 64 rows the logits kernel streams x and w_router through shared
+ * memory by TMA and waits on its own copies with bounded waits
+ * (wait_timeout_us); should one run out (the copies never landing), the
+ * kernel leaves the logits of its unfinished tiles unwritten.  moe_route has
+ * no error word to record that in; moe_layer records MOE_ERR_TIMEOUT in its
+ * workspace's.
  */
 moe_status_t moe_route(const moe_config_t* cfg, const void* x_bf16, const float* w_router,
                        const float* bias, const uint8_t* row_valid, int32_t R,
