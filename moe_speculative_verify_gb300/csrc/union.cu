@@ -46,7 +46,7 @@ __device__ int block_exclusive_scan(int v, int* s_warp, int* total) {
 
 // Shared memory of the union build, in bytes.
 __host__ __device__ inline size_t union_smem_bytes(int R, int E) {
-    const size_t words = size_t(E) * ((R + 31) / 32);
+    const size_t words = size_t(E) * (((R + 31) / 32) | 1);
     return words * 4 + ((words + 1) & ~size_t(1)) * 2 + ((R + 15) & ~15) + size_t(4 * E + 8) * 4;
 }
 
@@ -56,9 +56,13 @@ __host__ __device__ inline size_t union_smem_bytes(int R, int E) {
 __device__ void union_block(const int32_t* ids, int R, int E, int K, int S, int n_tile,
                             int32_t* __restrict__ ub, const UnionLayout& L, uint32_t* sm) {
     const int W = (R + 31) / 32;
-    uint32_t* bm = sm;                                                   // [E][W] row bitmaps
-    uint16_t* wpre = reinterpret_cast<uint16_t*>(bm + size_t(E) * W);    // [E][W] rows before word
-    uint8_t* s_valid = reinterpret_cast<uint8_t*>(wpre + ((size_t(E) * W + 1) & ~size_t(1)));
+    // an odd stride between experts: the lanes of a warp that touch word w of
+    // different experts then fall on different shared-memory banks (with W a
+    // multiple of 32 they all hit one bank)
+    const int WS = W | 1;
+    uint32_t* bm = sm;                                                   // [E][WS] row bitmaps
+    uint16_t* wpre = reinterpret_cast<uint16_t*>(bm + size_t(E) * WS);   // [E][WS] rows before word
+    uint8_t* s_valid = reinterpret_cast<uint8_t*>(wpre + ((size_t(E) * WS + 1) & ~size_t(1)));
     int* s_cnt = reinterpret_cast<int*>(s_valid + ((R + 15) & ~15));     // [E+1]
     int* s_off = s_cnt + (E + 1);                                        // [E+2]
     int* s_ioff = s_off + (E + 2);                                       // [E+1]
@@ -67,7 +71,7 @@ __device__ void union_block(const int32_t* ids, int R, int E, int K, int S, int 
     const int tid = threadIdx.x;
     const int KS = K + S;
 
-    for (int i = tid; i < E * W; i += kUnionThreads) bm[i] = 0u;
+    for (int i = tid; i < E * WS; i += kUnionThreads) bm[i] = 0u;
     if (tid == 0) {
         s_err = 0;
         s_nvalid = 0;
@@ -102,7 +106,7 @@ __device__ void union_block(const int32_t* ids, int R, int E, int K, int S, int 
     for (int i = tid; i < R * K; i += kUnionThreads) {
         const int r = i / K;
         if (!s_valid[r]) continue;
-        atomicOr(&bm[size_t(ids[i]) * W + (r >> 5)], 1u << (r & 31));
+        atomicOr(&bm[size_t(ids[i]) * WS + (r >> 5)], 1u << (r & 31));
     }
     __syncthreads();
 
@@ -115,8 +119,8 @@ __device__ void union_block(const int32_t* ids, int R, int E, int K, int S, int 
         for (int e = tid; e < E; e += kUnionThreads) {
             int c = 0;
             for (int w = 0; w < W; ++w) {
-                wpre[size_t(e) * W + w] = static_cast<uint16_t>(c);
-                c += __popc(bm[size_t(e) * W + w]);
+                wpre[size_t(e) * WS + w] = static_cast<uint16_t>(c);
+                c += __popc(bm[size_t(e) * WS + w]);
             }
             s_cnt[e] = c;
         }
@@ -125,7 +129,7 @@ __device__ void union_block(const int32_t* ids, int R, int E, int K, int S, int 
         const int per = (W + 31) / 32;
         const int w0 = min(W, lane * per), w1 = min(W, w0 + per);
         for (int e = warp; e < E; e += kUnionThreads / 32) {
-            const uint32_t* bme = bm + size_t(e) * W;
+            const uint32_t* bme = bm + size_t(e) * WS;
             int c = 0;
             for (int w = w0; w < w1; ++w) c += __popc(bme[w]);
             int incl = c;
@@ -136,7 +140,7 @@ __device__ void union_block(const int32_t* ids, int R, int E, int K, int S, int 
             }
             int run = incl - c;
             for (int w = w0; w < w1; ++w) {
-                wpre[size_t(e) * W + w] = static_cast<uint16_t>(run);
+                wpre[size_t(e) * WS + w] = static_cast<uint16_t>(run);
                 run += __popc(bme[w]);
             }
             if (lane == 31) s_cnt[e] = incl;
@@ -180,8 +184,8 @@ __device__ void union_block(const int32_t* ids, int R, int E, int K, int S, int 
         if (!s_valid[r]) continue;
         const int e = ids[i];
         const int w = r >> 5;
-        const uint32_t below = bm[size_t(e) * W + w] & ((1u << (r & 31)) - 1u);
-        const int p = s_off[e] + wpre[size_t(e) * W + w] + __popc(below);
+        const uint32_t below = bm[size_t(e) * WS + w] & ((1u << (r & 31)) - 1u);
+        const int p = s_off[e] + wpre[size_t(e) * WS + w] + __popc(below);
         ub[L.pos + r * KS + k] = p;
         ub[L.src + p] = r * KS + k;
     }
