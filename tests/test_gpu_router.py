@@ -1,0 +1,90 @@
+"""The large-row router logits kernel against the oracle, bit for bit.
+
+Above 64 rows moe_route's logits come from a persistent kernel that takes
+tiles of 32 rows x 32 experts, streams x and the router weights through
+shared memory in stages of two 128-column blocks, keeps each 1024-column
+chunk's lane sums in tensor memory and ends each pair's reduction tree by
+recursive halving.  Its logits must be the header's fixed-order IEEE sums,
+i.e. the oracle's bits, at every edge of that structure:
+
+* row counts with a ragged last row tile (65, 100, 333) and the maximum, 4096;
+* expert counts that leave a partial expert tile (48, 72 of 32) or a single
+  one (16);
+* hidden sizes whose 128-column block count is odd (a stage's second half
+  past the end: 384, 1152, 6272) or fits one chunk (no chunk sums kept:
+  384, 1024), and the GLM-5.2 width 6144 (six chunks);
+* pad rows anywhere (their logits stay untouched: a sentinel survives).
+
+ids and weights are compared bit for bit too (the selection reads the
+logits).
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_speculative_verify_gb300 as m
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+SENTINEL = np.float32(-12345.5)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    m.build()
+    m.load()
+    oracle.lib()
+    torch.cuda.set_device(0)
+
+
+def _shape(H, E, G, TG, K):
+    return synth.LayerShape(hidden=H, inter=128, n_experts=E, n_groups=G, topk_groups=TG,
+                            topk=K, n_shared=1, routed_scaling=2.5)
+
+
+def _route(shape, R, pads, seed):
+    wl = synth.Workload("router", shape, rows=R, pads=tuple(pads), seed=seed)
+    ri = synth.make_router_inputs(wl, device="cpu")
+    E, K = shape.n_experts, shape.topk
+    cfg = m.Config.from_shape(shape)
+    ids = torch.empty((R, K), dtype=torch.int32, device="cuda")
+    w = torch.empty((R, K), dtype=torch.float32, device="cuda")
+    lg = torch.full((R, E), float(SENTINEL), dtype=torch.float32, device="cuda")
+    m.moe_route(cfg, ri["x"].cuda(), ri["wr"].cuda(), ri["bias"].cuda(),
+                ri["row_valid"].cuda(), ids, w, lg)
+    torch.cuda.synchronize()
+    h = synth.to_numpy(ri)
+    return h, ids.cpu().numpy(), w.cpu().numpy(), lg.cpu().numpy()
+
+
+def _check(shape, R, pads, seed, rows=None):
+    h, ids, w, lg = _route(shape, R, pads, seed)
+    valid = h["row_valid"] != 0
+    assert np.all(lg[~valid] == SENTINEL)
+    sel = np.arange(R) if rows is None else np.asarray(rows)
+    sel = sel[valid[sel]]
+    ref_ids, ref_w, ref_lg = oracle.route(shape, h["x"][sel], h["wr"], h["bias"])
+    assert np.array_equal(lg[sel].view(np.uint32), ref_lg.view(np.uint32))
+    assert np.array_equal(ids[sel], ref_ids)
+    assert np.array_equal(w[sel].view(np.uint32), ref_w.view(np.uint32))
+    assert np.all(ids[~valid] == -1) and np.all(w[~valid] == 0)
+
+
+@pytest.mark.parametrize("R,pads", [(65, (64,)), (100, (0, 37, 99)), (333, (200,))])
+@pytest.mark.parametrize("H", [384, 1024, 1152, 6272])
+def test_ragged_rows_and_odd_blocks(R, pads, H):
+    _check(_shape(H, 48, 4, 2, 6), R, pads, seed=R + H)
+
+
+@pytest.mark.parametrize("E,G,TG,K", [(16, 2, 1, 4), (72, 8, 4, 8), (256, 8, 4, 8)])
+def test_expert_tiles(E, G, TG, K):
+    _check(_shape(1152, E, G, TG, K), 97, (3, 50), seed=E)
+
+
+def test_full_size_sampled_rows():
+    # 4096 rows at the GLM-5.2 router shape: every pad and a sample of rows
+    R = 4096
+    rows = np.unique(np.r_[np.arange(0, 40), np.arange(R - 40, R), np.arange(0, R, 97)])
+    _check(_shape(6144, 256, 8, 4, 8), R, (1, 2047, 4095), seed=5, rows=rows)
