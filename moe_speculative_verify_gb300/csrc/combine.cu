@@ -35,30 +35,44 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       int S, uint16_t* __restrict__ out) {
     pdl_wait();
     pdl_launch_dependents();
-    if (!combine_union_ok(ub, R, E, K, S)) return;
     const int r = blockIdx.x;
     const int h = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
     if (h >= H) return;
     const int KS = K + S;
+    const float* w = wts + size_t(r) * K;
+    // The union's shape words, the row's pad word, the shared row and the
+    // first four slots are requested together (their addresses do not depend
+    // on the union's contents and lie inside the call's buffers), then
+    // checked: one memory round trip before the first fmas instead of three.
+    const int pos0 = ub[L.pos + size_t(r) * KS];
+    float4 ysh = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (S) ysh = __ldg(reinterpret_cast<const float4*>(y_shared + size_t(r) * H + h));
+    float4 y[4];
+    float wk[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        if (u < K) {
+            y[u] = __ldg(reinterpret_cast<const float4*>(y_slots + (size_t(r) * K + u) * H + h));
+            wk[u] = w[u];
+        }
+    }
+    if (!combine_union_ok(ub, R, E, K, S)) return;
     uint2* dst = reinterpret_cast<uint2*>(out + size_t(r) * H + h);
-    if (ub[L.pos + size_t(r) * KS] < 0) {
+    if (pos0 < 0) {
         *dst = make_uint2(0u, 0u);
         return;
     }
-    const float* w = wts + size_t(r) * K;
-    // the shared row first, then the K slots in k order, four rows requested
-    // at a time (few registers: more blocks per SM keep more rows in flight)
-    float4 ysh = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if (S) ysh = __ldg(reinterpret_cast<const float4*>(y_shared + size_t(r) * H + h));
+    // the K slots in k order, four rows requested at a time (few registers:
+    // more blocks per SM keep more rows in flight)
     float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
     for (int k0 = 0; k0 < K; k0 += 4) {
-        float4 y[4];
-        float wk[4];
+        if (k0 > 0) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            if (k0 + u < K) {
-                y[u] = __ldg(reinterpret_cast<const float4*>(y_slots + (size_t(r) * K + k0 + u) * H + h));
-                wk[u] = w[k0 + u];
+            for (int u = 0; u < 4; ++u) {
+                if (k0 + u < K) {
+                    y[u] = __ldg(reinterpret_cast<const float4*>(y_slots + (size_t(r) * K + k0 + u) * H + h));
+                    wk[u] = w[k0 + u];
+                }
             }
         }
 #pragma unroll
