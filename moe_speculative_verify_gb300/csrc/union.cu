@@ -278,20 +278,24 @@ __global__ void __launch_bounds__(256) dispatch_kernel(const uint16_t* __restric
     // the fused expert GEMM's per-item counters start at zero every call
     if (blockIdx.x == 0 && blockIdx.y == 0)
         for (int i = threadIdx.x; i < n_ready; i += blockDim.x) ready[i] = 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x;
+    const int HB = H / kBlock;
+    const int b = blockIdx.y * 8 + warp;
+    // the union's shape words, the row's first position and the x block are
+    // requested together (none of their addresses depends on the union's
+    // contents), then checked
+    const int32_t* pos = ub + L.pos + size_t(r) * KS;
+    const int p0 = (b < HB) ? pos[0] : -1;
+    uint2 xv = make_uint2(0u, 0u);
+    if (b < HB) xv = __ldg(reinterpret_cast<const uint2*>(x + size_t(r) * H + b * kBlock + 4 * lane));
     // a union built for another call: its positions may lie outside xg
     if (!union_fits(ub, R, ushape)) {
         if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
             record_error(err, MOE_ERR_INVALID_ARG);
         return;
     }
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = blockIdx.x;
-    const int HB = H / kBlock;
-    const int b = blockIdx.y * 8 + warp;
-    if (b >= HB) return;
-    const int32_t* pos = ub + L.pos + size_t(r) * KS;
-    if (pos[0] < 0) return;  // pad row
-    const uint2 xv = __ldg(reinterpret_cast<const uint2*>(x + size_t(r) * H + b * kBlock + 4 * lane));
+    if (b >= HB || p0 < 0) return;  // past the row's blocks, or a pad row
     const float f0 = bf16_bits_to_f32(xv.x & 0xFFFFu), f1 = bf16_bits_to_f32(xv.x >> 16);
     const float f2 = bf16_bits_to_f32(xv.y & 0xFFFFu), f3 = bf16_bits_to_f32(xv.y >> 16);
     float amax = fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3)));
@@ -301,7 +305,7 @@ __global__ void __launch_bounds__(256) dispatch_kernel(const uint16_t* __restric
     const uint32_t q = to_e4m3x4(__fdiv_rn(f0, sc), __fdiv_rn(f1, sc), __fdiv_rn(f2, sc),
                                  __fdiv_rn(f3, sc));
     for (int k = 0; k < KS; ++k) {
-        const int p = pos[k];
+        const int p = (k == 0) ? p0 : pos[k];
         reinterpret_cast<uint32_t*>(xg + size_t(p) * H + b * kBlock)[lane] = q;
         if (lane == 0) xs[size_t(p) * HB + b] = sc;
     }
