@@ -142,15 +142,32 @@ __global__ void __launch_bounds__(kNormThreads) combine_add_rmsnorm_kernel(
     cg::cluster_group cl = cg::this_cluster();
     pdl_wait();
     pdl_launch_dependents();
-    // the same words for every CTA of every cluster: all leave here or none
-    if (!combine_union_ok(ub, R, E, K, S)) return;
     const int r = blockIdx.x / kNormCluster;
     const int rank = static_cast<int>(cl.block_rank());
     const int KS = K + S;
     const int nchunks = H / 4 / kNormCluster;                 // float4 chunks of this CTA
     const int c0 = rank * nchunks;
+    const float* w = wts + size_t(r) * K;
+    // chunk c's K slots, shared row and residual
+    float4 y[MOE_MAX_TOPK + 1];
+    uint2 rb = make_uint2(0u, 0u);
+    auto load_chunk = [&](int c) {
+        const int h = 4 * (c0 + c);
+#pragma unroll
+        for (int k = 0; k < MOE_MAX_TOPK; ++k)
+            if (k < K) y[k] = __ldg(reinterpret_cast<const float4*>(y_slots + (size_t(r) * K + k) * H + h));
+        if (S) y[MOE_MAX_TOPK] = __ldg(reinterpret_cast<const float4*>(y_shared + size_t(r) * H + h));
+        rb = *reinterpret_cast<const uint2*>(residual + size_t(r) * H + h);
+    };
+    // The union's words, the row's pad word and the first chunk's rows are
+    // requested together (their addresses do not depend on the union's
+    // contents), then checked.
+    const int pos0 = ub[L.pos + size_t(r) * KS];
+    if (threadIdx.x < nchunks) load_chunk(threadIdx.x);
+    // the same words for every CTA of every cluster: all leave here or none
+    if (!combine_union_ok(ub, R, E, K, S)) return;
     // the same for every CTA of the cluster: all leave here or none
-    const bool valid = ub[L.pos + size_t(r) * KS] >= 0;
+    const bool valid = pos0 >= 0;
     if (!valid) {
         for (int c = threadIdx.x; c < nchunks; c += kNormThreads) {
             reinterpret_cast<uint2*>(residual_out + size_t(r) * H)[c0 + c] = make_uint2(0u, 0u);
@@ -158,7 +175,6 @@ __global__ void __launch_bounds__(kNormThreads) combine_add_rmsnorm_kernel(
         }
         return;
     }
-    const float* w = wts + size_t(r) * K;
     float4 z[kNormMaxChunks];
     float ss = 0.0f;
 #pragma unroll
@@ -166,11 +182,7 @@ __global__ void __launch_bounds__(kNormThreads) combine_add_rmsnorm_kernel(
         const int c = threadIdx.x + i * kNormThreads;
         if (c < nchunks) {
             const int h = 4 * (c0 + c);
-            float4 y[MOE_MAX_TOPK + 1];
-#pragma unroll
-            for (int k = 0; k < MOE_MAX_TOPK; ++k)
-                if (k < K) y[k] = __ldg(reinterpret_cast<const float4*>(y_slots + (size_t(r) * K + k) * H + h));
-            if (S) y[MOE_MAX_TOPK] = __ldg(reinterpret_cast<const float4*>(y_shared + size_t(r) * H + h));
+            if (i > 0) load_chunk(c);
             const float w0 = w[0];
             float a0 = __fmul_rn(w0, y[0].x), a1 = __fmul_rn(w0, y[0].y),
                   a2 = __fmul_rn(w0, y[0].z), a3 = __fmul_rn(w0, y[0].w);
@@ -190,7 +202,6 @@ __global__ void __launch_bounds__(kNormThreads) combine_add_rmsnorm_kernel(
                 a2 = __fadd_rn(a2, y[MOE_MAX_TOPK].z);
                 a3 = __fadd_rn(a3, y[MOE_MAX_TOPK].w);
             }
-            const uint2 rb = *reinterpret_cast<const uint2*>(residual + size_t(r) * H + h);
             float4 zz;
             zz.x = __fadd_rn(bf16_bits_to_f32(rb.x & 0xFFFFu), a0);
             zz.y = __fadd_rn(bf16_bits_to_f32(rb.x >> 16), a1);
