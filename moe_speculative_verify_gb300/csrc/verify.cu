@@ -24,7 +24,7 @@ namespace moe {
 
 namespace {
 
-constexpr int kArgmaxThreads = 256;
+constexpr int kArgmaxThreads = 512;
 constexpr int kArgmaxCluster = 8;      // CTAs per row
 
 __device__ __forceinline__ uint64_t argmax_key(float v, uint32_t idx) {
@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(kArgmaxThreads) row_argmax_kernel(const void* 
         const uint16_t* row = static_cast<const uint16_t*>(logits) + size_t(r) * V;
         if (VEC) {
             const uint4* rv = reinterpret_cast<const uint4*>(row);
-#pragma unroll 4
+#pragma unroll 8
             for (int i = lo + threadIdx.x; i < hi; i += kArgmaxThreads) {
                 const uint4 q = __ldg(rv + i);
                 const uint32_t w[4] = {q.x, q.y, q.z, q.w};
@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kArgmaxThreads) row_argmax_kernel(const void* 
         const float* row = static_cast<const float*>(logits) + size_t(r) * V;
         if (VEC) {
             const float4* rv = reinterpret_cast<const float4*>(row);
-#pragma unroll 4
+#pragma unroll 8
             for (int i = lo + threadIdx.x; i < hi; i += kArgmaxThreads) {
                 const float4 q = __ldg(rv + i);
                 best = max64(best, argmax_key(q.x, 4 * i));
