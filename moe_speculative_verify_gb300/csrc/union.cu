@@ -110,41 +110,17 @@ __device__ void union_block(const int32_t* ids, int R, int E, int K, int S, int 
     }
     __syncthreads();
 
-    // 3. per-expert counts and per-word prefix counts.  Up to 128 rows (a few
-    //    words per expert): a thread per expert.  More: one warp per expert,
-    //    lane l taking a contiguous run of the expert's words (a thread per
-    //    expert would put a whole warp on one shared-memory bank: experts are
-    //    W words apart), then an exclusive scan over the lanes
-    if (W <= 4) {
-        for (int e = tid; e < E; e += kUnionThreads) {
-            int c = 0;
-            for (int w = 0; w < W; ++w) {
-                wpre[size_t(e) * WS + w] = static_cast<uint16_t>(c);
-                c += __popc(bm[size_t(e) * WS + w]);
-            }
-            s_cnt[e] = c;
+    // 3. per-expert counts and per-word prefix counts, a thread per expert
+    //    (the odd stride puts the experts' words on different banks; at 512
+    //    and 4096 rows this measured faster than a warp per expert, 16.4 ->
+    //    12.4 and 54.2 -> 51.2 us)
+    for (int e = tid; e < E; e += kUnionThreads) {
+        int c = 0;
+        for (int w = 0; w < W; ++w) {
+            wpre[size_t(e) * WS + w] = static_cast<uint16_t>(c);
+            c += __popc(bm[size_t(e) * WS + w]);
         }
-    } else {
-        const int warp = tid >> 5, lane = tid & 31;
-        const int per = (W + 31) / 32;
-        const int w0 = min(W, lane * per), w1 = min(W, w0 + per);
-        for (int e = warp; e < E; e += kUnionThreads / 32) {
-            const uint32_t* bme = bm + size_t(e) * WS;
-            int c = 0;
-            for (int w = w0; w < w1; ++w) c += __popc(bme[w]);
-            int incl = c;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const int o = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-                if (lane >= d) incl += o;
-            }
-            int run = incl - c;
-            for (int w = w0; w < w1; ++w) {
-                wpre[size_t(e) * WS + w] = static_cast<uint16_t>(run);
-                run += __popc(bme[w]);
-            }
-            if (lane == 31) s_cnt[e] = incl;
-        }
+        s_cnt[e] = c;
     }
     if (tid == 0) s_cnt[E] = S ? s_nvalid : 0;
     __syncthreads();
