@@ -1,0 +1,94 @@
+"""Degenerate batches through the whole layer on the GPU.
+
+* Every row a pad row, at 8 rows (selection + union in one block, one fused
+  GEMM launch), 37 rows (16-row tiles) and 100 rows (separate selection and
+  union kernels, the gate/up and down GEMM launches): the union is empty, no
+  GEMM tile exists, and the layer must still return +0.0 rows, ids -1, weights
+  0 and a clean device status -- also through the w8a16 layer.
+* One valid row among pads (a union of a single row): parity with the oracle.
+* All-pad, normal and all-pad calls in a row on one workspace: the GEMMs' tile
+  scheduler words, reset by the last CTA of each launch, leave the following
+  call unaffected (its outputs match a fresh workspace's bit for bit).
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_speculative_verify_gb300 as m
+import oracle
+import synth
+from gpu_helpers import MEDIUM, TOL, bf16_bits_to_f64, bf16_to_np, rel_fro, run_layer
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    m.build()
+    m.load()
+    oracle.lib()
+    torch.cuda.set_device(0)
+
+
+def _layer(shape, R, pads, seed=3):
+    wl = synth.Workload("edge", shape, rows=R, pads=tuple(pads), seed=seed)
+    t_cpu = synth.make_layer(wl, device="cpu")
+    return t_cpu, {k: v.cuda() for k, v in t_cpu.items()}
+
+
+@pytest.mark.parametrize("shape,R", [(synth.TINY, 8), (MEDIUM, 37), (MEDIUM, 100)])
+def test_all_rows_pad(shape, R):
+    _, t = _layer(shape, R, range(R))
+    cfg = m.Config.from_shape(shape)
+    out, ids, w, _ = run_layer(cfg, t, R)
+    assert np.all(bf16_to_np(out) == 0)
+    assert np.all(ids.cpu().numpy() == -1)
+    assert np.all(w.cpu().numpy().view(np.uint32) == 0)
+
+
+def test_all_rows_pad_w8a16():
+    shape, R = synth.TINY, 8
+    _, t = _layer(shape, R, range(R))
+    cfg = m.Config.from_shape(shape)
+    ws = torch.zeros(m.moe_workspace_bytes(cfg, R), dtype=torch.uint8, device="cuda")
+    out = torch.full((R, shape.hidden), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty((R, shape.topk), dtype=torch.int32, device="cuda")
+    w = torch.empty((R, shape.topk), dtype=torch.float32, device="cuda")
+    m.moe_layer_w8a16(cfg, t["x"], t["wr"], t["bias"], m.Weights.from_tensors(t),
+                      t["row_valid"], out, ws, topk_ids=ids, topk_w=w)
+    torch.cuda.synchronize()
+    assert m.moe_get_device_error(ws) == 0
+    assert np.all(bf16_to_np(out) == 0)
+    assert np.all(ids.cpu().numpy() == -1)
+
+
+@pytest.mark.parametrize("R,keep", [(8, 5), (100, 0), (100, 99)])
+def test_single_valid_row(R, keep):
+    shape = MEDIUM
+    t_cpu, t = _layer(shape, R, [r for r in range(R) if r != keep], seed=R + keep)
+    cfg = m.Config.from_shape(shape)
+    out, ids, w, _ = run_layer(cfg, t, R)
+    h = synth.to_numpy(t_cpu)
+    ref = oracle.moe_layer(shape, h)
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    assert np.array_equal(w.cpu().numpy().view(np.uint32), ref["wts"].view(np.uint32))
+    y = bf16_bits_to_f64(bf16_to_np(out))
+    assert rel_fro(y[keep], ref["y_acc"][keep]) <= TOL
+    pads = np.arange(R) != keep
+    assert np.all(bf16_to_np(out)[pads] == 0)
+
+
+@pytest.mark.parametrize("R", [8, 100])
+def test_pad_calls_leave_workspace_clean(R):
+    shape = MEDIUM
+    cfg = m.Config.from_shape(shape)
+    _, t_pad = _layer(shape, R, range(R), seed=1)
+    _, t = _layer(shape, R, (R - 1,), seed=2)
+    fresh, _, _, _ = run_layer(cfg, t, R)
+    ws = torch.zeros(m.moe_workspace_bytes(cfg, R), dtype=torch.uint8, device="cuda")
+    for tt in (t_pad, t, t_pad, t):
+        out, _, _, _ = run_layer(cfg, tt, R, ws=ws)
+        if tt is t:
+            assert np.array_equal(bf16_to_np(out), bf16_to_np(fresh))
+        else:
+            assert np.all(bf16_to_np(out) == 0)
