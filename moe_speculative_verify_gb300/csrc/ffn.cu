@@ -94,7 +94,7 @@ struct FfnCfg {
 };
 
 constexpr int kMaxStages = 16;
-constexpr int kStagesNt16 = 8;   // ring depth where the weight stream counts (see launch_ffn_t)
+constexpr int kStagesNt16 = 10;   // ring depth where the weight stream counts (see launch_ffn_t)
 constexpr int kStagesWide = 6;        // ring depth of the separate kernels at 64-row tiles ...
 constexpr int kStagesWideDecode = 7;  // ... and in calls of at most 512 rows
 // Per K-block (not per stage) synchronisation, on two rings of barriers
@@ -815,11 +815,13 @@ static cudaError_t launch_ffn_t(const FfnMaps& mp, FfnArgs args, int n_sms, int 
     const int KB_H = args.H / kBlock, KB_I = args.I / kBlock;
     const int kbmax = (MODE == kFfnGateUp) ? KB_H : (MODE == kFfnDown) ? KB_I : max(KB_H, KB_I);
     // HBM streams 16 KB tiles fastest with about 8 of them in flight per SM
-    // (a TMA probe: 7.2 TB/s at 6-8, 6.5 at 12).  Measured: 8 stages are
-    // faster at 16-row tiles and in the separate gate/up and down kernels at
-    // 32 rows; in those at 64 rows 7 up to 512 rows (decode512's GEMMs 1.141
-    // -> 1.125 ms) and 6 above (prefill4096's 3.92 -> 3.82 ms); the fused
-    // kernel at 32 and 64 rows keeps every stage that fits.
+    // (a TMA probe: 7.2 TB/s at 6-8, 6.5 at 12).  Measured: 10 stages at
+    // 16-row tiles and in the separate gate/up and down kernels at 32 rows
+    // (verify8's layer 0.2439 -> 0.2415 ms against 8, the same from 10 to 14:
+    // the first tile requests more weights before its dependent-launch wait);
+    // in those at 64 rows 7 up to 512 rows (decode512's GEMMs 1.141 -> 1.125
+    // ms) and 6 above (prefill4096's 3.92 -> 3.82 ms); the fused kernel at 32
+    // and 64 rows keeps every stage that fits.
     int stages = kMaxStages;
     if (NT == 16 || (MODE != kFfnFused && NT == 32)) stages = kStagesNt16;
     if (MODE != kFfnFused && NT == 64) stages = (args.R <= 512) ? kStagesWideDecode : kStagesWide;
