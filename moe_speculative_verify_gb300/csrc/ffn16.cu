@@ -65,6 +65,10 @@ constexpr int kACols = 64;                   // a bf16 128x128 tile in TMEM: 2 p
 constexpr int kAColBase = kAccBufs * kAccCols;
 constexpr int kTmemCols = 512;
 static_assert(kAColBase + kSlots * kACols <= kTmemCols, "tensor memory");
+// every dequant group owns its own operand slots (step n uses slot
+// n % kSlots, group g the steps g, g + kDqGroups, ...): a variant with slots
+// shared between groups (4 slots) faulted on the GPU and is not supported
+static_assert(kSlots % kDqGroups == 0, "operand slots a multiple of the dequant groups");
 static_assert(kSlotBytes % 1024 == 0, "operand slots stay 1024-byte aligned");
 
 // Tiles are handed out at run time, as in the fp8 GEMM: a CTA's first tile
