@@ -7,7 +7,10 @@ on either side of the kernels' switches (64 rows: selection + union in one
 block and one fused GEMM; 65-256: 32-row tiles; above: 64-row tiles and the
 TMA router), with pad rows anywhere.  Routing ids and weights must be
 bit-exact, every valid row within the parity tolerance and every pad row +0.0.
-The seeds are fixed, so a failure names a case that reproduces.
+The same cases also go through the step-by-step entry points (the union's
+words equal to the oracle's union of the same ids, the combined output
+bit-identical to moe_layer's) and, at 64 rows or fewer, through the w8a16
+layer against the oracle's w8a16 variant.  The seeds are fixed, so a failure names a case that reproduces.
 """
 import numpy as np
 import pytest
@@ -68,3 +71,75 @@ def test_random_shape_against_oracle(seed):
     for r in np.nonzero(valid)[0]:
         assert rel_fro(y[r], ref["y_acc"][r]) <= TOL, (shape, R, r)
     assert np.all(ob[~valid] == 0)
+
+
+@pytest.mark.parametrize("seed", range(N_CASES))
+def test_random_shape_stepwise_and_union(seed):
+    """The step-by-step entry points on the same cases: the union's words as the
+    oracle's union of the same ids, and the combined output bit-identical to
+    moe_layer's."""
+    shape, R, pads = _draw(seed)
+    wl = synth.Workload(f"fuzz{seed}", shape, rows=R, pads=pads, seed=seed)
+    t_cpu = synth.make_layer(wl, device="cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    cfg = m.Config.from_shape(shape)
+    E, K, H, S = shape.n_experts, shape.topk, shape.hidden, shape.n_shared
+    dev = torch.device("cuda")
+    ids = torch.empty((R, K), dtype=torch.int32, device=dev)
+    w = torch.empty((R, K), dtype=torch.float32, device=dev)
+    logits = torch.zeros((R, E), dtype=torch.float32, device=dev)
+    m.moe_route(cfg, t["x"], t["wr"], t["bias"], t["row_valid"], ids, w, logits)
+    ub = torch.zeros(m.moe_union_bytes(cfg, R) // 4, dtype=torch.int32, device=dev)
+    m.moe_build_union(cfg, ids, ub)
+    u = ub.cpu().numpy()
+    ref = oracle.build_union(shape, ids.cpu().numpy())
+    lay = m.union_layout(cfg, R)
+    # The oracle always lays out a shared slot (K + 1 per row, the shared rows
+    # gathered after every expert's); without a shared expert the library keeps
+    # K per row and stops at the routed rows, so compare the routed part.
+    KS = K + S
+    T = int(ref["offsets"][E + S])
+    assert u[0] == ref["n_union"] and u[1] == ref["n_valid"] and u[2] == T
+    assert u[4] == m.rows_per_item(R) and u[5] == 0
+    assert np.array_equal(u[lay["counts"]:lay["counts"] + E], ref["counts"][:E])
+    assert np.array_equal(u[lay["offsets"]:lay["offsets"] + E + 1], ref["offsets"][:E + 1])
+    assert np.array_equal(u[lay["ulist"]:lay["ulist"] + ref["n_union"] + 1], ref["ulist"])
+    pos = u[lay["pos"]:lay["pos"] + R * KS].reshape(R, KS)
+    assert np.array_equal(pos, ref["pos"][:, :KS])
+    rs, ks = np.divmod(ref["src"][:T], K + 1)
+    assert np.array_equal(u[lay["src"]:lay["src"] + T], rs * KS + ks)
+    ws = torch.zeros(m.moe_ffn_workspace_bytes(cfg, R), dtype=torch.uint8, device=dev)
+    y_slots = torch.full((R * K, H), float("nan"), dtype=torch.float32, device=dev)
+    y_sh = torch.full((R, H), float("nan"), dtype=torch.float32, device=dev) if S else None
+    m.moe_expert_ffn_fp8(cfg, t["x"], m.Weights.from_tensors(t), ub, y_slots, y_sh, ws)
+    out = torch.full((R, H), float("nan"), dtype=torch.bfloat16, device=dev)
+    m.moe_combine(cfg, y_slots, y_sh, w, ub, out)
+    torch.cuda.synchronize()
+    assert m.moe_get_device_error(ws) == 0
+    layer_out, _, _, _ = run_layer(cfg, t, R)
+    assert np.array_equal(bf16_to_np(out), bf16_to_np(layer_out))
+
+
+@pytest.mark.parametrize("seed", [s for s in range(N_CASES) if _draw(s)[1] <= m.W8A16_MAX_ROWS])
+def test_random_shape_w8a16(seed):
+    shape, R, pads = _draw(seed)
+    wl = synth.Workload(f"fuzz{seed}", shape, rows=R, pads=pads, seed=seed)
+    t_cpu = synth.make_layer(wl, device="cpu")
+    t = {k: v.cuda() for k, v in t_cpu.items()}
+    h = synth.to_numpy(t_cpu)
+    cfg = m.Config.from_shape(shape)
+    ws = torch.zeros(m.moe_workspace_bytes(cfg, R), dtype=torch.uint8, device="cuda")
+    out = torch.full((R, shape.hidden), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty((R, shape.topk), dtype=torch.int32, device="cuda")
+    w = torch.empty((R, shape.topk), dtype=torch.float32, device="cuda")
+    m.moe_layer_w8a16(cfg, t["x"], t["wr"], t["bias"], m.Weights.from_tensors(t),
+                      t["row_valid"], out, ws, topk_ids=ids, topk_w=w)
+    torch.cuda.synchronize()
+    assert m.moe_get_device_error(ws) == 0
+    ref = oracle.moe_layer(shape, h, variant="w8a16")
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    y = bf16_bits_to_f64(bf16_to_np(out))
+    valid = h["row_valid"] != 0
+    for r in np.nonzero(valid)[0]:
+        assert rel_fro(y[r], ref["y_acc"][r]) <= TOL, (shape, R, r)
+    assert np.all(bf16_to_np(out)[~valid] == 0)
