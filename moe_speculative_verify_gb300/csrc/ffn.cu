@@ -85,8 +85,9 @@ struct FfnCfg {
                                      : (ACC_BUFS * ACC_COLS <= 128) ? 128
                                      : (ACC_BUFS * ACC_COLS <= 256) ? 256 : 512;
     static_assert(ACC_BUFS * ACC_COLS <= 512, "tensor memory");
-    // suspend-time hint of the role loops' barrier waits: at 32- and 64-row
-    // tiles waiting warps then leave their issue slots to the epilogue warps
+    // suspend-time hint of the producer's and MMA issuers' barrier waits: at
+    // 32- and 64-row tiles waiting warps then leave their issue slots to the
+    // epilogue warps
     // (measured: decode512's GEMMs 1.259 -> 1.220 ms, prefill4096's 4.09 ->
     // 4.02); at 16-row tiles, where the HBM stream bounds the kernel, none
     static constexpr uint32_t WAIT_HINT_NS = (NT >= 32) ? 20000u : 0u;
@@ -639,8 +640,13 @@ __global__ void __maxnreg__((FfnCfg<NT, MODE>::MAX_REGS))
             // tile keeps the plain loop, 1% faster there)
             const bool live = NT == 16 || cg * CW < nrow;
             for (int kb = 0; kb < KB && ok; ++kb) {
-                // a failed wait is acted on by the whole warp (tcgen05.ld is warp-wide)
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait<C::WAIT_HINT_NS>(
+                // a failed wait is acted on by the whole warp (tcgen05.ld is warp-wide).
+                // No suspend hint here: the epilogue releases the partials the
+                // MMA waits for, so it polls (measured: prefill4096's GEMMs
+                // 3.788 -> 3.721 ms, decode512's 1.097 -> 1.089; the producer and
+                // the MMA issuers keep the hint, and a sleep between their polls
+                // was slower still)
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait<0>(
                                                  &kbrel[je % kKbRing], (je / kKbRing) & 1u, p.err,
                                                  p.timeout_ns))) {
                     ok = false;
