@@ -23,6 +23,7 @@ __all__ = [
     "moe_diag_wait_timeout", "moe_status_string", "moe_dispatch", "moe_gate_up_fp8",
     "moe_down_fp8", "ffn_layout", "moe_layer_noalloc", "moe_expert_gemms_fp8",
     "moe_greedy_verify", "moe_combine_add_rmsnorm", "union_layout", "rows_per_item",
+    "router_rows_per_warp",
     "MOE_MAX_ROWS", "moe_expert_ffn_w8a16", "moe_layer_w8a16", "W8A16_MAX_ROWS",
     "moe_tile_weights", "tile_weights", "LAYOUT_ROW_MAJOR", "LAYOUT_TILED",
     "moe_workspace_size",
@@ -320,6 +321,21 @@ def moe_diag_wait_timeout(ws, timeout_us: int, stream=None) -> None:
 
 # ---------------------------------------------------------------- layouts --
 W8A16_MAX_ROWS = 64          # the w8a16 variant's row limit (mirrors the library)
+
+def router_rows_per_warp(R: int, E: int, n_sms: int = None) -> int:
+    """Rows a consumer warp of the large-R router kernel takes per tile (tiles
+    of 4x that many rows): 8 or 6 (mirrors the library's choice; n_sms
+    defaults to the current device's SM count)."""
+    if n_sms is None:
+        import torch
+        n_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+
+    def busiest(rt):
+        tiles = -(-R // (4 * rt)) * -(-E // 32)
+        grid = min(tiles, max(n_sms, 1))
+        return -(-tiles // grid) * (rt + 3)
+    return 6 if busiest(6) < busiest(8) else 8
+
 
 def rows_per_item(R: int) -> int:
     """Rows per GEMM work item chosen for a call with R rows (mirrors the library)."""

@@ -121,14 +121,17 @@ moe_status_t check_weights(const moe_config_t* c, const moe_weights_t* w) {
 // The large-R router's maps: x bf16 [R, H] and w fp32 [E, H], boxes of
 // kRouterStageCols columns x 32 rows, unswizzled; rows and columns past the
 // end read as zero.
-bool make_router_maps(const void* x, const float* wr, int R, int H, int E, moe::RouterMaps* m) {
+bool make_router_maps(const void* x, const float* wr, int R, int H, int E, int n_sms,
+                      moe::RouterMaps* m) {
     auto fn = encode_fn();
     if (!fn) return false;
+    m->rt = moe::router_rows_per_warp(R, E, n_sms);
+    const cuuint32_t xbox[2] = {cuuint32_t(moe::kRouterStageCols), cuuint32_t(4 * m->rt)};
     const cuuint32_t box[2] = {cuuint32_t(moe::kRouterStageCols), 32};
     const cuuint32_t es[2] = {1, 1};
     const cuuint64_t xd[2] = {cuuint64_t(H), cuuint64_t(R)}, xs[1] = {cuuint64_t(H) * 2};
     const cuuint64_t wd[2] = {cuuint64_t(H), cuuint64_t(E)}, wst[1] = {cuuint64_t(H) * 4};
-    return fn(&m->x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), xd, xs, box, es,
+    return fn(&m->x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), xd, xs, xbox, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
                CUDA_SUCCESS &&
@@ -142,12 +145,14 @@ moe_status_t route_impl(const moe_config_t* c, const void* x, const float* wr, c
                         const uint8_t* valid, int32_t R, int32_t* ids, float* wts, float* logits,
                         int32_t* err, cudaStream_t s) {
     moe::RouterMaps maps;
-    if (R > moe::kRouteUnionMaxRows && !make_router_maps(x, wr, R, c->hidden, c->n_experts, &maps))
+    const int sms = device_info().sms;
+    if (R > moe::kRouteUnionMaxRows &&
+        !make_router_maps(x, wr, R, c->hidden, c->n_experts, sms, &maps))
         return MOE_ERR_CUDA;
     return cuda_status(moe::launch_router(static_cast<const uint16_t*>(x), wr, bias, valid, R,
                                           c->hidden, c->n_experts, c->n_groups, c->topk_groups,
                                           c->topk, c->routed_scaling, ids, wts, logits, &maps,
-                                          device_info().sms, err, timeout_ns(c), s));
+                                          sms, err, timeout_ns(c), s));
 }
 
 moe_status_t union_impl(const moe_config_t* c, const int32_t* ids, int32_t R, int32_t* ub,

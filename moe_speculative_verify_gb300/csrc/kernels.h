@@ -78,15 +78,34 @@ cudaError_t launch_dispatch16(const uint16_t* x, const int32_t* ub, const UnionL
                               int n_ready, int32_t* err, cudaStream_t stream);
 cudaError_t launch_ffn16(const FfnMaps& mp, Ffn16Args args, int n_sms, int smem_limit,
                          cudaStream_t stream);
-// Tensor maps of the large-R router logits kernel: x bf16 [R, H] and the
-// router weights fp32 [E, H], unswizzled boxes of kRouterStageCols columns x
-// 32 rows.
+// Tensor maps of the large-R router logits kernel: x bf16 [R, H] in boxes of
+// 4 * rt rows and the router weights fp32 [E, H] in boxes of 32 rows,
+// unswizzled, kRouterStageCols columns wide; rt = rows of a consumer warp
+// (router_rows_per_warp).
 // Two 128-column blocks a stage: measured at 4096 rows, 410 -> 354 us
 // against one (half as many barrier waits and releases per column).
 constexpr int kRouterStageCols = 256;
 struct RouterMaps {
     CUtensorMap x, w;
+    int rt;
 };
+
+// Rows a consumer warp of the large-R router kernel takes per tile (tiles of
+// 4x that many rows x 32 experts): 8, or 6 where that makes the busiest of the
+// n_sms CTAs finish sooner.  A CTA's time is its tile count times a tile's
+// cost, about rt + 3 rows of a warp's work (measured: a 24-row tile takes
+// 0.82 of a 32-row tile's time).  So 6 wins where the tiles fit in one wave
+// either way (moe_route at 72 and 333 rows: 53 -> 46 us), 8 at 4096 rows,
+// where 24-row tiles would even out the SMs' loads (9 tiles each instead of
+// 7 on some and 6 on others) but cost 5 % more in all.
+inline int router_rows_per_warp(int R, int E, int n_sms) {
+    auto busiest = [&](int rt) {
+        const int tiles = ((R + 4 * rt - 1) / (4 * rt)) * ((E + 31) / 32);
+        const int grid = tiles < n_sms ? tiles : (n_sms > 0 ? n_sms : 1);
+        return ((tiles + grid - 1) / grid) * (rt + 3);
+    };
+    return busiest(6) < busiest(8) ? 6 : 8;
+}
 // Above 64 rows `maps` is required; a wait that runs out records
 // MOE_ERR_TIMEOUT in *err (when err is not null).
 cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const uint8_t* row_valid,

@@ -105,13 +105,15 @@ __global__ void __launch_bounds__(MAXT, MINB) router_logits_kernel(
     }
 }
 
-// Large-R variant, persistent (one CTA per SM): tiles of kLR rows x kLE
-// experts, tile t at rows (t / n_eb) * kLR and experts (t % n_eb) * kLE, taken
-// by the CTAs in turn.  Consumer warp w owns the tile's rows (w / 2) * 8 .. +7
-// and experts (w % 2) * 16 .. +15, and lane l of the warp is lane l of the
-// reduction tree for those 128 (row, expert) pairs: each row's x is widened
-// from bf16 once for 16 experts (measured at 4096 rows: 319.5 -> 309.2 us
-// against 16 rows x 8 experts, at 25 % more shared-memory reads).
+// Large-R variant, persistent (one CTA per SM): tiles of LR = 4 * RT rows x
+// kLE experts, tile t at rows (t / n_eb) * LR and experts (t % n_eb) * kLE,
+// taken by the CTAs in turn.  Consumer warp w owns the tile's rows
+// (w / 2) * RT .. +RT-1 and experts (w % 2) * 16 .. +15, and lane l of the
+// warp is lane l of the reduction tree for those RT * 16 (row, expert) pairs:
+// each row's x is widened from bf16 once for 16 experts (measured at 4096
+// rows: 319.5 -> 309.2 us against 16 rows x 8 experts, at 25 % more
+// shared-memory reads).  RT = 8 (32-row tiles) or 6 (24-row tiles), as
+// router_rows_per_warp chooses.
 //
 // Per stage of kLCols columns, x [kLR][kLCols] bf16 and w [kLE][kLCols] fp32
 // arrive by TMA in a ring of kLStages slots (a full and an empty barrier
@@ -129,11 +131,12 @@ __global__ void __launch_bounds__(MAXT, MINB) router_logits_kernel(
 // tree by recursive halving: at distance d = 16 .. 1 each lane keeps half of
 // its values and adds its partner's copy of them, which are the xor
 // butterfly's additions (v[l] + v[l ^ d], IEEE addition commutes) with every
-// value summed in one lane only; lane l ends with pairs 4l .. 4l + 3.  The
-// same IEEE operations in the same order as the small-R kernel.
-constexpr int kLR = 32, kLE = 32;
-constexpr int kLPE = 16, kLRT = 8, kLNP = kLRT * kLPE;   // experts, rows, pairs of a thread
-constexpr int kLWarps = (kLR / kLRT) * (kLE / kLPE);       // consumer warps
+// value summed in one lane only; lane l ends with pairs RT*l/2 .. RT*l/2 + RT/2 - 1.
+// The same IEEE operations in the same order as the small-R kernel, at
+// either RT.
+constexpr int kLE = 32;
+constexpr int kLPE = 16;                                    // experts of a thread
+constexpr int kLWarps = 4 * (kLE / kLPE);                   // consumer warps
 constexpr int kLThreads = 32 * (4 + kLWarps);              // + the producer warpgroup
 constexpr int kLProdRegs = 40, kLConsRegs = 232, kLLaunchRegs = 65536 / kLThreads / 8 * 8;
 static_assert(kLWarps == 8, "two consumer warpgroups");
@@ -141,12 +144,20 @@ static_assert(128 * kLProdRegs + 32 * kLWarps * kLConsRegs <= kLThreads * kLLaun
               "register split within the launch's registers");
 constexpr int kLCols = kRouterStageCols;                 // columns per stage
 constexpr int kLBlk = kLCols / 128;                      // 128-column blocks per stage
-constexpr int kLStages = 1024 / kLCols;                  // 192 KB of stages
-constexpr int kLXBytes = kLR * kLCols * 2, kLWBytes = kLE * kLCols * 4;
-constexpr int kLStageBytes = kLXBytes + kLWBytes;
-constexpr uint32_t kLTmemCols = (kLWarps / 4) * kLNP;    // warps per lane quarter x pairs
-constexpr size_t kLSmem = size_t(kLStages) * kLStageBytes + 256;
+constexpr int kLStages = 1024 / kLCols;                  // up to 192 KB of stages
+constexpr int kLWBytes = kLE * kLCols * 4;
+constexpr uint32_t kLTmemCols = 256;                     // (warps per lane quarter) x pairs, <= 256
 static_assert(kLBlk >= 1 && 8 % kLBlk == 0, "a stage holds whole blocks of one chunk");
+template <int RT>
+struct RouterTile {
+    static constexpr int LR = 4 * RT;                    // rows of a tile
+    static constexpr int NP = RT * kLPE;                 // pairs of a thread
+    static constexpr int XBytes = LR * kLCols * 2;
+    static constexpr int StageBytes = XBytes + kLWBytes;
+    static constexpr size_t Smem = size_t(kLStages) * StageBytes + 256;
+    static_assert(NP % 32 == 0 && (kLWarps / 4) * NP <= int(kLTmemCols), "pairs per lane, TMEM");
+    static_assert(XBytes % 128 == 0 && StageBytes % 128 == 0, "TMA destinations 128-byte aligned");
+};
 
 __device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float* v) {
     asm volatile(
@@ -177,10 +188,14 @@ __device__ __forceinline__ void halve(float (&v)[M], int lane) {
     }
 }
 
+template <int RT>
 __global__ void __launch_bounds__(kLThreads, 1) router_logits_tma_kernel(
     const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
     const uint8_t* __restrict__ row_valid, int R, int H, int E, float* __restrict__ logits,
     int32_t* err, uint64_t timeout_ns) {
+    using T = RouterTile<RT>;
+    constexpr int kLR = T::LR, kLRT = RT, kLNP = T::NP;
+    constexpr int kLXBytes = T::XBytes, kLStageBytes = T::StageBytes;
     extern __shared__ __align__(1024) uint8_t lsm[];
     uint64_t* full = reinterpret_cast<uint64_t*>(lsm + kLStages * kLStageBytes);
     uint64_t* empty = full + kLStages;                               // consumers done with it
@@ -347,13 +362,17 @@ __global__ void __launch_bounds__(kLThreads, 1) router_logits_tma_kernel(
             halve<kLNP, kLNP / 4, 4>(p, lane);
             halve<kLNP, kLNP / 8, 2>(p, lane);
             halve<kLNP, kLNP / 16, 1>(p, lane);
-            // lane l holds pairs 4l .. 4l + 3: row 4l / kLPE, experts from (4l) % kLPE
-            const int r = (t / n_eb) * kLR + wrow + (4 * lane) / kLPE;
-            const int e = (t % n_eb) * kLE + wexp + (4 * lane) % kLPE;
-            if (r < R && (row_valid == nullptr || row_valid[r] != 0)) {
+            // lane l holds pairs NL*l .. NL*l + NL-1 (NL = kLNP / 32), pair k
+            // being row k / kLPE and expert k % kLPE of the warp's block
+            constexpr int NL = kLNP / 32;
+            const int r0 = (t / n_eb) * kLR + wrow;
+            const int e0 = (t % n_eb) * kLE + wexp;
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (e + j < E) logits[size_t(r) * E + e + j] = p[j];
+            for (int j = 0; j < NL; ++j) {
+                const int k = NL * lane + j;
+                const int r = r0 + k / kLPE, e = e0 + k % kLPE;
+                if (r < R && e < E && (row_valid == nullptr || row_valid[r] != 0))
+                    logits[size_t(r) * E + e] = p[j];
             }
         }
     }
@@ -404,6 +423,26 @@ __global__ void __launch_bounds__(kSelWarps * 32) route_select_kernel(
 }
 
 // ----------------------------------------------------------- launchers ----
+template <int RT>
+static cudaError_t launch_router_tma(const CUtensorMap& xmap, const CUtensorMap& wmap,
+                                     const uint8_t* row_valid, int R, int H, int E, float* logits,
+                                     int n_sms, int32_t* err, uint64_t timeout_ns,
+                                     cudaStream_t stream) {
+    using T = RouterTile<RT>;
+    const int n_tiles = ((R + T::LR - 1) / T::LR) * ((E + kLE - 1) / kLE);
+    cudaError_t e = cudaFuncSetAttribute(router_logits_tma_kernel<RT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(T::Smem));
+    if (e != cudaSuccess) return e;
+    // the warpgroups' register split needs the launch's full share
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, router_logits_tma_kernel<RT>)) != cudaSuccess) return e;
+    if (fa.numRegs < kLLaunchRegs) return cudaErrorInvalidConfiguration;
+    return launch_pdl(router_logits_tma_kernel<RT>, dim3(min(n_tiles, max(n_sms, 1))),
+                      dim3(kLThreads), T::Smem, stream, xmap, wmap, row_valid, R, H, E, logits,
+                      err, timeout_ns);
+}
+
 cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const uint8_t* row_valid,
                                  int R, int H, int E, float* logits, const RouterMaps* maps,
                                  int n_sms, int32_t* err, uint64_t timeout_ns,
@@ -425,18 +464,12 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const uint8
         if (e != cudaSuccess) return e;
     } else {
         if (maps == nullptr) return cudaErrorInvalidValue;
-        const int n_tiles = ((R + kLR - 1) / kLR) * ((E + kLE - 1) / kLE);
-        cudaError_t e = cudaFuncSetAttribute(router_logits_tma_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kLSmem));
-        if (e != cudaSuccess) return e;
-        // the warpgroups' register split needs the launch's full share
-        cudaFuncAttributes fa;
-        if ((e = cudaFuncGetAttributes(&fa, router_logits_tma_kernel)) != cudaSuccess) return e;
-        if (fa.numRegs < kLLaunchRegs) return cudaErrorInvalidConfiguration;
-        e = launch_pdl(router_logits_tma_kernel, dim3(min(n_tiles, max(n_sms, 1))),
-                       dim3(kLThreads), kLSmem, stream, maps->x, maps->w, row_valid, R, H, E,
-                       logits, err, timeout_ns);
+        if (maps->rt != 6 && maps->rt != 8) return cudaErrorInvalidValue;
+        cudaError_t e = (maps->rt == 6)
+                            ? launch_router_tma<6>(maps->x, maps->w, row_valid, R, H, E, logits,
+                                                   n_sms, err, timeout_ns, stream)
+                            : launch_router_tma<8>(maps->x, maps->w, row_valid, R, H, E, logits,
+                                                   n_sms, err, timeout_ns, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();

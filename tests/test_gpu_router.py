@@ -1,13 +1,16 @@
 """The large-row router logits kernel against the oracle, bit for bit.
 
 Above 64 rows moe_route's logits come from a persistent kernel that takes
-tiles of 32 rows x 32 experts, streams x and the router weights through
+tiles of 32 rows (or 24, where that finishes sooner) x 32 experts, streams x
+and the router weights through
 shared memory in stages of two 128-column blocks, keeps each 1024-column
 chunk's lane sums in tensor memory and ends each pair's reduction tree by
 recursive halving.  Its logits must be the header's fixed-order IEEE sums,
 i.e. the oracle's bits, at every edge of that structure:
 
 * row counts with a ragged last row tile (65, 100, 333) and the maximum, 4096;
+  both tile heights, on either side of the switch between them (456 rows
+  take 24-row tiles at 256 experts, 457 rows 32-row tiles);
 * expert counts that leave a partial expert tile (48, 72 of 32) or a single
   one (16);
 * hidden sizes whose 128-column block count is odd (a stage's second half
@@ -81,6 +84,13 @@ def test_ragged_rows_and_odd_blocks(R, pads, H):
 @pytest.mark.parametrize("E,G,TG,K", [(16, 2, 1, 4), (72, 8, 4, 8), (256, 8, 4, 8)])
 def test_expert_tiles(E, G, TG, K):
     _check(_shape(1152, E, G, TG, K), 97, (3, 50), seed=E)
+
+
+@pytest.mark.parametrize("R", [456, 457])
+def test_tile_height_switch(R):
+    assert m.router_rows_per_warp(R, 256) == (6 if R == 456 else 8)
+    rows = np.unique(np.r_[np.arange(0, 30), np.arange(R - 30, R), np.arange(0, R, 23)])
+    _check(_shape(6144, 256, 8, 4, 8), R, (0, R // 2, R - 1), seed=R, rows=rows)
 
 
 def test_full_size_sampled_rows():
