@@ -278,6 +278,24 @@ __global__ void __launch_bounds__(kLThreads, 1) router_logits_tma_kernel(
         for (int ti = 0; ti < my_tiles && ok; ++ti) {
             const int t = blockIdx.x + ti * gridDim.x;
             float p[kLNP];   // pair k = kLPE * row + expert of the warp's kLRT x kLPE
+            // p += the chunk sums held in tensor memory, 32 pairs a load and
+            // two loads in flight per wait
+            auto fold = [&](float (&pp)[kLNP]) {
+#pragma unroll
+                for (int j = 0; j < kLNP / 32; j += 2) {
+                    float q0[32], q1[32];
+                    tmem_ld32(tq + 32 * j, q0);
+                    if (j + 1 < kLNP / 32) tmem_ld32(tq + 32 * (j + 1), q1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) pp[32 * j + i] = __fadd_rn(q0[i], pp[32 * j + i]);
+                    if (j + 1 < kLNP / 32) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            pp[32 * (j + 1) + i] = __fadd_rn(q1[i], pp[32 * (j + 1) + i]);
+                    }
+                }
+            };
             for (int s = 0; s < NSt; ++s, ++g) {
                 const int st = g % kLStages;
                 const uint32_t par = (g / kLStages) & 1;
@@ -331,31 +349,16 @@ __global__ void __launch_bounds__(kLThreads, 1) router_logits_tma_kernel(
                 const int lastblk = min(s * kLBlk + kLBlk, NB) - 1;
                 if ((lastblk & 7) == 7 && lastblk != NB - 1) {
                     __syncwarp();
+                    if (lastblk >= 8) fold(p);
 #pragma unroll
-                    for (int j = 0; j < kLNP / 32; ++j) {
-                        if (lastblk >= 8) {
-                            float q[32];
-                            tmem_ld32(tq + 32 * j, q);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) p[32 * j + i] = __fadd_rn(q[i], p[32 * j + i]);
-                        }
-                        tmem_st32f(tq + 32 * j, p + 32 * j);
-                    }
+                    for (int j = 0; j < kLNP / 32; ++j) tmem_st32f(tq + 32 * j, p + 32 * j);
                     tmem_wait_st();
                 }
             }
             if (!ok) break;
             if (NB > 8) {   // the last chunk: q + p, kept in registers
                 __syncwarp();
-#pragma unroll
-                for (int j = 0; j < kLNP / 32; ++j) {
-                    float q[32];
-                    tmem_ld32(tq + 32 * j, q);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) p[32 * j + i] = __fadd_rn(q[i], p[32 * j + i]);
-                }
+                fold(p);
             }
             halve<kLNP, kLNP, 16>(p, lane);
             halve<kLNP, kLNP / 2, 8>(p, lane);
