@@ -121,8 +121,51 @@ moe_status_t check_weights(const moe_config_t* c, const moe_weights_t* w) {
 // The large-R router's maps: x bf16 [R, H] and w fp32 [E, H], boxes of
 // kRouterStageCols columns x 32 rows, unswizzled; rows and columns past the
 // end read as zero.
+// The last few tensor-map sets built on this thread, keyed by everything
+// that goes into them (pointers, sizes, boxes, layout): a call on the same
+// buffers reuses them instead of encoding them again (each encoding is a
+// host call on the path of every layer).  Keys are compared bytewise and
+// built from zeroed memory.
+template <typename Key, typename Val, int N = 4>
+struct MapCache {
+    Key key[N];
+    Val val[N];
+    bool used[N] = {};
+    int next = 0;
+    const Val* find(const Key& k) const {
+        for (int i = 0; i < N; ++i)
+            if (used[i] && std::memcmp(&key[i], &k, sizeof(Key)) == 0) return &val[i];
+        return nullptr;
+    }
+    void put(const Key& k, const Val& v) {
+        key[next] = k;
+        val[next] = v;
+        used[next] = true;
+        next = (next + 1) % N;
+    }
+};
+
+struct RouterMapKey {
+    const void* x;
+    const void* wr;
+    int R, H, E, n_sms;
+};
+
 bool make_router_maps(const void* x, const float* wr, int R, int H, int E, int n_sms,
                       moe::RouterMaps* m) {
+    RouterMapKey k;
+    std::memset(&k, 0, sizeof(k));
+    k.x = x;
+    k.wr = wr;
+    k.R = R;
+    k.H = H;
+    k.E = E;
+    k.n_sms = n_sms;
+    thread_local MapCache<RouterMapKey, moe::RouterMaps> cache;
+    if (const moe::RouterMaps* hit = cache.find(k)) {
+        *m = *hit;
+        return true;
+    }
     auto fn = encode_fn();
     if (!fn) return false;
     m->rt = moe::router_rows_per_warp(R, E, n_sms);
@@ -138,7 +181,8 @@ bool make_router_maps(const void* x, const float* wr, int R, int H, int E, int n
            fn(&m->w, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(wr), wd, wst, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-               CUDA_SUCCESS;
+               CUDA_SUCCESS &&
+           (cache.put(k, *m), true);
 }
 
 moe_status_t route_impl(const moe_config_t* c, const void* x, const float* wr, const float* bias,
@@ -216,20 +260,45 @@ bool make_wmap(CUtensorMap* m, const void* base, int layout, uint64_t rows, uint
                                       : make_map(m, base, rows, cols, 128);
 }
 
+struct FfnMapKey {
+    const void* p[8];
+    int64_t rows;
+    int H, I, E, S, layout, nt;
+};
+
 // The eight tensor maps of the expert GEMMs.  Shared-expert maps fall back to
 // the routed tensors when there is no shared expert (never read then).
 bool make_maps(const moe_config_t* c, const moe_weights_t* w, const FfnCall& f, moe::FfnMaps* mp) {
     const int H = c->hidden, I = c->inter, E = c->n_experts, S = c->n_shared;
+    FfnMapKey k;
+    std::memset(&k, 0, sizeof(k));
+    const void* ps[8] = {w->w_gate, w->w_up, S ? w->sh_gate : w->w_gate, S ? w->sh_up : w->w_up,
+                         f.xg, w->w_down, S ? w->sh_down : w->w_down, f.hq};
+    for (int i = 0; i < 8; ++i) k.p[i] = ps[i];
+    k.rows = f.FL.rows;
+    k.H = H;
+    k.I = I;
+    k.E = E;
+    k.S = S;
+    k.layout = w->layout;
+    k.nt = f.nt;
+    thread_local MapCache<FfnMapKey, moe::FfnMaps> cache;
+    if (const moe::FfnMaps* hit = cache.find(k)) {
+        *mp = *hit;
+        return true;
+    }
     const uint64_t srows = S ? uint64_t(S) : 1ull;
     const int lo = w->layout;
-    return make_wmap(&mp->g, w->w_gate, lo, uint64_t(E) * I, H) &&
-           make_wmap(&mp->u, w->w_up, lo, uint64_t(E) * I, H) &&
-           make_wmap(&mp->sg, S ? w->sh_gate : w->w_gate, lo, srows * I, H) &&
-           make_wmap(&mp->su, S ? w->sh_up : w->w_up, lo, srows * I, H) &&
-           make_map(&mp->x, f.xg, f.FL.rows, H, f.nt) &&
-           make_wmap(&mp->d, w->w_down, lo, uint64_t(E) * H, I) &&
-           make_wmap(&mp->sd, S ? w->sh_down : w->w_down, lo, srows * H, I) &&
-           make_map(&mp->h, f.hq, f.FL.rows, I, f.nt);
+    const bool ok = make_wmap(&mp->g, w->w_gate, lo, uint64_t(E) * I, H) &&
+                    make_wmap(&mp->u, w->w_up, lo, uint64_t(E) * I, H) &&
+                    make_wmap(&mp->sg, ps[2], lo, srows * I, H) &&
+                    make_wmap(&mp->su, ps[3], lo, srows * I, H) &&
+                    make_map(&mp->x, f.xg, f.FL.rows, H, f.nt) &&
+                    make_wmap(&mp->d, w->w_down, lo, uint64_t(E) * H, I) &&
+                    make_wmap(&mp->sd, ps[6], lo, srows * H, I) &&
+                    make_map(&mp->h, f.hq, f.FL.rows, I, f.nt);
+    if (ok) cache.put(k, *mp);
+    return ok;
 }
 
 moe::FfnArgs ffn_args(const moe_config_t* c, const moe_weights_t* w, const int32_t* ub, int32_t R,

@@ -16,6 +16,31 @@
 namespace moe {
 
 constexpr int kBlock = MOE_BLOCK;      // 128: quantisation block and GEMM K-block
+
+// Host: cudaFuncSetAttribute(MaxDynamicSharedMemorySize) only when a launch
+// needs more than this thread last allowed for the kernel on the current
+// device (a runtime call per launch otherwise, on the path of every layer).
+inline cudaError_t ensure_dyn_smem(const void* func, int bytes) {
+    struct Entry {
+        const void* f;
+        int dev, bytes;
+    };
+    thread_local Entry tab[32];
+    thread_local int n = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    for (int i = 0; i < n; ++i) {
+        if (tab[i].f != func || tab[i].dev != dev) continue;
+        if (tab[i].bytes >= bytes) return cudaSuccess;
+        e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e == cudaSuccess) tab[i].bytes = bytes;
+        return e;
+    }
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && n < 32) tab[n++] = Entry{func, dev, bytes};
+    return e;
+}
 constexpr int kCtlBytes = 256;         // control block at the head of a workspace
 
 // Control block of a workspace: the device error word and a spare word.

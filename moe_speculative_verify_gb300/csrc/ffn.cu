@@ -838,8 +838,8 @@ static cudaError_t launch_ffn_t(const FfnMaps& mp, FfnArgs args, int n_sms, int 
     }
     if (L.bytes > smem_limit) return cudaErrorInvalidConfiguration;
     args.n_stages = stages;
-    cudaError_t e = cudaFuncSetAttribute(ffn_kernel<NT, MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L.bytes);
+    cudaError_t e =
+        ensure_dyn_smem(reinterpret_cast<const void*>(ffn_kernel<NT, MODE>), L.bytes);
     if (e != cudaSuccess) return e;
     e = launch_pdl(ffn_kernel<NT, MODE>, dim3(max(1, n_sms)), dim3(C::THREADS), L.bytes, stream,
                    mp.g, mp.u, mp.sg, mp.su, mp.x, mp.d, mp.sd, mp.h, args);

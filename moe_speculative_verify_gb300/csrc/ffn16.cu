@@ -686,8 +686,7 @@ cudaError_t launch_ffn16(const FfnMaps& mp, Ffn16Args args, int n_sms, int smem_
     while (nw > kDqGroups && L.bytes > smem_limit) L = smem16(--nw);
     if (L.bytes > smem_limit) return cudaErrorInvalidConfiguration;
     args.n_wstages = nw;
-    cudaError_t e = cudaFuncSetAttribute(ffn16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         L.bytes);
+    cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(ffn16_kernel), L.bytes);
     if (e != cudaSuccess) return e;
     e = launch_pdl(ffn16_kernel, dim3(max(1, n_sms)), dim3(kThreads16), L.bytes, stream, mp.g, mp.u,
                    mp.sg, mp.su, mp.x, mp.d, mp.sd, mp.h, args);

@@ -9,6 +9,8 @@
 // a fixed order (the order is part of the ABI contract in moe_verify.h), so
 // the chosen expert ids do not depend on launch shape, batch slot or compiler
 // contraction.
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "select.cuh"
@@ -433,14 +435,18 @@ static cudaError_t launch_router_tma(const CUtensorMap& xmap, const CUtensorMap&
                                      cudaStream_t stream) {
     using T = RouterTile<RT>;
     const int n_tiles = ((R + T::LR - 1) / T::LR) * ((E + kLE - 1) / kLE);
-    cudaError_t e = cudaFuncSetAttribute(router_logits_tma_kernel<RT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(T::Smem));
+    cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void*>(router_logits_tma_kernel<RT>),
+                                    static_cast<int>(T::Smem));
     if (e != cudaSuccess) return e;
-    // the warpgroups' register split needs the launch's full share
-    cudaFuncAttributes fa;
-    if ((e = cudaFuncGetAttributes(&fa, router_logits_tma_kernel<RT>)) != cudaSuccess) return e;
-    if (fa.numRegs < kLLaunchRegs) return cudaErrorInvalidConfiguration;
+    // the warpgroups' register split needs the launch's full share (the
+    // compiled count, read once)
+    static std::atomic<int> regs{0};
+    if (regs.load(std::memory_order_relaxed) == 0) {
+        cudaFuncAttributes fa;
+        if ((e = cudaFuncGetAttributes(&fa, router_logits_tma_kernel<RT>)) != cudaSuccess) return e;
+        regs.store(fa.numRegs, std::memory_order_relaxed);
+    }
+    if (regs.load(std::memory_order_relaxed) < kLLaunchRegs) return cudaErrorInvalidConfiguration;
     return launch_pdl(router_logits_tma_kernel<RT>, dim3(min(n_tiles, max(n_sms, 1))),
                       dim3(kLThreads), T::Smem, stream, xmap, wmap, row_valid, R, H, E, logits,
                       err, timeout_ns);

@@ -290,8 +290,8 @@ __global__ void __launch_bounds__(256) dispatch_kernel(const uint16_t* __restric
 cudaError_t launch_union(const int32_t* ids, int R, int E, int K, int S, int n_tile,
                          int32_t* ub, const UnionLayout& L, cudaStream_t stream) {
     const size_t smem = union_smem_bytes(R, E);
-    cudaError_t e = cudaFuncSetAttribute(union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e =
+        ensure_dyn_smem(reinterpret_cast<const void*>(union_kernel), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     e = launch_pdl(union_kernel, dim3(1), dim3(kUnionThreads), smem, stream, ids, R, E, K, S, n_tile,
                    ub, L);
@@ -316,9 +316,8 @@ cudaError_t launch_route_union(const float* logits, const float* bias, const uin
                                cudaStream_t stream) {
     if (R > kRouteUnionMaxRows) return cudaErrorInvalidValue;
     const size_t smem = size_t(32) * E * 4 + size_t((R * K + 3) & ~3) * 4 + union_smem_bytes(R, E);
-    cudaError_t e = cudaFuncSetAttribute(route_union_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e =
+        ensure_dyn_smem(reinterpret_cast<const void*>(route_union_kernel), static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     e = launch_pdl(route_union_kernel, dim3(1), dim3(kUnionThreads), smem, stream, logits, bias,
                    row_valid, R, E, G, TG, K, scaling, ids, wts, S, n_tile, ub, L);
