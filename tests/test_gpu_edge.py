@@ -92,3 +92,37 @@ def test_pad_calls_leave_workspace_clean(R):
             assert np.array_equal(bf16_to_np(out), bf16_to_np(fresh))
         else:
             assert np.all(bf16_to_np(out) == 0)
+
+
+@pytest.mark.parametrize("R", [8, 100])
+def test_alternating_buffers_reuse_no_stale_maps(R):
+    """The library keeps the tensor maps of recent calls per thread, keyed by
+    the buffers they describe.  Calls that alternate between two workspaces,
+    two copies of the weights (one zeroed: its maps must not be reused for
+    the other) and two row counts give each call's own bits."""
+    shape = MEDIUM
+    cfg = m.Config.from_shape(shape)
+    t_cpu, t = _layer(shape, R, (0,), seed=R)
+    W1 = m.Weights.from_tensors(t)
+    t2 = {k: v.clone() for k, v in t.items()}
+    for k in ("w_gate", "w_up", "w_down"):
+        t2[k].zero_()
+    W2 = m.Weights.from_tensors(t2)
+    ws_a = torch.zeros(m.moe_workspace_bytes(cfg, R), dtype=torch.uint8, device="cuda")
+    ws_b = torch.zeros(m.moe_workspace_bytes(cfg, R), dtype=torch.uint8, device="cuda")
+
+    def call(W, ws, rows=R):
+        out = torch.full((rows, shape.hidden), float("nan"), dtype=torch.bfloat16, device="cuda")
+        m.moe_layer(cfg, t["x"][:rows], t["wr"], t["bias"], W, t["row_valid"][:rows], out, ws)
+        torch.cuda.synchronize()
+        assert m.moe_get_device_error(ws) == 0
+        return bf16_to_np(out)
+
+    ref1, ref2 = call(W1, ws_a), call(W2, ws_b)
+    assert not np.array_equal(ref1, ref2)
+    for W, ws, ref in ((W1, ws_b, ref1), (W2, ws_a, ref2), (W1, ws_a, ref1), (W2, ws_b, ref2)):
+        assert np.array_equal(call(W, ws), ref)
+    # a smaller call on the same workspace, then the full one again
+    small = call(W1, ws_a, rows=R // 2)
+    assert np.array_equal(small, ref1[: R // 2])
+    assert np.array_equal(call(W1, ws_a), ref1)
