@@ -126,3 +126,45 @@ def test_alternating_buffers_reuse_no_stale_maps(R):
     small = call(W1, ws_a, rows=R // 2)
     assert np.array_equal(small, ref1[: R // 2])
     assert np.array_equal(call(W1, ws_a), ref1)
+
+
+def test_two_host_threads_two_shapes():
+    """Two host threads, each on its own stream, call moe_layer on shapes whose
+    expert GEMM needs different amounts of shared memory (the kernel attribute
+    that allows it is process-wide and only ever raised): every call keeps its
+    single-threaded bits and a clean status."""
+    import threading
+    cases = []
+    for shape, R, seed in ((synth.TINY, 8, 11), (MEDIUM, 8, 12)):
+        t_cpu, t = _layer(shape, R, (), seed=seed)
+        cfg = m.Config.from_shape(shape)
+        ref, _, _, _ = run_layer(cfg, t, R)
+        cases.append((shape, R, cfg, t, bf16_to_np(ref)))
+    errors = []
+
+    def worker(case):
+        shape, R, cfg, t, ref = case
+        try:
+            stream = torch.cuda.Stream()
+            ws = torch.zeros(m.moe_workspace_bytes(cfg, R), dtype=torch.uint8, device="cuda")
+            W = m.Weights.from_tensors(t)
+            for _ in range(10):
+                out = torch.full((R, shape.hidden), float("nan"), dtype=torch.bfloat16,
+                                 device="cuda")
+                with torch.cuda.stream(stream):
+                    m.moe_layer(cfg, t["x"], t["wr"], t["bias"], W, t["row_valid"], out, ws,
+                                stream=stream)
+                stream.synchronize()
+                if (m.moe_get_device_error(ws, stream=stream) != 0
+                        or not np.array_equal(bf16_to_np(out), ref)):
+                    errors.append(shape)
+                    return
+        except Exception as e:      # reported below, in the main thread
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(c,)) for c in cases]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
