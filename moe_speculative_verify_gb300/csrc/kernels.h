@@ -5,9 +5,42 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "layout.h"
 
 namespace moe {
+
+// Host: cudaFuncSetAttribute(MaxDynamicSharedMemorySize) only when a launch
+// needs more than the kernel already allows on the current device (a runtime
+// call per launch otherwise, on the path of every layer).  The attribute
+// belongs to the process, so the record is process-wide and the allowance
+// only ever grows: a launch that needs less than another thread set runs
+// under the larger allowance.
+inline cudaError_t ensure_dyn_smem(const void* func, int bytes) {
+    struct Entry {
+        const void* f;
+        int dev, bytes;
+    };
+    static std::mutex mu;
+    static Entry tab[64];
+    static int n = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    Entry* hit = nullptr;
+    for (int i = 0; i < n && !hit; ++i)
+        if (tab[i].f == func && tab[i].dev == dev) hit = &tab[i];
+    if (hit && hit->bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    if (hit)
+        hit->bytes = bytes;
+    else if (n < 64)
+        tab[n++] = Entry{func, dev, bytes};
+    return cudaSuccess;
+}
 
 // Modes of the persistent expert-GEMM kernel (ffn.cu).
 constexpr int kFfnGateUp = 0;   // gate/up GEMMs + SiLU*mul + h quantisation
