@@ -61,7 +61,7 @@ def kernels_per_step(R: int) -> int:
 # was taken on: `kernel_sha16` is the hash of that source (ffn_source_sha16()),
 # and a bench run on other source reports the traffic as null.
 FFN_TRAFFIC = {"per_alg_byte": 1.0031, "profile": "profiles/ffn_fused_profile8.md",
-               "kernel_sha16": "b97e167673a46026"}
+               "kernel_sha16": "51438ff6819ee307"}
 FFN_SOURCES = ("moe_speculative_verify_gb300/csrc/ffn.cu",
                "moe_speculative_verify_gb300/csrc/common.cuh")
 HOST_AHEAD_CYCLES = 400_000   # GPU sleep before each step so the host enqueues it whole
