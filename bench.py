@@ -16,7 +16,8 @@ layer has no exchange step on one GPU): scaling "weak".
 
 `e2e` measures the same metric through moe_layer with host buffers: per step
 the rows go from pinned host memory to the device, the layer runs, and the
-bf16 output comes back to pinned host memory.
+bf16 output comes back to pinned host memory; `e2e.graph_replay` is the same
+step with moe_layer captured once in a CUDA graph and replayed.
 
 `--impl reference` times the CPU oracle (the plain restatement the tests
 check the kernels against) on the host cores, on a bounded sample of the same
@@ -620,6 +621,40 @@ def main() -> None:
         e2e_times.append(time.perf_counter() - t0)
     e2e_s = statistics.mean(e2e_times)
     e2e_same = bool(torch.equal(out_host.to(dev), res["out"]))
+
+    # the same end to end step with moe_layer captured once in a CUDA graph
+    # and replayed (how a serving loop calls it: the row count fixes the
+    # launches, the valid mask is read at kernel time), the copies outside it
+    gstream = torch.cuda.Stream()
+    gstream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(gstream):
+        m2.moe_layer(cfg, x_dev, ri["wr"], ri["bias"], W, v_dev, out_dev, lws, stream=gstream)
+    gstream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gstream):
+        m2.moe_layer(cfg, x_dev, ri["wr"], ri["bias"], W, v_dev, out_dev, lws, stream=gstream)
+    torch.cuda.synchronize()
+
+    def e2e_graph_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        v_dev.copy_(v_host, non_blocking=True)
+        graph.replay()
+        out_host.copy_(out_dev, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(3):
+        flush.zero_()
+        e2e_graph_step()
+    g_times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_graph_step()
+        g_times.append(time.perf_counter() - t0)
+    e2e_graph_s = statistics.mean(g_times)
+    e2e_graph_same = bool(torch.equal(out_host.to(dev), res["out"]))
+    del graph
     # the same layer on the row-major codes gives the same bits
     m2.moe_layer(cfg, x_dev, ri["wr"], ri["bias"], W_rm, v_dev, out_dev, lws)
     torch.cuda.synchronize()
@@ -664,7 +699,12 @@ def main() -> None:
                     "h2d_bytes_per_step": x_host.numel() * 2 + v_host.numel(),
                     "d2h_bytes_per_step": out_host.numel() * 2,
                     "note": "moe_layer, pinned host x -> device -> pinned host out, per step",
-                    "bit_identical_to_step_path": e2e_same},
+                    "bit_identical_to_step_path": e2e_same,
+                    "graph_replay": {"value": round(world * R / e2e_graph_s, 1),
+                                     "unit": "rows/s",
+                                     "note": "the same step with moe_layer captured once in a "
+                                             "CUDA graph and replayed, copies outside it",
+                                     "bit_identical_to_step_path": e2e_graph_same}},
             "gpu_launches": kernels_per_step(R) * args.steps,
             "clocks": clocks,
             "also": extra,
