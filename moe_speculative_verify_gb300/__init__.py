@@ -324,17 +324,20 @@ W8A16_MAX_ROWS = 64          # the w8a16 variant's row limit (mirrors the librar
 
 def router_rows_per_warp(R: int, E: int, n_sms: int = None) -> int:
     """Rows a consumer warp of the large-R router kernel takes per tile (tiles
-    of 4x that many rows): 8 or 6 (mirrors the library's choice; n_sms
+    of 4x that many rows): 6, 7, 8 or 9 (mirrors the library's choice; n_sms
     defaults to the current device's SM count)."""
     if n_sms is None:
         import torch
         n_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-
-    def busiest(rt):
+    cost = {6: 45, 7: 50, 8: 55, 9: 62}
+    best, best_cost = 6, None
+    for rt in (6, 7, 8, 9):
         tiles = -(-R // (4 * rt)) * -(-E // 32)
         grid = min(tiles, max(n_sms, 1))
-        return -(-tiles // grid) * (rt + 3)
-    return 6 if busiest(6) < busiest(8) else 8
+        c = -(-tiles // grid) * cost[rt]
+        if best_cost is None or c < best_cost:
+            best, best_cost = rt, c
+    return best
 
 
 def rows_per_item(R: int) -> int:

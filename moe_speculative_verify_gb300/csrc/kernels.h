@@ -124,20 +124,29 @@ struct RouterMaps {
 };
 
 // Rows a consumer warp of the large-R router kernel takes per tile (tiles of
-// 4x that many rows x 32 experts): 8, or 6 where that makes the busiest of the
-// n_sms CTAs finish sooner.  A CTA's time is its tile count times a tile's
-// cost, about rt + 3 rows of a warp's work (measured: a 24-row tile takes
-// 0.82 of a 32-row tile's time).  So 6 wins where the tiles fit in one wave
-// either way (moe_route at 72 and 333 rows: 53 -> 46 us), 8 at 4096 rows,
-// where 24-row tiles would even out the SMs' loads (9 tiles each instead of
-// 7 on some and 6 on others) but cost 5 % more in all.
+// 4x that many rows x 32 experts): 6, 7, 8 or 9, whichever makes the busiest
+// of the n_sms CTAs finish first.  A CTA's time is its tile count times a
+// tile's cost; measured at 4096 rows and 256 experts (bit-identical logits at
+// every height), a wave of tiles took 36.2, 39.6, 43.6 and 49.2 us at 6, 7, 8
+// and 9 rows a warp, the costs 45 : 50 : 55 : 62 below.  So 6 rows where the
+// tiles fit in one wave (up to 456 rows at 256 experts), 7 at 512 and 1000
+// rows (moe_route 57.3 -> 55.2 and 100.4 -> 92.2 us against 8), 9 at 2048 and
+// 4096, where 912 tiles fill six waves of 152 exactly (182.3 -> 155.8 and
+// 308.3 -> 295.4 us).
 inline int router_rows_per_warp(int R, int E, int n_sms) {
-    auto busiest = [&](int rt) {
-        const int tiles = ((R + 4 * rt - 1) / (4 * rt)) * ((E + 31) / 32);
-        const int grid = tiles < n_sms ? tiles : (n_sms > 0 ? n_sms : 1);
-        return ((tiles + grid - 1) / grid) * (rt + 3);
-    };
-    return busiest(6) < busiest(8) ? 6 : 8;
+    constexpr int kCost[4] = {45, 50, 55, 62};
+    int best = 6;
+    long long best_cost = -1;
+    for (int rt = 6; rt <= 9; ++rt) {
+        const long long tiles = static_cast<long long>((R + 4 * rt - 1) / (4 * rt)) * ((E + 31) / 32);
+        const long long grid = tiles < n_sms ? tiles : (n_sms > 0 ? n_sms : 1);
+        const long long c = ((tiles + grid - 1) / grid) * kCost[rt - 6];
+        if (best_cost < 0 || c < best_cost) {
+            best = rt;
+            best_cost = c;
+        }
+    }
+    return best;
 }
 // Above 64 rows `maps` is required; a wait that runs out records
 // MOE_ERR_TIMEOUT in *err (when err is not null).

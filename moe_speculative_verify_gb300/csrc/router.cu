@@ -114,7 +114,7 @@ __global__ void __launch_bounds__(MAXT, MINB) router_logits_kernel(
 // warp is lane l of the reduction tree for those RT * 16 (row, expert) pairs:
 // each row's x is widened from bf16 once for 16 experts (measured at 4096
 // rows: 319.5 -> 309.2 us against 16 rows x 8 experts, at 25 % more
-// shared-memory reads).  RT = 8 (32-row tiles) or 6 (24-row tiles), as
+// shared-memory reads).  RT = 6 to 9 (24- to 36-row tiles), as
 // router_rows_per_warp chooses.
 //
 // Per stage of kLCols columns, x [kLR][kLCols] bf16 and w [kLE][kLCols] fp32
@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(MAXT, MINB) router_logits_kernel(
 // phase and refills it; the 8 consumer warps of warpgroups 1 and 2 only wait
 // for full slots and arrive on empty ones (no round trip), so they drift apart
 // instead of meeting at every stage.  The producer warpgroup gives up its
-// registers (setmaxnreg: 40 a thread) to the consumers (232), whose 8 x 16
+// registers (setmaxnreg: 40 a thread) to the consumers (232), whose RT x 16
 // pair tiles need them: 4 x 32 x 40 + 8 x 32 x 232 = 384 x 168, the launch's.
 // A thread forms its lane partials
 // of the current 1024-column chunk in registers (fma in column order) and
@@ -133,9 +133,10 @@ __global__ void __launch_bounds__(MAXT, MINB) router_logits_kernel(
 // tree by recursive halving: at distance d = 16 .. 1 each lane keeps half of
 // its values and adds its partner's copy of them, which are the xor
 // butterfly's additions (v[l] + v[l ^ d], IEEE addition commutes) with every
-// value summed in one lane only; lane l ends with pairs RT*l/2 .. RT*l/2 + RT/2 - 1.
-// The same IEEE operations in the same order as the small-R kernel, at
-// either RT.
+// value summed in one lane only; lane l ends with pairs RT*l/2 .. RT*l/2 + RT/2 - 1
+// (for odd RT the last level's sums are formed in both lanes of a pair and
+// stored alternately).  The same IEEE operations in the same order as the
+// small-R kernel, at every RT.
 constexpr int kLE = 32;
 constexpr int kLPE = 16;                                    // experts of a thread
 constexpr int kLWarps = 4 * (kLE / kLPE);                   // consumer warps
@@ -148,7 +149,6 @@ constexpr int kLCols = kRouterStageCols;                 // columns per stage
 constexpr int kLBlk = kLCols / 128;                      // 128-column blocks per stage
 constexpr int kLStages = 1024 / kLCols;                  // up to 192 KB of stages
 constexpr int kLWBytes = kLE * kLCols * 4;
-constexpr uint32_t kLTmemCols = 256;                     // (warps per lane quarter) x pairs, <= 256
 static_assert(kLBlk >= 1 && 8 % kLBlk == 0, "a stage holds whole blocks of one chunk");
 template <int RT>
 struct RouterTile {
@@ -157,7 +157,11 @@ struct RouterTile {
     static constexpr int XBytes = LR * kLCols * 2;
     static constexpr int StageBytes = XBytes + kLWBytes;
     static constexpr size_t Smem = size_t(kLStages) * StageBytes + 256;
-    static_assert(NP % 32 == 0 && (kLWarps / 4) * NP <= int(kLTmemCols), "pairs per lane, TMEM");
+    // chunk sums: the two warps of a lane quarter at columns 0 and NPCols
+    // (32-column aligned), in a power-of-two allocation
+    static constexpr int NPCols = (NP + 31) / 32 * 32;
+    static constexpr uint32_t TmemCols = ((kLWarps / 4) * NPCols <= 256) ? 256u : 512u;
+    static_assert(NP % 16 == 0 && (kLWarps / 4) * NPCols <= int(TmemCols), "pairs per lane, TMEM");
     static_assert(XBytes % 128 == 0 && StageBytes % 128 == 0, "TMA destinations 128-byte aligned");
 };
 
@@ -171,6 +175,16 @@ __device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float* v) {
         "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]),
         "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]),
         "f"(v[29]), "f"(v[30]), "f"(v[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16f(uint32_t taddr, const float* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+        "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
+        "f"(v[15])
         : "memory");
 }
 
@@ -197,6 +211,11 @@ __global__ void __launch_bounds__(kLThreads, 1) router_logits_tma_kernel(
     int32_t* err, uint64_t timeout_ns) {
     using T = RouterTile<RT>;
     constexpr int kLR = T::LR, kLRT = RT, kLNP = T::NP;
+    // the weight columns of a block held for 8 experts at a time (each x row
+    // then widened twice), which frees 32 registers for the RT x 16
+    // accumulators: measured at 4096 rows, 316.0 -> 295.4 us at RT = 9 and
+    // 308.3 -> 305.1 at RT = 8; 2048 rows at RT = 7 170.0 -> 167.2 us
+    constexpr int kEG = (RT >= 7) ? 2 : 1;
     constexpr int kLXBytes = T::XBytes, kLStageBytes = T::StageBytes;
     extern __shared__ __align__(1024) uint8_t lsm[];
     uint64_t* full = reinterpret_cast<uint64_t*>(lsm + kLStages * kLStageBytes);
@@ -236,7 +255,7 @@ __global__ void __launch_bounds__(kLThreads, 1) router_logits_tma_kernel(
         fence_barrier_init();
     }
     if (warp == 0) {
-        tmem_alloc(tslot, kLTmemCols);
+        tmem_alloc(tslot, T::TmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -275,13 +294,13 @@ __global__ void __launch_bounds__(kLThreads, 1) router_logits_tma_kernel(
         const int cw = warp - 4;   // consumer warp
         const int wrow = (cw / (kLE / kLPE)) * kLRT, wexp = (cw % (kLE / kLPE)) * kLPE;
         const uint32_t tq = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) +
-                            static_cast<uint32_t>(cw >> 2) * kLNP;
+                            static_cast<uint32_t>(cw >> 2) * T::NPCols;
         int g = 0;
         for (int ti = 0; ti < my_tiles && ok; ++ti) {
             const int t = blockIdx.x + ti * gridDim.x;
             float p[kLNP];   // pair k = kLPE * row + expert of the warp's kLRT x kLPE
             // p += the chunk sums held in tensor memory, 32 pairs a load and
-            // two loads in flight per wait
+            // two loads in flight per wait (a last 16 pairs where RT is odd)
             auto fold = [&](float (&pp)[kLNP]) {
 #pragma unroll
                 for (int j = 0; j < kLNP / 32; j += 2) {
@@ -296,6 +315,14 @@ __global__ void __launch_bounds__(kLThreads, 1) router_logits_tma_kernel(
                         for (int i = 0; i < 32; ++i)
                             pp[32 * (j + 1) + i] = __fadd_rn(q1[i], pp[32 * (j + 1) + i]);
                     }
+                }
+                if constexpr (kLNP % 32 != 0) {
+                    constexpr int j0 = kLNP - 16;
+                    float q0[16];
+                    tmem_ld16(tq + j0, q0);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) pp[j0 + i] = __fadd_rn(q0[i], pp[j0 + i]);
                 }
             };
             for (int s = 0; s < NSt; ++s, ++g) {
@@ -318,27 +345,31 @@ __global__ void __launch_bounds__(kLThreads, 1) router_logits_tma_kernel(
 #pragma unroll
                             for (int k = 0; k < kLNP; ++k) p[k] = 0.0f;
                         }
-                        float4 wv[kLPE];
 #pragma unroll
-                        for (int b = 0; b < kLPE; ++b)
-                            wv[b] = *reinterpret_cast<const float4*>(ws + (wexp + b) * kLCols + i * 128 +
-                                                                     4 * lane);
+                        for (int eg = 0; eg < kEG; ++eg) {
+                            float4 wv[kLPE / kEG];
 #pragma unroll
-                        for (int a = 0; a < kLRT; ++a) {
-                            const uint2 xv = *reinterpret_cast<const uint2*>(
-                                xs + (wrow + a) * kLCols + i * 128 + 4 * lane);
-                            const float x0 = bf16_bits_to_f32(xv.x & 0xFFFFu);
-                            const float x1 = bf16_bits_to_f32(xv.x >> 16);
-                            const float x2 = bf16_bits_to_f32(xv.y & 0xFFFFu);
-                            const float x3 = bf16_bits_to_f32(xv.y >> 16);
+                            for (int b = 0; b < kLPE / kEG; ++b)
+                                wv[b] = *reinterpret_cast<const float4*>(
+                                    ws + (wexp + eg * (kLPE / kEG) + b) * kLCols + i * 128 + 4 * lane);
 #pragma unroll
-                            for (int b = 0; b < kLPE; ++b) {
-                                float q = p[a * kLPE + b];
-                                q = __fmaf_rn(x0, wv[b].x, q);
-                                q = __fmaf_rn(x1, wv[b].y, q);
-                                q = __fmaf_rn(x2, wv[b].z, q);
-                                q = __fmaf_rn(x3, wv[b].w, q);
-                                p[a * kLPE + b] = q;
+                            for (int a = 0; a < kLRT; ++a) {
+                                const uint2 xv = *reinterpret_cast<const uint2*>(
+                                    xs + (wrow + a) * kLCols + i * 128 + 4 * lane);
+                                const float x0 = bf16_bits_to_f32(xv.x & 0xFFFFu);
+                                const float x1 = bf16_bits_to_f32(xv.x >> 16);
+                                const float x2 = bf16_bits_to_f32(xv.y & 0xFFFFu);
+                                const float x3 = bf16_bits_to_f32(xv.y >> 16);
+#pragma unroll
+                                for (int b = 0; b < kLPE / kEG; ++b) {
+                                    const int k = a * kLPE + eg * (kLPE / kEG) + b;
+                                    float q = p[k];
+                                    q = __fmaf_rn(x0, wv[b].x, q);
+                                    q = __fmaf_rn(x1, wv[b].y, q);
+                                    q = __fmaf_rn(x2, wv[b].z, q);
+                                    q = __fmaf_rn(x3, wv[b].w, q);
+                                    p[k] = q;
+                                }
                             }
                         }
                     }
@@ -354,6 +385,7 @@ __global__ void __launch_bounds__(kLThreads, 1) router_logits_tma_kernel(
                     if (lastblk >= 8) fold(p);
 #pragma unroll
                     for (int j = 0; j < kLNP / 32; ++j) tmem_st32f(tq + 32 * j, p + 32 * j);
+                    if constexpr (kLNP % 32 != 0) tmem_st16f(tq + kLNP - 16, p + kLNP - 16);
                     tmem_wait_st();
                 }
             }
@@ -366,18 +398,35 @@ __global__ void __launch_bounds__(kLThreads, 1) router_logits_tma_kernel(
             halve<kLNP, kLNP / 2, 8>(p, lane);
             halve<kLNP, kLNP / 4, 4>(p, lane);
             halve<kLNP, kLNP / 8, 2>(p, lane);
-            halve<kLNP, kLNP / 16, 1>(p, lane);
-            // lane l holds pairs NL*l .. NL*l + NL-1 (NL = kLNP / 32), pair k
-            // being row k / kLPE and expert k % kLPE of the warp's block
-            constexpr int NL = kLNP / 32;
+            // lanes 2m and 2m+1 now hold the same RT pairs, RT*m .. RT*m + RT-1
             const int r0 = (t / n_eb) * kLR + wrow;
             const int e0 = (t % n_eb) * kLE + wexp;
+            if constexpr (kLRT % 2 == 0) {
+                halve<kLNP, kLRT, 1>(p, lane);
+                // lane l holds pairs NL*l .. NL*l + NL-1 (NL = RT / 2), pair k
+                // being row k / kLPE and expert k % kLPE of the warp's block
+                constexpr int NL = kLRT / 2;
 #pragma unroll
-            for (int j = 0; j < NL; ++j) {
-                const int k = NL * lane + j;
-                const int r = r0 + k / kLPE, e = e0 + k % kLPE;
-                if (r < R && e < E && (row_valid == nullptr || row_valid[r] != 0))
-                    logits[size_t(r) * E + e] = p[j];
+                for (int j = 0; j < NL; ++j) {
+                    const int k = NL * lane + j;
+                    const int r = r0 + k / kLPE, e = e0 + k % kLPE;
+                    if (r < R && e < E && (row_valid == nullptr || row_valid[r] != 0))
+                        logits[size_t(r) * E + e] = p[j];
+                }
+            } else {
+                // RT pairs do not halve: both lanes of a pair form the last
+                // level's sums (the same bits: IEEE addition commutes) and
+                // store alternate ones
+#pragma unroll
+                for (int j = 0; j < kLRT; ++j) p[j] = __fadd_rn(p[j], __shfl_xor_sync(0xFFFFFFFFu, p[j], 1));
+#pragma unroll
+                for (int j = 0; j < kLRT; ++j) {
+                    const int k = kLRT * (lane >> 1) + j;
+                    const int r = r0 + k / kLPE, e = e0 + k % kLPE;
+                    if ((j & 1) == (lane & 1) && r < R && e < E &&
+                        (row_valid == nullptr || row_valid[r] != 0))
+                        logits[size_t(r) * E + e] = p[j];
+                }
             }
         }
     }
@@ -399,7 +448,7 @@ __global__ void __launch_bounds__(kLThreads, 1) router_logits_tma_kernel(
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, kLTmemCols);
+        tmem_dealloc(tmem, T::TmemCols);
     }
 }
 
@@ -473,12 +522,14 @@ cudaError_t launch_router_logits(const uint16_t* x, const float* wr, const uint8
         if (e != cudaSuccess) return e;
     } else {
         if (maps == nullptr) return cudaErrorInvalidValue;
-        if (maps->rt != 6 && maps->rt != 8) return cudaErrorInvalidValue;
-        cudaError_t e = (maps->rt == 6)
-                            ? launch_router_tma<6>(maps->x, maps->w, row_valid, R, H, E, logits,
-                                                   n_sms, err, timeout_ns, stream)
-                            : launch_router_tma<8>(maps->x, maps->w, row_valid, R, H, E, logits,
-                                                   n_sms, err, timeout_ns, stream);
+        cudaError_t e;
+        switch (maps->rt) {
+            case 6: e = launch_router_tma<6>(maps->x, maps->w, row_valid, R, H, E, logits, n_sms, err, timeout_ns, stream); break;
+            case 7: e = launch_router_tma<7>(maps->x, maps->w, row_valid, R, H, E, logits, n_sms, err, timeout_ns, stream); break;
+            case 8: e = launch_router_tma<8>(maps->x, maps->w, row_valid, R, H, E, logits, n_sms, err, timeout_ns, stream); break;
+            case 9: e = launch_router_tma<9>(maps->x, maps->w, row_valid, R, H, E, logits, n_sms, err, timeout_ns, stream); break;
+            default: return cudaErrorInvalidValue;
+        }
         if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();

@@ -1,16 +1,18 @@
 """The large-row router logits kernel against the oracle, bit for bit.
 
 Above 64 rows moe_route's logits come from a persistent kernel that takes
-tiles of 32 rows (or 24, where that finishes sooner) x 32 experts, streams x
-and the router weights through
+tiles of 24, 28, 32 or 36 rows (whichever finishes sooner) x 32 experts,
+streams x and the router weights through
 shared memory in stages of two 128-column blocks, keeps each 1024-column
 chunk's lane sums in tensor memory and ends each pair's reduction tree by
 recursive halving.  Its logits must be the header's fixed-order IEEE sums,
 i.e. the oracle's bits, at every edge of that structure:
 
 * row counts with a ragged last row tile (65, 100, 333) and the maximum, 4096;
-  both tile heights, on either side of the switch between them (456 rows
-  take 24-row tiles at 256 experts, 457 rows 32-row tiles);
+  every tile height, each at the first row count that takes it at 256
+  experts (456 rows: 24-row tiles, 457: 28, 533: 32, 609: 36, and 685 back to
+  24 in two waves) -- the odd heights end each pair's reduction without the
+  last halving;
 * expert counts that leave a partial expert tile (48, 72 of 32) or a single
   one (16);
 * hidden sizes whose 128-column block count is odd (a stage's second half
@@ -86,9 +88,9 @@ def test_expert_tiles(E, G, TG, K):
     _check(_shape(1152, E, G, TG, K), 97, (3, 50), seed=E)
 
 
-@pytest.mark.parametrize("R", [456, 457])
-def test_tile_height_switch(R):
-    assert m.router_rows_per_warp(R, 256) == (6 if R == 456 else 8)
+@pytest.mark.parametrize("R,rt", [(456, 6), (457, 7), (533, 8), (609, 9), (685, 6)])
+def test_tile_height_switch(R, rt):
+    assert m.router_rows_per_warp(R, 256) == rt
     rows = np.unique(np.r_[np.arange(0, 30), np.arange(R - 30, R), np.arange(0, R, 23)])
     _check(_shape(6144, 256, 8, 4, 8), R, (0, R // 2, R - 1), seed=R, rows=rows)
 
