@@ -66,8 +66,12 @@ constexpr int kAColBase = kAccBufs * kAccCols;
 constexpr int kTmemCols = 512;
 static_assert(kAColBase + kSlots * kACols <= kTmemCols, "tensor memory");
 // every dequant group owns its own operand slots (step n uses slot
-// n % kSlots, group g the steps g, g + kDqGroups, ...): a variant with slots
-// shared between groups (4 slots) faulted on the GPU and is not supported
+// n % kSlots, group g the steps g, g + kDqGroups, ...), so a slot's uses come
+// in order from one group that finishes each before it starts the next, and
+// a parity wait on the slot's barriers never has more than one phase pending.
+// With slots shared between groups a group can run two uses ahead of a
+// pending one, and its parity wait then passes on the older phase (a variant
+// with 4 slots and 3 groups faulted on the GPU).
 static_assert(kSlots % kDqGroups == 0, "operand slots a multiple of the dequant groups");
 static_assert(kSlotBytes % 1024 == 0, "operand slots stay 1024-byte aligned");
 
