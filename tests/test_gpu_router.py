@@ -18,7 +18,9 @@ i.e. the oracle's bits, at every edge of that structure:
 * hidden sizes whose 128-column block count is odd (a stage's second half
   past the end: 384, 1152, 6272) or fits one chunk (no chunk sums kept:
   384, 1024), and the GLM-5.2 width 6144 (six chunks);
-* pad rows anywhere (their logits stay untouched: a sentinel survives).
+* pad rows anywhere (their logits stay untouched: a sentinel survives);
+* 16 seeded shapes (48 to 256 experts, hidden 384 to 6144, random groups and
+  top-k) at 400 to 2200 rows, which between them take every tile height.
 
 ids and weights are compared bit for bit too (the selection reads the
 logits).
@@ -100,3 +102,34 @@ def test_full_size_sampled_rows():
     R = 4096
     rows = np.unique(np.r_[np.arange(0, 40), np.arange(R - 40, R), np.arange(0, R, 97)])
     _check(_shape(6144, 256, 8, 4, 8), R, (1, 2047, 4095), seed=5, rows=rows)
+
+
+def _draw_router(seed):
+    """A seeded router shape and row count between 400 and 2200 rows, where
+    every tile height occurs at one expert count or another."""
+    rng = np.random.default_rng(5000 + seed)
+    E = int(rng.choice([48, 64, 96, 128, 160, 256]))
+    H = 128 * int(rng.choice([3, 9, 16, 48]))
+    R = int(rng.integers(400, 2200))
+    groups = [g for g in (1, 2, 4, 8, 16, 32) if E % g == 0 and E // g <= 32]
+    G = int(rng.choice(groups))
+    TG = int(rng.integers(1, G + 1))
+    K = int(rng.integers(1, min(16, TG * (E // G)) + 1))
+    pads = tuple(sorted(int(p) for p in rng.choice(R, size=3, replace=False)))
+    return _shape(H, E, G, TG, K), R, pads
+
+
+N_ROUTER_CASES = 16
+
+
+def test_random_cases_cover_every_tile_height():
+    heights = {m.router_rows_per_warp(R, s.n_experts)
+               for s, R, _ in (_draw_router(i) for i in range(N_ROUTER_CASES))}
+    assert heights == {6, 7, 8, 9}
+
+
+@pytest.mark.parametrize("seed", range(N_ROUTER_CASES))
+def test_random_router_shapes(seed):
+    shape, R, pads = _draw_router(seed)
+    rows = np.unique(np.r_[np.arange(0, 12), np.arange(R - 12, R), np.arange(0, R, 37), list(pads)])
+    _check(shape, R, pads, seed=seed, rows=rows)
