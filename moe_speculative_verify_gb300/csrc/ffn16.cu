@@ -26,8 +26,9 @@
 //   warps 2..13  : dequant, three groups of four taking turns -- a staged
 //                  tile to bf16, written straight into a tensor-memory
 //                  operand slot (tcgen05.st; the dequantised tile never
-//                  touches shared memory); the group's leader also loads the
-//                  K-block's 16 rows (bf16) into the slot's shared part;
+//                  touches shared memory); one warp of the group, a
+//                  different one each step, also loads the K-block's 16 rows
+//                  (bf16) into the slot's shared part;
 //   warps 14..17 : epilogue -- gate/up: h = silu(g) * u rounded to bf16, row
 //                  stores; down: fp32 rows to their slot.
 // Every wait is bounded; a timeout records MOE_ERR_TIMEOUT and winds down.
@@ -433,7 +434,6 @@ __global__ void __maxnreg__(kMaxRegs16)
         const int grp = dw / kDqGroupWarps;
         const int qd = warp & 3;
         const int row = 32 * qd + lane;
-        const bool leader = (dw % kDqGroupWarps) == 0 && lane == 0;
         uint32_t n = 0;              // the CTA's step counter (every group counts every step)
         bool ok = true;
         pdl_wait();   // gathered rows and the counters belong to the previous kernel
@@ -481,6 +481,12 @@ __global__ void __maxnreg__(kMaxRegs16)
                     break;
                 }
                 tc_fence_after();
+                // the group's warps take turns at the step's copies (and
+                // the wait for h), which a fixed leader warp would add to
+                // every step of its group (measured at 8 rows: 294.0 ->
+                // 290.0 us)
+                const bool leader = lane == 0 && static_cast<int>((nj / kDqGroups) % kDqGroupWarps) ==
+                                                     dw % kDqGroupWarps;
                 if (leader) {
                     if (!h_ready) {
                         // h of this item comes from this launch's gate/up tiles
