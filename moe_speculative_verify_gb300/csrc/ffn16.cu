@@ -59,7 +59,7 @@ constexpr int kWBytes = 128 * 128;           // e4m3 weight tile
 constexpr int kBBytes = kNT * 128 * 2;       // bf16 rows: two K halves of kNT x 128 B
 constexpr int kSlotBytes = kBBytes;          // shared-memory part of an operand slot
 constexpr int kSlots = 6;                    // operand slots (dequant -> MMA)
-constexpr int kMaxWStages = 12;
+constexpr int kMaxWStages = 8;    // weight ring (measured at 8 rows: 12 stages 290.0 us, 10 289.4, 6-8 287.8)
 constexpr int kAccCols = 2 * kNT;
 constexpr int kAccBufs = 4;
 constexpr int kACols = 64;                   // a bf16 128x128 tile in TMEM: 2 per 32-bit column
