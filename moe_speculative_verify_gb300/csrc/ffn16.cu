@@ -26,9 +26,10 @@
 //   warps 2..13  : dequant, three groups of four taking turns -- a staged
 //                  tile to bf16, written straight into a tensor-memory
 //                  operand slot (tcgen05.st; the dequantised tile never
-//                  touches shared memory); one warp of the group, a
-//                  different one each step, also loads the K-block's 16 rows
-//                  (bf16) into the slot's shared part;
+//                  touches shared memory);
+//   warp 19 lane 0: row copies -- each step's 16 rows (bf16) into the
+//                  slot's shared part once the slot is free (for a down tile
+//                  once the item's h is complete);
 //   warps 14..17 : epilogue -- gate/up: h = silu(g) * u rounded to bf16, row
 //                  stores; down: fp32 rows to their slot.
 // Every wait is bounded; a timeout records MOE_ERR_TIMEOUT and winds down.
@@ -49,9 +50,12 @@ constexpr int kDqWarps = kDqGroups * kDqGroupWarps;
 constexpr int kEpiWarps = 4;
 // warp 0 producer, warp 1 MMA issuer, dequant warps, epilogue warps, second
 // MMA issuer (measured: one thread issuing these small-N MMAs was busy 60 % of
-// the kernel, ~107 cycles per MMA, and set the pace)
+// the kernel, ~107 cycles per MMA, and set the pace), row-copy warp
 constexpr int kMma2Warp = 2 + kDqWarps + kEpiWarps;
-constexpr int kThreads16 = 32 * (3 + kDqWarps + kEpiWarps);
+// row copies in a warp of their own (measured at 8 rows: 287.7 -> 285.7 us
+// against one of the dequant warps taking each step's copies in turn)
+constexpr int kBLoadWarp = kMma2Warp + 1;
+constexpr int kThreads16 = 32 * (4 + kDqWarps + kEpiWarps);
 // registers a thread for one block per SM: each SM sub-partition holds 16K
 // registers and ceil(warps / 4) of the block's warps; in steps of 8
 constexpr int kMaxRegs16 = (16384 / (((kThreads16 / 32 + 3) / 4) * 32)) / 8 * 8;
@@ -422,6 +426,55 @@ __global__ void __maxnreg__(kMaxRegs16)
             }
             if (!ok) *s_abort = 1;
         }
+    } else if (warp == kBLoadWarp) {
+        if (lane == 0) {
+            // ---------------------------------------------- row copies
+            int slot = 0;
+            uint32_t sph = 0;
+            bool ok = true;
+            pdl_wait();   // gathered rows and the counters belong to the previous kernel
+            for (uint32_t kq = 0; ok; ++kq) {
+                if (*s_abort ||
+                    !mbar_wait(&tq_full[kq % kTq16], (kq / kTq16) & 1u, p.err, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                const TileEntry16 en = tq[kq % kTq16];
+                if (en.t >= n_tiles) break;
+                const bool gu = en.gu != 0;
+                const int4 it = items[en.item];
+                const int NS = gu ? 2 * KB_H : KB_I;
+                bool h_ready = gu;
+                for (int j = 0; j < NS; ++j) {
+                    const int s_cur = slot;
+                    const uint32_t ph = sph;
+                    if (++slot == kSlots) {
+                        slot = 0;
+                        sph ^= 1u;
+                    }
+                    if (*s_abort || !mbar_wait(&a_empty[s_cur], ph ^ 1u, p.err, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    if (!h_ready) {
+                        // h of this item comes from this launch's gate/up tiles
+                        if (!wait_ready(p.ready + en.item, MB_I, p.err, p.timeout_ns, s_abort)) {
+                            ok = false;
+                            break;
+                        }
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        h_ready = true;
+                    }
+                    const int kb = gu ? (j >> 1) : j;
+                    const CUtensorMap* bm = gu ? &map_x : &map_h;
+                    uint8_t* sl = slots + s_cur * kSlotBytes;
+                    mbar_arrive_expect_tx(&a_full[s_cur], kBBytes);
+                    tma_load_2d(sl, bm, &a_full[s_cur], kb * kBlock, it.y);
+                    tma_load_2d(sl + kBBytes / 2, bm, &a_full[s_cur], kb * kBlock + 64, it.y);
+                }
+            }
+            if (!ok) *s_abort = 1;
+        }
     } else if (warp < 2 + kDqWarps) {
         // --------------------------------------------------------- dequant
         // kDqGroups groups of four warps take turns over the CTA's step
@@ -460,7 +513,6 @@ __global__ void __maxnreg__(kMaxRegs16)
             auto scale_of = [&](int j) -> float {
                 return tl.gu ? __ldg(((j & 1) ? su : sg) + sbase + (j >> 1)) : __ldg(sd + sbase + j);
             };
-            bool h_ready = tl.gu;
             // this group's first step of the tile
             const int j0 = (grp - static_cast<int>(n % kDqGroups) + kDqGroups) % kDqGroups;
             float s_next = (j0 < NS) ? scale_of(j0) : 0.0f;
@@ -481,27 +533,6 @@ __global__ void __maxnreg__(kMaxRegs16)
                     break;
                 }
                 tc_fence_after();
-                // the group's warps take turns at the step's copies (and
-                // the wait for h), which a fixed leader warp would add to
-                // every step of its group (measured at 8 rows: 294.0 ->
-                // 290.0 us)
-                const bool leader = lane == 0 && static_cast<int>((nj / kDqGroups) % kDqGroupWarps) ==
-                                                     dw % kDqGroupWarps;
-                if (leader) {
-                    if (!h_ready) {
-                        // h of this item comes from this launch's gate/up tiles
-                        if (!wait_ready(p.ready + tl.item, MB_I, p.err, p.timeout_ns, s_abort))
-                            *s_abort = 1;
-                        asm volatile("fence.proxy.async.global;" ::: "memory");
-                        h_ready = true;
-                    }
-                    const int kb = tl.gu ? (j >> 1) : j;
-                    const CUtensorMap* bm = tl.gu ? &map_x : &map_h;
-                    uint8_t* sl = slots + slot * kSlotBytes;
-                    mbar_arrive_expect_tx(&a_full[slot], kBBytes);
-                    tma_load_2d(sl, bm, &a_full[slot], kb * kBlock, it.y);
-                    tma_load_2d(sl + kBBytes / 2, bm, &a_full[slot], kb * kBlock + 64, it.y);
-                }
                 got = !*s_abort && mbar_wait(&w_full[ws], wph, p.err, p.timeout_ns);
                 if (!__all_sync(0xFFFFFFFFu, got)) {
                     ok = false;
