@@ -489,7 +489,9 @@ __global__ void __maxnreg__(kMaxRegs16)
         const int row = 32 * qd + lane;
         uint32_t n = 0;              // the CTA's step counter (every group counts every step)
         bool ok = true;
-        pdl_wait();   // gathered rows and the counters belong to the previous kernel
+        // nothing here reads the previous kernel's outputs; the wait only
+        // keeps the roles together (converting before it measured the same)
+        pdl_wait();
         for (uint32_t kq = 0; ok; ++kq) {
             bool got = !*s_abort &&
                        mbar_wait(&tq_full[kq % kTq16], (kq / kTq16) & 1u, p.err, p.timeout_ns);
