@@ -535,14 +535,16 @@ __global__ void __maxnreg__(kMaxRegs16)
                 const uint32_t sph = (nj / kSlots) & 1u;
                 const float s = s_next;
                 if (j + kDqGroups < NS) s_next = scale_of(j + kDqGroups);
-                // every wait's outcome is made uniform across the warp before use
-                bool got = !*s_abort && mbar_wait(&a_empty[slot], sph ^ 1u, p.err, p.timeout_ns);
+                // every wait's outcome is made uniform across the warp before use;
+                // no abort-flag read before these bounded waits (as in the MMA
+                // threads; measured 270.6 -> 267.2 us at 8 rows)
+                bool got = mbar_wait(&a_empty[slot], sph ^ 1u, p.err, p.timeout_ns);
                 if (!__all_sync(0xFFFFFFFFu, got)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                got = !*s_abort && mbar_wait(&w_full[ws], wph, p.err, p.timeout_ns);
+                got = mbar_wait(&w_full[ws], wph, p.err, p.timeout_ns);
                 if (!__all_sync(0xFFFFFFFFu, got)) {
                     ok = false;
                     break;
